@@ -1,0 +1,386 @@
+"""Plain fp64 CPU oracle for one Medusa draft-and-verify decode step.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this module.  The CUDA library
+never calls it, and it shares no code with the CUDA path: the only common
+dependency is the seeded input generator ``medusa_synth``.
+
+Everything here is written for clarity, not speed: float64 numpy, one library
+matmul per projection, explicit loops over sequences, tree nodes and paths.
+
+Sources (web pages about Medusa, cited by page title and section):
+  [DD]   "Medusa deep dive" (aicassindra, transformer math series)
+  [GL]   "Medusa Heads" (inferensys glossary)
+  [D89]  "day89" (skandtandon blog), section "Tree-based attention"
+  [GU]   "Medusa Decoding Heads" (aiunderstanding.org guide), "Deep Dive"
+  [SD2]  "Speculative Decoding Deep Dive II: Medusa, MTP" (zackli.ai)
+
+Readings taken where the pages are silent or disagree (each is restated at
+the function that uses it):
+  R1  Head offsets: the base LM head predicts t+1, Medusa head i predicts
+      t+i+1 ([DD] "What this deep dive assumes"; [SD2] "Medusa", Training:
+      Head 0 is the base head).  Tree depth d is drafted by head d.
+  R2  Head form: u_i = h + SiLU(W_i h), logits = LMproj u_i, no bias, one
+      LM projection shared by the base head and every Medusa head ([DD] "The
+      heads are residual blocks, not linear layers").
+  R3  Top-s order: value descending, then token id ascending.  Argmax ties
+      go to the lowest id.
+  R4  Tree: every depth-d rank tuple (r_1..r_d), r_j < s_j, kept when the
+      ranks sum to at most max_rank_sum (no limit for a full tree); nodes in
+      breadth-first order = by depth, then lexicographic tuple.  Node 0 is the
+      root (the base head's token).  Mask row i = Anc(i), i itself and the
+      root ([SD2] "Medusa"; [DD] "From top-k heads to a sparse candidate tree").
+  R5  Verify layer: one attention layer.  x = Emb[token]; q, k, v = x Wq^T,
+      x Wk^T, x Wv^T; scale 1/sqrt(dh); joint softmax over the prefix and
+      the masked tree rows; GQA: query head j reads KV head j // (Hq/Hkv);
+      y = o Wo^T; no residual, no norm, no position encoding.
+  R6  Typical acceptance ([DD] "Typical acceptance, not exact rejection
+      sampling"; [D89] "Tree-based attention"): child c passes when
+      p_parent(tok_c) > min(eps, delta * exp(-H_parent)); temperature 1,
+      natural log, strict inequality.  Greedy: tok_c == argmax of the parent
+      row ([GU] "Deep Dive": accept the longest prefix that matches what the
+      model would have produced).
+  R7  Longest accepted path: deepest node whose every edge passes; ties go to
+      the lowest breadth-first index.  L = its depth; the step emits L + 1
+      tokens (the root and the path); next_root = argmax of the verify row at
+      the path's last node ([GL] early stop, rollback, next token from the
+      base model).
+  R8  KV compaction: cache rows P_b + path[j] move to P_b + j for j = 0..L,
+      then P_b += L + 1 ([GL] "Speculative KV Cache", rollback).
+  R9  bf16 workloads: the oracle rounds to bf16 exactly where the stored
+      tensors are bf16 (U, q/k/v, o, y); logits and statistics stay fp64.
+"""
+from __future__ import annotations
+
+import itertools
+import math
+from typing import Dict, List, Sequence, Tuple
+
+import numpy as np
+
+
+# ----------------------------------------------------------------------------
+# bf16 rounding of an fp64 value: nearest value with an 8-bit significand,
+# ties to even.  x = m * 2^e with 0.5 <= |m| < 1, so m * 2^8 is the
+# significand scaled to an integer range [128, 256).
+# ----------------------------------------------------------------------------
+
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)
+    return np.ldexp(np.rint(m * 256.0) / 256.0, e)
+
+
+def maybe_round(x: np.ndarray, dtype: str) -> np.ndarray:
+    return round_bf16(x) if dtype == "bf16" else x
+
+
+# ----------------------------------------------------------------------------
+# A1: Medusa heads' residual blocks.  [DD] "The heads are residual blocks,
+# not linear layers": head_i(h) = LMproj(h + SiLU(W_i h)).  SiLU(a) =
+# a * sigmoid(a) = a / (1 + e^-a).  Row 0 is the base LM head's input, h.
+# ----------------------------------------------------------------------------
+
+def silu(a: np.ndarray) -> np.ndarray:
+    return a / (1.0 + np.exp(-a))
+
+
+def heads_residual(h: np.ndarray, W: np.ndarray, dtype: str) -> np.ndarray:
+    """h [B, d], W [K, d_out, d_in] -> U [B, K+1, d]."""
+    B, d = h.shape
+    K = W.shape[0]
+    U = np.empty((B, K + 1, d))
+    U[:, 0, :] = h
+    for i in range(K):
+        a = h @ W[i].T
+        U[:, i + 1, :] = h + silu(a)
+    return maybe_round(U, dtype)
+
+
+# ----------------------------------------------------------------------------
+# A2: shared LM projection and per-head shortlists.  [DD] "From top-k heads
+# to a sparse candidate tree": keep the top k_1 tokens of head 1, the top k_2
+# of head 2, ...; the base head's argmax is the root (R1, R3).
+# ----------------------------------------------------------------------------
+
+def sorted_ids(z: np.ndarray) -> np.ndarray:
+    """Token ids of one logit row, by value descending then id ascending."""
+    return np.lexsort((np.arange(z.shape[0]), -z))
+
+
+def draft(U: np.ndarray, lm: np.ndarray, shortlist: Sequence[int]) -> Dict[str, np.ndarray]:
+    """U [B, K+1, d], lm [V, d] -> root [B], topk_id/topk_val [B, K, smax].
+
+    Also returns margins: ``root_gap`` = top-1 minus top-2 logit of the base
+    row, ``topk_gap`` [B, K] = smallest gap between consecutive sorted logits
+    among ranks 0..s_i (the order and the cut of head i's shortlist).
+    Unused entries (rank >= s_i) hold id -1 and value -inf.
+    """
+    B, K1, d = U.shape
+    K = K1 - 1
+    smax = max(shortlist)
+    root = np.empty(B, np.int64)
+    root_gap = np.empty(B)
+    topk_id = np.full((B, K, smax), -1, np.int64)
+    topk_val = np.full((B, K, smax), -np.inf)
+    topk_gap = np.empty((B, K))
+    for b in range(B):
+        z = U[b] @ lm.T                      # [K+1, V]
+        order = sorted_ids(z[0])
+        root[b] = order[0]
+        root_gap[b] = z[0, order[0]] - z[0, order[1]]
+        for i in range(K):
+            s = shortlist[i]
+            order = sorted_ids(z[i + 1])
+            vals = z[i + 1, order[: s + 1]]
+            topk_id[b, i, :s] = order[:s]
+            topk_val[b, i, :s] = vals[:s]
+            topk_gap[b, i] = np.min(vals[:-1] - vals[1:])
+    return dict(root=root, root_gap=root_gap, topk_id=topk_id,
+                topk_val=topk_val, topk_gap=topk_gap)
+
+
+# ----------------------------------------------------------------------------
+# A3: the candidate tree.  [SD2] "Medusa": for shortlist sizes s_1, s_2, ...
+# the tree has s_1 + s_1 s_2 + ... nodes, Anc(i) = ancestors of node i.
+# [DD]: the tree is fixed ahead of time, laid out as a flat node sequence
+# with an attention mask so a node attends only to its ancestors (R4).
+# ----------------------------------------------------------------------------
+
+def tree_tuples(shortlist: Sequence[int], max_rank_sum: int) -> List[Tuple[int, ...]]:
+    """Every kept rank tuple, root () first, breadth-first (R4)."""
+    K = len(shortlist)
+    kept = set()
+    for full in itertools.product(*[range(s) for s in shortlist]):
+        for depth in range(K + 1):
+            t = full[:depth]
+            if max_rank_sum < 0 or sum(t) <= max_rank_sum:
+                kept.add(t)
+    return sorted(kept, key=lambda t: (len(t), t))
+
+
+def build_tree(shortlist: Sequence[int], max_rank_sum: int) -> Dict[str, np.ndarray]:
+    tuples = tree_tuples(shortlist, max_rank_sum)
+    N = len(tuples)
+    index = {t: i for i, t in enumerate(tuples)}
+    parent = np.array([-1] + [index[t[:-1]] for t in tuples[1:]], np.int64)
+    depth = np.array([len(t) for t in tuples], np.int64)
+    rank = np.array([t[-1] if t else 0 for t in tuples], np.int64)
+    mask = np.zeros((N, N), bool)
+    for i, ti in enumerate(tuples):
+        for j, tj in enumerate(tuples):
+            mask[i, j] = ti[: len(tj)] == tj       # tj is a prefix of ti
+    return dict(tuples=tuples, N=N, parent=parent, depth=depth, rank=rank, mask=mask)
+
+
+def pack_mask(mask: np.ndarray) -> np.ndarray:
+    """bool [N, N] -> uint64 [N, ceil(N/64)]: bit j%64 of word j//64."""
+    N = mask.shape[0]
+    words = (N + 63) // 64
+    out = np.zeros((N, words), np.uint64)
+    for i in range(N):
+        for j in range(N):
+            if mask[i, j]:
+                out[i, j // 64] |= np.uint64(1) << np.uint64(j % 64)
+    return out
+
+
+def fill_tokens(root: np.ndarray, topk_id: np.ndarray, depth: np.ndarray,
+                rank: np.ndarray) -> np.ndarray:
+    """tok[b, 0] = root; tok[b, n] = head depth_n's rank_n-th token (R1)."""
+    B = root.shape[0]
+    N = depth.shape[0]
+    tok = np.empty((B, N), np.int64)
+    for b in range(B):
+        tok[b, 0] = root[b]
+        for n in range(1, N):
+            tok[b, n] = topk_id[b, depth[n] - 1, rank[n]]
+    return tok
+
+
+# ----------------------------------------------------------------------------
+# A4: tree attention, one verify layer (R5).  [GL]: every candidate branch
+# shares the prefix KV; all tree nodes are scored in one pass.  [D89]: the
+# mask lets each candidate attend to its own prefix.
+# ----------------------------------------------------------------------------
+
+def tree_attention(tok: np.ndarray, P: np.ndarray, mask: np.ndarray,
+                   emb: np.ndarray, wq: np.ndarray, wk: np.ndarray, wv: np.ndarray,
+                   wo: np.ndarray, kc: np.ndarray, vc: np.ndarray,
+                   Hq: int, Hkv: int, dh: int, dtype: str) -> Dict[str, np.ndarray]:
+    """Returns q, k, v [B, N, H*dh], o [B, N, Hq*dh], y [B, N, d] and the
+    caches with the tree rows written at P_b .. P_b+N-1 (copies)."""
+    B, N = tok.shape
+    g = Hq // Hkv
+    x = emb[tok]                                         # [B, N, d]
+    q = maybe_round(x @ wq.T, dtype)
+    k = maybe_round(x @ wk.T, dtype)
+    v = maybe_round(x @ wv.T, dtype)
+    kc = kc.copy()
+    vc = vc.copy()
+    o = np.empty((B, N, Hq * dh))
+    scale = 1.0 / math.sqrt(dh)
+    for b in range(B):
+        Pb = int(P[b])
+        for n in range(N):
+            kc[b, :, Pb + n, :] = k[b, n].reshape(Hkv, dh)
+            vc[b, :, Pb + n, :] = v[b, n].reshape(Hkv, dh)
+        for n in range(N):
+            slots = list(range(Pb)) + [Pb + m for m in range(N) if mask[n, m]]
+            for hq in range(Hq):
+                hk = hq // g
+                keys = kc[b, hk, slots, :]               # [S, dh]
+                vals = vc[b, hk, slots, :]
+                qv = q[b, n, hq * dh:(hq + 1) * dh]
+                s = keys @ qv * scale
+                s = s - s.max()
+                p = np.exp(s)
+                p = p / p.sum()
+                o[b, n, hq * dh:(hq + 1) * dh] = p @ vals
+    o = maybe_round(o, dtype)
+    y = maybe_round(o @ wo.T, dtype)
+    return dict(x=x, q=q, k=k, v=v, o=o, y=y, kc=kc, vc=vc)
+
+
+# ----------------------------------------------------------------------------
+# A5: verify logits and the statistics acceptance needs.  Entropy H of the
+# softmax at temperature 1, natural log ([DD] "Typical acceptance").
+# ----------------------------------------------------------------------------
+
+def verify_stats(y: np.ndarray, lm: np.ndarray, tok: np.ndarray,
+                 parent: np.ndarray) -> Dict[str, np.ndarray]:
+    """y [B, N, d] -> argmax, argmax_gap, m, lse, H [B, N]; childlogit [B, N]
+    (entry c = logit of tok_c in its parent's row, entry 0 unused = nan)."""
+    B, N, d = y.shape
+    argmax = np.empty((B, N), np.int64)
+    gap = np.empty((B, N))
+    mx = np.empty((B, N))
+    lse = np.empty((B, N))
+    H = np.empty((B, N))
+    child = np.full((B, N), np.nan)
+    for b in range(B):
+        l = y[b] @ lm.T                                  # [N, V]
+        for n in range(N):
+            row = l[n]
+            order = sorted_ids(row)
+            argmax[b, n] = order[0]
+            gap[b, n] = row[order[0]] - row[order[1]]
+            m = row[order[0]]
+            e = np.exp(row - m)
+            S = e.sum()
+            p = e / S
+            mx[b, n] = m
+            lse[b, n] = m + math.log(S)
+            pos = p[p > 0.0]
+            H[b, n] = -np.sum(pos * np.log(pos))
+        for c in range(1, N):
+            child[b, c] = l[parent[c], tok[b, c]]
+    return dict(argmax=argmax, argmax_gap=gap, m=mx, lse=lse, H=H, childlogit=child)
+
+
+# ----------------------------------------------------------------------------
+# A6: per-edge acceptance test (R6), with the decision margin of each edge.
+# ----------------------------------------------------------------------------
+
+def accept_edges(mode: str, eps: float, delta: float, tok: np.ndarray,
+                 parent: np.ndarray, st: Dict[str, np.ndarray]) -> Tuple[np.ndarray, np.ndarray]:
+    """ok [B, N] (entry 0 = True), margin [B, N] (entry 0 = inf).
+
+    Greedy margin: the parent row's top-1 minus top-2 logit gap.  Typical
+    margin: |ln p - ln threshold| (inf when the threshold is 0)."""
+    B, N = tok.shape
+    ok = np.ones((B, N), bool)
+    margin = np.full((B, N), np.inf)
+    for b in range(B):
+        for c in range(1, N):
+            pa = parent[c]
+            if mode == "greedy":
+                ok[b, c] = tok[b, c] == st["argmax"][b, pa]
+                margin[b, c] = st["argmax_gap"][b, pa]
+            else:
+                p = math.exp(st["childlogit"][b, c] - st["lse"][b, pa])
+                thr = min(eps, delta * math.exp(-st["H"][b, pa]))
+                ok[b, c] = p > thr
+                if thr > 0.0:
+                    margin[b, c] = abs(math.log(p) - math.log(thr))
+    return ok, margin
+
+
+# ----------------------------------------------------------------------------
+# A7: longest accepted path (R7): check every node's whole root path.
+# ----------------------------------------------------------------------------
+
+def longest_path(ok: np.ndarray, parent: np.ndarray, depth: np.ndarray,
+                 argmax: np.ndarray, K: int) -> Dict[str, np.ndarray]:
+    B, N = ok.shape
+    L = np.zeros(B, np.int64)
+    path = np.full((B, K + 1), -1, np.int64)
+    next_root = np.empty(B, np.int64)
+    for b in range(B):
+        best = 0
+        for n in range(N):
+            chain = []
+            a = n
+            while a != 0:
+                chain.append(a)
+                a = parent[a]
+            if all(ok[b, c] for c in chain) and depth[n] > depth[best]:
+                best = n                                 # first (lowest) index wins ties
+        chain = [best]
+        while chain[-1] != 0:
+            chain.append(parent[chain[-1]])
+        chain.reverse()
+        L[b] = depth[best]
+        path[b, : len(chain)] = chain
+        next_root[b] = argmax[b, best]
+    return dict(L=L, path=path, next_root=next_root)
+
+
+# ----------------------------------------------------------------------------
+# A8: commit the accepted path's tree KV into the cache (R8).
+# ----------------------------------------------------------------------------
+
+def compact_kv(kc: np.ndarray, vc: np.ndarray, P: np.ndarray, L: np.ndarray,
+               path: np.ndarray) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
+    kc = kc.copy()
+    vc = vc.copy()
+    Pn = P.astype(np.int64).copy()
+    for b in range(kc.shape[0]):
+        Pb = int(P[b])
+        src = [Pb + int(path[b, j]) for j in range(L[b] + 1)]
+        tk = kc[b][:, src, :].copy()
+        tv = vc[b][:, src, :].copy()
+        kc[b][:, Pb:Pb + L[b] + 1, :] = tk
+        vc[b][:, Pb:Pb + L[b] + 1, :] = tv
+        Pn[b] = Pb + L[b] + 1
+    return kc, vc, Pn
+
+
+# ----------------------------------------------------------------------------
+# The whole step, canonical order: heads, draft, tree, attention, verify,
+# accept, longest path, compaction.
+# ----------------------------------------------------------------------------
+
+def step(w, f64: Dict[str, np.ndarray], P: np.ndarray, mode: str,
+         batch: Sequence[int] = None) -> Dict[str, object]:
+    """One step on inputs ``f64`` (float64 copies of the stored inputs:
+    h, W, lm, emb, wq, wk, wv, wo, kc, vc).  ``batch`` restricts the step to
+    some sequences (their rows of h, kc, vc, P).  Returns every
+    intermediate."""
+    sel = list(range(w.B)) if batch is None else list(batch)
+    h = f64["h"][sel]
+    kc = f64["kc"][sel]
+    vc = f64["vc"][sel]
+    Psel = np.asarray(P)[sel]
+    U = heads_residual(h, f64["W"], w.dtype)
+    dr = draft(U, f64["lm"], w.shortlist)
+    tr = build_tree(w.shortlist, w.max_rank_sum)
+    tok = fill_tokens(dr["root"], dr["topk_id"], tr["depth"], tr["rank"])
+    at = tree_attention(tok, Psel, tr["mask"], f64["emb"], f64["wq"], f64["wk"],
+                        f64["wv"], f64["wo"], kc, vc, w.Hq, w.Hkv, w.dh, w.dtype)
+    st = verify_stats(at["y"], f64["lm"], tok, tr["parent"])
+    ok, margin = accept_edges(mode, w.eps, w.delta, tok, tr["parent"], st)
+    lp = longest_path(ok, tr["parent"], tr["depth"], st["argmax"], w.K)
+    kc2, vc2, Pn = compact_kv(at["kc"], at["vc"], Psel, lp["L"], lp["path"])
+    return dict(batch=sel, U=U, draft=dr, tree=tr, tok=tok, attn=at, stats=st,
+                ok=ok, margin=margin, path=lp, kc=kc2, vc=vc2, P=Pn)

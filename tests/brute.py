@@ -1,0 +1,76 @@
+"""Independent brute-force re-derivations used to pin the oracle.
+
+Nothing here calls the oracle's attention, tree or acceptance code; each
+function rebuilds its result from the plain definitions a different way:
+  * ordinary causal self-attention over an explicit token sequence (dense
+    score matrix with a lower-triangular mask), which is what tree attention
+    must equal for every root-to-node path ("Medusa Heads": all branches share
+    the prefix KV; "day89", "Tree-based attention": each candidate attends to
+    its own prefix);
+  * sequential greedy decoding with the same one-layer verifier, which greedy
+    acceptance must reproduce ("Medusa Decoding Heads", "Deep Dive": accept
+    the longest prefix matching what the model would have produced anyway).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def project(tokens, emb, wq, wk, wv):
+    x = emb[np.asarray(tokens)]
+    return np.einsum("td,od->to", x, wq), np.einsum("td,od->to", x, wk), np.einsum("td,od->to", x, wv)
+
+
+def causal_layer(prefix_k, prefix_v, tokens, emb, wq, wk, wv, wo, Hq, Hkv, dh):
+    """One attention layer over [prefix ; tokens] with a causal mask.
+
+    prefix_k/v: [Hkv, P, dh].  Returns y [len(tokens), d] for the new tokens.
+    Builds the full (P+T) x (P+T) score matrix per head and masks j > i.
+    """
+    T = len(tokens)
+    P = prefix_k.shape[1]
+    q, k, v = project(tokens, emb, wq, wk, wv)
+    g = Hq // Hkv
+    S = P + T
+    out = np.zeros((T, Hq * dh))
+    for hq in range(Hq):
+        hk = hq // g
+        Kall = np.concatenate([prefix_k[hk], k[:, hk * dh:(hk + 1) * dh]], axis=0)
+        Vall = np.concatenate([prefix_v[hk], v[:, hk * dh:(hk + 1) * dh]], axis=0)
+        Qnew = q[:, hq * dh:(hq + 1) * dh]
+        scores = np.full((S, S), -np.inf)
+        scores[P:, :] = Qnew @ Kall.T / np.sqrt(dh)
+        allowed = np.tril(np.ones((S, S), bool))
+        scores = np.where(allowed, scores, -np.inf)
+        rows = scores[P:]
+        rows = rows - rows.max(axis=1, keepdims=True)
+        w = np.exp(rows)
+        w /= w.sum(axis=1, keepdims=True)
+        out[:, hq * dh:(hq + 1) * dh] = w @ Vall
+    return out @ wo.T, k, v
+
+
+def greedy_decode(prefix_k, prefix_v, first, steps, emb, wq, wk, wv, wo, lm, Hq, Hkv, dh):
+    """Tokens x_0 = first, x_{t+1} = argmax(LMproj . y_t), t = 0..steps-1,
+    recomputing the whole causal layer from scratch at every step."""
+    seq = [int(first)]
+    for _ in range(steps):
+        y, _, _ = causal_layer(prefix_k, prefix_v, seq, emb, wq, wk, wv, wo, Hq, Hkv, dh)
+        logits = lm @ y[-1]
+        best = 0
+        for t in range(1, logits.shape[0]):
+            if logits[t] > logits[best]:
+                best = t
+        seq.append(best)
+    return seq
+
+
+def paths_from_parents(parent):
+    """Root-to-node index chains by following parent pointers."""
+    out = []
+    for n in range(len(parent)):
+        chain = [n]
+        while chain[-1] != 0:
+            chain.append(int(parent[chain[-1]]))
+        out.append(chain[::-1])
+    return out

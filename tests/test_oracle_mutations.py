@@ -1,0 +1,155 @@
+"""Plant plausible mistakes in copies of the oracle's functions (on the CPU)
+and check that at least one pin in test_oracle_pins.py catches each one."""
+from __future__ import annotations
+
+import math
+import types
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import medusa_oracle as mo
+from tests import test_oracle_pins as pins
+
+
+def mutant(**replace):
+    ns = types.SimpleNamespace(**{k: getattr(mo, k) for k in dir(mo) if not k.startswith("_")})
+    for k, v in replace.items():
+        setattr(ns, k, v)
+    return ns
+
+
+# --- mutated functions --------------------------------------------------------
+
+def heads_sigmoid_only(h, W, dtype):
+    U = mo.heads_residual(h, W * 0, dtype)
+    for i in range(W.shape[0]):
+        a = h @ W[i].T
+        U[:, i + 1] = h + 1.0 / (1.0 + np.exp(-a))
+    return U
+
+
+def heads_no_residual(h, W, dtype):
+    U = mo.heads_residual(h, W, dtype)
+    for i in range(W.shape[0]):
+        U[:, i + 1] -= h
+    return U
+
+
+def heads_untransposed(h, W, dtype):
+    return mo.heads_residual(h, np.transpose(W, (0, 2, 1)), dtype)
+
+
+def tree_mask_no_self(shortlist, mrs):
+    tr = mo.build_tree(shortlist, mrs)
+    tr["mask"] = tr["mask"].copy()
+    np.fill_diagonal(tr["mask"], False)
+    tr["mask"][0, 0] = True
+    return tr
+
+
+def tree_parent_shift(shortlist, mrs):
+    tr = mo.build_tree(shortlist, mrs)
+    tr["parent"] = tr["parent"].copy()
+    tr["parent"][2:] = np.maximum(tr["parent"][2:] - 1, 0)
+    return tr
+
+
+def sorted_ids_high_id_first(z):
+    return np.lexsort((-np.arange(z.shape[0]), -z))
+
+
+def attention_with(kind):
+    def f(tok, P, mask, emb, wq, wk, wv, wo, kc, vc, Hq, Hkv, dh, dtype):
+        if kind == "mask_T":
+            mask = mask.T
+        if kind == "gqa_mod":
+            # query head j reads KV head j % Hkv instead of j // (Hq/Hkv)
+            perm = [j % Hkv * (Hq // Hkv) + j // Hkv for j in range(Hq)]
+            wq = wq.reshape(Hq, dh, -1)[perm].reshape(Hq * dh, -1)
+            r = mo.tree_attention(tok, P, mask, emb, wq, wk, wv, wo, kc, vc, Hq, Hkv, dh, dtype)
+            inv = np.argsort(perm)
+            o = r["o"].reshape(r["o"].shape[0], r["o"].shape[1], Hq, dh)[:, :, inv].reshape(r["o"].shape)
+            return dict(r, y=o @ wo.T)
+        if kind == "no_scale":
+            wq = wq * math.sqrt(dh)
+        if kind == "prefix_short":
+            P = np.maximum(np.asarray(P) - 1, 0)
+            r = mo.tree_attention(tok, P, mask, emb, wq, wk, wv, wo, kc, vc, Hq, Hkv, dh, dtype)
+            return r
+        return mo.tree_attention(tok, P, mask, emb, wq, wk, wv, wo, kc, vc, Hq, Hkv, dh, dtype)
+    return f
+
+
+def verify_entropy_log2(y, lm, tok, parent):
+    st = mo.verify_stats(y, lm, tok, parent)
+    st["H"] = st["H"] / math.log(2.0)
+    return st
+
+
+def accept_own_row(mode, eps, delta, tok, parent, st):
+    # evaluates the child's token under the child's own row instead of the parent's
+    N = tok.shape[1]
+    fake_parent = np.arange(N)
+    fake_parent[0] = -1
+    st2 = dict(st)
+    return mo.accept_edges(mode, eps, delta, tok, parent, {**st2, "lse": st["lse"][:, :],
+                                                           "H": np.roll(st["H"], -1, axis=1)})
+
+
+def longest_path_high_index(ok, parent, depth, argmax, K):
+    B, N = ok.shape
+    r = mo.longest_path(ok[:, ::-1].copy(), parent, depth, argmax, K)   # wrong: reversed order
+    return r
+
+
+def compact_skip_root(kc, vc, P, L, path):
+    path2 = path.copy()
+    path2[:, 0] = np.where(L > 0, path[:, 1], 0)
+    return mo.compact_kv(kc, vc, P, L, path2)
+
+
+def round_truncate(x):
+    x = np.asarray(x, np.float64)
+    m, e = np.frexp(x)
+    return np.ldexp(np.trunc(m * 256.0) / 256.0, e)
+
+
+CASES = [
+    ("heads: sigmoid instead of SiLU", dict(heads_residual=heads_sigmoid_only), [pins.check_heads_torch]),
+    ("heads: residual dropped", dict(heads_residual=heads_no_residual), [pins.check_zero_heads, pins.check_heads_torch]),
+    ("heads: W transposed", dict(heads_residual=heads_untransposed), [pins.check_heads_torch]),
+    ("tree: mask misses the node itself", dict(build_tree=tree_mask_no_self), [pins.check_tree_golden, pins.check_mask_is_ancestors]),
+    ("tree: parent index shifted", dict(build_tree=tree_parent_shift), [pins.check_tree_golden, pins.check_mask_is_ancestors]),
+    ("top-s: ties to the higher id", dict(sorted_ids=sorted_ids_high_id_first), [pins.check_topk]),
+    ("attention: mask transposed", dict(tree_attention=attention_with("mask_T")), [pins.check_attention_per_path]),
+    ("attention: GQA head map j % Hkv", dict(tree_attention=attention_with("gqa_mod")), [pins.check_attention_per_path]),
+    ("attention: no 1/sqrt(dh)", dict(tree_attention=attention_with("no_scale")), [pins.check_attention_per_path]),
+    ("attention: prefix one short", dict(tree_attention=attention_with("prefix_short")), [pins.check_attention_per_path]),
+    ("verify: entropy in bits", dict(verify_stats=verify_entropy_log2), [pins.check_verify_stats]),
+    ("accept: wrong row's entropy", dict(accept_edges=accept_own_row), [pins.check_typical_direct]),
+    ("path: ties to the highest index", dict(longest_path=longest_path_high_index), [pins.check_longest_path_golden, pins.check_longest_path_brute]),
+    ("compaction: root row dropped", dict(compact_kv=compact_skip_root), [pins.check_compaction]),
+    ("bf16: truncation instead of rounding", dict(round_bf16=round_truncate), [pins.check_round_bf16]),
+]
+
+
+@pytest.mark.filterwarnings("ignore::RuntimeWarning")
+@pytest.mark.parametrize("name,repl,checks", CASES, ids=[c[0] for c in CASES])
+def test_pins_catch_planted_mistake(name, repl, checks):
+    orc = mutant(**repl)
+    caught = False
+    for chk in checks:
+        try:
+            chk(orc)
+        except (AssertionError, IndexError, ValueError):
+            caught = True
+    assert caught, f"no pin caught: {name}"
+
+
+def test_unmutated_passes_all_listed_checks():
+    orc = mutant()
+    for _, _, checks in CASES:
+        for chk in checks:
+            chk(orc)

@@ -1,0 +1,456 @@
+"""Pins of the fp64 oracle against what the pages and the mathematics fix.
+
+Every check here is independent of the oracle's own code path: printed
+counts and closed forms, hand-worked fixtures under tests/golden/, special
+cases that reduce to a library routine (torch, scipy), and brute-force
+re-derivations (tests/brute.py).  ``tests/test_oracle_mutations.py`` plants
+plausible mistakes in copies of oracle functions and checks that these pins
+catch them; the ``check_*`` functions therefore take the oracle module (or a
+stand-in with the same function names) as an argument.
+"""
+from __future__ import annotations
+
+import math
+import os
+import types
+
+import numpy as np
+import pytest
+import scipy.special
+import scipy.stats
+import torch
+
+import medusa_synth as ms
+import oracle
+from tests import brute
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+def golden_lines(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return [ln.strip() for ln in f if ln.strip() and not ln.startswith("#")]
+
+
+def tiny(seed=0, B=2, d=32, V=40, Hq=4, Hkv=2, dh=8, shortlist=(3, 2, 2), mrs=-1,
+         P=(5, 9), dtype="f32"):
+    w = ms.Workload("t", dtype, B=B, d=d, V=V, Hq=Hq, Hkv=Hkv, dh=dh, K=len(shortlist),
+                    shortlist=tuple(shortlist), max_rank_sum=mrs, P=P, accept="greedy",
+                    seed=seed)
+    x = ms.make_inputs(w)
+    f = {k: ms.as_f64(v, w.dtype) for k, v in x.items() if k != "P"}
+    return w, f, x["P"]
+
+
+# ---------------------------------------------------------------------------
+# Tree: counts, golden layout, Anc(i)
+# ---------------------------------------------------------------------------
+
+def check_tree_counts(orc):
+    for ln in golden_lines("tree_counts.txt"):
+        sl, mrs, nodes, paths = [t.strip() for t in ln.split(";")]
+        s = tuple(int(v) for v in sl.split(","))
+        tr = orc.build_tree(s, int(mrs))
+        assert tr["N"] - 1 == int(nodes), (s, tr["N"])
+        if paths != "-":
+            assert int(np.sum(tr["depth"] == len(s))) == int(paths)
+    # closed form sum_d prod_{j<=d} s_j on random full trees
+    rng = np.random.default_rng(5)
+    for _ in range(20):
+        K = int(rng.integers(1, 5))
+        s = tuple(int(v) for v in rng.integers(1, 5, size=K))
+        closed = sum(math.prod(s[:dd]) for dd in range(1, K + 1))
+        tr = orc.build_tree(s, -1)
+        assert tr["N"] - 1 == closed
+        assert int(np.sum(tr["depth"] == K)) == math.prod(s)
+
+
+def check_tree_golden(orc):
+    tr = orc.build_tree((2, 2), -1)
+    for i, ln in enumerate(golden_lines("tree_s22_mask.txt")):
+        left, row = ln.split("|")
+        f = left.split()
+        assert int(f[0]) == i
+        assert tr["parent"][i] == int(f[2])
+        assert tr["depth"][i] == int(f[3])
+        assert tr["rank"][i] == int(f[4])
+        assert "".join("1" if b else "0" for b in tr["mask"][i]) == row.strip()
+
+
+def check_mask_is_ancestors(orc):
+    for s, mrs in [((3, 2, 2), -1), ((8, 4, 2, 2, 1), 3), ((4, 3, 2, 2), -1), ((5, 1, 3), 2)]:
+        tr = orc.build_tree(s, mrs)
+        N = tr["N"]
+        # parents come first (breadth-first), depth = parent depth + 1
+        for n in range(1, N):
+            assert tr["parent"][n] < n
+            assert tr["depth"][n] == tr["depth"][tr["parent"][n]] + 1
+        for n, chain in enumerate(brute.paths_from_parents(tr["parent"])):
+            want = np.zeros(N, bool)
+            want[chain] = True
+            assert np.array_equal(tr["mask"][n], want), (s, n)
+        words = orc.pack_mask(tr["mask"])
+        for n in range(N):
+            for j in range(N):
+                bit = (int(words[n, j // 64]) >> (j % 64)) & 1
+                assert bit == int(tr["mask"][n, j])
+
+
+def test_tree_counts():
+    check_tree_counts(oracle)
+
+
+def test_tree_golden():
+    check_tree_golden(oracle)
+
+
+def test_mask_is_ancestors():
+    check_mask_is_ancestors(oracle)
+
+
+def test_token_fill_matches_rank_tuples():
+    tr = oracle.build_tree((3, 2, 2), -1)
+    root = np.array([7, 9])
+    topk = np.arange(2 * 3 * 3).reshape(2, 3, 3) + 100
+    tok = oracle.fill_tokens(root, topk, tr["depth"], tr["rank"])
+    for b in range(2):
+        assert tok[b, 0] == root[b]
+        for n, t in enumerate(tr["tuples"]):
+            if n:
+                assert tok[b, n] == topk[b, len(t) - 1, t[-1]]
+
+
+# ---------------------------------------------------------------------------
+# Heads and shortlists
+# ---------------------------------------------------------------------------
+
+def check_heads_torch(orc):
+    w, f, _ = tiny(seed=3, B=3, d=48)
+    U = orc.heads_residual(f["h"], f["W"] * 50.0, "f32")   # larger W: SiLU far from linear
+    h = torch.from_numpy(f["h"])
+    for i in range(w.K):
+        Wi = torch.from_numpy(f["W"][i] * 50.0)
+        ref = h + torch.nn.functional.silu(torch.nn.functional.linear(h, Wi))
+        np.testing.assert_allclose(U[:, i + 1], ref.numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_array_equal(U[:, 0], f["h"])
+
+
+def check_zero_heads(orc):
+    # W_i = 0: u_i = h + SiLU(0) = h, so every head's top-1 is the root.
+    w = ms.Workload("z", "bf16", B=3, d=64, V=300, Hq=2, Hkv=2, dh=32, K=3,
+                    shortlist=(3, 2, 2), max_rank_sum=-1, P=(4, 4), accept="greedy")
+    x = ms.make_inputs(w, zero_heads=True)
+    f = {k: ms.as_f64(v, w.dtype) for k, v in x.items() if k != "P"}
+    U = orc.heads_residual(f["h"], f["W"], w.dtype)
+    for i in range(w.K):
+        np.testing.assert_array_equal(U[:, i + 1], f["h"])
+    dr = orc.draft(U, f["lm"], w.shortlist)
+    for i in range(w.K):
+        np.testing.assert_array_equal(dr["topk_id"][:, i, 0], dr["root"])
+
+
+def check_topk(orc):
+    for ln in golden_lines("topk_ties.txt"):
+        z, s, ids = [t.strip() for t in ln.split("|")]
+        z = np.array([float(v) for v in z.split()])
+        got = orc.sorted_ids(z)[: int(s)]
+        assert list(got) == [int(v) for v in ids.split()]
+    # brute force: repeated extraction of (max value, then smallest id)
+    rng = np.random.default_rng(1)
+    for _ in range(30):
+        z = np.round(rng.standard_normal(50) * 2) / 2     # many exact ties
+        rest = list(range(50))
+        want = []
+        for _ in range(8):
+            best = rest[0]
+            for t in rest:
+                if z[t] > z[best] or (z[t] == z[best] and t < best):
+                    best = t
+            want.append(best)
+            rest.remove(best)
+        assert list(orc.sorted_ids(z)[:8]) == want
+
+
+def check_draft_vs_torch(orc):
+    w, f, _ = tiny(seed=4, B=2, d=32, V=200, shortlist=(4, 3, 2))
+    U = orc.heads_residual(f["h"], f["W"], "f32")
+    dr = orc.draft(U, f["lm"], w.shortlist)
+    z = torch.from_numpy(U) @ torch.from_numpy(f["lm"]).T
+    for b in range(w.B):
+        assert dr["root"][b] == int(torch.argmax(z[b, 0]))
+        for i, s in enumerate(w.shortlist):
+            v, idx = torch.topk(z[b, i + 1], s)
+            assert list(dr["topk_id"][b, i, :s]) == idx.tolist()
+            np.testing.assert_allclose(dr["topk_val"][b, i, :s], v.numpy(), rtol=1e-12)
+
+
+def test_heads_torch():
+    check_heads_torch(oracle)
+
+
+def test_zero_heads():
+    check_zero_heads(oracle)
+
+
+def test_topk():
+    check_topk(oracle)
+
+
+def test_draft_vs_torch():
+    check_draft_vs_torch(oracle)
+
+
+# ---------------------------------------------------------------------------
+# Tree attention = per-path causal attention
+# ---------------------------------------------------------------------------
+
+def check_attention_per_path(orc, shortlist=(3, 2, 2), mrs=-1, Hq=4, Hkv=2, seed=0):
+    w, f, P = tiny(seed=seed, B=2, shortlist=shortlist, mrs=mrs, Hq=Hq, Hkv=Hkv, P=(3, 11))
+    tr = orc.build_tree(w.shortlist, w.max_rank_sum)
+    tok = ms.random_tokens(seed, w.B, tr["N"], w.V).astype(np.int64)
+    at = orc.tree_attention(tok, P, tr["mask"], f["emb"], f["wq"], f["wk"], f["wv"],
+                            f["wo"], f["kc"], f["vc"], w.Hq, w.Hkv, w.dh, "f32")
+    for b in range(w.B):
+        Pb = int(P[b])
+        for n, chain in enumerate(brute.paths_from_parents(tr["parent"])):
+            y, k, v = brute.causal_layer(f["kc"][b][:, :Pb], f["vc"][b][:, :Pb],
+                                         tok[b, chain], f["emb"], f["wq"], f["wk"], f["wv"],
+                                         f["wo"], w.Hq, w.Hkv, w.dh)
+            np.testing.assert_allclose(at["y"][b, n], y[-1], rtol=1e-10, atol=1e-12)
+        # tree K/V rows land at P_b + n; the prefix is untouched
+        _, k, v = brute.project(tok[b], f["emb"], f["wq"], f["wk"], f["wv"])
+        for n in range(tr["N"]):
+            np.testing.assert_allclose(at["kc"][b][:, Pb + n, :].reshape(-1), k[n], rtol=1e-12)
+            np.testing.assert_allclose(at["vc"][b][:, Pb + n, :].reshape(-1), v[n], rtol=1e-12)
+        np.testing.assert_array_equal(at["kc"][b][:, :Pb], f["kc"][b][:, :Pb])
+
+
+def test_attention_per_path():
+    check_attention_per_path(oracle)
+
+
+def test_attention_per_path_sparse_gqa():
+    check_attention_per_path(oracle, shortlist=(4, 2, 2, 1), mrs=2, Hq=6, Hkv=2, seed=7)
+
+
+def test_attention_chain_is_causal():
+    # max_rank_sum = 0 keeps one chain: tree attention = plain causal attention
+    check_attention_per_path(oracle, shortlist=(2, 2, 2, 2), mrs=0, Hq=2, Hkv=2, seed=2)
+
+
+def test_attention_root_only_is_decode():
+    w, f, P = tiny(seed=9, B=1)
+    tok = np.array([[5]])
+    at = oracle.tree_attention(tok, P, np.ones((1, 1), bool), f["emb"], f["wq"], f["wk"],
+                               f["wv"], f["wo"], f["kc"], f["vc"], w.Hq, w.Hkv, w.dh, "f32")
+    Pb = int(P[0])
+    y, _, _ = brute.causal_layer(f["kc"][0][:, :Pb], f["vc"][0][:, :Pb], [5], f["emb"],
+                                 f["wq"], f["wk"], f["wv"], f["wo"], w.Hq, w.Hkv, w.dh)
+    np.testing.assert_allclose(at["y"][0, 0], y[0], rtol=1e-10, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# Verify statistics
+# ---------------------------------------------------------------------------
+
+def check_verify_stats(orc):
+    w, f, P = tiny(seed=5, B=2, V=70)
+    rng = np.random.default_rng(0)
+    y = rng.standard_normal((2, 6, w.d))
+    parent = np.array([-1, 0, 0, 1, 1, 2])
+    tok = rng.integers(0, w.V, size=(2, 6))
+    st = orc.verify_stats(y, f["lm"], tok, parent)
+    for b in range(2):
+        l = y[b] @ f["lm"].T
+        for n in range(6):
+            np.testing.assert_allclose(st["lse"][b, n], scipy.special.logsumexp(l[n]), rtol=1e-13)
+            pr = scipy.special.softmax(l[n])
+            np.testing.assert_allclose(st["H"][b, n], scipy.stats.entropy(pr), rtol=1e-12)
+            assert st["H"][b, n] <= math.log(w.V) + 1e-12
+            assert st["argmax"][b, n] == int(np.argmax(l[n]))
+        for c in range(1, 6):
+            np.testing.assert_allclose(st["childlogit"][b, c],
+                                       float(f["lm"][tok[b, c]] @ y[b, parent[c]]), rtol=1e-12)
+    # uniform logits: H = ln V and the argmax is the lowest id
+    st = orc.verify_stats(y, np.zeros_like(f["lm"]), tok, parent)
+    np.testing.assert_allclose(st["H"], math.log(w.V), rtol=1e-14)
+    assert np.all(st["argmax"] == 0)
+
+
+def test_verify_stats():
+    check_verify_stats(oracle)
+
+
+# ---------------------------------------------------------------------------
+# Acceptance and the longest accepted path
+# ---------------------------------------------------------------------------
+
+def check_longest_path_golden(orc):
+    tr = orc.build_tree((2, 2), -1)
+    argmax = np.arange(7)[None, :] + 50
+    for ln in golden_lines("longest_path_cases.txt"):
+        bits, L, path = [t.strip() for t in ln.split("|")]
+        ok = np.array([[True] + [c == "1" for c in bits]])
+        r = orc.longest_path(ok, tr["parent"], tr["depth"], argmax, 2)
+        want = [int(v) for v in path.split()]
+        assert r["L"][0] == int(L), (bits, r)
+        assert list(r["path"][0, : len(want)]) == want
+        assert all(v == -1 for v in r["path"][0, len(want):])
+        assert r["next_root"][0] == 50 + want[-1]
+
+
+def check_longest_path_brute(orc):
+    rng = np.random.default_rng(11)
+    for s, mrs in [((3, 2, 2), -1), ((8, 4, 2, 2, 1), 3)]:
+        tr = orc.build_tree(s, mrs)
+        chains = brute.paths_from_parents(tr["parent"])
+        for _ in range(40):
+            ok = rng.random((1, tr["N"])) < 0.6
+            ok[0, 0] = True
+            r = orc.longest_path(ok, tr["parent"], tr["depth"], np.zeros((1, tr["N"]), np.int64), len(s))
+            good = [n for n, ch in enumerate(chains) if all(ok[0, c] for c in ch)]
+            deepest = max(len(chains[n]) for n in good)
+            best = min(n for n in good if len(chains[n]) == deepest)
+            assert r["L"][0] == deepest - 1
+            assert list(r["path"][0, :deepest]) == chains[best]
+
+
+def check_typical_direct(orc):
+    w, f, P = tiny(seed=6, B=2, V=60)
+    rng = np.random.default_rng(3)
+    tr = orc.build_tree(w.shortlist, -1)
+    y = rng.standard_normal((2, tr["N"], w.d)) * 0.3
+    tok = rng.integers(0, w.V, size=(2, tr["N"]))
+    st = orc.verify_stats(y, f["lm"], tok, tr["parent"])
+    for eps, delta in [(0.09, 0.3), (0.02, 5.0), (1.0, 0.5)]:
+        ok, _ = orc.accept_edges("typical", eps, delta, tok, tr["parent"], st)
+        for b in range(2):
+            for c in range(1, tr["N"]):
+                pr = scipy.special.softmax(f["lm"] @ y[b, tr["parent"][c]])
+                thr = min(eps, delta * math.exp(-scipy.stats.entropy(pr)))
+                assert ok[b, c] == (pr[tok[b, c]] > thr)
+    # delta = 0: threshold 0, every child passes (softmax is positive): L = K
+    ok, _ = orc.accept_edges("typical", 0.09, 0.0, tok, tr["parent"], st)
+    assert ok.all()
+    r = orc.longest_path(ok, tr["parent"], tr["depth"], st["argmax"], w.K)
+    assert np.all(r["L"] == w.K)
+    first_leaf = tr["tuples"].index((0,) * w.K)
+    assert np.all(r["path"][:, -1] == first_leaf)
+    # threshold min(1, huge) = 1: nothing passes
+    ok, _ = orc.accept_edges("typical", 1.0, 1e30, tok, tr["parent"], st)
+    assert not ok[:, 1:].any()
+
+
+def check_greedy_lossless(orc, plant_depth, seed):
+    """Greedy acceptance reproduces sequential greedy decoding: plant the
+    first ``plant_depth`` greedy tokens along one branch of the draft."""
+    w, f, P = tiny(seed=seed, B=1, V=40, shortlist=(3, 2, 2))
+    tr = orc.build_tree(w.shortlist, -1)
+    Pb = int(P[0])
+    root = 13
+    seq = brute.greedy_decode(f["kc"][0][:, :Pb], f["vc"][0][:, :Pb], root, w.K + 1,
+                              f["emb"], f["wq"], f["wk"], f["wv"], f["wo"], f["lm"],
+                              w.Hq, w.Hkv, w.dh)
+    rng = np.random.default_rng(seed)
+    branch = (1, 0, 1)
+    topk = np.zeros((1, w.K, 3), np.int64)
+    for i in range(w.K):
+        cand = [t for t in rng.permutation(w.V) if t != seq[i + 1]][:3]
+        topk[0, i, :] = cand
+        if i < plant_depth:
+            topk[0, i, branch[i]] = seq[i + 1]
+    tok = orc.fill_tokens(np.array([root]), topk, tr["depth"], tr["rank"])
+    at = orc.tree_attention(tok, P, tr["mask"], f["emb"], f["wq"], f["wk"], f["wv"],
+                            f["wo"], f["kc"], f["vc"], w.Hq, w.Hkv, w.dh, "f32")
+    st = orc.verify_stats(at["y"], f["lm"], tok, tr["parent"])
+    ok, _ = orc.accept_edges("greedy", 0, 0, tok, tr["parent"], st)
+    r = orc.longest_path(ok, tr["parent"], tr["depth"], st["argmax"], w.K)
+    L = int(r["L"][0])
+    assert L == plant_depth
+    emitted = [int(tok[0, n]) for n in r["path"][0, : L + 1]] + [int(r["next_root"][0])]
+    assert emitted == seq[: L + 2]
+
+
+def test_longest_path_golden():
+    check_longest_path_golden(oracle)
+
+
+def test_longest_path_brute():
+    check_longest_path_brute(oracle)
+
+
+def test_typical_direct_and_special_cases():
+    check_typical_direct(oracle)
+
+
+@pytest.mark.parametrize("plant_depth,seed", [(3, 0), (2, 1), (1, 2), (0, 3), (3, 4)])
+def test_greedy_lossless(plant_depth, seed):
+    check_greedy_lossless(oracle, plant_depth, seed)
+
+
+# ---------------------------------------------------------------------------
+# KV compaction = the cache sequential decoding of the accepted tokens builds
+# ---------------------------------------------------------------------------
+
+def check_compaction(orc):
+    w, f, P = tiny(seed=8, B=3, shortlist=(3, 2, 2), P=(4, 10))
+    tr = orc.build_tree(w.shortlist, -1)
+    tok = ms.random_tokens(8, w.B, tr["N"], w.V).astype(np.int64)
+    at = orc.tree_attention(tok, P, tr["mask"], f["emb"], f["wq"], f["wk"], f["wv"],
+                            f["wo"], f["kc"], f["vc"], w.Hq, w.Hkv, w.dh, "f32")
+    chains = brute.paths_from_parents(tr["parent"])
+    picks = [0, tr["tuples"].index((2, 1)), tr["tuples"].index((1, 1, 1))]   # L = 0, 2, 3
+    L = np.array([len(chains[n]) - 1 for n in picks])
+    path = np.full((w.B, w.K + 1), -1)
+    for b, n in enumerate(picks):
+        path[b, : L[b] + 1] = chains[n]
+    kc, vc, Pn = orc.compact_kv(at["kc"], at["vc"], P, L, path)
+    for b in range(w.B):
+        Pb = int(P[b])
+        assert Pn[b] == Pb + L[b] + 1
+        accepted = [int(tok[b, n]) for n in chains[picks[b]]]
+        _, k, v = brute.project(accepted, f["emb"], f["wq"], f["wk"], f["wv"])
+        for j in range(L[b] + 1):
+            np.testing.assert_allclose(kc[b][:, Pb + j].reshape(-1), k[j], rtol=1e-12)
+            np.testing.assert_allclose(vc[b][:, Pb + j].reshape(-1), v[j], rtol=1e-12)
+        np.testing.assert_array_equal(kc[b][:, :Pb], f["kc"][b][:, :Pb])
+
+
+def test_compaction():
+    check_compaction(oracle)
+
+
+# ---------------------------------------------------------------------------
+# bf16 rounding
+# ---------------------------------------------------------------------------
+
+def check_round_bf16(orc):
+    rng = np.random.default_rng(2)
+    x = rng.standard_normal(20000).astype(np.float32).astype(np.float64) * 10.0 ** rng.integers(-6, 6, 20000)
+    want = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(orc.round_bf16(x), want)
+    # halfway cases: ties go to the even significand
+    one = 1.0
+    assert orc.round_bf16(np.array([one + 2.0 ** -8]))[0] == 1.0
+    assert orc.round_bf16(np.array([one + 3 * 2.0 ** -8]))[0] == one + 2.0 ** -6
+    assert orc.round_bf16(np.array([-(one + 2.0 ** -8 + 2.0 ** -30)]))[0] == -(one + 2.0 ** -7)
+
+
+def test_round_bf16():
+    check_round_bf16(oracle)
+
+
+# ---------------------------------------------------------------------------
+# The whole step on the tiny fp32 workload runs and is self-consistent
+# ---------------------------------------------------------------------------
+
+def test_step_config0_consistent():
+    w = ms.workload(0)
+    x = ms.make_inputs(w)
+    f = {k: ms.as_f64(v, w.dtype) for k, v in x.items() if k != "P"}
+    r = oracle.step(w, f, x["P"], "greedy")
+    assert r["tree"]["N"] == 15
+    assert r["P"][0] == x["P"][0] + r["path"]["L"][0] + 1
+    assert r["tok"][0, 0] == r["draft"]["root"][0]
