@@ -1,0 +1,358 @@
+#!/usr/bin/env python3
+"""Benchmark: one Medusa draft-and-verify step on one B300 (per rank).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload vicuna7b-b1]
+
+A step = medusa_heads -> tree_attention -> lm_verify -> verify_accept ->
+compact_kv on the seeded synthetic workload (default: the Vicuna-7B-shaped
+batch-1 workload, d=4096, V=32000, 32 heads x 128, K=4, tree (4,3,2,2),
+prefix 2048, typical acceptance).  Inputs are resident in HBM; each step's
+bytes (about 0.8 GB) exceed the 126 MB L2, so no L2 flush is inserted.  The
+prefix length is restored before every step (one 4-byte device copy), so
+every timed step verifies against the same prefix length.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the fp64 CPU
+oracle on this host instead (a bounded sample of the same workload).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import medusa_synth as ms  # noqa: E402
+
+METRIC = "Medusa draft+verify steps/s"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return dict(hbm=float(j["hbm_gbs"]), bf16=float(j["bf16_tflops"]),
+                    bf16_sustained=float(j.get("bf16_tflops_sustained", j["bf16_tflops"])),
+                    src="measured")
+    return dict(hbm=6400.0, bf16=1800.0, bf16_sustained=1400.0, src="fallback")
+
+
+def step_bytes(w, N):
+    """Algorithmic HBM bytes of one step (bf16): each weight and the prefix
+    KV read once, small activations and outputs added."""
+    e = 2 if w.dtype == "bf16" else 4
+    d, V, K, B = w.d, w.V, w.K, w.B
+    qkv = (w.Hq + 2 * w.Hkv) * w.dh * d * e
+    wo = d * w.Hq * w.dh * e
+    return dict(heads=K * d * d * e, lm=V * d * e, qkv=qkv, wo=wo)
+
+
+def lm_verify_bytes(w, N):
+    e = 2 if w.dtype == "bf16" else 4
+    rows = w.B * N
+    return w.V * w.d * e + rows * w.d * e + rows * (4 * 4 + 4 + 4) + rows * 4
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for ln in f:
+                c = [v.strip() for v in ln.split(",")]
+                if len(c) < 9:
+                    continue
+                try:
+                    sm.append(float(c[1]))
+                    smax = float(c[2])
+                except ValueError:
+                    continue
+                for nm, v in zip(names, c[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def oracle_sample(w, x, budget_s=15.0):
+    """Time the fp64 oracle's step on this host for up to ~budget_s."""
+    import oracle
+    try:
+        from threadpoolctl import threadpool_info
+        cores = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    except Exception:
+        cores = os.cpu_count() or 1
+    f = {k: ms.as_f64(x[k], w.dtype) for k in ("h", "W", "lm", "emb", "wq", "wk", "wv", "wo")}
+    f["kc"] = ms.as_f64(x["kc"][:1], w.dtype)
+    f["vc"] = ms.as_f64(x["vc"][:1], w.dtype)
+    f["h"] = f["h"][:1]
+    mode = "greedy" if w.accept == "greedy" else "typical"
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        oracle.step(w, f, x["P"][:1], mode, batch=[0])
+        n += 1
+        if time.perf_counter() - t0 >= budget_s or n >= 50:
+            break
+    dt = time.perf_counter() - t0
+    # one oracle step processes one sequence; a GPU step processes B
+    return dict(value=n / dt / w.B, unit="steps/s", cores=cores, kind="oracle",
+                sample=f"{n} oracle step(s) of one sequence of {w.name} "
+                       f"(scaled by 1/B={w.B} to whole-batch steps/s)"), n, dt
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    x = ms.make_inputs(w)
+    cb, n, dt = oracle_sample(w, x, budget_s=max(5.0, min(60.0, 3.0 * args.steps)))
+    line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "steps/s",
+            "n_gpus": args.gpus, "steps": n, "warmup": 0, "ms_per_step": 1e3 * dt / n,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w.name, "B": w.B, "d": w.d, "V": w.V,
+                                            "K": w.K, "shortlist": list(w.shortlist),
+                                            "prefix": list(w.P)},
+            "cpu_baseline": cb, "e2e": {"value": cb["value"], "unit": "steps/s",
+                                        "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+    import speculative_decoding_08_b300 as mds
+    from speculative_decoding_08_b300 import build as mbuild
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    if rank == 0 or world == 1:
+        mbuild.build()
+    if world > 1:
+        dist.barrier()
+    mds.load()
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    x = ms.make_inputs(w)
+
+    def t(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(a).to(dev)
+
+    wt = {k: t(x[k]) for k in ("W", "lm", "emb", "wqkv", "wo", "kc", "vc")}
+    P0 = torch.from_numpy(x["P"]).to(dev)
+    P = P0.clone()
+    h = t(x["h"])
+    mode = 0 if w.accept == "greedy" else 1
+    step = mds.MedusaStep(W=wt["W"], lm=wt["lm"], emb=wt["emb"], wqkv=wt["wqkv"], wo=wt["wo"],
+                          Kc=wt["kc"], Vc=wt["vc"], P=P, shortlist=w.shortlist,
+                          max_rank_sum=w.max_rank_sum, Hq=w.Hq, Hkv=w.Hkv, B=w.B)
+    N = step.N
+
+    def one():
+        P.copy_(P0)
+        step.run(h, mode=mode, eps=w.eps, delta=w.delta)
+
+    s = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(s):
+        for _ in range(max(args.warmup, 3)):
+            one()
+    s.synchronize()
+    # capture the step in a CUDA graph
+    g = torch.cuda.CUDAGraph()
+    n0 = mds.launch_count()
+    with torch.cuda.graph(g, stream=s):
+        one()
+    per_step_kernels = mds.launch_count() - n0
+    for _ in range(max(args.warmup, 3)):
+        g.replay()
+    torch.cuda.synchronize()
+    assert mds.status_check(step.ws) == 0, "device latched a data error"
+
+    clocks = Clocks(dev.index)
+    clocks.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        e0.record(s)
+        for _ in range(args.steps):
+            g.replay()
+        e1.record(s)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms_total = e0.elapsed_time(e1)
+
+    # per-call device time (eager launches, events on the launching stream)
+    calls = ["medusa_heads", "tree_attention", "lm_verify", "verify_accept", "compact_kv"]
+    per = {c: 0.0 for c in calls}
+    reps = max(args.steps, 5)
+    with torch.cuda.stream(s):
+        for _ in range(reps):
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+            P.copy_(P0)
+            ev[0].record(s)
+            mds.medusa_heads(h, step.W, step.lm, step.shortlist, step.smax, step.U, step.root,
+                             step.topk_id, step.topk_val, step.ws)
+            ev[1].record(s)
+            mds.tree_attention(step.P, step.tok, step.mask, step.emb, step.wqkv, step.wo,
+                               step.Kc, step.Vc, step.y, step.ws, Hq=step.Hq, Hkv=step.Hkv,
+                               K=step.K, smax=step.smax, root=step.root, topk_id=step.topk_id,
+                               depth=step.depth, rank=step.rank)
+            ev[2].record(s)
+            mds.lm_verify(step.y, step.lm, step.tok, step.parent, step.argmax, step.stats,
+                          step.childlogit, step.ws)
+            ev[3].record(s)
+            mds.verify_accept(mode, w.eps, w.delta, step.parent, step.depth, step.tok,
+                              step.argmax, step.stats, step.childlogit, step.L, step.path,
+                              step.next_root, step.ws, ok=step.ok)
+            ev[4].record(s)
+            mds.compact_kv(step.L, step.path, step.Kc, step.Vc, step.P, step.ws)
+            ev[5].record(s)
+            s.synchronize()
+            for i, c in enumerate(calls):
+                per[c] += ev[i].elapsed_time(ev[i + 1]) / reps
+    clk = clocks.stop()
+
+    # end to end through the public API with host buffers: pinned h in,
+    # emitted tokens (L, path, tree tokens, next_root) out, every step
+    h_host = torch.empty_like(h, device="cpu").pin_memory()
+    h_host.copy_(h.cpu())
+    outs = [torch.empty(step.L.shape, dtype=torch.int32).pin_memory(),
+            torch.empty(step.path.shape, dtype=torch.int32).pin_memory(),
+            torch.empty(step.tok.shape, dtype=torch.int32).pin_memory(),
+            torch.empty(step.next_root.shape, dtype=torch.int32).pin_memory()]
+    h_dev = torch.empty_like(h)
+    e2e_steps = max(args.steps // 2, 3)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        with torch.cuda.stream(s):
+            h_dev.copy_(h_host, non_blocking=True)
+            P.copy_(P0)
+            step.run(h_dev, mode=mode, eps=w.eps, delta=w.delta)
+            for o, src in zip(outs, (step.L, step.path, step.tok, step.next_root)):
+                o.copy_(src, non_blocking=True)
+        s.synchronize()
+    e2e_dt = time.perf_counter() - t0
+    h2d = h.numel() * h.element_size()
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+    L_host = outs[0].numpy().copy()
+
+    # max over ranks
+    tmax = torch.tensor([ms_total], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
+    ms_total = float(tmax.item())
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    ms_step = ms_total / args.steps
+    steps_per_s = world * args.steps / (ms_total / 1e3)
+    mean_emit = float(np.mean(L_host + 1))
+    pk = peaks()
+    lmv_bytes = lm_verify_bytes(w, N)
+    lmv_s = per["lm_verify"] / 1e3
+    achieved = lmv_bytes / lmv_s / 1e9
+    sb = step_bytes(w, N)
+    prefix_bytes = int(np.sum(x["P"])) * w.Hkv * w.dh * 2 * (2 if w.dtype == "bf16" else 4)
+    total_bytes = sb["heads"] + 2 * sb["lm"] + sb["qkv"] + sb["wo"] + prefix_bytes
+    line = {
+        "metric": METRIC, "value": steps_per_s, "unit": "steps/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic (seeded; value laws of the workload description)",
+        "config": {"workload": w.name, "B": w.B, "d": w.d, "V": w.V, "Hq": w.Hq, "Hkv": w.Hkv,
+                   "dh": w.dh, "K": w.K, "shortlist": list(w.shortlist),
+                   "max_rank_sum": w.max_rank_sum, "prefix": list(w.P), "accept": w.accept,
+                   "parallelism": f"replicas x{world}", "cuda_graph": True,
+                   "l2": "per-step bytes (~%.0f MB) exceed the 126 MB L2; no flush" % (total_bytes / 1e6)},
+        "accepted_tok_per_s": steps_per_s * w.B * mean_emit,
+        "mean_tokens_per_step": mean_emit,
+        "step_hbm_gbs": total_bytes / (ms_step / 1e3) / 1e9,
+        "step_hbm_frac": total_bytes / (ms_step / 1e3) / 1e9 / pk["hbm"],
+        "per_call_us": {c: 1e3 * v for c, v in per.items()},
+        "roofline": {"kernel": "lm_verify (LM-projection stream, verify rows)", "bound": "hbm",
+                     "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
+                     "frac": achieved / pk["hbm"], "traffic": None,
+                     "peak_src": pk["src"], "algorithmic_bytes_per_launch": lmv_bytes},
+        "gpu_launches": per_step_kernels * args.steps,
+        "clocks": clk,
+        "e2e": {"value": e2e_steps / e2e_dt, "unit": "steps/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+    }
+    if not args.no_cpu_baseline:
+        cb, _, _ = oracle_sample(w, x, budget_s=args.cpu_budget)
+        line["cpu_baseline"] = cb
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="vicuna7b-b1")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = ms.workload(args.workload)
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,223 @@
+/*
+ * medusa.h -- C ABI of a B300 (sm_103a) library for one Medusa
+ * draft-and-verify decode step.
+ *
+ * The method (web pages about Medusa, cited by title and section):
+ *   [DD]  "Medusa deep dive" (aicassindra)
+ *   [GL]  "Medusa Heads" (inferensys glossary)
+ *   [D89] "day89" (skandtandon), "Tree-based attention"
+ *   [GU]  "Medusa Decoding Heads" (aiunderstanding.org), "Deep Dive"
+ *   [SD2] "Speculative Decoding Deep Dive II: Medusa, MTP" (zackli.ai), "Medusa"
+ *
+ * One step, in call order:
+ *   mds_medusa_heads     K heads + base head, shortlists          [DD] heads, top-k
+ *   mds_build_tree_mask  fixed candidate tree + ancestor bitmask  [DD], [SD2]
+ *                        (once per tree shape)
+ *   mds_tree_attention   one verify layer over prefix + tree      [GL], [D89]
+ *   mds_lm_verify        verify logits -> argmax / lse / entropy  [DD] typical acceptance
+ *   mds_verify_accept    per-edge test + longest accepted path    [GL], [GU], [DD]
+ *   mds_compact_kv       commit the accepted path's KV            [GL] KV cache, rollback
+ *
+ * Conventions shared by every call
+ *  - Pointers marked "device" are CUDA device pointers on the current device;
+ *    "host" pointers are read before the call returns.  The caller owns every
+ *    buffer; the library allocates no device memory per call.
+ *  - Tensors are dense, row-major, with the shapes written next to them.
+ *    Element type of "void*" tensors is given by `dtype`: MDS_F32 (float) or
+ *    MDS_BF16 (bfloat16, stored as 16-bit patterns).  Accumulation is fp32.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  All device
+ *    work is enqueued on it and is asynchronous.  No call synchronises the
+ *    host except mds_status_check.
+ *  - Argument errors are detected on the host and returned synchronously
+ *    (MDS_EINVAL, MDS_EWORKSPACE, MDS_EUNSUPPORTED) before anything is
+ *    enqueued.  A failed launch returns MDS_ECUDA.
+ *  - Data errors found on the device (a token id outside [0, V), a tree index
+ *    outside [0, N), P_b + N > Pmax, L > K, a wait that timed out) never
+ *    cause an out-of-bounds access: the offending work item is skipped and
+ *    the first error code is latched in the workspace status word, to be
+ *    read with mds_status_check (which returns MDS_EDEVICE in that case).
+ *  - A workspace is used by one stream at a time (calls are not thread-safe
+ *    per workspace).  Size it with mds_workspace_size; it must be 256-byte
+ *    aligned and zero-filled once before first use.
+ *  - Limits: N (tree rows incl. root) <= 128, K <= 8, s_i <= 8, d % 64 == 0,
+ *    dh in {64, 128}, Hq % Hkv == 0.  Larger shapes return MDS_EUNSUPPORTED.
+ */
+#ifndef MEDUSA_B300_H
+#define MEDUSA_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MDS_API __attribute__((visibility("default")))
+#else
+#define MDS_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MDS_OK = 0,
+  MDS_EINVAL = -1,        /* bad argument (null pointer, negative size, ...) */
+  MDS_EWORKSPACE = -2,    /* workspace missing, misaligned or too small      */
+  MDS_EUNSUPPORTED = -3,  /* shape outside the limits above                  */
+  MDS_ECUDA = -4,         /* a CUDA runtime call or launch failed            */
+  MDS_EDEVICE = -5        /* the device latched a data error (status check)  */
+} mds_status;
+
+typedef enum { MDS_F32 = 0, MDS_BF16 = 1 } mds_dtype;
+
+/* Device error codes latched in the workspace status word. */
+enum {
+  MDS_DEV_TOKEN_RANGE = 1,  /* token id outside [0, V)                */
+  MDS_DEV_TREE_INDEX = 2,   /* parent/path index outside [0, N)      */
+  MDS_DEV_KV_CAPACITY = 3,  /* P_b + N > Pmax, or P_b < 0             */
+  MDS_DEV_PATH_LENGTH = 4,  /* L outside [0, K]                       */
+  MDS_DEV_TIMEOUT = 5       /* a bounded pipeline wait gave up        */
+};
+
+/* Library version (major*10000 + minor*100 + patch). */
+MDS_API int mds_version(void);
+
+/* Human-readable name of a mds_status value. */
+MDS_API const char* mds_status_string(int status);
+
+/* Number of tree rows N (root included) for shortlist sizes s[0..K-1]
+ * (host) keeping rank tuples whose zero-based ranks sum to at most
+ * max_rank_sum (-1 = no limit, the full tree).  Full tree:
+ * N = 1 + s1 + s1 s2 + ... ([SD2] "Medusa", tree-node count).
+ * Returns N >= 1, or a negative mds_status. */
+MDS_API int mds_tree_size(int K, const int32_t* shortlist, int max_rank_sum);
+
+/* Bytes of workspace one step with these shapes needs (covers every call
+ * below).  N = tree rows incl. root; smax = max shortlist size. */
+MDS_API size_t mds_workspace_size(int dtype, int B, int d, int V, int K, int N,
+                          int Hq, int Hkv, int dh, int smax);
+
+/* Build the fixed candidate tree ([DD] "From top-k heads to a sparse
+ * candidate tree": a fixed sparse tree laid out as a flat node sequence with
+ * an attention mask; [SD2] "Medusa": Anc(i)).
+ *   Nodes are the rank tuples (r_1..r_d), r_j < s_j, d = 0..K, kept when
+ *   sum(r) <= max_rank_sum; breadth-first order (by depth, then
+ *   lexicographic); node 0 = root = ().
+ *   shortlist  host  [K]
+ *   N_out      host  [1]      number of rows N
+ *   parent     device [Nmax]  parent index (-1 for the root)
+ *   depth      device [Nmax]  d (head that drafts the node; root 0)
+ *   rank       device [Nmax]  r_d (root 0)
+ *   mask       device [Nmax * words] uint64; bit j%64 of word j/64 of row i
+ *              is set iff node j is an ancestor of i, i itself or the root.
+ *   words      >= ceil(N/64).  Nmax >= N. */
+MDS_API int mds_build_tree_mask(int K, const int32_t* shortlist, int max_rank_sum, int Nmax,
+                        int32_t* N_out, int32_t* parent, int32_t* depth, int32_t* rank,
+                        uint64_t* mask, int words, void* stream);
+
+/* Medusa heads and the base LM head over one shared LM projection
+ * ([DD] "The heads are residual blocks, not linear layers":
+ *  head_i(h) = LMproj(h + SiLU(W_i h)); "What this deep dive assumes": the
+ *  base head owns t+1, head i owns t+i+1; "From top-k heads ...": keep the
+ *  top s_i tokens of head i).
+ *   h        device [B, d]           hidden state h_t
+ *   W        device [K, d, d]        W_i as (out, in)
+ *   lm       device [V, d]           LM projection (out, in)
+ *   shortlist host  [K]              s_i, 1 <= s_i <= smax <= 8
+ *   U        device [B, K+1, d]      out: row 0 = h, row i = h + SiLU(W_i h)
+ *   root     device [B] int32        out: argmax of the base head's logits
+ *   topk_id  device [B, K, smax]     out: head i's top s_i ids, logit
+ *                                    descending then id ascending; -1 pad
+ *   topk_val device [B, K, smax] f32 out: their logits; -inf pad
+ *   Argmax ties go to the lowest id. */
+MDS_API int mds_medusa_heads(int dtype, int B, int d, int V, int K, const void* h, const void* W,
+                     const void* lm, const int32_t* shortlist, int smax, void* U,
+                     int32_t* root, int32_t* topk_id, float* topk_val,
+                     void* ws, size_t ws_bytes, void* stream);
+
+/* One tree-attention verify layer ([GL] tree attention: every branch shares
+ * the prefix KV and all candidates are scored in one pass; [D89]: the mask
+ * lets each candidate attend to its own prefix).
+ *   Token fill (optional): when root != NULL, tok[b,0] = root[b] and
+ *   tok[b,n] = topk_id[b, depth[n]-1, rank[n]] are written first (tok is
+ *   then an output); when root == NULL, tok is an input.
+ *   x = Emb[tok]; q|k|v = x Wqkv^T; k, v of row n are written to cache slot
+ *   P_b + n; o = softmax(q k^T / sqrt(dh)) v over the prefix slots [0, P_b)
+ *   and the tree slots P_b + m with mask(n, m) set, query head j reading KV
+ *   head j / (Hq/Hkv); y = o Wo^T.  No residual, norm or position encoding.
+ *   P        device [B] int32        prefix lengths (read only)
+ *   tok      device [B, N] int32     in or out (see above)
+ *   root, topk_id, depth, rank      device, as produced above (or NULL)
+ *   mask     device [N * words]      from mds_build_tree_mask
+ *   emb      device [V, d]
+ *   wqkv     device [(Hq+2Hkv) dh, d]  q rows, then k rows, then v rows
+ *   wo       device [d, Hq dh]
+ *   Kc, Vc   device [B, Hkv, Pmax, dh] caches; slots P_b..P_b+N-1 overwritten
+ *   o_out    device [B, N, Hq dh] or NULL: attention output before Wo
+ *   y        device [B, N, d]        out */
+MDS_API int mds_tree_attention(int dtype, int B, int N, int d, int V, int Hq, int Hkv, int dh,
+                       int Pmax, int K, int smax, const int32_t* P, int32_t* tok,
+                       const int32_t* root, const int32_t* topk_id, const int32_t* depth,
+                       const int32_t* rank, const uint64_t* mask, int words,
+                       const void* emb, const void* wqkv, const void* wo,
+                       void* Kc, void* Vc, void* o_out, void* y,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/* Verify logits l = LMproj y for every tree row and the statistics the
+ * acceptance test needs ([DD] "Typical acceptance": entropy H of the model's
+ * distribution at the step; temperature 1, natural log).
+ *   y        device [B, N, d]
+ *   tok      device [B, N] int32, parent device [N] int32
+ *   argmax   device [B, N] int32    out: argmax_v l (lowest id on ties)
+ *   stats    device [B, N, 4] f32   out: m = max l, lse = ln sum e^l,
+ *                                   H = lse - sum(l e^l)/sum(e^l), 0
+ *   childlogit device [B, N] f32    out: entry c >= 1 = l_{parent(c)}[tok_c];
+ *                                   entry 0 = 0 */
+MDS_API int mds_lm_verify(int dtype, int B, int N, int d, int V, const void* y, const void* lm,
+                  const int32_t* tok, const int32_t* parent, int32_t* argmax, float* stats,
+                  float* childlogit, void* ws, size_t ws_bytes, void* stream);
+
+/* Acceptance and the longest accepted path ([GL] verification pass: early
+ * stop at the first rejection, rollback to the last accepted position, the
+ * next token comes from the base model; [GU] "Deep Dive": accept the longest
+ * prefix that matches; [DD] "Typical acceptance": accept when
+ * p > min(eps, delta exp(-H))).
+ *   mode 0 = greedy: child c passes iff tok_c == argmax of its parent row.
+ *   mode 1 = typical: passes iff l_parent[tok_c] - lse_parent >
+ *            min(ln eps, ln delta - H_parent)  (eps, delta >= 0).
+ *   The accepted node is the deepest node whose every edge passes, ties to
+ *   the lowest breadth-first index.
+ *   ok       device [B, N] uint8 or NULL   out: per-edge result (root = 1)
+ *   L        device [B] int32               out: accepted depth
+ *   path     device [B, K+1] int32          out: node indices root..accepted,
+ *                                           -1 after position L
+ *   next_root device [B] int32              out: argmax at the accepted node */
+MDS_API int mds_verify_accept(int B, int N, int K, int mode, float eps, float delta,
+                      const int32_t* parent, const int32_t* depth, const int32_t* tok,
+                      const int32_t* argmax, const float* stats, const float* childlogit,
+                      uint8_t* ok, int32_t* L, int32_t* path, int32_t* next_root,
+                      void* ws, size_t ws_bytes, void* stream);
+
+/* Commit the accepted path's tree KV ([GL] "Speculative KV Cache"; rollback
+ * to the last accepted position): for j = 0..L, cache slot P_b + path[j]
+ * moves to P_b + j (K and V, every KV head); then P_b += L + 1.  Sources
+ * are read before any slot is written, so overlapping moves are safe.
+ *   Kc, Vc   device [B, Hkv, Pmax, dh]   updated in place
+ *   P        device [B] int32             updated in place */
+MDS_API int mds_compact_kv(int dtype, int B, int Hkv, int dh, int Pmax, int K, const int32_t* L,
+                   const int32_t* path, void* Kc, void* Vc, int32_t* P,
+                   void* ws, size_t ws_bytes, void* stream);
+
+/* Number of kernels this library has enqueued since it was loaded (a host
+ * counter; launches captured into a CUDA graph count once, at capture). */
+MDS_API long long mds_launch_count(void);
+
+/* Wait for `stream`, read and clear the workspace status word.
+ * *device_status_out receives the latched MDS_DEV_* code (0 = none).
+ * Returns MDS_OK, MDS_EDEVICE when a code was latched, or an error. */
+MDS_API int mds_status_check(void* ws, int32_t* device_status_out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MEDUSA_B300_H */

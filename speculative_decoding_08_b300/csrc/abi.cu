@@ -1,0 +1,260 @@
+// C ABI entry points: host-side argument checks, workspace carving, and
+// dispatch to the kernels.  Every data-path operation runs in a kernel.
+#include <atomic>
+#include <string.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+using namespace mds;
+
+namespace mds {
+static std::atomic<long long> g_launches{0};
+void count_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+}  // namespace mds
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+inline bool valid_dtype(int dtype) { return dtype == MDS_F32 || dtype == MDS_BF16; }
+inline size_t esize(int dtype) { return dtype == MDS_F32 ? 4 : 2; }
+inline cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+// Node count of the tree, counted exactly as the build kernel enumerates it.
+int count_tree(int K, const int32_t* s, int max_rank_sum) {
+  int sums[kMaxN * kMaxS];
+  int lo = 0, hi = 1, cnt = 1;
+  sums[0] = 0;
+  for (int d = 1; d <= K; ++d) {
+    for (int p = lo; p < hi; ++p)
+      for (int r = 0; r < s[d - 1]; ++r) {
+        const int sum = sums[p] + r;
+        if (max_rank_sum >= 0 && sum > max_rank_sum) continue;
+        if (cnt >= kMaxN) return kMaxN + 1;
+        sums[cnt++] = sum;
+      }
+    lo = hi;
+    hi = cnt;
+  }
+  return cnt;
+}
+
+bool ws_ok(void* ws, size_t ws_bytes, size_t need) {
+  return ws && (reinterpret_cast<uintptr_t>(ws) % kAlign) == 0 && ws_bytes >= need;
+}
+
+char* scratch(void* ws) { return static_cast<char*>(ws) + kWsScratch; }
+
+bool shape_ok(int d, int dh) { return d > 0 && d % 64 == 0 && (dh == 64 || dh == 128); }
+
+size_t need_heads(int dtype, int B, int d, int V, int K) {
+  (void)dtype; (void)d;
+  return kWsScratch + align_up((size_t)B * (K + 1) * V * 4);
+}
+size_t need_attention(int dtype, int B, int N, int d, int Hq) {
+  const size_t rows = (size_t)B * N;
+  return kWsScratch + align_up(rows * d * esize(dtype)) + 2 * align_up(rows * Hq * 128 * esize(dtype));
+}
+size_t need_verify(int B, int N, int V) {
+  return kWsScratch + align_up((size_t)B * N * V * 4);
+}
+
+}  // namespace
+
+extern "C" {
+
+int mds_version(void) { return 100; }
+
+const char* mds_status_string(int status) {
+  switch (status) {
+    case MDS_OK: return "ok";
+    case MDS_EINVAL: return "invalid argument";
+    case MDS_EWORKSPACE: return "workspace missing, misaligned or too small";
+    case MDS_EUNSUPPORTED: return "unsupported shape";
+    case MDS_ECUDA: return "CUDA error";
+    case MDS_EDEVICE: return "device latched a data error";
+    default: return "unknown status";
+  }
+}
+
+int mds_tree_size(int K, const int32_t* shortlist, int max_rank_sum) {
+  if (!shortlist || K < 1) return MDS_EINVAL;
+  if (K > kMaxK) return MDS_EUNSUPPORTED;
+  for (int i = 0; i < K; ++i) {
+    if (shortlist[i] < 1) return MDS_EINVAL;
+    if (shortlist[i] > kMaxS) return MDS_EUNSUPPORTED;
+  }
+  const int n = count_tree(K, shortlist, max_rank_sum);
+  return n > kMaxN ? MDS_EUNSUPPORTED : n;
+}
+
+size_t mds_workspace_size(int dtype, int B, int d, int V, int K, int N, int Hq, int Hkv,
+                          int dh, int smax) {
+  (void)Hkv; (void)dh; (void)smax;
+  if (!valid_dtype(dtype) || B < 1 || d < 1 || V < 1 || K < 1 || N < 1 || Hq < 1) return 0;
+  size_t need = need_heads(dtype, B, d, V, K);
+  const size_t a = need_attention(dtype, B, N, d, Hq);
+  const size_t v = need_verify(B, N, V);
+  if (a > need) need = a;
+  if (v > need) need = v;
+  return need;
+}
+
+int mds_build_tree_mask(int K, const int32_t* shortlist, int max_rank_sum, int Nmax,
+                        int32_t* N_out, int32_t* parent, int32_t* depth, int32_t* rank,
+                        uint64_t* mask, int words, void* stream) {
+  if (!N_out || !parent || !depth || !rank || !mask) return MDS_EINVAL;
+  const int N = mds_tree_size(K, shortlist, max_rank_sum);
+  if (N < 0) return N;
+  if (Nmax < N || words < (N + 63) / 64) return MDS_EINVAL;
+  Shortlist sl{};
+  sl.K = K;
+  for (int i = 0; i < K; ++i) sl.s[i] = shortlist[i];
+  *N_out = N;
+  return build_tree(sl, max_rank_sum, N, parent, depth, rank, mask, words, as_stream(stream));
+}
+
+int mds_medusa_heads(int dtype, int B, int d, int V, int K, const void* h, const void* W,
+                     const void* lm, const int32_t* shortlist, int smax, void* U,
+                     int32_t* root, int32_t* topk_id, float* topk_val, void* ws,
+                     size_t ws_bytes, void* stream) {
+  if (!valid_dtype(dtype) || !h || !W || !lm || !shortlist || !U || !root || !topk_id ||
+      !topk_val)
+    return MDS_EINVAL;
+  if (B < 1 || V < 2 || K < 1 || smax < 1) return MDS_EINVAL;
+  if (K > kMaxK || smax > kMaxS || d % 64 != 0 || d <= 0) return MDS_EUNSUPPORTED;
+  Shortlist sl{};
+  sl.K = K;
+  for (int i = 0; i < K; ++i) {
+    if (shortlist[i] < 1 || shortlist[i] > smax || shortlist[i] > V) return MDS_EINVAL;
+    sl.s[i] = shortlist[i];
+  }
+  if (!ws_ok(ws, ws_bytes, need_heads(dtype, B, d, V, K))) return MDS_EWORKSPACE;
+  cudaStream_t st = as_stream(stream);
+  EpiArgs e;
+  e.kind = EPI_HEADS;
+  e.out = U;
+  e.h = h;
+  e.d = d;
+  e.K = K;
+  int rc = gemm_simple(dtype, h, B, W, K * d, d, e, st);
+  if (rc) return rc;
+  float* logits = reinterpret_cast<float*>(scratch(ws));
+  EpiArgs el;
+  el.kind = EPI_LOGITS;
+  el.out = logits;
+  el.ldo = V;
+  rc = gemm_simple(dtype, U, B * (K + 1), lm, V, d, el, st);
+  if (rc) return rc;
+  return draft_select(logits, B, K, V, sl, smax, root, topk_id, topk_val, st);
+}
+
+int mds_tree_attention(int dtype, int B, int N, int d, int V, int Hq, int Hkv, int dh,
+                       int Pmax, int K, int smax, const int32_t* P, int32_t* tok,
+                       const int32_t* root, const int32_t* topk_id, const int32_t* depth,
+                       const int32_t* rank, const uint64_t* mask, int words,
+                       const void* emb, const void* wqkv, const void* wo, void* Kc, void* Vc,
+                       void* o_out, void* y, void* ws, size_t ws_bytes, void* stream) {
+  if (!valid_dtype(dtype) || !P || !tok || !mask || !emb || !wqkv || !wo || !Kc || !Vc || !y)
+    return MDS_EINVAL;
+  if (root && (!topk_id || !depth || !rank)) return MDS_EINVAL;
+  if (B < 1 || N < 1 || V < 1 || Hq < 1 || Hkv < 1 || Pmax < N || K < 1 || smax < 1)
+    return MDS_EINVAL;
+  if (Hq % Hkv != 0) return MDS_EINVAL;
+  if (N > kMaxN || K > kMaxK || smax > kMaxS || !shape_ok(d, dh)) return MDS_EUNSUPPORTED;
+  if (words < (N + 63) / 64) return MDS_EINVAL;
+  if (!ws_ok(ws, ws_bytes, need_attention(dtype, B, N, d, Hq))) return MDS_EWORKSPACE;
+  cudaStream_t st = as_stream(stream);
+  const size_t rows = (size_t)B * N;
+  char* base = scratch(ws);
+  void* x = base;
+  void* q = base + align_up(rows * d * esize(dtype));
+  void* o = o_out ? o_out : static_cast<void*>(static_cast<char*>(q) + align_up(rows * Hq * 128 * esize(dtype)));
+  int rc = embed_gather(dtype, B, N, d, V, K, smax, tok, root, topk_id, depth, rank, emb, x,
+                        ws, st);
+  if (rc) return rc;
+  EpiArgs e;
+  e.kind = EPI_QKV;
+  e.out = q;
+  e.N = N;
+  e.Hq = Hq;
+  e.Hkv = Hkv;
+  e.dh = dh;
+  e.Pmax = Pmax;
+  e.P = P;
+  e.Kc = Kc;
+  e.Vc = Vc;
+  e.ws = ws;
+  rc = gemm_simple(dtype, x, (int)rows, wqkv, (Hq + 2 * Hkv) * dh, d, e, st);
+  if (rc) return rc;
+  rc = attention_simple(dtype, B, N, Hq, Hkv, dh, Pmax, P, mask, words, q, Kc, Vc, o, ws, st);
+  if (rc) return rc;
+  EpiArgs eo;
+  eo.kind = EPI_STORE;
+  eo.out = y;
+  eo.ldo = d;
+  return gemm_simple(dtype, o, (int)rows, wo, d, Hq * dh, eo, st);
+}
+
+int mds_lm_verify(int dtype, int B, int N, int d, int V, const void* y, const void* lm,
+                  const int32_t* tok, const int32_t* parent, int32_t* argmax, float* stats,
+                  float* childlogit, void* ws, size_t ws_bytes, void* stream) {
+  if (!valid_dtype(dtype) || !y || !lm || !tok || !parent || !argmax || !stats || !childlogit)
+    return MDS_EINVAL;
+  if (B < 1 || N < 1 || V < 2) return MDS_EINVAL;
+  if (N > kMaxN || d % 64 != 0 || d <= 0) return MDS_EUNSUPPORTED;
+  if (!ws_ok(ws, ws_bytes, need_verify(B, N, V))) return MDS_EWORKSPACE;
+  cudaStream_t st = as_stream(stream);
+  float* logits = reinterpret_cast<float*>(scratch(ws));
+  EpiArgs el;
+  el.kind = EPI_LOGITS;
+  el.out = logits;
+  el.ldo = V;
+  int rc = gemm_simple(dtype, y, B * N, lm, V, d, el, st);
+  if (rc) return rc;
+  return verify_reduce(logits, B, N, V, tok, parent, argmax, stats, childlogit, ws, st);
+}
+
+int mds_verify_accept(int B, int N, int K, int mode, float eps, float delta,
+                      const int32_t* parent, const int32_t* depth, const int32_t* tok,
+                      const int32_t* argmax, const float* stats, const float* childlogit,
+                      uint8_t* ok, int32_t* L, int32_t* path, int32_t* next_root, void* ws,
+                      size_t ws_bytes, void* stream) {
+  if (!parent || !depth || !tok || !argmax || !L || !path || !next_root) return MDS_EINVAL;
+  if (mode != 0 && mode != 1) return MDS_EINVAL;
+  if (mode == 1 && (!stats || !childlogit || !(eps >= 0.f) || !(delta >= 0.f)))
+    return MDS_EINVAL;
+  if (B < 1 || N < 1 || K < 1) return MDS_EINVAL;
+  if (N > kMaxN || K > kMaxK) return MDS_EUNSUPPORTED;
+  if (!ws_ok(ws, ws_bytes, kWsScratch)) return MDS_EWORKSPACE;
+  return accept_path(B, N, K, mode, eps, delta, parent, depth, tok, argmax, stats, childlogit,
+                     ok, L, path, next_root, ws, as_stream(stream));
+}
+
+int mds_compact_kv(int dtype, int B, int Hkv, int dh, int Pmax, int K, const int32_t* L,
+                   const int32_t* path, void* Kc, void* Vc, int32_t* P, void* ws,
+                   size_t ws_bytes, void* stream) {
+  if (!valid_dtype(dtype) || !L || !path || !Kc || !Vc || !P) return MDS_EINVAL;
+  if (B < 1 || Hkv < 1 || Pmax < 1 || K < 1) return MDS_EINVAL;
+  if (B > 1024 || K > kMaxK || !(dh == 64 || dh == 128)) return MDS_EUNSUPPORTED;
+  if (!ws_ok(ws, ws_bytes, kWsScratch)) return MDS_EWORKSPACE;
+  return compact(dtype, B, Hkv, dh, Pmax, K, L, path, Kc, Vc, P, ws, as_stream(stream));
+}
+
+long long mds_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int mds_status_check(void* ws, int32_t* device_status_out, void* stream) {
+  if (!ws || !device_status_out) return MDS_EINVAL;
+  cudaStream_t st = as_stream(stream);
+  int32_t v = 0;
+  MDS_CUDA_TRY(cudaMemcpyAsync(&v, static_cast<char*>(ws) + kWsStatus, 4, cudaMemcpyDeviceToHost, st));
+  MDS_CUDA_TRY(cudaStreamSynchronize(st));
+  MDS_CUDA_TRY(cudaMemsetAsync(static_cast<char*>(ws) + kWsStatus, 0, 4, st));
+  MDS_CUDA_TRY(cudaStreamSynchronize(st));
+  *device_status_out = v;
+  return v ? MDS_EDEVICE : MDS_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,183 @@
+// Acceptance, the longest accepted path, and KV compaction.
+//
+// "Medusa Heads", verification pass: a drafted token is accepted when it
+// clears the test; verification stops at the first rejection, rolls back to
+// the last accepted position, and the base model supplies the next token.
+// "Medusa Decoding Heads", "Deep Dive": accept the longest prefix that
+// matches what the model would have produced.  "Medusa deep dive",
+// "Typical acceptance, not exact rejection sampling": accept when the
+// model's probability clears min(eps, delta * exp(-H)).
+#include "common.cuh"
+#include "internal.h"
+
+namespace mds {
+namespace {
+
+// One warp per sequence.  Nodes are in breadth-first order, so a node's
+// parent always has a smaller index and a smaller depth.
+__global__ void __launch_bounds__(32) k_accept(int N, int K, int mode, float log_eps,
+                                               float log_delta, const int32_t* parent,
+                                               const int32_t* depth, const int32_t* tok,
+                                               const int32_t* argmax, const float* stats,
+                                               const float* childlogit, uint8_t* ok_out,
+                                               int32_t* L, int32_t* path, int32_t* next_root,
+                                               void* ws) {
+  __shared__ uint8_t s_ok[kMaxN], s_reach[kMaxN];
+  __shared__ int s_parent[kMaxN], s_depth[kMaxN];
+  const int b = blockIdx.x, lane = threadIdx.x;
+  const long long base = (long long)b * N;
+  bool bad = false;
+  for (int n = lane; n < N; n += 32) {
+    const int pa = parent[n];
+    const int dd = depth[n];
+    s_parent[n] = pa;
+    s_depth[n] = dd;
+    uint8_t okv = 1;
+    if (n > 0) {
+      if (pa < 0 || pa >= n || dd < 1 || dd > K) {
+        bad = true;
+        okv = 0;
+      } else if (mode == 0) {
+        okv = tok[base + n] == argmax[base + pa];
+      } else {
+        const float lse = stats[(base + pa) * 4 + 1];
+        const float H = stats[(base + pa) * 4 + 2];
+        const float lp = childlogit[base + n] - lse;
+        okv = lp > fminf(log_eps, log_delta - H);
+      }
+    }
+    s_ok[n] = okv;
+    s_reach[n] = n == 0;
+    if (ok_out) ok_out[base + n] = okv;
+  }
+  if (__any_sync(0xffffffffu, bad)) {
+    if (lane == 0) latch_error(ws, MDS_DEV_TREE_INDEX);
+  }
+  __syncwarp();
+  // reachability, one depth level at a time
+  for (int d = 1; d <= K; ++d) {
+    for (int n = lane; n < N; n += 32)
+      if (n > 0 && s_depth[n] == d) {
+        const int pa = s_parent[n];
+        s_reach[n] = (pa >= 0 && pa < n) ? (s_reach[pa] & s_ok[n]) : 0;
+      }
+    __syncwarp();
+  }
+  // deepest reachable node, lowest index on ties: key = depth * 256 + (255 - n)
+  unsigned key = 0;
+  for (int n = lane; n < N; n += 32)
+    if (s_reach[n]) {
+      const unsigned k = ((unsigned)s_depth[n] << 8) | (unsigned)(255 - n);
+      key = key > k ? key : k;
+    }
+  key = __reduce_max_sync(0xffffffffu, key);
+  const int best = 255 - (int)(key & 255u);
+  const int Lb = (int)(key >> 8);
+  // path: lane j <= L holds the depth-j ancestor of best
+  int a = best;
+  for (int j = Lb; j > lane; --j) a = s_parent[a];
+  if (lane <= K) path[(long long)b * (K + 1) + lane] = lane <= Lb ? a : -1;
+  if (lane == 0) {
+    L[b] = Lb;
+    next_root[b] = argmax[base + best];
+  }
+}
+
+// One block per (KV head, sequence).  All L+1 source slots are read into
+// shared memory before any is written, so moves that overlap are safe
+// (path[j] >= j, but path[j'] can equal some j < j').  The last block of a
+// sequence to finish advances P_b.
+template <typename T>
+__global__ void __launch_bounds__(128) k_compact(int Hkv, int dh, int Pmax, int K,
+                                                 const int32_t* L, const int32_t* path,
+                                                 T* __restrict__ Kc, T* __restrict__ Vc,
+                                                 int32_t* P, void* ws) {
+  extern __shared__ unsigned char smem_raw[];
+  T* sk = reinterpret_cast<T*>(smem_raw);
+  T* sv = sk + (K + 1) * dh;
+  const int hk = blockIdx.x, b = blockIdx.y;
+  __shared__ int s_ok, s_src[kMaxK + 1];
+  const int Lb = L[b];
+  const int Pb = P[b];
+  if (threadIdx.x == 0) {
+    int okv = 1;
+    if (Lb < 0 || Lb > K) {
+      okv = 0;
+      if (hk == 0) latch_error(ws, MDS_DEV_PATH_LENGTH);
+    } else if (Pb < 0) {
+      okv = 0;
+      if (hk == 0) latch_error(ws, MDS_DEV_KV_CAPACITY);
+    } else {
+      for (int j = 0; j <= Lb; ++j) {
+        const int p = path[(long long)b * (K + 1) + j];
+        if (p < j || Pb + p >= Pmax) {
+          okv = 0;
+          if (hk == 0) latch_error(ws, MDS_DEV_TREE_INDEX);
+          break;
+        }
+        s_src[j] = p;
+      }
+    }
+    s_ok = okv;
+  }
+  __syncthreads();
+  const int okv = s_ok;
+  const long long head = ((long long)b * Hkv + hk) * Pmax;
+  if (okv) {
+    for (int i = threadIdx.x; i < (Lb + 1) * dh; i += blockDim.x) {
+      const int j = i / dh, c = i % dh;
+      const long long src = (head + Pb + s_src[j]) * dh + c;
+      sk[i] = Kc[src];
+      sv[i] = Vc[src];
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < (Lb + 1) * dh; i += blockDim.x) {
+      const int j = i / dh, c = i % dh;
+      const long long dst = (head + Pb + j) * dh + c;
+      Kc[dst] = sk[i];
+      Vc[dst] = sv[i];
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    int* cnt = ws_counters(ws) + b;
+    const int prev = atomicAdd(cnt, 1);
+    if (prev == Hkv - 1) {
+      if (okv) P[b] = Pb + Lb + 1;
+      *cnt = 0;
+    }
+  }
+}
+
+}  // namespace
+
+int accept_path(int B, int N, int K, int mode, float eps, float delta, const int32_t* parent,
+                const int32_t* depth, const int32_t* tok, const int32_t* argmax,
+                const float* stats, const float* childlogit, uint8_t* ok, int32_t* L,
+                int32_t* path, int32_t* next_root, void* ws, cudaStream_t st) {
+  const float log_eps = logf(eps), log_delta = logf(delta);
+  k_accept<<<B, 32, 0, st>>>(N, K, mode, log_eps, log_delta, parent, depth, tok, argmax,
+                             stats, childlogit, ok, L, path, next_root, ws);
+  MDS_LAUNCH_CHECK();
+  return MDS_OK;
+}
+
+int compact(int dtype, int B, int Hkv, int dh, int Pmax, int K, const int32_t* L,
+            const int32_t* path, void* Kc, void* Vc, int32_t* P, void* ws, cudaStream_t st) {
+  dim3 grid(Hkv, B);
+  const size_t esz = dtype == MDS_F32 ? 4 : 2;
+  const size_t smem = 2 * (size_t)(K + 1) * dh * esz;
+  if (dtype == MDS_F32)
+    k_compact<float><<<grid, 128, smem, st>>>(Hkv, dh, Pmax, K, L, path,
+                                              static_cast<float*>(Kc), static_cast<float*>(Vc),
+                                              P, ws);
+  else
+    k_compact<__nv_bfloat16><<<grid, 128, smem, st>>>(
+        Hkv, dh, Pmax, K, L, path, static_cast<__nv_bfloat16*>(Kc),
+        static_cast<__nv_bfloat16*>(Vc), P, ws);
+  MDS_LAUNCH_CHECK();
+  return MDS_OK;
+}
+
+}  // namespace mds

@@ -1,0 +1,66 @@
+// Shared device helpers of the Medusa step library (internal).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/medusa.h"
+
+namespace mds {
+
+// Workspace layout (bytes from the workspace base; the base is 256-aligned):
+//   [0, 4)        latched device status word (int32)
+//   [256, 4352)   per-sequence counters used by "last block finishes" merges
+//   [8192, ...)   scratch regions, each 256-aligned, owned by one call
+constexpr size_t kWsStatus = 0;
+constexpr size_t kWsCounters = 256;
+constexpr size_t kWsScratch = 8192;
+constexpr int kMaxN = 128;
+constexpr int kMaxK = 8;
+constexpr int kMaxS = 8;
+
+__device__ __forceinline__ void latch_error(void* ws, int code) {
+  if (ws) atomicCAS(reinterpret_cast<int*>(static_cast<char*>(ws) + kWsStatus), 0, code);
+}
+
+__device__ __forceinline__ int* ws_counters(void* ws) {
+  return reinterpret_cast<int*>(static_cast<char*>(ws) + kWsCounters);
+}
+
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+  static __device__ __forceinline__ float load(const float* p) { return *p; }
+  static __device__ __forceinline__ void store(float* p, float v) { *p = v; }
+};
+template <> struct Elem<__nv_bfloat16> {
+  static __device__ __forceinline__ float load(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+  static __device__ __forceinline__ void store(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+};
+
+template <typename T> __device__ __forceinline__ float ld(const T* p) { return Elem<T>::load(p); }
+template <typename T> __device__ __forceinline__ void st(T* p, float v) { Elem<T>::store(p, v); }
+
+__device__ __forceinline__ float silu(float a) { return a / (1.0f + expf(-a)); }
+
+// (value desc, id asc) order: true when (va, ia) comes before (vb, ib).
+__device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+// Host-side count of enqueued kernels (see mds_launch_count).
+void count_launch(int n = 1);
+
+}  // namespace mds
+
+#define MDS_CUDA_TRY(expr)                      \
+  do {                                          \
+    cudaError_t _e = (expr);                    \
+    if (_e != cudaSuccess) return MDS_ECUDA;    \
+  } while (0)
+
+#define MDS_LAUNCH_CHECK()                                   \
+  do {                                                       \
+    if (cudaGetLastError() != cudaSuccess) return MDS_ECUDA; \
+    ::mds::count_launch();                                   \
+  } while (0)

@@ -1,0 +1,71 @@
+// Internal launchers of the Medusa step library (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace mds {
+
+// Epilogues of the projection GEMMs  Y[r, f] = sum_k X[r, k] W[f, k].
+enum EpiKind {
+  EPI_STORE = 0,      // out[r * ldo + f] = Y (element type of the GEMM)
+  EPI_HEADS = 1,      // U[b, 1 + f / d, f % d] = h[b, f % d] + SiLU(Y); row 0 = h
+  EPI_QKV = 2,        // q rows -> q buffer; k, v rows -> cache slot P_b + n
+  EPI_LOGITS = 3      // float out[r * ldo + f] = Y
+};
+
+struct EpiArgs {
+  int kind = EPI_STORE;
+  void* out = nullptr;
+  long long ldo = 0;
+  // EPI_HEADS
+  const void* h = nullptr;
+  int d = 0, K = 0;
+  // EPI_QKV
+  int N = 0, Hq = 0, Hkv = 0, dh = 0, Pmax = 0;
+  const int32_t* P = nullptr;
+  void* Kc = nullptr;
+  void* Vc = nullptr;
+  void* ws = nullptr;
+};
+
+struct Shortlist {
+  int K;
+  int s[8];
+};
+
+// Simple CUDA-core GEMM (fp32 accumulation), any shape.  T = float or bf16.
+int gemm_simple(int dtype, const void* X, int R, const void* W, int F, int Kd,
+                const EpiArgs& e, cudaStream_t st);
+
+// Row reductions over materialised fp32 logits [rows, V].
+int draft_select(const float* logits, int B, int K, int V, Shortlist sl, int smax,
+                 int32_t* root, int32_t* topk_id, float* topk_val, cudaStream_t st);
+int verify_reduce(const float* logits, int B, int N, int V, const int32_t* tok,
+                  const int32_t* parent, int32_t* argmax, float* stats, float* childlogit,
+                  void* ws, cudaStream_t st);
+
+// Tree kernels.
+int build_tree(Shortlist sl, int max_rank_sum, int N, int32_t* parent, int32_t* depth,
+               int32_t* rank, uint64_t* mask, int words, cudaStream_t st);
+
+// Embedding gather with optional token fill.
+int embed_gather(int dtype, int B, int N, int d, int V, int K, int smax, int32_t* tok,
+                 const int32_t* root, const int32_t* topk_id, const int32_t* depth,
+                 const int32_t* rank, const void* emb, void* x, void* ws, cudaStream_t st);
+
+// Attention over prefix + masked tree rows (CUDA cores, one warp per query row).
+int attention_simple(int dtype, int B, int N, int Hq, int Hkv, int dh, int Pmax,
+                     const int32_t* P, const uint64_t* mask, int words, const void* q,
+                     const void* Kc, const void* Vc, void* o, void* ws, cudaStream_t st);
+
+int accept_path(int B, int N, int K, int mode, float eps, float delta, const int32_t* parent,
+                const int32_t* depth, const int32_t* tok, const int32_t* argmax,
+                const float* stats, const float* childlogit, uint8_t* ok, int32_t* L,
+                int32_t* path, int32_t* next_root, void* ws, cudaStream_t st);
+
+int compact(int dtype, int B, int Hkv, int dh, int Pmax, int K, const int32_t* L,
+            const int32_t* path, void* Kc, void* Vc, int32_t* P, void* ws, cudaStream_t st);
+
+}  // namespace mds

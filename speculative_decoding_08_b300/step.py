@@ -1,0 +1,78 @@
+"""One Medusa draft-and-verify step as a sequence of C-ABI calls.
+
+``MedusaStep`` owns the device buffers of one step for fixed shapes and
+issues, in order: medusa_heads -> tree_attention (with the token fill) ->
+lm_verify -> verify_accept -> compact_kv.  The tree is built once at
+construction ("Medusa deep dive": the tree is chosen ahead of time).
+"""
+from __future__ import annotations
+
+from typing import Dict, Optional, Sequence
+
+import torch
+
+from . import (BF16, F32, GREEDY, TYPICAL, build_tree_mask, compact_kv, dtype_code, lm_verify,
+               medusa_heads, new_workspace, tree_attention, tree_size, verify_accept,
+               workspace_size)
+
+
+class MedusaStep:
+    def __init__(self, *, W: torch.Tensor, lm: torch.Tensor, emb: torch.Tensor,
+                 wqkv: torch.Tensor, wo: torch.Tensor, Kc: torch.Tensor, Vc: torch.Tensor,
+                 P: torch.Tensor, shortlist: Sequence[int], max_rank_sum: int, Hq: int,
+                 Hkv: int, B: int):
+        dev = lm.device
+        self.W, self.lm, self.emb, self.wqkv, self.wo = W, lm, emb, wqkv, wo
+        self.Kc, self.Vc, self.P = Kc, Vc, P
+        self.shortlist = tuple(int(s) for s in shortlist)
+        self.max_rank_sum = int(max_rank_sum)
+        self.K = len(self.shortlist)
+        self.smax = max(self.shortlist)
+        self.Hq, self.Hkv = Hq, Hkv
+        self.B = B
+        self.d = lm.shape[1]
+        self.V = lm.shape[0]
+        self.dh = Kc.shape[3]
+        self.dtype = lm.dtype
+        self.N = tree_size(self.shortlist, self.max_rank_sum)
+        N, K, i32 = self.N, self.K, torch.int32
+        words = (N + 63) // 64
+        self.parent = torch.empty(N, dtype=i32, device=dev)
+        self.depth = torch.empty(N, dtype=i32, device=dev)
+        self.rank = torch.empty(N, dtype=i32, device=dev)
+        self.mask = torch.empty((N, words), dtype=torch.int64, device=dev)
+        build_tree_mask(self.shortlist, self.max_rank_sum, self.parent, self.depth, self.rank,
+                        self.mask)
+        self.U = torch.empty((B, K + 1, self.d), dtype=self.dtype, device=dev)
+        self.root = torch.empty(B, dtype=i32, device=dev)
+        self.topk_id = torch.empty((B, K, self.smax), dtype=i32, device=dev)
+        self.topk_val = torch.empty((B, K, self.smax), dtype=torch.float32, device=dev)
+        self.tok = torch.empty((B, N), dtype=i32, device=dev)
+        self.y = torch.empty((B, N, self.d), dtype=self.dtype, device=dev)
+        self.argmax = torch.empty((B, N), dtype=i32, device=dev)
+        self.stats = torch.empty((B, N, 4), dtype=torch.float32, device=dev)
+        self.childlogit = torch.empty((B, N), dtype=torch.float32, device=dev)
+        self.ok = torch.empty((B, N), dtype=torch.uint8, device=dev)
+        self.L = torch.empty(B, dtype=i32, device=dev)
+        self.path = torch.empty((B, K + 1), dtype=i32, device=dev)
+        self.next_root = torch.empty(B, dtype=i32, device=dev)
+        nbytes = workspace_size(dtype_code(lm), B, self.d, self.V, K, N, Hq, Hkv, self.dh,
+                                self.smax)
+        self.ws = new_workspace(nbytes, dev)
+
+    def run(self, h: torch.Tensor, mode: int = TYPICAL, eps: float = 0.09,
+            delta: float = 0.3, commit: bool = True) -> None:
+        """Enqueue one step on the current stream (asynchronous)."""
+        medusa_heads(h, self.W, self.lm, self.shortlist, self.smax, self.U, self.root,
+                     self.topk_id, self.topk_val, self.ws)
+        tree_attention(self.P, self.tok, self.mask, self.emb, self.wqkv, self.wo, self.Kc,
+                       self.Vc, self.y, self.ws, Hq=self.Hq, Hkv=self.Hkv, K=self.K,
+                       smax=self.smax, root=self.root, topk_id=self.topk_id, depth=self.depth,
+                       rank=self.rank)
+        lm_verify(self.y, self.lm, self.tok, self.parent, self.argmax, self.stats,
+                  self.childlogit, self.ws)
+        verify_accept(mode, eps, delta, self.parent, self.depth, self.tok, self.argmax,
+                      self.stats, self.childlogit, self.L, self.path, self.next_root, self.ws,
+                      ok=self.ok)
+        if commit:
+            compact_kv(self.L, self.path, self.Kc, self.Vc, self.P, self.ws)

@@ -1,0 +1,128 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every symbol include/medusa.h declares, and its host logic (tree sizing,
+argument validation, workspace sizing) behaves.  No call here reaches the
+device: every call either is host-only or fails validation first."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import medusa_synth as ms
+import oracle
+import speculative_decoding_08_b300 as mds
+from speculative_decoding_08_b300 import build as mbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mbuild.build()
+    return mds.load()
+
+
+def header_symbols():
+    with open(os.path.join(ROOT, "include", "medusa.h")) as f:
+        text = f.read()
+    return re.findall(r"MDS_API\s+[\w\s\*]+?\b(mds_\w+)\s*\(", text)
+
+
+def test_exports_every_declared_symbol(lib):
+    syms = header_symbols()
+    assert len(syms) >= 11
+    for s in syms:
+        assert hasattr(lib, s), s
+    assert set(syms) == set(mds.EXPORTS)
+
+
+def test_version_and_strings(lib):
+    assert lib.mds_version() >= 100
+    for code in (0, -1, -2, -3, -4, -5):
+        assert lib.mds_status_string(code)
+
+
+@pytest.mark.parametrize("sl,mrs", [((2, 2, 2), -1), ((4, 3, 2, 2), -1), ((8, 4, 2, 2, 1), 3),
+                                    ((3,), -1), ((5, 1, 3), 2), ((2, 2, 2, 2), 0)])
+def test_tree_size_matches_oracle(lib, sl, mrs):
+    assert mds.tree_size(sl, mrs) == oracle.build_tree(sl, mrs)["N"]
+
+
+def test_tree_size_limits(lib):
+    arr = (ctypes.c_int32 * 3)(2, 2, 2)
+    assert lib.mds_tree_size(0, arr, -1) == -1
+    assert lib.mds_tree_size(3, None, -1) == -1
+    big = (ctypes.c_int32 * 4)(8, 8, 8, 8)
+    assert lib.mds_tree_size(4, big, -1) == -3          # > 128 rows
+    bad = (ctypes.c_int32 * 2)(9, 1)
+    assert lib.mds_tree_size(2, bad, -1) == -3          # s > 8
+
+
+def test_workspace_size_monotone(lib):
+    a = mds.workspace_size(1, 1, 4096, 32000, 4, 89, 32, 32, 128, 4)
+    b = mds.workspace_size(1, 16, 4096, 32000, 4, 89, 32, 32, 128, 4)
+    assert 0 < a < b
+    assert mds.workspace_size(7, 1, 64, 10, 1, 2, 1, 1, 64, 1) == 0
+
+
+def test_host_validation_rejects_before_launch(lib):
+    null = None
+    sl = (ctypes.c_int32 * 2)(2, 2)
+    # null pointers
+    assert lib.mds_medusa_heads(1, 1, 64, 100, 2, null, null, null, sl, 2, null, null, null,
+                                null, null, 0, null) == -1
+    # d not a multiple of 64
+    fake = ctypes.c_void_p(256)
+    assert lib.mds_medusa_heads(1, 1, 65, 100, 2, fake, fake, fake, sl, 2, fake, fake, fake,
+                                fake, fake, 1 << 30, null) == -3
+    # workspace too small
+    assert lib.mds_medusa_heads(1, 1, 64, 100, 2, fake, fake, fake, sl, 2, fake, fake, fake,
+                                fake, fake, 16, null) == -2
+    # misaligned workspace
+    assert lib.mds_medusa_heads(1, 1, 64, 100, 2, fake, fake, fake, sl, 2, fake, fake, fake,
+                                fake, ctypes.c_void_p(264), 1 << 30, null) == -2
+    # shortlist entry larger than smax
+    sl3 = (ctypes.c_int32 * 2)(3, 2)
+    assert lib.mds_medusa_heads(1, 1, 64, 100, 2, fake, fake, fake, sl3, 2, fake, fake, fake,
+                                fake, fake, 1 << 30, null) == -1
+    # verify_accept: bad mode, negative eps
+    assert lib.mds_verify_accept(1, 7, 2, 2, 0.1, 0.3, fake, fake, fake, fake, fake, fake,
+                                 null, fake, fake, fake, fake, 1 << 20, null) == -1
+    assert lib.mds_verify_accept(1, 7, 2, 1, -0.1, 0.3, fake, fake, fake, fake, fake, fake,
+                                 null, fake, fake, fake, fake, 1 << 20, null) == -1
+    # tree attention: Hq not a multiple of Hkv, N > 128, dh unsupported
+    args = [fake] * 7
+    assert lib.mds_tree_attention(1, 1, 7, 64, 100, 3, 2, 64, 256, 2, 2, *args, 1, fake, fake,
+                                  fake, fake, fake, null, fake, fake, 1 << 30, null) == -1
+    assert lib.mds_tree_attention(1, 1, 129, 64, 100, 2, 2, 64, 256, 2, 2, *args, 3, fake, fake,
+                                  fake, fake, fake, null, fake, fake, 1 << 30, null) == -3
+    assert lib.mds_tree_attention(1, 1, 7, 64, 100, 2, 2, 96, 256, 2, 2, *args, 1, fake, fake,
+                                  fake, fake, fake, null, fake, fake, 1 << 30, null) == -3
+    # compact: dh unsupported, B too large
+    assert lib.mds_compact_kv(1, 1, 2, 96, 64, 2, fake, fake, fake, fake, fake, fake, 1 << 20,
+                              null) == -3
+    assert lib.mds_compact_kv(1, 2000, 2, 64, 64, 2, fake, fake, fake, fake, fake, fake,
+                              1 << 20, null) == -3
+    # build_tree_mask: Nmax too small
+    n = ctypes.c_int32(0)
+    assert lib.mds_build_tree_mask(2, sl, -1, 3, ctypes.byref(n), fake, fake, fake, fake, 1,
+                                   null) == -1
+
+
+def test_python_binding_refuses_cpu_tensors(lib):
+    import torch
+    with pytest.raises(mds.MedusaError):
+        mds._ptr(torch.zeros(4))
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    saved = mds._lib
+    try:
+        mds._lib = None
+        with pytest.raises(mds.MedusaError):
+            mds.load(str(tmp_path / "nope.so"))
+    finally:
+        mds._lib = saved
