@@ -50,14 +50,16 @@ char* scratch(void* ws) { return static_cast<char*>(ws) + kWsScratch; }
 bool shape_ok(int d, int dh) { return d > 0 && d % 64 == 0 && (dh == 64 || dh == 128); }
 
 size_t need_heads(int dtype, int B, int d, int V, int K) {
-  (void)dtype; (void)d;
+  (void)d;
+  if (dtype == MDS_BF16) return kWsScratch + align_up(tc_partial_bytes(B * (K + 1), true));
   return kWsScratch + align_up((size_t)B * (K + 1) * V * 4);
 }
 size_t need_attention(int dtype, int B, int N, int d, int Hq) {
   const size_t rows = (size_t)B * N;
   return kWsScratch + align_up(rows * d * esize(dtype)) + 2 * align_up(rows * Hq * 128 * esize(dtype));
 }
-size_t need_verify(int B, int N, int V) {
+size_t need_verify(int dtype, int B, int N, int V) {
+  if (dtype == MDS_BF16) return kWsScratch + align_up(tc_partial_bytes(B * N, false));
   return kWsScratch + align_up((size_t)B * N * V * 4);
 }
 
@@ -96,7 +98,7 @@ size_t mds_workspace_size(int dtype, int B, int d, int V, int K, int N, int Hq, 
   if (!valid_dtype(dtype) || B < 1 || d < 1 || V < 1 || K < 1 || N < 1 || Hq < 1) return 0;
   size_t need = need_heads(dtype, B, d, V, K);
   const size_t a = need_attention(dtype, B, N, d, Hq);
-  const size_t v = need_verify(B, N, V);
+  const size_t v = need_verify(dtype, B, N, V);
   if (a > need) need = a;
   if (v > need) need = v;
   return need;
@@ -133,6 +135,11 @@ int mds_medusa_heads(int dtype, int B, int d, int V, int K, const void* h, const
   }
   if (!ws_ok(ws, ws_bytes, need_heads(dtype, B, d, V, K))) return MDS_EWORKSPACE;
   cudaStream_t st = as_stream(stream);
+  if (dtype == MDS_BF16) {
+    int rc = gemm_tc_heads(h, B, W, K, d, U, ws, st);
+    if (rc) return rc;
+    return lm_draft_tc(U, B, K, d, lm, V, sl, smax, root, topk_id, topk_val, scratch(ws), ws, st);
+  }
   EpiArgs e;
   e.kind = EPI_HEADS;
   e.out = U;
@@ -175,6 +182,13 @@ int mds_tree_attention(int dtype, int B, int N, int d, int V, int Hq, int Hkv, i
   int rc = embed_gather(dtype, B, N, d, V, K, smax, tok, root, topk_id, depth, rank, emb, x,
                         ws, st);
   if (rc) return rc;
+  if (dtype == MDS_BF16) {
+    rc = gemm_tc_qkv(x, B, N, d, wqkv, Hq, Hkv, dh, Pmax, P, q, Kc, Vc, ws, st);
+    if (rc) return rc;
+    rc = attention_simple(dtype, B, N, Hq, Hkv, dh, Pmax, P, mask, words, q, Kc, Vc, o, ws, st);
+    if (rc) return rc;
+    return gemm_tc_store(o, (int)rows, wo, d, Hq * dh, y, d, ws, st);
+  }
   EpiArgs e;
   e.kind = EPI_QKV;
   e.out = q;
@@ -205,8 +219,11 @@ int mds_lm_verify(int dtype, int B, int N, int d, int V, const void* y, const vo
     return MDS_EINVAL;
   if (B < 1 || N < 1 || V < 2) return MDS_EINVAL;
   if (N > kMaxN || d % 64 != 0 || d <= 0) return MDS_EUNSUPPORTED;
-  if (!ws_ok(ws, ws_bytes, need_verify(B, N, V))) return MDS_EWORKSPACE;
+  if (!ws_ok(ws, ws_bytes, need_verify(dtype, B, N, V))) return MDS_EWORKSPACE;
   cudaStream_t st = as_stream(stream);
+  if (dtype == MDS_BF16)
+    return lm_verify_tc(y, B, N, d, lm, V, tok, parent, argmax, stats, childlogit, scratch(ws),
+                        ws, st);
   float* logits = reinterpret_cast<float*>(scratch(ws));
   EpiArgs el;
   el.kind = EPI_LOGITS;

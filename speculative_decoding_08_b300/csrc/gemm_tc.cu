@@ -1,0 +1,755 @@
+// Streaming projection GEMM on the 5th-generation tensor cores (tcgen05),
+// bf16 inputs, fp32 accumulation in tensor memory:
+//
+//     Y[r, f] = sum_k X[r, k] * W[f, k]      X: [R, Kd] rows, W: [F, Kd] (out, in)
+//
+// The decode-time shapes are skinny: few rows (1..~5700) against a weight
+// matrix that is streamed once from HBM (the heads' W, the LM projection,
+// Wqkv, Wo).  Each CTA owns a contiguous range of weight rows (features),
+// split evenly over the SMs in units of 16, and streams it through a
+// 4-stage TMA ring; X tiles (the rows) are re-read from L2.  One thread
+// issues tcgen05.mma with M = 128 rows (X) and N = up to 256 features (W);
+// the fp32 accumulators live in tensor memory, double-buffered so that the
+// epilogue of one feature chunk overlaps the MMAs of the next.
+//
+// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = TMEM allocator and
+// MMA issuer, warps 2..5 = epilogue (one TMEM lane = one row per thread).
+//
+// Fused epilogues:
+//   STORE   Y -> bf16 out                                   (Wo projection)
+//   HEADS   U[b,1+i,j] = h[b,j] + SiLU(Y[b, i d + j])       ("Medusa deep dive",
+//           "The heads are residual blocks, not linear layers"); U[b,0] = h
+//   QKV     q rows -> q buffer, k/v rows -> KV-cache slot P_b + n
+//   DRAFT   per row running top-8 (value desc, id asc) over the CTA's range
+//           ("From top-k heads to a sparse candidate tree")
+//   VERIFY  per row running max / argmax / sum e^(z-m) / sum z e^(z-m)
+//           (entropy for "Typical acceptance, not exact rejection sampling")
+// DRAFT and VERIFY leave one partial record per (CTA, row); a merge kernel
+// combines them.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mds {
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kStageBytes = 48 * 1024;
+constexpr int kThreads = 192;
+constexpr int kTmemCols = 512;
+constexpr int kSmemBytes = kStages * kStageBytes + 2048;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
+constexpr int kBoxF = 16;                           // weight rows per TMA box
+constexpr int kMaxCta = 256;                        // partial records per row
+
+struct TcArgs {
+  int R, F, Kd;
+  int n_units, n_cta;
+  int G, NC;
+  int n_rgroups;
+  int kind;
+  void* out;
+  long long ldo;
+  const __nv_bfloat16* h;
+  int d, K;
+  int N, Hq, Hkv, dh, Pmax;
+  const int32_t* P;
+  __nv_bfloat16* Kc;
+  __nv_bfloat16* Vc;
+  void* partial;
+  void* ws;
+};
+
+enum { TC_STORE = 0, TC_HEADS = 1, TC_QKV = 2, TC_DRAFT = 3, TC_VERIFY = 4 };
+
+struct Range {
+  int f_begin, f_end, n_chunks;
+};
+
+__device__ __forceinline__ Range cta_range(const TcArgs& a, int c) {
+  Range r;
+  r.f_begin = 16 * (int)(((long long)c * a.n_units) / a.n_cta);
+  const int fe = 16 * (int)(((long long)(c + 1) * a.n_units) / a.n_cta);
+  r.f_end = fe < a.F ? fe : a.F;
+  r.n_chunks = r.f_end > r.f_begin ? (r.f_end - r.f_begin + a.NC - 1) / a.NC : 0;
+  return r;
+}
+
+// ------------------------------------------------------------- epilogues
+__device__ __forceinline__ void epi_store(const TcArgs& a, int row, int f0, int nv,
+                                          const float (&v)[32]) {
+  __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out) + (long long)row * a.ldo + f0;
+  if (nv == 32 && (a.ldo % 8) == 0) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4 pk;
+      __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(&pk);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) p2[e] = __floats2bfloat162_rn(v[q * 8 + 2 * e], v[q * 8 + 2 * e + 1]);
+      *reinterpret_cast<uint4*>(o + q * 8) = pk;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < nv) o[j] = __float2bfloat16_rn(v[j]);
+  }
+}
+
+__device__ __forceinline__ void epi_heads(const TcArgs& a, int b, int f0, int nv,
+                                          const float (&v)[32]) {
+  __nv_bfloat16* U = static_cast<__nv_bfloat16*>(a.out);
+  const __nv_bfloat16* hb = a.h + (long long)b * a.d;
+  const long long ubase = (long long)b * (a.K + 1) * a.d;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    if (j >= nv) break;
+    const int f = f0 + j;
+    const int i = f / a.d, jj = f - i * a.d;
+    const __nv_bfloat16 hraw = hb[jj];
+    const float hv = __bfloat162float(hraw);
+    U[ubase + (long long)(1 + i) * a.d + jj] = __float2bfloat16_rn(hv + silu(v[j]));
+    if (i == 0) U[ubase + jj] = hraw;
+  }
+}
+
+__device__ __forceinline__ void epi_qkv(const TcArgs& a, int r, int f0, int nv,
+                                        const float (&v)[32]) {
+  const int qd = a.Hq * a.dh, kd = a.Hkv * a.dh;
+  const int b = r / a.N, n = r - b * a.N;
+  const int Pb = a.P[b];
+  const bool cache_ok = Pb >= 0 && Pb + n < a.Pmax;
+  bool bad = false;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    if (j >= nv) break;
+    const int f = f0 + j;
+    if (f < qd) {
+      static_cast<__nv_bfloat16*>(a.out)[(long long)r * qd + f] = __float2bfloat16_rn(v[j]);
+    } else if (!cache_ok) {
+      bad = true;
+    } else {
+      const int f2 = f - qd;
+      const int which = f2 >= kd;
+      const int f3 = f2 - which * kd;
+      const int hk = f3 / a.dh, c = f3 - hk * a.dh;
+      __nv_bfloat16* cache = which ? a.Vc : a.Kc;
+      cache[(((long long)b * a.Hkv + hk) * a.Pmax + Pb + n) * a.dh + c] = __float2bfloat16_rn(v[j]);
+    }
+  }
+  if (bad) latch_error(a.ws, MDS_DEV_KV_CAPACITY);
+}
+
+struct TopList {
+  float v[kMaxS];
+  int id[kMaxS];
+  __device__ __forceinline__ void init() {
+#pragma unroll
+    for (int j = 0; j < kMaxS; ++j) {
+      v[j] = -INFINITY;
+      id[j] = 0x7fffffff;
+    }
+  }
+  // Insert keeping (value desc, id asc); ids arrive in increasing order, so
+  // an equal value never displaces an earlier (lower) id.
+  __device__ __forceinline__ void push(float x, int i) {
+    if (!(x > v[kMaxS - 1])) return;
+#pragma unroll
+    for (int j = 0; j < kMaxS; ++j) {
+      if (x > v[j]) {
+        const float tv = v[j];
+        const int ti = id[j];
+        v[j] = x;
+        id[j] = i;
+        x = tv;
+        i = ti;
+      }
+    }
+  }
+};
+
+struct SoftStat {
+  float m, S, Q;
+  int am;
+  __device__ __forceinline__ void init() {
+    m = -INFINITY;
+    S = 0.f;
+    Q = 0.f;
+    am = 0x7fffffff;
+  }
+  __device__ __forceinline__ void push32(const float (&z)[32], int f0, int nv) {
+    float lm = -INFINITY;
+    int li = 0x7fffffff;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const bool ok = j < nv;
+      if (ok && z[j] > lm) {
+        lm = z[j];
+        li = f0 + j;
+      }
+    }
+    if (lm > m) {
+      const float sc = __expf(m - lm);
+      S *= sc;
+      Q *= sc;
+      m = lm;
+      am = li;
+    }
+    if (m == -INFINITY) return;
+    float s = 0.f, q = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (j < nv) {
+        const float e = __expf(z[j] - m);
+        s += e;
+        q = fmaf(z[j], e, q);
+      }
+    }
+    S += s;
+    Q += q;
+  }
+};
+
+// ------------------------------------------------------------------ kernel
+__global__ void __launch_bounds__(kThreads, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+              TcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kStages;
+  uint64_t* tfull = bars + 2 * kStages;
+  uint64_t* tempty = bars + 2 * kStages + 2;
+  uint64_t* done = bars + 2 * kStages + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cta = blockIdx.x;
+  const Range rg = cta_range(a, cta);
+  const int nkb = a.Kd / 64;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(&tfull[s], 1);
+      ptx::mbar_init(&tempty[s], 4);
+    }
+    ptx::mbar_init(done, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+    ptx::tma_prefetch_desc(&tmX);
+    ptx::tma_prefetch_desc(&tmW);
+  }
+  if (warp == 1) ptx::tmem_alloc(tmem_slot, kTmemCols);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol_w = ptx::policy_evict_first();
+      const uint64_t pol_x = ptx::policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_phase[kStages];
+      bool issued[kStages];
+      for (int s = 0; s < kStages; ++s) issued[s] = false, issued_phase[s] = 0;
+      bool ok = true;
+      for (int g0 = 0; g0 < a.n_rgroups && ok; ++g0) {
+        const int row0 = g0 * 128 * a.G;
+        const int rem = a.R - row0;
+        const int Geff = min(a.G, (rem + 127) / 128);
+        for (int ch = 0; ch < rg.n_chunks && ok; ++ch) {
+          const int fc = rg.f_begin + ch * a.NC;
+          const int len = min(a.NC, rg.f_end - fc);
+          const int nbox = (len + kBoxF - 1) / kBoxF;
+          const uint32_t bytes = (uint32_t)Geff * 128 * 128 + (uint32_t)nbox * kBoxF * 128;
+          for (int kb = 0; kb < nkb; ++kb) {
+            if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, kWaitLimitNs)) {
+              ok = false;
+              break;
+            }
+            uint8_t* sA = smem + stage * kStageBytes;
+            uint8_t* sB = sA + a.G * 16384;
+            ptx::mbar_arrive_expect_tx(&full[stage], bytes);
+            for (int g = 0; g < Geff; ++g)
+              ptx::tma_load_2d(sA + g * 16384, &tmX, kb * 64, row0 + g * 128, &full[stage], pol_x);
+            for (int j = 0; j < nbox; ++j)
+              ptx::tma_load_2d(sB + j * kBoxF * 128, &tmW, kb * 64, fc + j * kBoxF, &full[stage],
+                               pol_w);
+            issued[stage] = true;
+            issued_phase[stage] = phase;
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+      if (!ok) {
+        latch_error(a.ws, MDS_DEV_TIMEOUT);
+        *abort_flag = 1;
+      }
+      // drain: every issued copy has landed before the CTA can exit
+      for (int s = 0; s < kStages; ++s)
+        if (issued[s]) ptx::mbar_wait(&full[s], issued_phase[s], abort_flag, kWaitLimitNs);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int item = 0;
+      bool ok = true;
+      for (int g0 = 0; g0 < a.n_rgroups && ok; ++g0) {
+        const int rem = a.R - g0 * 128 * a.G;
+        const int Geff = min(a.G, (rem + 127) / 128);
+        for (int ch = 0; ch < rg.n_chunks && ok; ++ch, ++item) {
+          const int fc = rg.f_begin + ch * a.NC;
+          const int len = min(a.NC, rg.f_end - fc);
+          const int npad = (len + 15) / 16 * 16;
+          const uint32_t idesc = ptx::idesc_bf16(128, npad);
+          const int acc = item & 1;
+          const uint32_t aphase = (item >> 1) & 1;
+          if (!ptx::mbar_wait(&tempty[acc], aphase ^ 1u, abort_flag, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          for (int kb = 0; kb < nkb; ++kb) {
+            if (!ptx::mbar_wait(&full[stage], phase, abort_flag, kWaitLimitNs)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t sA = ptx::smem_addr(smem + stage * kStageBytes);
+            const uint32_t sB = sA + a.G * 16384;
+            for (int g = 0; g < Geff; ++g) {
+              const uint32_t dcol = tmem_base + (uint32_t)(acc * a.G * a.NC + g * a.NC);
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const uint64_t ad = ptx::sdesc_k128(sA + g * 16384 + k * 32);
+                const uint64_t bd = ptx::sdesc_k128(sB + k * 32);
+                ptx::mma_bf16(dcol, ad, bd, idesc, (kb | k) != 0);
+              }
+            }
+            ptx::mma_commit(&empty[stage]);
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (ok) ptx::mma_commit(&tfull[acc]);
+        }
+      }
+      if (!ok) {
+        latch_error(a.ws, MDS_DEV_TIMEOUT);
+        *abort_flag = 1;
+      }
+      // every MMA issued by this thread is complete before TMEM is freed
+      ptx::mma_commit(done);
+      ptx::mbar_wait(done, 0, abort_flag, kWaitLimitNs);
+    }
+  } else {
+    // --------------------------------------------------------- epilogue
+    const int quarter = warp & 3;
+    const int trow = quarter * 32 + lane;
+    int item = 0;
+    bool ok = true;
+    for (int g0 = 0; g0 < a.n_rgroups && ok; ++g0) {
+      const int row0 = g0 * 128 * a.G;
+      const int rem = a.R - row0;
+      const int Geff = min(a.G, (rem + 127) / 128);
+      TopList tl[2];
+      SoftStat ss[2];
+      tl[0].init();
+      tl[1].init();
+      ss[0].init();
+      ss[1].init();
+      for (int ch = 0; ch < rg.n_chunks; ++ch, ++item) {
+        const int fc = rg.f_begin + ch * a.NC;
+        const int len = min(a.NC, rg.f_end - fc);
+        const int acc = item & 1;
+        const uint32_t aphase = (item >> 1) & 1;
+        if (!ptx::mbar_wait(&tfull[acc], aphase, abort_flag, kWaitLimitNs)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          if (g >= Geff) break;
+          const int row = row0 + g * 128 + trow;
+          const bool live = row < a.R;
+          for (int cb = 0; cb * 32 < len; ++cb) {
+            float v[32];
+            const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) +
+                                   (uint32_t)(acc * a.G * a.NC + g * a.NC + cb * 32);
+            ptx::tmem_ld32(taddr, v);
+            const int f0 = fc + cb * 32;
+            const int nv = min(32, len - cb * 32);
+            if (!live) continue;
+            switch (a.kind) {
+              case TC_STORE: epi_store(a, row, f0, nv, v); break;
+              case TC_HEADS: epi_heads(a, row, f0, nv, v); break;
+              case TC_QKV: epi_qkv(a, row, f0, nv, v); break;
+              case TC_DRAFT:
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (j < nv) tl[g].push(v[j], f0 + j);
+                break;
+              case TC_VERIFY: ss[g].push32(v, f0, nv); break;
+            }
+          }
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&tempty[acc]);
+      }
+      if (!ok) break;
+      if (rg.n_chunks > 0 && (a.kind == TC_DRAFT || a.kind == TC_VERIFY)) {
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          if (g >= Geff) break;
+          const int row = row0 + g * 128 + trow;
+          if (row >= a.R) continue;
+          const long long rec = (long long)cta * a.R + row;
+          if (a.kind == TC_VERIFY) {
+            float4 o = make_float4(ss[g].m, ss[g].S, ss[g].Q, __int_as_float(ss[g].am));
+            static_cast<float4*>(a.partial)[rec] = o;
+          } else {
+            float2* p = static_cast<float2*>(a.partial) + rec * kMaxS;
+#pragma unroll
+            for (int j = 0; j < kMaxS; ++j) p[j] = make_float2(tl[g].v[j], __int_as_float(tl[g].id[j]));
+          }
+        }
+      }
+    }
+    if (!ok) {
+      latch_error(a.ws, MDS_DEV_TIMEOUT);
+      *abort_flag = 1;
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 1) ptx::tmem_dealloc(tmem_base, kTmemCols);
+}
+
+// ----------------------------------------------------------- merge kernels
+// One warp per row: combine the per-CTA (m, S, Q, argmax) records.
+__global__ void __launch_bounds__(256) k_verify_merge(const float4* __restrict__ part, int n_cta,
+                                                      int R, int32_t* argmax, float* stats) {
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= R) return;
+  float m = -INFINITY, S = 0.f, Q = 0.f;
+  int am = 0x7fffffff;
+  for (int c = lane; c < n_cta; c += 32) {
+    const float4 p = part[(long long)c * R + row];
+    const int pam = __float_as_int(p.w);
+    if (p.y == 0.f && p.x == -INFINITY) continue;   // empty range
+    if (p.x > m || (p.x == m && pam < am)) {
+      const float sc = __expf(m - p.x);
+      S = S * sc + p.y;
+      Q = Q * sc + p.z;
+      if (p.x > m) m = p.x;
+      am = pam;
+    } else {
+      const float sc = __expf(p.x - m);
+      S += p.y * sc;
+      Q += p.z * sc;
+    }
+  }
+  for (int o = 16; o; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float S2 = __shfl_xor_sync(0xffffffffu, S, o);
+    const float Q2 = __shfl_xor_sync(0xffffffffu, Q, o);
+    const int a2 = __shfl_xor_sync(0xffffffffu, am, o);
+    const float mn = fmaxf(m, m2);
+    const float s1 = (m == -INFINITY) ? 0.f : __expf(m - mn);
+    const float s2 = (m2 == -INFINITY) ? 0.f : __expf(m2 - mn);
+    S = S * s1 + S2 * s2;
+    Q = Q * s1 + Q2 * s2;
+    if (m2 > m || (m2 == m && a2 < am)) am = a2;
+    m = mn;
+  }
+  if (lane == 0) {
+    const float lse = m + logf(S);
+    argmax[row] = am;
+    stats[(long long)row * 4 + 0] = m;
+    stats[(long long)row * 4 + 1] = lse;
+    stats[(long long)row * 4 + 2] = lse - Q / S;
+    stats[(long long)row * 4 + 3] = 0.f;
+  }
+}
+
+// One warp per head row (b, i): top s_i of the per-CTA candidate lists by
+// repeated extraction in (value desc, id asc) order.
+__global__ void __launch_bounds__(256) k_draft_merge(const float2* __restrict__ part, int n_cta,
+                                                     int R, int K, Shortlist sl, int smax,
+                                                     int32_t* root, int32_t* topk_id,
+                                                     float* topk_val) {
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= R) return;
+  const int b = row / (K + 1), i = row - b * (K + 1);
+  const int s = i == 0 ? 1 : sl.s[i - 1];
+  float pv = 0.f;
+  int pid = -1;
+  for (int t = 0; t < s; ++t) {
+    float bv = -INFINITY;
+    int bid = 0x7fffffff;
+    for (int c = lane; c < n_cta * kMaxS; c += 32) {
+      const float2 e = part[((long long)(c / kMaxS) * R + row) * kMaxS + (c % kMaxS)];
+      const float v = e.x;
+      const int id = __float_as_int(e.y);
+      if (id == 0x7fffffff) continue;
+      if (pid >= 0 && !ranks_before(pv, pid, v, id)) continue;
+      if (ranks_before(v, id, bv, bid)) {
+        bv = v;
+        bid = id;
+      }
+    }
+    for (int o = 16; o; o >>= 1) {
+      const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int i2 = __shfl_xor_sync(0xffffffffu, bid, o);
+      if (ranks_before(v2, i2, bv, bid)) {
+        bv = v2;
+        bid = i2;
+      }
+    }
+    if (lane == 0) {
+      if (i == 0) {
+        root[b] = bid;
+      } else {
+        topk_id[((long long)b * K + i - 1) * smax + t] = bid;
+        topk_val[((long long)b * K + i - 1) * smax + t] = bv;
+      }
+    }
+    pv = bv;
+    pid = bid;
+  }
+  if (i > 0 && lane >= s && lane < smax) {
+    topk_id[((long long)b * K + i - 1) * smax + lane] = -1;
+    topk_val[((long long)b * K + i - 1) * smax + lane] = -INFINITY;
+  }
+}
+
+// childlogit[b, c] = y[b, parent(c)] . lm[tok[b, c]], one warp per child.
+__global__ void __launch_bounds__(256) k_child_dot(const __nv_bfloat16* __restrict__ y,
+                                                   const __nv_bfloat16* __restrict__ lm, int N,
+                                                   int d, int V, const int32_t* tok,
+                                                   const int32_t* parent, float* child,
+                                                   void* ws) {
+  const int b = blockIdx.x;
+  const int lane = threadIdx.x & 31;
+  for (int c = threadIdx.x >> 5; c < N; c += blockDim.x >> 5) {
+    float acc = 0.f;
+    bool valid = false;
+    if (c > 0) {
+      const int pa = parent[c];
+      const int t = tok[(long long)b * N + c];
+      if (pa < 0 || pa >= N) {
+        if (lane == 0) latch_error(ws, MDS_DEV_TREE_INDEX);
+      } else if (t < 0 || t >= V) {
+        if (lane == 0) latch_error(ws, MDS_DEV_TOKEN_RANGE);
+      } else {
+        valid = true;
+        const uint4* yr = reinterpret_cast<const uint4*>(y + ((long long)b * N + pa) * d);
+        const uint4* lr = reinterpret_cast<const uint4*>(lm + (long long)t * d);
+        for (int k = lane; k < d / 8; k += 32) {
+          const uint4 ya = yr[k], la = lr[k];
+          const __nv_bfloat162* y2 = reinterpret_cast<const __nv_bfloat162*>(&ya);
+          const __nv_bfloat162* l2 = reinterpret_cast<const __nv_bfloat162*>(&la);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 yf = __bfloat1622float2(y2[e]);
+            const float2 lf = __bfloat1622float2(l2[e]);
+            acc = fmaf(yf.x, lf.x, acc);
+            acc = fmaf(yf.y, lf.y, acc);
+          }
+        }
+      }
+    }
+    for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) child[(long long)b * N + c] = valid ? acc : 0.f;
+  }
+}
+
+// ------------------------------------------------------------------ host
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+int g_num_sms = 0;
+
+int init_host() {
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return MDS_ECUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    if (cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes) != cudaSuccess)
+      return MDS_ECUDA;
+  }
+  if (!g_num_sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MDS_ECUDA;
+    if (cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return MDS_ECUDA;
+  }
+  return MDS_OK;
+}
+
+int grid_ctas(int F) {
+  const int n_units = (F + 15) / 16;
+  int n = g_num_sms < kMaxCta ? g_num_sms : kMaxCta;
+  return n_units < n ? n_units : n;
+}
+
+int make_map(CUtensorMap* m, const void* base, int rows, int cols, int box_rows) {
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+                              dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MDS_OK : MDS_ECUDA;
+}
+
+int launch_tc(TcArgs a, const void* X, const void* W, cudaStream_t st) {
+  int rc = init_host();
+  if (rc) return rc;
+  if (a.R <= 0 || a.F <= 0) return MDS_OK;
+  if (a.Kd % 64 != 0) return MDS_EUNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(X) | reinterpret_cast<uintptr_t>(W)) & 15) return MDS_EINVAL;
+  a.G = a.R <= 128 ? 1 : 2;
+  a.NC = 256 / a.G;
+  a.n_rgroups = (a.R + 128 * a.G - 1) / (128 * a.G);
+  a.n_units = (a.F + 15) / 16;
+  a.n_cta = grid_ctas(a.F);
+  CUtensorMap mx, mw;
+  rc = make_map(&mx, X, a.R, a.Kd, 128);
+  if (rc) return rc;
+  rc = make_map(&mw, W, a.F, a.Kd, kBoxF);
+  if (rc) return rc;
+  k_gemm_tc<<<a.n_cta, kThreads, kSmemBytes, st>>>(mx, mw, a);
+  MDS_LAUNCH_CHECK();
+  return MDS_OK;
+}
+
+}  // namespace
+
+int gemm_tc_heads(const void* h, int B, const void* W, int K, int d, void* U, void* ws,
+                  cudaStream_t st) {
+  TcArgs a{};
+  a.R = B;
+  a.F = K * d;
+  a.Kd = d;
+  a.kind = TC_HEADS;
+  a.out = U;
+  a.h = static_cast<const __nv_bfloat16*>(h);
+  a.d = d;
+  a.K = K;
+  a.ws = ws;
+  return launch_tc(a, h, W, st);
+}
+
+int gemm_tc_store(const void* X, int R, const void* W, int F, int Kd, void* out, long long ldo,
+                  void* ws, cudaStream_t st) {
+  TcArgs a{};
+  a.R = R;
+  a.F = F;
+  a.Kd = Kd;
+  a.kind = TC_STORE;
+  a.out = out;
+  a.ldo = ldo;
+  a.ws = ws;
+  return launch_tc(a, X, W, st);
+}
+
+int gemm_tc_qkv(const void* x, int B, int N, int d, const void* wqkv, int Hq, int Hkv, int dh,
+                int Pmax, const int32_t* P, void* q, void* Kc, void* Vc, void* ws,
+                cudaStream_t st) {
+  TcArgs a{};
+  a.R = B * N;
+  a.F = (Hq + 2 * Hkv) * dh;
+  a.Kd = d;
+  a.kind = TC_QKV;
+  a.out = q;
+  a.N = N;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.dh = dh;
+  a.Pmax = Pmax;
+  a.P = P;
+  a.Kc = static_cast<__nv_bfloat16*>(Kc);
+  a.Vc = static_cast<__nv_bfloat16*>(Vc);
+  a.ws = ws;
+  return launch_tc(a, x, wqkv, st);
+}
+
+size_t tc_partial_bytes(int R, bool draft) {
+  // one record per (CTA, row), at most kMaxCta CTAs
+  const size_t per = draft ? (size_t)kMaxS * 8 : 16;
+  return (size_t)kMaxCta * R * per;
+}
+
+int lm_draft_tc(const void* U, int B, int K, int d, const void* lm, int V, Shortlist sl, int smax,
+                int32_t* root, int32_t* topk_id, float* topk_val, void* partial, void* ws,
+                cudaStream_t st) {
+  TcArgs a{};
+  a.R = B * (K + 1);
+  a.F = V;
+  a.Kd = d;
+  a.kind = TC_DRAFT;
+  a.partial = partial;
+  a.ws = ws;
+  int rc = launch_tc(a, U, lm, st);
+  if (rc) return rc;
+  const int n_cta = grid_ctas(V);
+  k_draft_merge<<<(a.R + 7) / 8, 256, 0, st>>>(static_cast<const float2*>(partial), n_cta, a.R,
+                                                K, sl, smax, root, topk_id, topk_val);
+  MDS_LAUNCH_CHECK();
+  return MDS_OK;
+}
+
+int lm_verify_tc(const void* y, int B, int N, int d, const void* lm, int V, const int32_t* tok,
+                 const int32_t* parent, int32_t* argmax, float* stats, float* childlogit,
+                 void* partial, void* ws, cudaStream_t st) {
+  TcArgs a{};
+  a.R = B * N;
+  a.F = V;
+  a.Kd = d;
+  a.kind = TC_VERIFY;
+  a.partial = partial;
+  a.ws = ws;
+  int rc = launch_tc(a, y, lm, st);
+  if (rc) return rc;
+  const int n_cta = grid_ctas(V);
+  k_verify_merge<<<(a.R + 7) / 8, 256, 0, st>>>(static_cast<const float4*>(partial), n_cta, a.R,
+                                                 argmax, stats);
+  MDS_LAUNCH_CHECK();
+  k_child_dot<<<B, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(y),
+                                 static_cast<const __nv_bfloat16*>(lm), N, d, V, tok, parent,
+                                 childlogit, ws);
+  MDS_LAUNCH_CHECK();
+  return MDS_OK;
+}
+
+}  // namespace mds

@@ -68,4 +68,20 @@ int accept_path(int B, int N, int K, int mode, float eps, float delta, const int
 int compact(int dtype, int B, int Hkv, int dh, int Pmax, int K, const int32_t* L,
             const int32_t* path, void* Kc, void* Vc, int32_t* P, void* ws, cudaStream_t st);
 
+// Tensor-core (tcgen05) path, bf16 inputs.
+size_t tc_partial_bytes(int R, bool draft);
+int gemm_tc_heads(const void* h, int B, const void* W, int K, int d, void* U, void* ws,
+                  cudaStream_t st);
+int gemm_tc_store(const void* X, int R, const void* W, int F, int Kd, void* out, long long ldo,
+                  void* ws, cudaStream_t st);
+int gemm_tc_qkv(const void* x, int B, int N, int d, const void* wqkv, int Hq, int Hkv, int dh,
+                int Pmax, const int32_t* P, void* q, void* Kc, void* Vc, void* ws,
+                cudaStream_t st);
+int lm_draft_tc(const void* U, int B, int K, int d, const void* lm, int V, Shortlist sl, int smax,
+                int32_t* root, int32_t* topk_id, float* topk_val, void* partial, void* ws,
+                cudaStream_t st);
+int lm_verify_tc(const void* y, int B, int N, int d, const void* lm, int V, const int32_t* tok,
+                 const int32_t* parent, int32_t* argmax, float* stats, float* childlogit,
+                 void* partial, void* ws, cudaStream_t st);
+
 }  // namespace mds

@@ -66,12 +66,16 @@ def close_float(got: np.ndarray, want: np.ndarray, dtype: str, kind: str, what: 
         err = np.abs(got - want)
         assert float(err.max()) <= BF16_ATTN_ATOL, (what, float(err.max()))
         return float(err.max())
-    # bf16-stored value: both sides round to bf16; a rounding-boundary flip
-    # moves the value by one bf16 unit (<= 2^-7 relative).
-    err = np.abs(got - want) / np.maximum(np.abs(want), 1e-30)
-    bad = (err > 2.0 ** -7 + 1e-9) & (np.abs(got - want) > 1e-6)
-    assert not bad.any(), (what, float(err.max()))
-    return float(err.max())
+    # bf16-stored value: both sides round to bf16 at the same point; a
+    # rounding-boundary flip moves the value by one bf16 unit (<= 2^-7 of it).
+    # Where the stored value is a sum that cancels (h + SiLU(W h) ~ 0), the
+    # fp32 pre-rounding error (~1e-6 of the operands) dominates, so an
+    # absolute floor of 2^-15 of the tensor's rms is allowed as well.
+    rms = float(np.sqrt(np.mean(want ** 2))) if want.size else 0.0
+    lim = 2.0 ** -7 * np.abs(want) + 2.0 ** -15 * rms
+    excess = np.abs(got - want) - lim
+    assert not (excess > 0).any(), (what, float(np.max(np.abs(got - want))), float(excess.max()))
+    return float(np.max(np.abs(got - want) / np.maximum(np.abs(want), 1e-30)))
 
 
 def tol_logit(dtype: str, scale: float = 1.0) -> float:
