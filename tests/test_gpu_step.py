@@ -53,8 +53,8 @@ def compare_step(mds, w, sample, modes):
              topk_val=host(step.topk_val), tok=host(step.tok), y=host(step.y),
              argmax=host(step.argmax), stats=host(step.stats), child=host(step.childlogit),
              kc=None, vc=None, P=host(step.P))
-    f = f64_inputs(w, x, sample)
-    r = oracle.step(w, f, x["P"], final_mode, batch=sample)
+    f = f64_inputs(w, x, sample)           # h, kc, vc already restricted to the sample
+    r = oracle.step(w, f, x["P"][sample], final_mode, batch=list(range(len(sample))))
     ties = NearTies()
     compared_paths = 0
     for i, b in enumerate(sample):
