@@ -134,6 +134,29 @@ MDS_API int mds_medusa_heads(int dtype, int B, int d, int V, int K, const void* 
                      int32_t* root, int32_t* topk_id, float* topk_val,
                      void* ws, size_t ws_bytes, void* stream);
 
+/* mds_medusa_heads for callers that cannot allocate device memory (the pages
+ * have no counterpart: this is a deployment variant, not a step of the
+ * method).  A runtime that sizes all device memory once at start-up, or code
+ * running inside an allocator callback, cannot hand over a fresh workspace;
+ * this call takes none.  Its scratch (1 MiB of per-CTA candidate lists plus
+ * a status word) is a fixed array inside the library, which every GPU that
+ * loads the library holds until the process exits.  Arithmetic and outputs
+ * are those of mds_medusa_heads with dtype = MDS_BF16.
+ *   Same arguments as mds_medusa_heads (bf16 only), without ws / ws_bytes.
+ *   device_status device [1] int32 or NULL: receives the latched MDS_DEV_*
+ *                 code of this call (0 = none), stream-ordered.
+ *   Limits: B * (K + 1) <= 64; larger returns MDS_EUNSUPPORTED before any
+ *   work is enqueued.  It calls no cudaMalloc or cudaFree.
+ *   The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.  All calls share the one array: calls that
+ *   overlap on the GPU (other streams, other host threads) race and must be
+ *   serialised by the caller. */
+MDS_API int mds_medusa_heads_noalloc(int B, int d, int V, int K, const void* h, const void* W,
+                             const void* lm, const int32_t* shortlist, int smax, void* U,
+                             int32_t* root, int32_t* topk_id, float* topk_val,
+                             int32_t* device_status, void* stream);
+
 /* One tree-attention verify layer ([GL] tree attention: every branch shares
  * the prefix KV and all candidates are scored in one pass; [D89]: the mask
  * lets each candidate attend to its own prefix).

@@ -31,6 +31,7 @@ _SIGS = {
     "mds_build_tree_mask": ([_c_int, _p, _c_int, _c_int, _p, _p, _p, _p, _p, _c_int, _p], _c_int),
     "mds_medusa_heads": ([_c_int, _c_int, _c_int, _c_int, _c_int, _p, _p, _p, _p, _c_int, _p, _p,
                           _p, _p, _p, _c_size, _p], _c_int),
+    "mds_medusa_heads_noalloc": ([_c_int] * 4 + [_p] * 4 + [_c_int] + [_p] * 6, _c_int),
     "mds_tree_attention": ([_c_int] * 11 + [_p] * 7 + [_c_int] + [_p] * 8 + [_c_size, _p],
                            _c_int),
     "mds_lm_verify": ([_c_int] * 5 + [_p] * 8 + [_c_size, _p], _c_int),
@@ -138,6 +139,18 @@ def medusa_heads(h, W, lm, shortlist, smax, U, root, topk_id, topk_val, ws):
                                  _i32(shortlist), smax, _ptr(U), _ptr(root), _ptr(topk_id),
                                  _ptr(topk_val), _ptr(ws), ws.numel(), _stream())
     _check(rc, "medusa_heads")
+
+
+def medusa_heads_noalloc(h, W, lm, shortlist, smax, U, root, topk_id, topk_val,
+                         device_status=None):
+    """mds_medusa_heads without a workspace (bf16; scratch held by the library)."""
+    B, d = h.shape
+    K = W.shape[0]
+    V = lm.shape[0]
+    rc = load().mds_medusa_heads_noalloc(B, d, V, K, _ptr(h), _ptr(W), _ptr(lm), _i32(shortlist),
+                                         smax, _ptr(U), _ptr(root), _ptr(topk_id),
+                                         _ptr(topk_val), _ptr(device_status), _stream())
+    _check(rc, "medusa_heads_noalloc")
 
 
 def tree_attention(P, tok, mask, emb, wqkv, wo, Kc, Vc, y, ws, *, Hq, Hkv, K, smax,

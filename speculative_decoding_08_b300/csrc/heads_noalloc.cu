@@ -1,0 +1,95 @@
+// mds_medusa_heads_noalloc: the draft heads (mds_medusa_heads, bf16) with
+// their scratch memory held by the library instead of a caller workspace.
+//
+// Who needs this: callers that cannot allocate device memory at the point
+// where they run the draft step.  Examples are a serving runtime that sizes
+// every device buffer once at start-up and forbids allocation afterwards, an
+// allocator or pool callback that must not re-enter the allocator, and host
+// code linked without access to the CUDA allocator of the process that owns
+// the tensors.  Such a caller still passes the inputs and outputs; the
+// per-CTA candidate lists and the device status word live in a fixed
+// file-scope device array instead of a workspace.
+//
+// The array is a static __device__ symbol, so every GPU that loads this
+// library holds kNoAllocBytes of it until the process exits.  Host code
+// cannot use the symbol's name as a device address: the address is looked
+// up with cudaGetSymbolAddress once per device, with that device current,
+// on the first call made on it.
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace mds {
+namespace {
+
+// Rows B * (K + 1) one call may draft.  Each row needs one candidate list of
+// kMaxS (value, id) pairs per CTA of the LM-projection pass (at most 256
+// CTAs): 256 * 8 * 8 bytes = 16 KiB per row, 1 MiB for 64 rows.
+constexpr int kNoAllocMaxRows = 64;
+constexpr size_t kNoAllocPartialBytes = (size_t)kNoAllocMaxRows * 256 * kMaxS * 8;
+constexpr size_t kNoAllocBytes = kWsScratch + kNoAllocPartialBytes;
+constexpr int kNoAllocMaxDevices = 64;
+
+// Layout matches a caller workspace: status word at offset 0, candidate
+// lists from kWsScratch on.
+static __device__ __align__(256) unsigned char g_heads_scratch[kNoAllocBytes];
+
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kNoAllocMaxDevices] = {};
+
+// Device address of g_heads_scratch on the current device (looked up once
+// per device, under a lock).
+int scratch_address(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MDS_ECUDA;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return MDS_EUNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_heads_scratch) != cudaSuccess || !p) return MDS_ECUDA;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return MDS_OK;
+}
+
+}  // namespace
+}  // namespace mds
+
+using namespace mds;
+
+extern "C" int mds_medusa_heads_noalloc(int B, int d, int V, int K, const void* h,
+                                        const void* W, const void* lm,
+                                        const int32_t* shortlist, int smax, void* U,
+                                        int32_t* root, int32_t* topk_id, float* topk_val,
+                                        int32_t* device_status, void* stream) {
+  if (!h || !W || !lm || !shortlist || !U || !root || !topk_id || !topk_val) return MDS_EINVAL;
+  if (B < 1 || V < 2 || K < 1 || smax < 1) return MDS_EINVAL;
+  if (K > kMaxK || smax > kMaxS || d % 64 != 0 || d <= 0) return MDS_EUNSUPPORTED;
+  Shortlist sl{};
+  sl.K = K;
+  for (int i = 0; i < K; ++i) {
+    if (shortlist[i] < 1 || shortlist[i] > smax || shortlist[i] > V) return MDS_EINVAL;
+    sl.s[i] = shortlist[i];
+  }
+  const long long rows = (long long)B * (K + 1);
+  if (rows > kNoAllocMaxRows || tc_partial_bytes((int)rows, true) > kNoAllocPartialBytes)
+    return MDS_EUNSUPPORTED;
+  void* scratch = nullptr;
+  int rc = scratch_address(&scratch);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // The array keeps the previous call's contents; only the status word must
+  // start at zero (every candidate list is written before it is read).
+  MDS_CUDA_TRY(cudaMemsetAsync(scratch, 0, 256, st));
+  rc = gemm_tc_heads(h, B, W, K, d, U, scratch, st);
+  if (rc) return rc;
+  rc = lm_draft_tc(U, B, K, d, lm, V, sl, smax, root, topk_id, topk_val,
+                   static_cast<char*>(scratch) + kWsScratch, scratch, st);
+  if (rc) return rc;
+  if (device_status)
+    MDS_CUDA_TRY(cudaMemcpyAsync(device_status, scratch, sizeof(int32_t),
+                                 cudaMemcpyDeviceToDevice, st));
+  return MDS_OK;
+}
