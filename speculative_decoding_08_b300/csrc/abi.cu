@@ -54,9 +54,12 @@ size_t need_heads(int dtype, int B, int d, int V, int K) {
   if (dtype == MDS_BF16) return kWsScratch + align_up(tc_partial_bytes(B * (K + 1), true));
   return kWsScratch + align_up((size_t)B * (K + 1) * V * 4);
 }
-size_t need_attention(int dtype, int B, int N, int d, int Hq) {
+size_t need_attention(int dtype, int B, int N, int d, int Hq, int Hkv, int dh) {
   const size_t rows = (size_t)B * N;
-  return kWsScratch + align_up(rows * d * esize(dtype)) + 2 * align_up(rows * Hq * 128 * esize(dtype));
+  size_t n = kWsScratch + align_up(rows * d * esize(dtype)) + 2 * align_up(rows * Hq * 128 * esize(dtype));
+  if (dtype == MDS_BF16 && Hkv > 0 && Hq % Hkv == 0)
+    n += align_up(attention_tc_partial_bytes(N, Hq / Hkv, dh));
+  return n;
 }
 size_t need_verify(int dtype, int B, int N, int V) {
   if (dtype == MDS_BF16) return kWsScratch + align_up(tc_partial_bytes(B * N, false));
@@ -94,10 +97,10 @@ int mds_tree_size(int K, const int32_t* shortlist, int max_rank_sum) {
 
 size_t mds_workspace_size(int dtype, int B, int d, int V, int K, int N, int Hq, int Hkv,
                           int dh, int smax) {
-  (void)Hkv; (void)dh; (void)smax;
+  (void)smax;
   if (!valid_dtype(dtype) || B < 1 || d < 1 || V < 1 || K < 1 || N < 1 || Hq < 1) return 0;
   size_t need = need_heads(dtype, B, d, V, K);
-  const size_t a = need_attention(dtype, B, N, d, Hq);
+  const size_t a = need_attention(dtype, B, N, d, Hq, Hkv, dh);
   const size_t v = need_verify(dtype, B, N, V);
   if (a > need) need = a;
   if (v > need) need = v;
@@ -172,7 +175,8 @@ int mds_tree_attention(int dtype, int B, int N, int d, int V, int Hq, int Hkv, i
   if (Hq % Hkv != 0) return MDS_EINVAL;
   if (N > kMaxN || K > kMaxK || smax > kMaxS || !shape_ok(d, dh)) return MDS_EUNSUPPORTED;
   if (words < (N + 63) / 64) return MDS_EINVAL;
-  if (!ws_ok(ws, ws_bytes, need_attention(dtype, B, N, d, Hq))) return MDS_EWORKSPACE;
+  if (dtype == MDS_BF16 && !attention_tc_supported(B, N, Hq / Hkv, dh)) return MDS_EUNSUPPORTED;
+  if (!ws_ok(ws, ws_bytes, need_attention(dtype, B, N, d, Hq, Hkv, dh))) return MDS_EWORKSPACE;
   cudaStream_t st = as_stream(stream);
   const size_t rows = (size_t)B * N;
   char* base = scratch(ws);
@@ -185,7 +189,8 @@ int mds_tree_attention(int dtype, int B, int N, int d, int V, int Hq, int Hkv, i
   if (dtype == MDS_BF16) {
     rc = gemm_tc_qkv(x, B, N, d, wqkv, Hq, Hkv, dh, Pmax, P, q, Kc, Vc, ws, st);
     if (rc) return rc;
-    rc = attention_simple(dtype, B, N, Hq, Hkv, dh, Pmax, P, mask, words, q, Kc, Vc, o, ws, st);
+    void* part = static_cast<char*>(q) + 2 * align_up(rows * Hq * 128 * esize(dtype));
+    rc = attention_tc(B, N, Hq, Hkv, dh, Pmax, P, mask, words, q, Kc, Vc, o, part, ws, st);
     if (rc) return rc;
     return gemm_tc_store(o, (int)rows, wo, d, Hq * dh, y, d, ws, st);
   }

@@ -1,0 +1,784 @@
+// Tree attention on the 5th-generation tensor cores (tcgen05), bf16, fp32
+// accumulation.
+//
+// "Medusa Heads", how it works: all candidates of the tree are scored in one
+// pass and every branch shares the prefix KV cache; "day89", "Tree-based
+// attention": the mask lets each candidate attend only to its own prefix.
+// For sequence b, KV head h and query row r = n g + j (tree row n, query
+// head h g + j of the g = Hq / Hkv heads that share KV head h):
+//
+//     o_r = sum_k softmax_k(q_r . K_k / sqrt(dh)) V_k
+//
+// over the keys k in [0, P_b) (the prefix) and k = P_b + m for the tree rows
+// m with mask(n, m) set (the ancestors of n, n itself and the root).
+//
+// Design.  One work unit is (b, h, group of up to 3 query tiles of 128 rows);
+// its keys [0, P_b + N) are cut into tiles of 64.  The tiles of all units are
+// laid end to end and split evenly over the CTAs (one per SM), so ragged
+// prefixes and any batch balance across the GPU (stream-K).  A CTA streams
+// its key tiles through a TMA ring once; every query tile of the unit uses
+// each key tile while it is in shared memory:
+//
+//   S = Q K^T      tcgen05, M = 128 query rows, N = 64 keys, K = dh      -> TMEM
+//   softmax        one thread per query row reads its S row from TMEM,
+//                  masks, keeps a running max m (log2 domain) and sum l,
+//                  writes P = 2^(S - m) as bf16 into shared memory
+//   O += P V       tcgen05, M = 128, N = dh, K = 64 keys, V read MN-major -> TMEM
+//
+// The running max is raised lazily: O is rescaled only when a row's maximum
+// grows by more than 2^8, so the accumulator in TMEM is rarely touched; the
+// final O / l is exact for any reference value.  A unit whose tiles span
+// several CTAs leaves one partial (O, m, l) per CTA; the last CTA to finish
+// (an atomic counter per unit and row quarter) merges them.  No CTA ever
+// waits for another.
+//
+// Warp roles (192 threads): warp 0 TMA producer, warp 1 TMEM owner and MMA
+// issuer, warps 2..5 softmax / epilogue (thread = TMEM lane = query row).
+// Every mbarrier wait is bounded; on timeout the CTA latches MDS_DEV_TIMEOUT,
+// drains its own copies and MMAs, frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mds {
+namespace {
+
+constexpr int kBN = 64;                 // keys per tile
+constexpr int kThreads = 192;
+constexpr int kMaxNM = 3;               // query tiles per unit
+constexpr int kMaxCtaAttn = 160;
+constexpr int kMaxBAttn = 256;
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr float kRescaleLog2 = 8.0f;    // rescale O when the max grows by > 2^8
+constexpr int kSmemLimit = 232448;      // 227 KB
+
+struct AttnArgs {
+  int B, N, Hq, Hkv, g, Pmax;
+  int Mrows;        // N * g query rows per (b, h)
+  int NM;           // query tiles per unit
+  int n_mg;         // units per (b, h)
+  int stages;
+  int G;            // CTAs
+  float scale_log2; // log2(e) / sqrt(dh)
+  const int32_t* P;
+  const uint64_t* mask;
+  int words;
+  __nv_bfloat16* o;       // [B, N, Hq, dh]
+  float* part;            // partial records
+  int* counters;          // [kMaxCtaAttn * 4]
+  void* ws;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
+          taddr),
+      "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]),
+      "f"(v[8]), "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]),
+      "f"(v[15]), "f"(v[16]), "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]),
+      "f"(v[22]), "f"(v[23]), "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]),
+      "f"(v[29]), "f"(v[30]), "f"(v[31])
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Descriptor of an MN-major operand with the 128-byte swizzle: 64-element
+// (128 B) rows along N, 8-row groups along K 1024 B apart (stride byte
+// offset), consecutive 64-element N chunks `lbo` bytes apart (leading byte
+// offset).
+__device__ __forceinline__ uint64_t sdesc_mn128(uint32_t saddr, uint32_t lbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)(1024u >> 4) << 32;
+  d |= (uint64_t)1u << 46;
+  d |= (uint64_t)2u << 61;
+  return d;
+}
+
+// --------------------------------------------------------- work partition
+// Tiles of sequence b's units: ceil((P_b + N) / 64), or 0 when P_b is out of
+// range (reported once).
+__device__ __forceinline__ int tiles_of(const AttnArgs& a, int Pb) {
+  if (Pb < 0 || Pb + a.N > a.Pmax) return 0;
+  return (Pb + a.N + kBN - 1) / kBN;
+}
+
+struct Seg {
+  int b, h, mg;     // unit
+  int unit;         // (b * Hkv + h) * n_mg + mg
+  int Pb, nt;       // prefix length, tiles of the unit
+  int j0, j1;       // tile range of this segment within the unit
+  long long U0;     // first global tile of the unit
+};
+
+// Walks the segments of the CTA's global tile range [t, end).  pre[b] =
+// first global tile of sequence b (shared memory, B + 1 entries).
+struct SegIter {
+  long long t, end;
+  __device__ __forceinline__ bool next(const AttnArgs& a, const int* pre, Seg& s) {
+    if (t >= end) return false;
+    int lo = 0, hi = a.B;          // largest b with pre[b] <= t
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (pre[mid] <= t) lo = mid; else hi = mid;
+    }
+    const int b = lo;
+    const int Pb = a.P[b];
+    const int nt = tiles_of(a, Pb);
+    const long long off = t - (long long)pre[b];
+    const int idx = (int)(off / nt);
+    s.b = b;
+    s.h = idx / a.n_mg;
+    s.mg = idx - s.h * a.n_mg;
+    s.unit = (b * a.Hkv + s.h) * a.n_mg + s.mg;
+    s.Pb = Pb;
+    s.nt = nt;
+    s.U0 = (long long)pre[b] + (long long)idx * nt;
+    s.j0 = (int)(t - s.U0);
+    const long long stop = end < s.U0 + nt ? end : s.U0 + nt;
+    s.j1 = (int)(stop - s.U0);
+    t = stop;
+    return true;
+  }
+};
+
+__device__ __forceinline__ long long cta_start(long long Ttot, int G, int c) {
+  return (Ttot * c) / G;
+}
+
+// --------------------------------------------------------------- kernel
+template <int DH, int NM>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_tree_attention_tc(const __grid_constant__ CUtensorMap tmQ,
+                        const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, AttnArgs a) {
+  constexpr int kHalves = DH / 64;
+  constexpr uint32_t kQTileBytes = 128 * DH * 2;
+  constexpr uint32_t kKVHalfBytes = kBN * 128;            // 64 keys x 64 dh x 2 B
+  constexpr uint32_t kStageBytes = 2 * kHalves * kKVHalfBytes;
+  constexpr uint32_t kPBytes = 128 * kBN * 2;
+  constexpr uint32_t kSCol0 = 0;                          // S: 2 x 64 columns
+  constexpr uint32_t kOCol0 = 2 * kBN;                    // O: NM x DH columns
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const int S = a.stages;
+  uint8_t* sQ = smem;
+  uint8_t* sP = sQ + NM * kQTileBytes;
+  uint8_t* sKV = sP + 2 * kPBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + S * kStageBytes);
+  uint64_t* kv_full = bars;               // [S]
+  uint64_t* kv_empty = bars + 8;          // [S]
+  uint64_t* s_full = bars + 16;           // [2]
+  uint64_t* s_empty = bars + 18;          // [2]
+  uint64_t* p_full = bars + 20;           // [2]
+  uint64_t* p_empty = bars + 22;          // [2]
+  uint64_t* q_full = bars + 28;
+  uint64_t* q_empty = bars + 29;
+  uint64_t* o_empty = bars + 30;
+  uint64_t* done = bars + 31;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 32);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* pre = reinterpret_cast<int*>(bars + 34);   // [B + 1]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cta = blockIdx.x;
+
+  // tile prefix over sequences (every thread reads P; thread 0 scans)
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    bool bad = false;
+    for (int b = 0; b < a.B; ++b) {
+      pre[b] = acc;
+      const int Pb = a.P[b];
+      const int nt = tiles_of(a, Pb);
+      if (nt == 0) bad = true;
+      acc += a.Hkv * a.n_mg * nt;
+    }
+    pre[a.B] = acc;
+    if (bad && cta == 0) latch_error(a.ws, MDS_DEV_KV_CAPACITY);
+    for (int s = 0; s < S; ++s) {
+      ptx::mbar_init(&kv_full[s], 1);
+      ptx::mbar_init(&kv_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&s_full[i], 1);
+      ptx::mbar_init(&s_empty[i], 4);
+      ptx::mbar_init(&p_full[i], 4);
+      ptx::mbar_init(&p_empty[i], 1);
+    }
+    ptx::mbar_init(q_full, 1);
+    ptx::mbar_init(q_empty, 1);
+    ptx::mbar_init(o_empty, 4);
+    ptx::mbar_init(done, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+    ptx::tma_prefetch_desc(&tmQ);
+    ptx::tma_prefetch_desc(&tmK);
+    ptx::tma_prefetch_desc(&tmV);
+  }
+  if (warp == 1) ptx::tmem_alloc(tmem_slot, 512);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const long long Ttot = (long long)pre[a.B];
+  SegIter iter;
+  iter.t = cta_start(Ttot, a.G, cta);
+  iter.end = cta_start(Ttot, a.G, cta + 1);
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol_kv = ptx::policy_evict_first();
+      const uint64_t pol_q = ptx::policy_evict_last();
+      int kvt = 0, segc = 0;
+      bool ok = true;
+      Seg s;
+      while (ok && iter.next(a, pre, s)) {
+        if (!ptx::mbar_wait(q_empty, (segc & 1) ^ 1u, abort_flag, kWaitNs)) { ok = false; break; }
+        const int qrow0 = (s.b * a.Hkv + s.h) * a.Mrows + s.mg * NM * 128;
+        ptx::mbar_arrive_expect_tx(q_full, NM * kQTileBytes);
+        for (int m = 0; m < NM; ++m)
+          for (int hh = 0; hh < kHalves; ++hh)
+            ptx::tma_load_2d(sQ + m * kQTileBytes + hh * 16384, &tmQ, hh * 64, qrow0 + m * 128,
+                             q_full, pol_q);
+        ++segc;
+        const int kvrow0 = (s.b * a.Hkv + s.h) * a.Pmax;
+        for (int j = s.j0; j < s.j1; ++j, ++kvt) {
+          const int st = kvt % S;
+          if (!ptx::mbar_wait(&kv_empty[st], ((kvt / S) & 1) ^ 1u, abort_flag, kWaitNs)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sk = sKV + st * kStageBytes;
+          uint8_t* sv = sk + kHalves * kKVHalfBytes;
+          ptx::mbar_arrive_expect_tx(&kv_full[st], kStageBytes);
+          for (int hh = 0; hh < kHalves; ++hh) {
+            ptx::tma_load_2d(sk + hh * kKVHalfBytes, &tmK, hh * 64, kvrow0 + j * kBN,
+                             &kv_full[st], pol_kv);
+            ptx::tma_load_2d(sv + hh * kKVHalfBytes, &tmV, hh * 64, kvrow0 + j * kBN,
+                             &kv_full[st], pol_kv);
+          }
+        }
+      }
+      if (!ok) {
+        latch_error(a.ws, MDS_DEV_TIMEOUT);
+        *abort_flag = 1;
+      }
+      // drain: the copies issued last into each stage and into Q have landed
+      for (int i = 0; i < S && i < kvt; ++i) {
+        const int t = kvt - 1 - i;
+        ptx::mbar_wait(&kv_full[t % S], (t / S) & 1, abort_flag, kWaitNs);
+      }
+      if (segc > 0) ptx::mbar_wait(q_full, (segc - 1) & 1, abort_flag, kWaitNs);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer
+    const uint32_t idS = ptx::idesc_bf16(128, kBN);
+    const uint32_t idO = ptx::idesc_bf16(128, DH) | (1u << 16);   // B (V) MN-major
+    int it = 0, kvt = 0, segc = 0;
+    int pv_it = -1, pv_m = 0, pv_stage = 0, pv_first = 0, pv_lastm = 0;   // pending P V
+    bool ok = true;
+    auto wait = [&](uint64_t* bar, uint32_t par) {
+      if (!ok) return false;
+      if (!ptx::mbar_wait(bar, par, abort_flag, kWaitNs)) ok = false;
+      return ok;
+    };
+    // O[m] += P[it % 2] V[stage]
+    auto issue_pv = [&]() {
+      const int pb = pv_it & 1;
+      if (!wait(&p_full[pb], (pv_it >> 1) & 1)) return;
+      ptx::tc_fence_after();
+      if (lane == 0) {
+        const uint32_t aP = ptx::smem_addr(sP + pb * kPBytes);
+        const uint32_t bV = ptx::smem_addr(sKV + pv_stage * kStageBytes + kHalves * kKVHalfBytes);
+        const uint32_t dO = tmem + kOCol0 + (uint32_t)(pv_m * DH);
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          ptx::mma_bf16(dO, ptx::sdesc_k128(aP + kk * 32), sdesc_mn128(bV + kk * 2048, kKVHalfBytes),
+                        idO, (pv_first && kk == 0) ? 0u : 1u);
+        ptx::mma_commit(&p_empty[pb]);
+        if (pv_lastm) ptx::mma_commit(&kv_empty[pv_stage]);
+      }
+      __syncwarp();
+    };
+    Seg s;
+    while (ok && iter.next(a, pre, s)) {
+      if (!wait(q_full, segc & 1)) break;
+      const int Lk = s.Pb + a.N;
+      for (int j = s.j0; j < s.j1 && ok; ++j, ++kvt) {
+        const int st = kvt % S;
+        if (!wait(&kv_full[st], (kvt / S) & 1)) break;
+        const int nv = Lk - j * kBN;
+        if (nv < kBN) {
+          // keys past the unit's end: zero their V rows so that stale cache
+          // contents (never weighted, P = 0) cannot inject NaN into O
+          uint8_t* sv = sKV + st * kStageBytes + kHalves * kKVHalfBytes;
+          for (int hh = 0; hh < kHalves; ++hh)
+            for (int i = nv * 8 + lane; i < kBN * 8; i += 32)
+              reinterpret_cast<uint4*>(sv + hh * kKVHalfBytes)[i] = make_uint4(0, 0, 0, 0);
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        for (int m = 0; m < NM; ++m, ++it) {
+          const int sb = it & 1;
+          if (!wait(&s_empty[sb], ((it >> 1) & 1) ^ 1u)) break;
+          ptx::tc_fence_after();
+          if (lane == 0) {
+            const uint32_t aQ = ptx::smem_addr(sQ + m * kQTileBytes);
+            const uint32_t bK = ptx::smem_addr(sKV + st * kStageBytes);
+            const uint32_t dS = tmem + kSCol0 + (uint32_t)(sb * kBN);
+#pragma unroll
+            for (int kk = 0; kk < DH / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+              const uint32_t offk = (kk >> 2) * kKVHalfBytes + (kk & 3) * 32;
+              ptx::mma_bf16(dS, ptx::sdesc_k128(aQ + off), ptx::sdesc_k128(bK + offk), idS,
+                            kk ? 1u : 0u);
+            }
+            ptx::mma_commit(&s_full[sb]);
+            if (j == s.j1 - 1 && m == NM - 1) ptx::mma_commit(q_empty);
+          }
+          __syncwarp();
+          if (pv_it >= 0) issue_pv();
+          if (!ok) break;
+          // the O tiles are free once the previous segment's epilogue read them
+          if (j == s.j0 && m == 0 && segc > 0 && !wait(o_empty, (segc - 1) & 1)) break;
+          pv_it = it;
+          pv_m = m;
+          pv_stage = st;
+          pv_first = j == s.j0;
+          pv_lastm = m == NM - 1;
+        }
+      }
+      ++segc;
+    }
+    if (ok && pv_it >= 0) issue_pv();
+    if (!ok) {
+      latch_error(a.ws, MDS_DEV_TIMEOUT);
+      *abort_flag = 1;
+    }
+    if (lane == 0) {
+      ptx::mma_commit(done);
+      ptx::mbar_wait(done, 0, abort_flag, kWaitNs);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------- softmax and epilogue
+    const int quarter = warp & 3;
+    const int t = quarter * 32 + lane;                // TMEM lane = row in tile
+    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    const int g = a.g;
+    int it = 0, segc = 0;
+    bool ok = true;
+    auto wait = [&](uint64_t* bar, uint32_t par) {
+      if (!ok) return false;
+      if (!ptx::mbar_wait(bar, par, abort_flag, kWaitNs)) ok = false;
+      return ok;
+    };
+    Seg s;
+    while (ok && iter.next(a, pre, s)) {
+      float mref[kMaxNM], lsum[kMaxNM];
+      uint64_t mw0[kMaxNM], mw1[kMaxNM];
+      bool live[kMaxNM];
+#pragma unroll
+      for (int m = 0; m < kMaxNM; ++m) {
+        mref[m] = -INFINITY;
+        lsum[m] = 0.f;
+        mw0[m] = mw1[m] = 0ull;
+        live[m] = false;
+        if (m < NM) {
+          const int r = (s.mg * NM + m) * 128 + t;
+          if (r < a.Mrows) {
+            const int n = r / g;
+            live[m] = true;
+            mw0[m] = a.mask[(long long)n * a.words];
+            mw1[m] = a.words > 1 ? a.mask[(long long)n * a.words + 1] : 0ull;
+          }
+        }
+      }
+      const int Pb = s.Pb;
+      for (int j = s.j0; j < s.j1 && ok; ++j) {
+        const int key0 = j * kBN;
+        for (int m = 0; m < NM; ++m, ++it) {
+          const int sb = it & 1;
+          if (!wait(&s_full[sb], (it >> 1) & 1)) break;
+          ptx::tc_fence_after();
+          float sv[kBN];
+          {
+            float tmp[32];
+            ptx::tmem_ld32(lane_base + kSCol0 + sb * kBN, tmp);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) sv[c] = tmp[c];
+            ptx::tmem_ld32(lane_base + kSCol0 + sb * kBN + 32, tmp);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) sv[32 + c] = tmp[c];
+          }
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&s_empty[sb]);
+          // mask and scale (log2 domain)
+          float mx = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < kBN; ++c) {
+            const int key = key0 + c;
+            bool valid;
+            if (key < Pb) {
+              valid = true;
+            } else {
+              const int mm = key - Pb;
+              const uint64_t w = mm < 64 ? mw0[m] : mw1[m];
+              valid = mm < a.N && ((w >> (mm & 63)) & 1ull);
+            }
+            valid = valid && live[m];
+            const float x = valid ? sv[c] * a.scale_log2 : -INFINITY;
+            sv[c] = x;
+            mx = fmaxf(mx, x);
+          }
+          const float mold = mref[m];
+          const float mnew = fmaxf(mold, mx);
+          const bool need = mold != -INFINITY && mnew > mold + kRescaleLog2;
+          if (__any_sync(0xffffffffu, need)) {
+            // rescale this tile's O: every earlier P V must be complete.  The
+            // commit on p_empty after P V (it - 1) covers all earlier MMAs;
+            // P V (it - 3) was awaited one item ago, so the phase is exact.
+            if (!wait(&p_empty[(it - 1) & 1], ((it - 1) >> 1) & 1)) break;
+            ptx::tc_fence_after();
+            const float f = need ? ex2(mold - mnew) : 1.f;
+            const uint32_t ocol = lane_base + kOCol0 + (uint32_t)(m * DH);
+#pragma unroll
+            for (int cb = 0; cb < DH / 32; ++cb) {
+              float ov[32];
+              ptx::tmem_ld32(ocol + cb * 32, ov);
+#pragma unroll
+              for (int c = 0; c < 32; ++c) ov[c] *= f;
+              tmem_st32(ocol + cb * 32, ov);
+            }
+            ptx::tc_fence_before();
+            if (need) {
+              lsum[m] *= f;
+              mref[m] = mnew;
+            }
+          }
+          if (mref[m] == -INFINITY) mref[m] = mnew;
+          const float mr = mref[m];
+          // P = 2^(s - m) rounded to bf16; l sums the rounded values
+          uint32_t pk[kBN / 2];
+          float ls = 0.f;
+#pragma unroll
+          for (int c = 0; c < kBN; c += 2) {
+            const float p0 = mr == -INFINITY ? 0.f : ex2(sv[c] - mr);
+            const float p1 = mr == -INFINITY ? 0.f : ex2(sv[c + 1] - mr);
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+            const float2 r2 = __bfloat1622float2(b2);
+            ls += r2.x + r2.y;
+            pk[c / 2] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
+          lsum[m] += ls;
+          if (!wait(&p_empty[sb], ((it >> 1) & 1) ^ 1u)) break;
+          uint8_t* prow = sP + sb * kPBytes + t * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(prow + ((c ^ (t & 7)) << 4)) =
+                make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&p_full[sb]);
+        }
+      }
+      if (!ok) break;
+      // ---- segment epilogue: final rows, or a partial record + merge
+      const bool whole = s.j0 == 0 && s.j1 == s.nt;
+      const long long U1 = s.U0 + s.nt;
+      int slot = 0;
+      if (!whole) slot = 2 * cta + (cta_start(Ttot, a.G, cta) >= s.U0 ? 0 : 1);
+      const int rows_unit = NM * 128;
+      // every P V of the segment is complete once P V (it - 1) is
+      if (!wait(&p_empty[(it - 1) & 1], ((it - 1) >> 1) & 1)) break;
+      ptx::tc_fence_after();
+      for (int m = 0; m < NM && ok; ++m) {
+        const int r = (s.mg * NM + m) * 128 + t;
+        const uint32_t ocol = lane_base + kOCol0 + (uint32_t)(m * DH);
+        if (whole) {
+          const float inv = lsum[m] > 0.f ? 1.f / lsum[m] : 0.f;
+          __nv_bfloat16* dst = nullptr;
+          if (live[m]) {
+            const int n = r / g, jj = r - n * g;
+            dst = a.o + (((long long)s.b * a.N + n) * a.Hq + s.h * g + jj) * DH;
+          }
+#pragma unroll
+          for (int cb = 0; cb < DH / 32; ++cb) {
+            float ov[32];
+            ptx::tmem_ld32(ocol + cb * 32, ov);
+            if (dst) {
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                uint4 pkd;
+                __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(&pkd);
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                  p2[e] = __floats2bfloat162_rn(ov[q * 8 + 2 * e] * inv, ov[q * 8 + 2 * e + 1] * inv);
+                *reinterpret_cast<uint4*>(dst + cb * 32 + q * 8) = pkd;
+              }
+            }
+          }
+        } else {
+          float* po = a.part + ((long long)slot * rows_unit + m * 128 + t) * DH;
+          float* pml = a.part + (long long)2 * a.G * rows_unit * DH +
+                       ((long long)slot * rows_unit + m * 128 + t) * 2;
+#pragma unroll
+          for (int cb = 0; cb < DH / 32; ++cb) {
+            float ov[32];
+            ptx::tmem_ld32(ocol + cb * 32, ov);
+            if (live[m]) {
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                *reinterpret_cast<float4*>(po + cb * 32 + q * 4) =
+                    make_float4(ov[4 * q], ov[4 * q + 1], ov[4 * q + 2], ov[4 * q + 3]);
+            }
+          }
+          if (live[m]) *reinterpret_cast<float2*>(pml) = make_float2(mref[m], lsum[m]);
+        }
+      }
+      if (!ok) break;
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(o_empty);
+      ++segc;
+      if (!whole) {
+        // CTAs covering this unit: c0 (holds the unit's first tile) .. c1
+        // (CTAs with an empty range hold no segment and are skipped)
+        int c0 = (int)((s.U0 * a.G) / Ttot);
+        while (c0 + 1 < a.G && cta_start(Ttot, a.G, c0 + 1) <= s.U0) ++c0;
+        while (c0 > 0 && cta_start(Ttot, a.G, c0) > s.U0) --c0;
+        int c1 = c0;   // one past the last CTA covering the unit
+        while (c1 < a.G && cta_start(Ttot, a.G, c1) < U1) ++c1;
+        int nseg = 0;
+        for (int c = c0; c < c1; ++c)
+          if (cta_start(Ttot, a.G, c + 1) > cta_start(Ttot, a.G, c)) ++nseg;
+        __threadfence();
+        __syncwarp();
+        int prev = 0;
+        if (lane == 0) prev = atomicAdd(&a.counters[c0 * 4 + quarter], 1);
+        prev = __shfl_sync(0xffffffffu, prev, 0);
+        if (prev == nseg - 1) {
+          __threadfence();
+          // this warp merges its 32 rows of every query tile of the unit
+          for (int m = 0; m < NM; ++m) {
+            if (!live[m]) continue;
+            const int r = (s.mg * NM + m) * 128 + t;
+            float M = -INFINITY;
+            for (int c = c0; c < c1; ++c) {
+              if (cta_start(Ttot, a.G, c + 1) == cta_start(Ttot, a.G, c)) continue;
+              const int sl = 2 * c + (cta_start(Ttot, a.G, c) >= s.U0 ? 0 : 1);
+              const float2 ml = __ldcg(reinterpret_cast<const float2*>(
+                  a.part + (long long)2 * a.G * rows_unit * DH +
+                  ((long long)sl * rows_unit + m * 128 + t) * 2));
+              M = fmaxf(M, ml.x);
+            }
+            float L = 0.f;
+            float acc[DH];
+#pragma unroll
+            for (int e = 0; e < DH; ++e) acc[e] = 0.f;
+            for (int c = c0; c < c1; ++c) {
+              if (cta_start(Ttot, a.G, c + 1) == cta_start(Ttot, a.G, c)) continue;
+              const int sl = 2 * c + (cta_start(Ttot, a.G, c) >= s.U0 ? 0 : 1);
+              const float2 ml = __ldcg(reinterpret_cast<const float2*>(
+                  a.part + (long long)2 * a.G * rows_unit * DH +
+                  ((long long)sl * rows_unit + m * 128 + t) * 2));
+              const float w = ml.x == -INFINITY ? 0.f : ex2(ml.x - M);
+              L += w * ml.y;
+              const float4* po = reinterpret_cast<const float4*>(
+                  a.part + ((long long)sl * rows_unit + m * 128 + t) * DH);
+#pragma unroll
+              for (int q = 0; q < DH / 4; ++q) {
+                const float4 v = __ldcg(po + q);
+                acc[4 * q] = fmaf(w, v.x, acc[4 * q]);
+                acc[4 * q + 1] = fmaf(w, v.y, acc[4 * q + 1]);
+                acc[4 * q + 2] = fmaf(w, v.z, acc[4 * q + 2]);
+                acc[4 * q + 3] = fmaf(w, v.w, acc[4 * q + 3]);
+              }
+            }
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+            const int n = r / g, jj = r - n * g;
+            __nv_bfloat16* dst = a.o + (((long long)s.b * a.N + n) * a.Hq + s.h * g + jj) * DH;
+#pragma unroll
+            for (int q = 0; q < DH / 8; ++q) {
+              uint4 pkd;
+              __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(&pkd);
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                p2[e] = __floats2bfloat162_rn(acc[q * 8 + 2 * e] * inv, acc[q * 8 + 2 * e + 1] * inv);
+              *reinterpret_cast<uint4*>(dst + q * 8) = pkd;
+            }
+          }
+          if (lane == 0) a.counters[c0 * 4 + quarter] = 0;
+        }
+      }
+    }
+    if (!ok) {
+      latch_error(a.ws, MDS_DEV_TIMEOUT);
+      *abort_flag = 1;
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 1) ptx::tmem_dealloc(tmem, 512);
+}
+
+// ----------------------------------------------------------------- host
+struct Plan {
+  int NM, n_mg, stages, G;
+  size_t smem;
+};
+
+Plan plan(int N, int g, int dh, int num_sms) {
+  Plan p{};
+  const int mtiles = (N * g + 127) / 128;
+  p.n_mg = (mtiles + kMaxNM - 1) / kMaxNM;
+  p.NM = (mtiles + p.n_mg - 1) / p.n_mg;
+  const size_t q = (size_t)p.NM * 128 * dh * 2;
+  const size_t pbuf = 2 * (size_t)128 * kBN * 2;
+  const size_t stage = 2 * (size_t)kBN * dh * 2;
+  const size_t fixed = 1024 /*align*/ + 34 * 8 + (kMaxBAttn + 1) * 4;
+  int st = (int)((kSmemLimit - q - pbuf - fixed) / stage);
+  p.stages = st > 6 ? 6 : st;
+  p.smem = q + pbuf + (size_t)p.stages * stage + fixed;
+  p.G = num_sms < kMaxCtaAttn ? num_sms : kMaxCtaAttn;
+  return p;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode_attn = nullptr;
+int g_sms_attn = 0;
+bool g_attr_set[2][kMaxNM + 1] = {};
+
+template <int DH, int NM>
+int launch_one(const Plan& p, const CUtensorMap& mq, const CUtensorMap& mk,
+               const CUtensorMap& mv, const AttnArgs& a, cudaStream_t st);
+
+template <int DH>
+int launch_nm(const Plan& p, const CUtensorMap& mq, const CUtensorMap& mk,
+              const CUtensorMap& mv, const AttnArgs& a, cudaStream_t st) {
+  switch (a.NM) {
+    case 1: return launch_one<DH, 1>(p, mq, mk, mv, a, st);
+    case 2: return launch_one<DH, 2>(p, mq, mk, mv, a, st);
+    case 3: return launch_one<DH, 3>(p, mq, mk, mv, a, st);
+    default: return MDS_EUNSUPPORTED;
+  }
+}
+
+int make_map_attn(CUtensorMap* m, const void* base, long long rows, int cols, int box_rows) {
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  const CUresult r = g_encode_attn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+                                   dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MDS_OK : MDS_ECUDA;
+}
+
+template <int DH, int NM>
+int launch_one(const Plan& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+               const AttnArgs& a, cudaStream_t st) {
+  bool& set = g_attr_set[DH == 128 ? 1 : 0][NM];
+  if (!set) {
+    if (cudaFuncSetAttribute(k_tree_attention_tc<DH, NM>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit) != cudaSuccess)
+      return MDS_ECUDA;
+    set = true;
+  }
+  k_tree_attention_tc<DH, NM><<<p.G, kThreads, p.smem, st>>>(mq, mk, mv, a);
+  return MDS_OK;
+}
+
+}  // namespace
+
+size_t attention_tc_partial_bytes(int N, int g, int dh) {
+  const Plan p = plan(N, g, dh, kMaxCtaAttn);
+  const size_t rows = (size_t)p.NM * 128;
+  return 2 * (size_t)kMaxCtaAttn * rows * (dh + 2) * 4;
+}
+
+int attention_tc_supported(int B, int N, int g, int dh) {
+  if (dh != 64 && dh != 128) return 0;
+  if (B > kMaxBAttn) return 0;
+  const Plan p = plan(N, g, dh, kMaxCtaAttn);
+  return p.stages >= 2 ? 1 : 0;
+}
+
+int attention_tc(int B, int N, int Hq, int Hkv, int dh, int Pmax, const int32_t* P,
+                 const uint64_t* mask, int words, const void* q, const void* Kc, const void* Vc,
+                 void* o, void* partial, void* ws, cudaStream_t st) {
+  if (!g_encode_attn) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &qr) != cudaSuccess ||
+        qr != cudaDriverEntryPointSuccess || !fn)
+      return MDS_ECUDA;
+    g_encode_attn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  if (!g_sms_attn) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MDS_ECUDA;
+    if (cudaDeviceGetAttribute(&g_sms_attn, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return MDS_ECUDA;
+  }
+  const int gq = Hq / Hkv;
+  if (!attention_tc_supported(B, N, gq, dh)) return MDS_EUNSUPPORTED;
+  const Plan p = plan(N, gq, dh, g_sms_attn);
+  AttnArgs a{};
+  a.B = B;
+  a.N = N;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.g = gq;
+  a.Pmax = Pmax;
+  a.Mrows = N * gq;
+  a.NM = p.NM;
+  a.n_mg = p.n_mg;
+  a.stages = p.stages;
+  a.G = p.G;
+  a.scale_log2 = 1.4426950408889634f / sqrtf((float)dh);
+  a.P = P;
+  a.mask = mask;
+  a.words = words;
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.part = static_cast<float*>(partial);
+  a.counters = reinterpret_cast<int*>(static_cast<char*>(ws) + kWsAttnCounters);
+  a.ws = ws;
+  CUtensorMap mq, mk, mv;
+  int rc = make_map_attn(&mq, q, (long long)B * Hkv * a.Mrows, dh, 128);
+  if (rc) return rc;
+  rc = make_map_attn(&mk, Kc, (long long)B * Hkv * Pmax, dh, kBN);
+  if (rc) return rc;
+  rc = make_map_attn(&mv, Vc, (long long)B * Hkv * Pmax, dh, kBN);
+  if (rc) return rc;
+  rc = dh == 128 ? launch_nm<128>(p, mq, mk, mv, a, st) : launch_nm<64>(p, mq, mk, mv, a, st);
+  if (rc) return rc;
+  MDS_LAUNCH_CHECK();
+  return MDS_OK;
+}
+
+}  // namespace mds

@@ -19,7 +19,8 @@
 //   STORE   Y -> bf16 out                                   (Wo projection)
 //   HEADS   U[b,1+i,j] = h[b,j] + SiLU(Y[b, i d + j])       ("Medusa deep dive",
 //           "The heads are residual blocks, not linear layers"); U[b,0] = h
-//   QKV     q rows -> q buffer, k/v rows -> KV-cache slot P_b + n
+//   QKV     q -> q buffer [B, Hkv, N g, dh] (the tree-attention kernel's
+//           layout), k/v rows -> KV-cache slot P_b + n
 //   DRAFT   per row running top-8 (value desc, id asc) over the CTA's range
 //           ("From top-k heads to a sparse candidate tree")
 //   VERIFY  per row running max / argmax / sum e^(z-m) / sum z e^(z-m)
@@ -127,7 +128,12 @@ __device__ __forceinline__ void epi_qkv(const TcArgs& a, int r, int f0, int nv,
     if (j >= nv) break;
     const int f = f0 + j;
     if (f < qd) {
-      static_cast<__nv_bfloat16*>(a.out)[(long long)r * qd + f] = __float2bfloat16_rn(v[j]);
+      // q in the attention kernel's layout [B, Hkv, N * g, dh]
+      const int g = a.Hq / a.Hkv;
+      const int hq = f / a.dh, c = f - hq * a.dh;
+      const int hk = hq / g, jj = hq - hk * g;
+      static_cast<__nv_bfloat16*>(a.out)[(((long long)b * a.Hkv + hk) * a.N * g + n * g + jj) * a.dh + c] =
+          __float2bfloat16_rn(v[j]);
     } else if (!cache_ok) {
       bad = true;
     } else {

@@ -68,6 +68,14 @@ int accept_path(int B, int N, int K, int mode, float eps, float delta, const int
 int compact(int dtype, int B, int Hkv, int dh, int Pmax, int K, const int32_t* L,
             const int32_t* path, void* Kc, void* Vc, int32_t* P, void* ws, cudaStream_t st);
 
+// Tree attention on tcgen05 (bf16).  q is laid out [B, Hkv, N * g, dh]
+// (row n * g + j = query head h * g + j of tree row n); o is [B, N, Hq, dh].
+size_t attention_tc_partial_bytes(int N, int g, int dh);
+int attention_tc_supported(int B, int N, int g, int dh);
+int attention_tc(int B, int N, int Hq, int Hkv, int dh, int Pmax, const int32_t* P,
+                 const uint64_t* mask, int words, const void* q, const void* Kc, const void* Vc,
+                 void* o, void* partial, void* ws, cudaStream_t st);
+
 // Tensor-core (tcgen05) path, bf16 inputs.
 size_t tc_partial_bytes(int R, bool draft);
 int gemm_tc_heads(const void* h, int B, const void* W, int K, int d, void* U, void* ws,

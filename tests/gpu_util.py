@@ -48,6 +48,14 @@ def f64_bits(arr: np.ndarray, dtype: str) -> np.ndarray:
     return ms.as_f64(arr, dtype)
 
 
+def bf16_ulp(x: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 values (8 significant bits) at |x|: 2^(e - 7) for
+    |x| in [2^e, 2^(e+1))."""
+    ax = np.abs(np.asarray(x, np.float64))
+    e = np.floor(np.log2(np.maximum(ax, 2.0 ** -126)))
+    return np.ldexp(1.0, (e - 7).astype(int))
+
+
 def close_float(got: np.ndarray, want: np.ndarray, dtype: str, kind: str, what: str = ""):
     """kind: 'logit' | 'attn' | 'stored' (a bf16-stored intermediate)."""
     got = np.asarray(got, np.float64)
@@ -63,8 +71,12 @@ def close_float(got: np.ndarray, want: np.ndarray, dtype: str, kind: str, what: 
         assert float(err.max()) <= BF16_LOGIT_ATOL, (what, float(err.max()))
         return float(err.max())
     if kind == "attn":
+        # o and y are stored as bf16 on both sides (rounded at the same
+        # point); the 1e-2 bound applies before that rounding, and a value
+        # at a rounding boundary may land one bf16 unit apart after it.
         err = np.abs(got - want)
-        assert float(err.max()) <= BF16_ATTN_ATOL, (what, float(err.max()))
+        lim = BF16_ATTN_ATOL + bf16_ulp(want)
+        assert not (err > lim).any(), (what, float(err.max()), float((err - lim).max()))
         return float(err.max())
     # bf16-stored value: both sides round to bf16 at the same point; a
     # rounding-boundary flip moves the value by one bf16 unit (<= 2^-7 of it).

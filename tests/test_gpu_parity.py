@@ -201,6 +201,47 @@ def test_tree_attention_token_fill(mds, w):
     check_attention(w, g, f, x["P"], want, list(range(w.B)))
 
 
+# Edge cases of the tensor-core tree attention: an empty prefix (tree rows
+# only), a prefix that fills the cache to capacity, stale NaN cache slots past
+# the tree (never weighted, must not reach the output), and prefix keys whose
+# scores grow along the sequence (the running maximum rises by far more than
+# the lazy-rescale threshold).  One shape per query-tile count: g = 1 (one
+# tile), g = 2 with dh = 64 (two tiles), g = 4 (three tiles).
+EDGE = [
+    ms.Workload("edge-g1", "bf16", B=3, d=256, V=500, Hq=2, Hkv=2, dh=128, K=4,
+                shortlist=(4, 3, 2, 2), max_rank_sum=-1, P=(0, 900), accept="typical", seed=21),
+    ms.Workload("edge-g2-dh64", "bf16", B=3, d=256, V=500, Hq=4, Hkv=2, dh=64, K=4,
+                shortlist=(4, 3, 2, 2), max_rank_sum=-1, P=(0, 900), accept="typical", seed=22),
+    ms.Workload("edge-g4", "bf16", B=3, d=512, V=500, Hq=8, Hkv=2, dh=128, K=5,
+                shortlist=(8, 4, 2, 2, 1), max_rank_sum=3, P=(0, 900), accept="typical", seed=23),
+    # about 8 key tiles per CTA: segments that span several tiles
+    ms.Workload("edge-multitile", "bf16", B=4, d=256, V=500, Hq=8, Hkv=8, dh=128, K=4,
+                shortlist=(4, 3, 2, 2), max_rank_sum=-1, P=(3000, 4000), accept="typical",
+                seed=24),
+]
+
+
+@pytest.mark.parametrize("w", EDGE, ids=lambda w: w.name)
+def test_tree_attention_edges(mds, w):
+    x = ms.make_inputs(w)
+    N = oracle.build_tree(w.shortlist, w.max_rank_sum)["N"]
+    P = x["P"].copy()
+    P[:3] = [0, 700, w.pmax - N]
+    x["P"] = P
+    kc = ms.bits_to_f32(x["kc"]).copy()
+    ramp = 1.0 + 3.0 * np.arange(P[1], dtype=np.float32) / P[1]
+    kc[1, :, :P[1], :] *= ramp[None, :, None]
+    x["kc"] = ms.bf16_bits(kc)
+    nan_bf16 = np.uint16(0x7FC0)
+    for b in range(w.B):
+        x["kc"][b, :, P[b] + N:, :] = nan_bf16
+        x["vc"][b, :, P[b] + N:, :] = nan_bf16
+    tok = ms.random_tokens(w.seed, w.B, N, w.V)
+    g = run_attention(mds, w, x, tok)
+    assert np.isfinite(g["o"]).all() and np.isfinite(g["y"]).all()
+    check_attention(w, g, f64_inputs(w, x), P, tok.astype(np.int64), list(range(w.B)))
+
+
 # ---------------------------------------------------------------------------
 # lm_verify
 # ---------------------------------------------------------------------------
