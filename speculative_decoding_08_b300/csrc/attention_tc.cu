@@ -28,9 +28,8 @@
 // The running max is raised lazily: O is rescaled only when a row's maximum
 // grows by more than 2^8, so the accumulator in TMEM is rarely touched; the
 // final O / l is exact for any reference value.  A unit whose tiles span
-// several CTAs leaves one partial (O, m, l) per CTA; the last CTA to finish
-// (an atomic counter per unit and row quarter) merges them.  No CTA ever
-// waits for another.
+// several CTAs leaves one partial (O, m, l) per CTA; a second kernel, one
+// warp per (unit, row), merges them.  No CTA ever waits for another.
 //
 // Warp roles (192 threads): warp 0 TMA producer, warp 1 TMEM owner and MMA
 // issuer, warps 2..5 softmax / epilogue (thread = TMEM lane = query row).
@@ -68,7 +67,6 @@ struct AttnArgs {
   int words;
   __nv_bfloat16* o;       // [B, N, Hq, dh]
   float* part;            // partial records
-  int* counters;          // [kMaxCtaAttn * 4]
   void* ws;
 };
 
@@ -290,6 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (segc > 0) ptx::mbar_wait(q_full, (segc - 1) & 1, abort_flag, kWaitNs);
     }
+    __syncwarp();   // the warp reaches the final barrier converged
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer
     const uint32_t idS = ptx::idesc_bf16(128, kBN);
@@ -434,24 +433,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tc_fence_before();
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive(&s_empty[sb]);
-          // mask and scale (log2 domain)
+          // mask; the row maximum is taken on raw scores (scale > 0)
           float mx = -INFINITY;
+          if (key0 + kBN <= Pb) {
+            // a tile inside the prefix: every key is visible to live rows
+            if (!live[m]) {
 #pragma unroll
-          for (int c = 0; c < kBN; ++c) {
-            const int key = key0 + c;
-            bool valid;
-            if (key < Pb) {
-              valid = true;
-            } else {
+              for (int c = 0; c < kBN; ++c) sv[c] = -INFINITY;
+            }
+#pragma unroll
+            for (int c = 0; c < kBN; ++c) mx = fmaxf(mx, sv[c]);
+          } else {
+#pragma unroll
+            for (int c = 0; c < kBN; ++c) {
+              const int key = key0 + c;
               const int mm = key - Pb;
               const uint64_t w = mm < 64 ? mw0[m] : mw1[m];
-              valid = mm < a.N && ((w >> (mm & 63)) & 1ull);
+              const bool valid = live[m] && (key < Pb || (mm < a.N && ((w >> (mm & 63)) & 1ull)));
+              sv[c] = valid ? sv[c] : -INFINITY;
+              mx = fmaxf(mx, sv[c]);
             }
-            valid = valid && live[m];
-            const float x = valid ? sv[c] * a.scale_log2 : -INFINITY;
-            sv[c] = x;
-            mx = fmaxf(mx, x);
           }
+          mx *= a.scale_log2;
           const float mold = mref[m];
           const float mnew = fmaxf(mold, mx);
           const bool need = mold != -INFINITY && mnew > mold + kRescaleLog2;
@@ -482,10 +485,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           // P = 2^(s - m) rounded to bf16; l sums the rounded values
           uint32_t pk[kBN / 2];
           float ls = 0.f;
+          const float sc = a.scale_log2;
+          const float nmr = mr == -INFINITY ? 0.f : -mr;
 #pragma unroll
           for (int c = 0; c < kBN; c += 2) {
-            const float p0 = mr == -INFINITY ? 0.f : ex2(sv[c] - mr);
-            const float p1 = mr == -INFINITY ? 0.f : ex2(sv[c + 1] - mr);
+            // 2^(s * scale - m); masked keys (s = -inf) give 0
+            const float p0 = mr == -INFINITY ? 0.f : ex2(fmaf(sv[c], sc, nmr));
+            const float p1 = mr == -INFINITY ? 0.f : ex2(fmaf(sv[c + 1], sc, nmr));
             const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
             const float2 r2 = __bfloat1622float2(b2);
             ls += r2.x + r2.y;
@@ -504,9 +510,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      // ---- segment epilogue: final rows, or a partial record + merge
+      // ---- segment epilogue: final rows, or a partial record that the
+      //      merge kernel combines with the unit's other segments
       const bool whole = s.j0 == 0 && s.j1 == s.nt;
-      const long long U1 = s.U0 + s.nt;
       int slot = 0;
       if (!whole) slot = 2 * cta + (cta_start(Ttot, a.G, cta) >= s.U0 ? 0 : 1);
       const int rows_unit = NM * 128;
@@ -562,76 +568,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(o_empty);
       ++segc;
-      if (!whole) {
-        // CTAs covering this unit: c0 (holds the unit's first tile) .. c1
-        // (CTAs with an empty range hold no segment and are skipped)
-        int c0 = (int)((s.U0 * a.G) / Ttot);
-        while (c0 + 1 < a.G && cta_start(Ttot, a.G, c0 + 1) <= s.U0) ++c0;
-        while (c0 > 0 && cta_start(Ttot, a.G, c0) > s.U0) --c0;
-        int c1 = c0;   // one past the last CTA covering the unit
-        while (c1 < a.G && cta_start(Ttot, a.G, c1) < U1) ++c1;
-        int nseg = 0;
-        for (int c = c0; c < c1; ++c)
-          if (cta_start(Ttot, a.G, c + 1) > cta_start(Ttot, a.G, c)) ++nseg;
-        __threadfence();
-        __syncwarp();
-        int prev = 0;
-        if (lane == 0) prev = atomicAdd(&a.counters[c0 * 4 + quarter], 1);
-        prev = __shfl_sync(0xffffffffu, prev, 0);
-        if (prev == nseg - 1) {
-          __threadfence();
-          // this warp merges its 32 rows of every query tile of the unit
-          for (int m = 0; m < NM; ++m) {
-            if (!live[m]) continue;
-            const int r = (s.mg * NM + m) * 128 + t;
-            float M = -INFINITY;
-            for (int c = c0; c < c1; ++c) {
-              if (cta_start(Ttot, a.G, c + 1) == cta_start(Ttot, a.G, c)) continue;
-              const int sl = 2 * c + (cta_start(Ttot, a.G, c) >= s.U0 ? 0 : 1);
-              const float2 ml = __ldcg(reinterpret_cast<const float2*>(
-                  a.part + (long long)2 * a.G * rows_unit * DH +
-                  ((long long)sl * rows_unit + m * 128 + t) * 2));
-              M = fmaxf(M, ml.x);
-            }
-            float L = 0.f;
-            float acc[DH];
-#pragma unroll
-            for (int e = 0; e < DH; ++e) acc[e] = 0.f;
-            for (int c = c0; c < c1; ++c) {
-              if (cta_start(Ttot, a.G, c + 1) == cta_start(Ttot, a.G, c)) continue;
-              const int sl = 2 * c + (cta_start(Ttot, a.G, c) >= s.U0 ? 0 : 1);
-              const float2 ml = __ldcg(reinterpret_cast<const float2*>(
-                  a.part + (long long)2 * a.G * rows_unit * DH +
-                  ((long long)sl * rows_unit + m * 128 + t) * 2));
-              const float w = ml.x == -INFINITY ? 0.f : ex2(ml.x - M);
-              L += w * ml.y;
-              const float4* po = reinterpret_cast<const float4*>(
-                  a.part + ((long long)sl * rows_unit + m * 128 + t) * DH);
-#pragma unroll
-              for (int q = 0; q < DH / 4; ++q) {
-                const float4 v = __ldcg(po + q);
-                acc[4 * q] = fmaf(w, v.x, acc[4 * q]);
-                acc[4 * q + 1] = fmaf(w, v.y, acc[4 * q + 1]);
-                acc[4 * q + 2] = fmaf(w, v.z, acc[4 * q + 2]);
-                acc[4 * q + 3] = fmaf(w, v.w, acc[4 * q + 3]);
-              }
-            }
-            const float inv = L > 0.f ? 1.f / L : 0.f;
-            const int n = r / g, jj = r - n * g;
-            __nv_bfloat16* dst = a.o + (((long long)s.b * a.N + n) * a.Hq + s.h * g + jj) * DH;
-#pragma unroll
-            for (int q = 0; q < DH / 8; ++q) {
-              uint4 pkd;
-              __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(&pkd);
-#pragma unroll
-              for (int e = 0; e < 4; ++e)
-                p2[e] = __floats2bfloat162_rn(acc[q * 8 + 2 * e] * inv, acc[q * 8 + 2 * e + 1] * inv);
-              *reinterpret_cast<uint4*>(dst + q * 8) = pkd;
-            }
-          }
-          if (lane == 0) a.counters[c0 * 4 + quarter] = 0;
-        }
-      }
     }
     if (!ok) {
       latch_error(a.ws, MDS_DEV_TIMEOUT);
@@ -643,6 +579,86 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   if (warp == 1) ptx::tmem_dealloc(tmem, 512);
+}
+
+// --------------------------------------------------------------- merge
+// One warp per (unit, query row) of the units whose key tiles were split over
+// several CTAs (units covered by one CTA were written by the main kernel):
+//   o = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s,   M = max_s m_s.
+// The partition is recomputed from P exactly as the main kernel computes it.
+template <int DH>
+__global__ void __launch_bounds__(256) k_attention_merge(AttnArgs a) {
+  __shared__ int pre[kMaxBAttn + 1];
+  for (int b = threadIdx.x; b < a.B; b += blockDim.x) pre[b + 1] = a.Hkv * a.n_mg * tiles_of(a, a.P[b]);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    pre[0] = 0;
+    for (int b = 0; b < a.B; ++b) pre[b + 1] += pre[b];
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int u = blockIdx.x;
+  const int mg = u % a.n_mg, bh = u / a.n_mg;
+  const int h = bh % a.Hkv, b = bh / a.Hkv;
+  const int nt = tiles_of(a, a.P[b]);
+  const int rows_unit = a.NM * 128;
+  const int rloc = blockIdx.y * 8 + warp;
+  const int r = mg * rows_unit + rloc;
+  if (nt == 0 || rloc >= rows_unit || r >= a.Mrows) return;
+  const long long Ttot = pre[a.B];
+  const long long U0 = (long long)pre[b] + (long long)(h * a.n_mg + mg) * nt;
+  const long long U1 = U0 + nt;
+  int c0 = (int)((U0 * a.G) / Ttot);
+  while (c0 + 1 < a.G && cta_start(Ttot, a.G, c0 + 1) <= U0) ++c0;
+  while (c0 > 0 && cta_start(Ttot, a.G, c0) > U0) --c0;
+  int c1 = c0;
+  while (c1 < a.G && cta_start(Ttot, a.G, c1) < U1) ++c1;
+  int nseg = 0;
+  for (int c = c0; c < c1; ++c)
+    if (cta_start(Ttot, a.G, c + 1) > cta_start(Ttot, a.G, c)) ++nseg;
+  if (nseg <= 1) return;
+  const float* pml = a.part + (long long)2 * a.G * rows_unit * DH;
+  float M = -INFINITY;
+  for (int c = c0; c < c1; ++c) {
+    if (cta_start(Ttot, a.G, c + 1) == cta_start(Ttot, a.G, c)) continue;
+    const int sl = 2 * c + (cta_start(Ttot, a.G, c) >= U0 ? 0 : 1);
+    M = fmaxf(M, __ldcg(reinterpret_cast<const float2*>(pml) + (long long)sl * rows_unit + rloc).x);
+  }
+  constexpr int E = DH / 32;                 // elements per lane
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  float L = 0.f;
+  for (int c = c0; c < c1; ++c) {
+    if (cta_start(Ttot, a.G, c + 1) == cta_start(Ttot, a.G, c)) continue;
+    const int sl = 2 * c + (cta_start(Ttot, a.G, c) >= U0 ? 0 : 1);
+    const float2 ml = __ldcg(reinterpret_cast<const float2*>(pml) + (long long)sl * rows_unit + rloc);
+    const float* po = a.part + ((long long)sl * rows_unit + rloc) * DH + lane * E;
+    float v[E];
+    if (E == 4) {
+      const float4 q = __ldcg(reinterpret_cast<const float4*>(po));
+      v[0] = q.x; v[1] = q.y; v[2 % E] = q.z; v[3 % E] = q.w;
+    } else {
+      const float2 q = __ldcg(reinterpret_cast<const float2*>(po));
+      v[0] = q.x; v[1 % E] = q.y;
+    }
+    const float w = ml.x == -INFINITY ? 0.f : ex2(ml.x - M);
+    L = fmaf(w, ml.y, L);
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = fmaf(w, v[e], acc[e]);
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  const int n = r / a.g, jj = r - n * a.g;
+  __nv_bfloat16* dst = a.o + (((long long)b * a.N + n) * a.Hq + h * a.g + jj) * DH + lane * E;
+  if (E == 4) {
+    uint2 pk;
+    __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(&pk);
+    p2[0] = __floats2bfloat162_rn(acc[0] * inv, acc[1 % E] * inv);
+    p2[1] = __floats2bfloat162_rn(acc[2 % E] * inv, acc[3 % E] * inv);
+    *reinterpret_cast<uint2*>(dst) = pk;
+  } else {
+    *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(acc[0] * inv, acc[1 % E] * inv);
+  }
 }
 
 // ----------------------------------------------------------------- host
@@ -766,7 +782,6 @@ int attention_tc(int B, int N, int Hq, int Hkv, int dh, int Pmax, const int32_t*
   a.words = words;
   a.o = static_cast<__nv_bfloat16*>(o);
   a.part = static_cast<float*>(partial);
-  a.counters = reinterpret_cast<int*>(static_cast<char*>(ws) + kWsAttnCounters);
   a.ws = ws;
   CUtensorMap mq, mk, mv;
   int rc = make_map_attn(&mq, q, (long long)B * Hkv * a.Mrows, dh, 128);
@@ -777,6 +792,12 @@ int attention_tc(int B, int N, int Hq, int Hkv, int dh, int Pmax, const int32_t*
   if (rc) return rc;
   rc = dh == 128 ? launch_nm<128>(p, mq, mk, mv, a, st) : launch_nm<64>(p, mq, mk, mv, a, st);
   if (rc) return rc;
+  MDS_LAUNCH_CHECK();
+  const dim3 mgrid(B * Hkv * p.n_mg, p.NM * 16);
+  if (dh == 128)
+    k_attention_merge<128><<<mgrid, 256, 0, st>>>(a);
+  else
+    k_attention_merge<64><<<mgrid, 256, 0, st>>>(a);
   MDS_LAUNCH_CHECK();
   return MDS_OK;
 }

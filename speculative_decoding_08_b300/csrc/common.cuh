@@ -12,12 +12,10 @@ namespace mds {
 // Workspace layout (bytes from the workspace base; the base is 256-aligned):
 //   [0, 4)        latched device status word (int32)
 //   [256, 4352)   per-sequence counters used by "last block finishes" merges
-//   [4352, 8192)  tree-attention merge counters (CTA x row quarter)
 //   [8192, ...)   scratch regions, each 256-aligned, owned by one call
 // Counters return to zero at the end of every launch that uses them.
 constexpr size_t kWsStatus = 0;
 constexpr size_t kWsCounters = 256;
-constexpr size_t kWsAttnCounters = 4352;
 constexpr size_t kWsScratch = 8192;
 constexpr int kMaxN = 128;
 constexpr int kMaxK = 8;

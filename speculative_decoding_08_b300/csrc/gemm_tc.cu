@@ -6,8 +6,14 @@
 // The decode-time shapes are skinny: few rows (1..~5700) against a weight
 // matrix that is streamed once from HBM (the heads' W, the LM projection,
 // Wqkv, Wo).  Each CTA owns a contiguous range of weight rows (features),
-// split evenly over the SMs in units of 16, and streams it through a
-// 4-stage TMA ring; X tiles (the rows) are re-read from L2.  One thread
+// split evenly over the SMs in units of 16, and streams it through a TMA
+// ring as deep as shared memory allows; X tiles (the rows) are re-read from
+// L2.  With at most 128 rows the MMA reads a 128-row X tile of which only
+// the first R rows matter (the other accumulator rows are never read), so the
+// X tiles of consecutive stages overlap: stage s starts ceil(R/8) KB after
+// stage s-1 and its don't-care rows are the next stages' data.  A stage then
+// costs ceil(R/8) KB of X plus the CTA's W tile, and the ring holds 2-4x
+// more weight bytes in flight than with whole 16 KB X tiles.  One thread
 // issues tcgen05.mma with M = 128 rows (X) and N = up to 256 features (W);
 // the fp32 accumulators live in tensor memory, double-buffered so that the
 // epilogue of one feature chunk overlaps the MMAs of the next.
@@ -37,11 +43,11 @@
 namespace mds {
 namespace {
 
-constexpr int kStages = 4;
-constexpr int kStageBytes = 48 * 1024;
+constexpr int kMaxStages = 16;
 constexpr int kThreads = 192;
 constexpr int kTmemCols = 512;
-constexpr int kSmemBytes = kStages * kStageBytes + 2048;
+constexpr int kSmemBytes = 232448;                  // 227 KB, the opt-in maximum
+constexpr int kBarBytes = 512;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
 constexpr int kBoxF = 16;                           // weight rows per TMA box
 constexpr int kMaxCta = 256;                        // partial records per row
@@ -50,6 +56,11 @@ struct TcArgs {
   int R, F, Kd;
   int n_units, n_cta;
   int G, NC;
+  int stages;       // TMA ring depth
+  int px;           // bytes between the X tiles of consecutive stages
+  int xregion;      // bytes of the X region (stages * px + tail)
+  int wst;          // bytes of one stage's W tile
+  int xbox;         // X rows per TMA box
   int n_rgroups;
   int kind;
   void* out;
@@ -225,13 +236,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  const int S = a.stages;
+  uint8_t* sXr = smem;                                   // X region
+  uint8_t* sWr = smem + a.xregion;                       // W region
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sWr + S * a.wst);
   uint64_t* full = bars;
-  uint64_t* empty = bars + kStages;
-  uint64_t* tfull = bars + 2 * kStages;
-  uint64_t* tempty = bars + 2 * kStages + 2;
-  uint64_t* done = bars + 2 * kStages + 4;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
+  uint64_t* empty = bars + kMaxStages;
+  uint64_t* tfull = bars + 2 * kMaxStages;
+  uint64_t* tempty = bars + 2 * kMaxStages + 2;
+  uint64_t* done = bars + 2 * kMaxStages + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kMaxStages + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -240,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nkb = a.Kd / 64;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       ptx::mbar_init(&full[s], 1);
       ptx::mbar_init(&empty[s], 1);
     }
@@ -267,9 +281,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_x = ptx::policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t issued_phase[kStages];
-      bool issued[kStages];
-      for (int s = 0; s < kStages; ++s) issued[s] = false, issued_phase[s] = 0;
+      uint32_t issued_phase[kMaxStages];
+      bool issued[kMaxStages];
+      for (int s = 0; s < kMaxStages; ++s) issued[s] = false, issued_phase[s] = 0;
       bool ok = true;
       for (int g0 = 0; g0 < a.n_rgroups && ok; ++g0) {
         const int row0 = g0 * 128 * a.G;
@@ -279,14 +293,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int fc = rg.f_begin + ch * a.NC;
           const int len = min(a.NC, rg.f_end - fc);
           const int nbox = (len + kBoxF - 1) / kBoxF;
-          const uint32_t bytes = (uint32_t)Geff * 128 * 128 + (uint32_t)nbox * kBoxF * 128;
+          const uint32_t xbytes = a.G == 1 ? (uint32_t)a.xbox * 128 : (uint32_t)Geff * 128 * 128;
+          const uint32_t bytes = xbytes + (uint32_t)nbox * kBoxF * 128;
           for (int kb = 0; kb < nkb; ++kb) {
             if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, kWaitLimitNs)) {
               ok = false;
               break;
             }
-            uint8_t* sA = smem + stage * kStageBytes;
-            uint8_t* sB = sA + a.G * 16384;
+            uint8_t* sA = sXr + stage * a.px;
+            uint8_t* sB = sWr + stage * a.wst;
             ptx::mbar_arrive_expect_tx(&full[stage], bytes);
             for (int g = 0; g < Geff; ++g)
               ptx::tma_load_2d(sA + g * 16384, &tmX, kb * 64, row0 + g * 128, &full[stage], pol_x);
@@ -295,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                pol_w);
             issued[stage] = true;
             issued_phase[stage] = phase;
-            if (++stage == kStages) {
+            if (++stage == S) {
               stage = 0;
               phase ^= 1u;
             }
@@ -307,9 +322,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 1;
       }
       // drain: every issued copy has landed before the CTA can exit
-      for (int s = 0; s < kStages; ++s)
+      for (int s = 0; s < S; ++s)
         if (issued[s]) ptx::mbar_wait(&full[s], issued_phase[s], abort_flag, kWaitLimitNs);
     }
+    __syncwarp();   // the warp reaches the final barrier converged
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer
     if (lane == 0) {
@@ -338,8 +354,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             ptx::tc_fence_after();
-            const uint32_t sA = ptx::smem_addr(smem + stage * kStageBytes);
-            const uint32_t sB = sA + a.G * 16384;
+            const uint32_t sA = ptx::smem_addr(sXr + stage * a.px);
+            const uint32_t sB = ptx::smem_addr(sWr + stage * a.wst);
             for (int g = 0; g < Geff; ++g) {
               const uint32_t dcol = tmem_base + (uint32_t)(acc * a.G * a.NC + g * a.NC);
 #pragma unroll
@@ -350,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
             ptx::mma_commit(&empty[stage]);
-            if (++stage == kStages) {
+            if (++stage == S) {
               stage = 0;
               phase ^= 1u;
             }
@@ -366,6 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mma_commit(done);
       ptx::mbar_wait(done, 0, abort_flag, kWaitLimitNs);
     }
+    __syncwarp();
   } else {
     // --------------------------------------------------------- epilogue
     const int quarter = warp & 3;
@@ -501,51 +518,109 @@ __global__ void __launch_bounds__(256) k_verify_merge(const float4* __restrict__
   }
 }
 
-// One warp per head row (b, i): top s_i of the per-CTA candidate lists by
-// repeated extraction in (value desc, id asc) order.
+// One block per head row (b, i): top s_i of the per-CTA candidate lists.
+// Each thread keeps a sorted top-8 of the entries it scans; each warp then
+// extracts its top-8 by repeated warp-wide maxima, and warp 0 extracts the
+// row's top s_i from the warps' lists.  Order: value desc, id asc.
+__device__ __forceinline__ void top8_insert(float (&v)[kMaxS], int (&id)[kMaxS], float x, int i) {
+  if (!ranks_before(x, i, v[kMaxS - 1], id[kMaxS - 1])) return;
+#pragma unroll
+  for (int j = 0; j < kMaxS; ++j) {
+    if (ranks_before(x, i, v[j], id[j])) {
+      const float tv = v[j];
+      const int ti = id[j];
+      v[j] = x;
+      id[j] = i;
+      x = tv;
+      i = ti;
+    }
+  }
+}
+
+// Warp-wide extraction of the best `count` entries from per-lane sorted
+// lists (heads at position `pos`); the result is valid in every lane.
+__device__ __forceinline__ void warp_extract(const float (&v)[kMaxS], const int (&id)[kMaxS],
+                                             int count, float* out_v, int* out_id) {
+  int pos = 0;
+  const int lane = threadIdx.x & 31;
+  for (int t = 0; t < count; ++t) {
+    float hv = -INFINITY;
+    int hid = 0x7fffffff;
+#pragma unroll
+    for (int j = 0; j < kMaxS; ++j)
+      if (j == pos) {
+        hv = v[j];
+        hid = id[j];
+      }
+    float bv = hv;
+    int bid = hid, bl = lane;
+    for (int o = 16; o; o >>= 1) {
+      const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int i2 = __shfl_xor_sync(0xffffffffu, bid, o);
+      const int l2 = __shfl_xor_sync(0xffffffffu, bl, o);
+      if (ranks_before(v2, i2, bv, bid) || (v2 == bv && i2 == bid && l2 < bl)) {
+        bv = v2;
+        bid = i2;
+        bl = l2;
+      }
+    }
+    if (lane == bl) ++pos;
+    out_v[t] = bv;
+    out_id[t] = bid;
+  }
+}
+
 __global__ void __launch_bounds__(256) k_draft_merge(const float2* __restrict__ part, int n_cta,
                                                      int R, int K, Shortlist sl, int smax,
                                                      int32_t* root, int32_t* topk_id,
                                                      float* topk_val) {
-  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= R) return;
+  __shared__ float s_v[8][kMaxS];
+  __shared__ int s_id[8][kMaxS];
+  const int row = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = row / (K + 1), i = row - b * (K + 1);
   const int s = i == 0 ? 1 : sl.s[i - 1];
-  float pv = 0.f;
-  int pid = -1;
-  for (int t = 0; t < s; ++t) {
-    float bv = -INFINITY;
-    int bid = 0x7fffffff;
-    for (int c = lane; c < n_cta * kMaxS; c += 32) {
-      const float2 e = part[((long long)(c / kMaxS) * R + row) * kMaxS + (c % kMaxS)];
-      const float v = e.x;
-      const int id = __float_as_int(e.y);
-      if (id == 0x7fffffff) continue;
-      if (pid >= 0 && !ranks_before(pv, pid, v, id)) continue;
-      if (ranks_before(v, id, bv, bid)) {
-        bv = v;
-        bid = id;
+  float v[kMaxS];
+  int id[kMaxS];
+#pragma unroll
+  for (int j = 0; j < kMaxS; ++j) {
+    v[j] = -INFINITY;
+    id[j] = 0x7fffffff;
+  }
+  for (int c = threadIdx.x; c < n_cta * kMaxS; c += blockDim.x) {
+    const float2 e = part[((long long)(c / kMaxS) * R + row) * kMaxS + (c % kMaxS)];
+    const int eid = __float_as_int(e.y);
+    if (eid != 0x7fffffff) top8_insert(v, id, e.x, eid);
+  }
+  float wv[kMaxS];
+  int wid[kMaxS];
+  warp_extract(v, id, kMaxS, wv, wid);
+  if (lane < kMaxS) {
+#pragma unroll
+    for (int j = 0; j < kMaxS; ++j)
+      if (j == lane) {
+        s_v[warp][j] = wv[j];
+        s_id[warp][j] = wid[j];
+      }
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  // warp 0: lane l holds warp l's list (lanes >= 8 hold nothing)
+#pragma unroll
+  for (int j = 0; j < kMaxS; ++j) {
+    v[j] = lane < 8 ? s_v[lane][j] : -INFINITY;
+    id[j] = lane < 8 ? s_id[lane][j] : 0x7fffffff;
+  }
+  warp_extract(v, id, s, wv, wid);
+  if (lane == 0) {
+    if (i == 0) {
+      root[b] = wid[0];
+    } else {
+      for (int t = 0; t < s; ++t) {
+        topk_id[((long long)b * K + i - 1) * smax + t] = wid[t];
+        topk_val[((long long)b * K + i - 1) * smax + t] = wv[t];
       }
     }
-    for (int o = 16; o; o >>= 1) {
-      const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int i2 = __shfl_xor_sync(0xffffffffu, bid, o);
-      if (ranks_before(v2, i2, bv, bid)) {
-        bv = v2;
-        bid = i2;
-      }
-    }
-    if (lane == 0) {
-      if (i == 0) {
-        root[b] = bid;
-      } else {
-        topk_id[((long long)b * K + i - 1) * smax + t] = bid;
-        topk_val[((long long)b * K + i - 1) * smax + t] = bv;
-      }
-    }
-    pv = bv;
-    pid = bid;
   }
   if (i > 0 && lane >= s && lane < smax) {
     topk_id[((long long)b * K + i - 1) * smax + lane] = -1;
@@ -553,7 +628,8 @@ __global__ void __launch_bounds__(256) k_draft_merge(const float2* __restrict__ 
   }
 }
 
-// childlogit[b, c] = y[b, parent(c)] . lm[tok[b, c]], one warp per child.
+// childlogit[b, c] = y[b, parent(c)] . lm[tok[b, c]], one warp per child
+// (grid: sequences x groups of 8 children).
 __global__ void __launch_bounds__(256) k_child_dot(const __nv_bfloat16* __restrict__ y,
                                                    const __nv_bfloat16* __restrict__ lm, int N,
                                                    int d, int V, const int32_t* tok,
@@ -561,7 +637,9 @@ __global__ void __launch_bounds__(256) k_child_dot(const __nv_bfloat16* __restri
                                                    void* ws) {
   const int b = blockIdx.x;
   const int lane = threadIdx.x & 31;
-  for (int c = threadIdx.x >> 5; c < N; c += blockDim.x >> 5) {
+  {
+    const int c = blockIdx.y * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (c >= N) return;
     float acc = 0.f;
     bool valid = false;
     if (c > 0) {
@@ -649,12 +727,30 @@ int launch_tc(TcArgs a, const void* X, const void* W, cudaStream_t st) {
   a.n_rgroups = (a.R + 128 * a.G - 1) / (128 * a.G);
   a.n_units = (a.F + 15) / 16;
   a.n_cta = grid_ctas(a.F);
+  // shared-memory plan: X stage pitch, W stage size, ring depth
+  int tail = 0;
+  if (a.G == 1) {
+    a.xbox = (a.R + 7) / 8 * 8;
+    a.px = a.xbox * 128;
+    tail = 16384 - a.px;           // the last stage's 128-row read stays inside
+  } else {
+    a.xbox = 128;
+    a.px = 2 * 16384;
+  }
+  const int units_max = (a.n_units + a.n_cta - 1) / a.n_cta;
+  const int nc_max = min(a.NC, units_max * 16);
+  a.wst = nc_max * 128;
+  const int budget = kSmemBytes - 1024 /*alignment*/ - kBarBytes - tail;
+  a.stages = min(kMaxStages, budget / (a.px + a.wst));
+  if (a.stages < 2) return MDS_EUNSUPPORTED;
+  a.xregion = a.stages * a.px + tail;
+  const int smem = 1024 + a.xregion + a.stages * a.wst + kBarBytes;
   CUtensorMap mx, mw;
-  rc = make_map(&mx, X, a.R, a.Kd, 128);
+  rc = make_map(&mx, X, a.R, a.Kd, a.xbox);
   if (rc) return rc;
   rc = make_map(&mw, W, a.F, a.Kd, kBoxF);
   if (rc) return rc;
-  k_gemm_tc<<<a.n_cta, kThreads, kSmemBytes, st>>>(mx, mw, a);
+  k_gemm_tc<<<a.n_cta, kThreads, smem, st>>>(mx, mw, a);
   MDS_LAUNCH_CHECK();
   return MDS_OK;
 }
@@ -729,7 +825,7 @@ int lm_draft_tc(const void* U, int B, int K, int d, const void* lm, int V, Short
   int rc = launch_tc(a, U, lm, st);
   if (rc) return rc;
   const int n_cta = grid_ctas(V);
-  k_draft_merge<<<(a.R + 7) / 8, 256, 0, st>>>(static_cast<const float2*>(partial), n_cta, a.R,
+  k_draft_merge<<<a.R, 256, 0, st>>>(static_cast<const float2*>(partial), n_cta, a.R,
                                                 K, sl, smax, root, topk_id, topk_val);
   MDS_LAUNCH_CHECK();
   return MDS_OK;
@@ -751,7 +847,7 @@ int lm_verify_tc(const void* y, int B, int N, int d, const void* lm, int V, cons
   k_verify_merge<<<(a.R + 7) / 8, 256, 0, st>>>(static_cast<const float4*>(partial), n_cta, a.R,
                                                  argmax, stats);
   MDS_LAUNCH_CHECK();
-  k_child_dot<<<B, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(y),
+  k_child_dot<<<dim3(B, (N + 7) / 8), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(y),
                                  static_cast<const __nv_bfloat16*>(lm), N, d, V, tok, parent,
                                  childlogit, ws);
   MDS_LAUNCH_CHECK();

@@ -54,17 +54,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase of `bar` with the given parity to complete.
-// Gives up after ~limit_ns of wall time or when *abort becomes non-zero;
-// returns false then.
+// Gives up after about limit_ns (counted in SM clock cycles at <= 2 GHz, so
+// at lower clocks the limit only grows) or when *abort becomes non-zero, and
+// returns false then.  The clock and the abort flag are read once every 256
+// unsuccessful polls, so the common case is a bare try_wait loop.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           volatile int* abort, uint64_t limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  for (uint32_t it = 1;; ++it) {
+  long long c0 = 0;
+  for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0) {
+    if ((it & 255u) == 255u) {
       if (*abort) return false;
-      if (globaltimer() - t0 > limit_ns) return false;
+      const long long now = clock64();
+      if (c0 == 0) c0 = now;
+      else if ((unsigned long long)(now - c0) > 2ull * limit_ns) return false;
     }
   }
 }
