@@ -230,39 +230,52 @@ def run_ours(args, w):
         dist.barrier()
     ms_total = e0.elapsed_time(e1)
 
-    # per-call device time (eager launches, events on the launching stream)
+    # per-call device time: each C-ABI call alone, captured 10 times back to
+    # back in a CUDA graph and replayed; CUDA events on the launching stream
     calls = ["medusa_heads", "tree_attention", "lm_verify", "verify_accept", "compact_kv"]
-    per = {c: 0.0 for c in calls}
-    reps = max(args.steps, 5)
+    fns = {
+        "medusa_heads": lambda: mds.medusa_heads(h, step.W, step.lm, step.shortlist, step.smax,
+                                                 step.U, step.root, step.topk_id,
+                                                 step.topk_val, step.ws),
+        "tree_attention": lambda: mds.tree_attention(
+            step.P, step.tok, step.mask, step.emb, step.wqkv, step.wo, step.Kc, step.Vc,
+            step.y, step.ws, Hq=step.Hq, Hkv=step.Hkv, K=step.K, smax=step.smax,
+            root=step.root, topk_id=step.topk_id, depth=step.depth, rank=step.rank),
+        "lm_verify": lambda: mds.lm_verify(step.y, step.lm, step.tok, step.parent, step.argmax,
+                                           step.stats, step.childlogit, step.ws),
+        "verify_accept": lambda: mds.verify_accept(mode, w.eps, w.delta, step.parent,
+                                                   step.depth, step.tok, step.argmax,
+                                                   step.stats, step.childlogit, step.L,
+                                                   step.path, step.next_root, step.ws,
+                                                   ok=step.ok),
+        "compact_kv": lambda: (P.copy_(P0), mds.compact_kv(step.L, step.path, step.Kc,
+                                                           step.Vc, step.P, step.ws)),
+    }
+    per = {}
+    reps = 10
     with torch.cuda.stream(s):
-        for _ in range(reps):
-            ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
-            P.copy_(P0)
-            ev[0].record(s)
-            mds.medusa_heads(h, step.W, step.lm, step.shortlist, step.smax, step.U, step.root,
-                             step.topk_id, step.topk_val, step.ws)
-            ev[1].record(s)
-            mds.tree_attention(step.P, step.tok, step.mask, step.emb, step.wqkv, step.wo,
-                               step.Kc, step.Vc, step.y, step.ws, Hq=step.Hq, Hkv=step.Hkv,
-                               K=step.K, smax=step.smax, root=step.root, topk_id=step.topk_id,
-                               depth=step.depth, rank=step.rank)
-            ev[2].record(s)
-            mds.lm_verify(step.y, step.lm, step.tok, step.parent, step.argmax, step.stats,
-                          step.childlogit, step.ws)
-            ev[3].record(s)
-            mds.verify_accept(mode, w.eps, w.delta, step.parent, step.depth, step.tok,
-                              step.argmax, step.stats, step.childlogit, step.L, step.path,
-                              step.next_root, step.ws, ok=step.ok)
-            ev[4].record(s)
-            mds.compact_kv(step.L, step.path, step.Kc, step.Vc, step.P, step.ws)
-            ev[5].record(s)
+        P.copy_(P0)
+        for c in calls:
+            gc = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gc, stream=s):
+                for _ in range(reps):
+                    fns[c]()
+            gc.replay()
             s.synchronize()
-            for i, c in enumerate(calls):
-                per[c] += ev[i].elapsed_time(ev[i + 1]) / reps
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ev0.record(s)
+            for _ in range(3):
+                gc.replay()
+            ev1.record(s)
+            s.synchronize()
+            per[c] = ev0.elapsed_time(ev1) / (3 * reps)
+            P.copy_(P0)
     clk = clocks.stop()
 
-    # end to end through the public API with host buffers: pinned h in,
-    # emitted tokens (L, path, tree tokens, next_root) out, every step
+    # end to end through the public API with host buffers: every step copies
+    # h in from pinned host memory, replays the captured step
+    # (MedusaStep.capture / replay) and copies the emitted tokens (L, path,
+    # tree tokens, next_root) back to pinned host memory, then waits for them
     h_host = torch.empty_like(h, device="cpu").pin_memory()
     h_host.copy_(h.cpu())
     outs = [torch.empty(step.L.shape, dtype=torch.int32).pin_memory(),
@@ -270,14 +283,19 @@ def run_ours(args, w):
             torch.empty(step.tok.shape, dtype=torch.int32).pin_memory(),
             torch.empty(step.next_root.shape, dtype=torch.int32).pin_memory()]
     h_dev = torch.empty_like(h)
-    e2e_steps = max(args.steps // 2, 3)
+    h_dev.copy_(h)
+    with torch.cuda.stream(s):
+        P.copy_(P0)
+        step.capture(h_dev, mode=mode, eps=w.eps, delta=w.delta)
+    s.synchronize()
+    e2e_steps = max(args.steps, 10)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
         with torch.cuda.stream(s):
             h_dev.copy_(h_host, non_blocking=True)
             P.copy_(P0)
-            step.run(h_dev, mode=mode, eps=w.eps, delta=w.delta)
+            step.replay()
             for o, src in zip(outs, (step.L, step.path, step.tok, step.next_root)):
                 o.copy_(src, non_blocking=True)
         s.synchronize()
@@ -320,7 +338,9 @@ def run_ours(args, w):
         "step_hbm_gbs": total_bytes / (ms_step / 1e3) / 1e9,
         "step_hbm_frac": total_bytes / (ms_step / 1e3) / 1e9 / pk["hbm"],
         "per_call_us": {c: 1e3 * v for c, v in per.items()},
-        "roofline": {"kernel": "lm_verify (LM-projection stream, verify rows)", "bound": "hbm",
+        "roofline": {"kernel": "lm_verify call: k_gemm_tc<VERIFY> LM-projection stream over the "
+                               "verify rows + its statistics merge and child-logit gather",
+                     "bound": "hbm",
                      "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
                      "frac": achieved / pk["hbm"], "traffic": None,
                      "peak_src": pk["src"], "algorithmic_bytes_per_launch": lmv_bytes},

@@ -23,6 +23,8 @@
  *    "host" pointers are read before the call returns.  The caller owns every
  *    buffer; the library allocates no device memory per call.
  *  - Tensors are dense, row-major, with the shapes written next to them.
+ *    Device tensors start on a 16-byte boundary (read and written with
+ *    16-byte vector accesses and TMA); a misaligned one returns MDS_EINVAL.
  *    Element type of "void*" tensors is given by `dtype`: MDS_F32 (float) or
  *    MDS_BF16 (bfloat16, stored as 16-bit patterns).  Accumulation is fp32.
  *  - `stream` is a cudaStream_t (NULL = legacy default stream).  All device

@@ -41,6 +41,9 @@ int count_tree(int K, const int32_t* s, int max_rank_sum) {
   return cnt;
 }
 
+// Device tensors are read and written with 16-byte vector accesses and TMA.
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
 bool ws_ok(void* ws, size_t ws_bytes, size_t need) {
   return ws && (reinterpret_cast<uintptr_t>(ws) % kAlign) == 0 && ws_bytes >= need;
 }
@@ -137,6 +140,7 @@ int mds_medusa_heads(int dtype, int B, int d, int V, int K, const void* h, const
     sl.s[i] = shortlist[i];
   }
   if (!ws_ok(ws, ws_bytes, need_heads(dtype, B, d, V, K))) return MDS_EWORKSPACE;
+  if (!aligned16(h) || !aligned16(W) || !aligned16(lm) || !aligned16(U)) return MDS_EINVAL;
   cudaStream_t st = as_stream(stream);
   if (dtype == MDS_BF16) {
     int rc = gemm_tc_heads(h, B, W, K, d, U, ws, st);
@@ -177,6 +181,9 @@ int mds_tree_attention(int dtype, int B, int N, int d, int V, int Hq, int Hkv, i
   if (words < (N + 63) / 64) return MDS_EINVAL;
   if (dtype == MDS_BF16 && !attention_tc_supported(B, N, Hq / Hkv, dh)) return MDS_EUNSUPPORTED;
   if (!ws_ok(ws, ws_bytes, need_attention(dtype, B, N, d, Hq, Hkv, dh))) return MDS_EWORKSPACE;
+  if (!aligned16(emb) || !aligned16(wqkv) || !aligned16(wo) || !aligned16(Kc) ||
+      !aligned16(Vc) || !aligned16(y) || (o_out && !aligned16(o_out)))
+    return MDS_EINVAL;
   cudaStream_t st = as_stream(stream);
   const size_t rows = (size_t)B * N;
   char* base = scratch(ws);
@@ -225,6 +232,7 @@ int mds_lm_verify(int dtype, int B, int N, int d, int V, const void* y, const vo
   if (B < 1 || N < 1 || V < 2) return MDS_EINVAL;
   if (N > kMaxN || d % 64 != 0 || d <= 0) return MDS_EUNSUPPORTED;
   if (!ws_ok(ws, ws_bytes, need_verify(dtype, B, N, V))) return MDS_EWORKSPACE;
+  if (!aligned16(y) || !aligned16(lm)) return MDS_EINVAL;
   cudaStream_t st = as_stream(stream);
   if (dtype == MDS_BF16)
     return lm_verify_tc(y, B, N, d, lm, V, tok, parent, argmax, stats, childlogit, scratch(ws),

@@ -120,7 +120,7 @@ __global__ void __launch_bounds__(128) k_compact(int Hkv, int dh, int Pmax, int 
     }
     s_ok = okv;
   }
-  __syncthreads();
+  block_sync();
   const int okv = s_ok;
   const long long head = ((long long)b * Hkv + hk) * Pmax;
   if (okv) {
@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(128) k_compact(int Hkv, int dh, int Pmax, int 
       sk[i] = Kc[src];
       sv[i] = Vc[src];
     }
-    __syncthreads();
+    block_sync();
     for (int i = threadIdx.x; i < (Lb + 1) * dh; i += blockDim.x) {
       const int j = i / dh, c = i % dh;
       const long long dst = (head + Pb + j) * dh + c;
@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(128) k_compact(int Hkv, int dh, int Pmax, int 
       Vc[dst] = sv[i];
     }
   }
-  __syncthreads();
+  block_sync();
   if (threadIdx.x == 0) {
     __threadfence();
     int* cnt = ws_counters(ws) + b;

@@ -43,7 +43,7 @@ __global__ void __launch_bounds__(256) k_embed(int N, int d, int V, int K, int s
     }
     s_tok = t;
   }
-  __syncthreads();
+  block_sync();
   const int t = s_tok;
   T* xr = x + (long long)r * d;
   if (t < 0) {

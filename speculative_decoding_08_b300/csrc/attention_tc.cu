@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == 1) ptx::tmem_alloc(tmem_slot, 512);
   ptx::tc_fence_before();
-  __syncthreads();
+  ptx::cta_barrier(1, kThreads);
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const long long Ttot = (long long)pre[a.B];
@@ -422,13 +422,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tc_fence_after();
           float sv[kBN];
           {
-            float tmp[32];
-            ptx::tmem_ld32(lane_base + kSCol0 + sb * kBN, tmp);
+            uint32_t r0[32], r1[32];
+            ptx::tmem_ld32_async(lane_base + kSCol0 + sb * kBN, r0);
+            ptx::tmem_ld32_async(lane_base + kSCol0 + sb * kBN + 32, r1);
+            ptx::tmem_wait32(r0);
+            ptx::tmem_wait32(r1);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) sv[c] = tmp[c];
-            ptx::tmem_ld32(lane_base + kSCol0 + sb * kBN + 32, tmp);
-#pragma unroll
-            for (int c = 0; c < 32; ++c) sv[32 + c] = tmp[c];
+            for (int c = 0; c < 32; ++c) {
+              sv[c] = __uint_as_float(r0[c]);
+              sv[32 + c] = __uint_as_float(r1[c]);
+            }
           }
           ptx::tc_fence_before();
           __syncwarp();
@@ -441,8 +444,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int c = 0; c < kBN; ++c) sv[c] = -INFINITY;
             }
+            float t8[8];
 #pragma unroll
-            for (int c = 0; c < kBN; ++c) mx = fmaxf(mx, sv[c]);
+            for (int c = 0; c < 8; ++c) t8[c] = sv[c];
+#pragma unroll
+            for (int c = 8; c < kBN; ++c) t8[c & 7] = fmaxf(t8[c & 7], sv[c]);
+            mx = fmaxf(fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3])),
+                       fmaxf(fmaxf(t8[4], t8[5]), fmaxf(t8[6], t8[7])));
           } else {
 #pragma unroll
             for (int c = 0; c < kBN; ++c) {
@@ -484,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float mr = mref[m];
           // P = 2^(s - m) rounded to bf16; l sums the rounded values
           uint32_t pk[kBN / 2];
-          float ls = 0.f;
+          float ls4[4] = {0.f, 0.f, 0.f, 0.f};
           const float sc = a.scale_log2;
           const float nmr = mr == -INFINITY ? 0.f : -mr;
 #pragma unroll
@@ -494,10 +502,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float p1 = mr == -INFINITY ? 0.f : ex2(fmaf(sv[c + 1], sc, nmr));
             const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
             const float2 r2 = __bfloat1622float2(b2);
-            ls += r2.x + r2.y;
+            ls4[(c >> 1) & 3] += r2.x + r2.y;
             pk[c / 2] = *reinterpret_cast<const uint32_t*>(&b2);
           }
-          lsum[m] += ls;
+          lsum[m] += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
           if (!wait(&p_empty[sb], ((it >> 1) & 1) ^ 1u)) break;
           uint8_t* prow = sP + sb * kPBytes + t * 128;
 #pragma unroll
@@ -576,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   ptx::tc_fence_before();
-  __syncthreads();
+  ptx::cta_barrier(2, kThreads);
   ptx::tc_fence_after();
   if (warp == 1) ptx::tmem_dealloc(tmem, 512);
 }
@@ -589,13 +597,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int DH>
 __global__ void __launch_bounds__(256) k_attention_merge(AttnArgs a) {
   __shared__ int pre[kMaxBAttn + 1];
+  __shared__ long long starts[kMaxCtaAttn + 1];   // first global tile of each CTA
   for (int b = threadIdx.x; b < a.B; b += blockDim.x) pre[b + 1] = a.Hkv * a.n_mg * tiles_of(a, a.P[b]);
-  __syncthreads();
+  block_sync();
   if (threadIdx.x == 0) {
     pre[0] = 0;
     for (int b = 0; b < a.B; ++b) pre[b + 1] += pre[b];
   }
-  __syncthreads();
+  block_sync();
+  for (int c = threadIdx.x; c <= a.G; c += blockDim.x) starts[c] = cta_start(pre[a.B], a.G, c);
+  block_sync();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int u = blockIdx.x;
   const int mg = u % a.n_mg, bh = u / a.n_mg;
@@ -609,19 +620,19 @@ __global__ void __launch_bounds__(256) k_attention_merge(AttnArgs a) {
   const long long U0 = (long long)pre[b] + (long long)(h * a.n_mg + mg) * nt;
   const long long U1 = U0 + nt;
   int c0 = (int)((U0 * a.G) / Ttot);
-  while (c0 + 1 < a.G && cta_start(Ttot, a.G, c0 + 1) <= U0) ++c0;
-  while (c0 > 0 && cta_start(Ttot, a.G, c0) > U0) --c0;
+  while (c0 + 1 < a.G && starts[c0 + 1] <= U0) ++c0;
+  while (c0 > 0 && starts[c0] > U0) --c0;
   int c1 = c0;
-  while (c1 < a.G && cta_start(Ttot, a.G, c1) < U1) ++c1;
+  while (c1 < a.G && starts[c1] < U1) ++c1;
   int nseg = 0;
   for (int c = c0; c < c1; ++c)
-    if (cta_start(Ttot, a.G, c + 1) > cta_start(Ttot, a.G, c)) ++nseg;
+    if (starts[c + 1] > starts[c]) ++nseg;
   if (nseg <= 1) return;
   const float* pml = a.part + (long long)2 * a.G * rows_unit * DH;
   float M = -INFINITY;
   for (int c = c0; c < c1; ++c) {
-    if (cta_start(Ttot, a.G, c + 1) == cta_start(Ttot, a.G, c)) continue;
-    const int sl = 2 * c + (cta_start(Ttot, a.G, c) >= U0 ? 0 : 1);
+    if (starts[c + 1] == starts[c]) continue;
+    const int sl = 2 * c + (starts[c] >= U0 ? 0 : 1);
     M = fmaxf(M, __ldcg(reinterpret_cast<const float2*>(pml) + (long long)sl * rows_unit + rloc).x);
   }
   constexpr int E = DH / 32;                 // elements per lane
@@ -630,8 +641,8 @@ __global__ void __launch_bounds__(256) k_attention_merge(AttnArgs a) {
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
   float L = 0.f;
   for (int c = c0; c < c1; ++c) {
-    if (cta_start(Ttot, a.G, c + 1) == cta_start(Ttot, a.G, c)) continue;
-    const int sl = 2 * c + (cta_start(Ttot, a.G, c) >= U0 ? 0 : 1);
+    if (starts[c + 1] == starts[c]) continue;
+    const int sl = 2 * c + (starts[c] >= U0 ? 0 : 1);
     const float2 ml = __ldcg(reinterpret_cast<const float2*>(pml) + (long long)sl * rows_unit + rloc);
     const float* po = a.part + ((long long)sl * rows_unit + rloc) * DH + lane * E;
     float v[E];
@@ -683,7 +694,6 @@ Plan plan(int N, int g, int dh, int num_sms) {
   return p;
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 g_encode_attn = nullptr;
 int g_sms_attn = 0;
 bool g_attr_set[2][kMaxNM + 1] = {};
 
@@ -700,18 +710,6 @@ int launch_nm(const Plan& p, const CUtensorMap& mq, const CUtensorMap& mk,
     case 3: return launch_one<DH, 3>(p, mq, mk, mv, a, st);
     default: return MDS_EUNSUPPORTED;
   }
-}
-
-int make_map_attn(CUtensorMap* m, const void* base, long long rows, int cols, int box_rows) {
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
-  cuuint32_t es[2] = {1, 1};
-  const CUresult r = g_encode_attn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
-                                   dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? MDS_OK : MDS_ECUDA;
 }
 
 template <int DH, int NM>
@@ -746,15 +744,6 @@ int attention_tc_supported(int B, int N, int g, int dh) {
 int attention_tc(int B, int N, int Hq, int Hkv, int dh, int Pmax, const int32_t* P,
                  const uint64_t* mask, int words, const void* q, const void* Kc, const void* Vc,
                  void* o, void* partial, void* ws, cudaStream_t st) {
-  if (!g_encode_attn) {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult qr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
-                                         &qr) != cudaSuccess ||
-        qr != cudaDriverEntryPointSuccess || !fn)
-      return MDS_ECUDA;
-    g_encode_attn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  }
   if (!g_sms_attn) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MDS_ECUDA;
@@ -784,11 +773,11 @@ int attention_tc(int B, int N, int Hq, int Hkv, int dh, int Pmax, const int32_t*
   a.part = static_cast<float*>(partial);
   a.ws = ws;
   CUtensorMap mq, mk, mv;
-  int rc = make_map_attn(&mq, q, (long long)B * Hkv * a.Mrows, dh, 128);
+  int rc = tensor_map_bf16(&mq, q, (long long)B * Hkv * a.Mrows, dh, 2, 128, 1);
   if (rc) return rc;
-  rc = make_map_attn(&mk, Kc, (long long)B * Hkv * Pmax, dh, kBN);
+  rc = tensor_map_bf16(&mk, Kc, (long long)B * Hkv * Pmax, dh, 2, kBN, 1);
   if (rc) return rc;
-  rc = make_map_attn(&mv, Vc, (long long)B * Hkv * Pmax, dh, kBN);
+  rc = tensor_map_bf16(&mv, Vc, (long long)B * Hkv * Pmax, dh, 2, kBN, 1);
   if (rc) return rc;
   rc = dh == 128 ? launch_nm<128>(p, mq, mk, mv, a, st) : launch_nm<64>(p, mq, mk, mv, a, st);
   if (rc) return rc;

@@ -44,9 +44,26 @@ template <typename T> __device__ __forceinline__ void st(T* p, float v) { Elem<T
 
 __device__ __forceinline__ float silu(float a) { return a / (1.0f + expf(-a)); }
 
+// 2^x by the hardware approximation (ex2.approx, relative error ~2^-22;
+// -inf gives 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // (value desc, id asc) order: true when (va, ia) comes before (vb, ib).
 __device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
+}
+
+// Block-wide barrier for code where lanes of a warp may have diverged (for
+// example after `if (threadIdx.x == 0) {...}`).  The warp reconverges first:
+// a block barrier reached by a warp in two parts counts it twice, which
+// releases the barrier one warp early.
+__device__ __forceinline__ void block_sync() {
+  __syncwarp();
+  __syncthreads();
 }
 
 // Host-side count of enqueued kernels (see mds_launch_count).

@@ -74,14 +74,14 @@ __global__ void __launch_bounds__(256) k_gemm_simple(const T* __restrict__ X, in
       const int rr = i / kTK, kk = i % kTK, r = r0 + rr, k = k0 + kk;
       Xs[rr][kk] = (r < R && k < Kd) ? ld(X + (long long)r * Kd + k) : 0.f;
     }
-    __syncthreads();
+    block_sync();
 #pragma unroll 8
     for (int kk = 0; kk < kTK; ++kk) {
       const float w = Ws[tx][kk];
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] = fmaf(Xs[ty * 8 + i][kk], w, acc[i]);
     }
-    __syncthreads();
+    block_sync();
   }
   const int f = f0 + tx;
   if (f >= F) return;
@@ -112,9 +112,9 @@ __device__ Cand block_best(Cand c, Cand* red) {
     c = better(c, x);
   }
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  __syncthreads();
+  block_sync();
   if (l == 0) red[w] = c;
-  __syncthreads();
+  block_sync();
   if (w == 0) {
     c = (l < (int)(blockDim.x >> 5)) ? red[l] : Cand{0.f, -1};
     for (int o = 16; o; o >>= 1) {
@@ -123,7 +123,7 @@ __device__ Cand block_best(Cand c, Cand* red) {
     }
     if (l == 0) red[32] = c;
   }
-  __syncthreads();
+  block_sync();
   return red[32];
 }
 
@@ -165,15 +165,15 @@ __global__ void __launch_bounds__(256) k_draft_select(const float* __restrict__ 
 __device__ float block_sum(float x, float* red) {
   for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  __syncthreads();
+  block_sync();
   if (l == 0) red[w] = x;
-  __syncthreads();
+  block_sync();
   if (w == 0) {
     x = (l < (int)(blockDim.x >> 5)) ? red[l] : 0.f;
     for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
     if (l == 0) red[32] = x;
   }
-  __syncthreads();
+  block_sync();
   return red[32];
 }
 

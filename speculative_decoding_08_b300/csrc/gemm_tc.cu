@@ -49,7 +49,6 @@ constexpr int kTmemCols = 512;
 constexpr int kSmemBytes = 232448;                  // 227 KB, the opt-in maximum
 constexpr int kBarBytes = 512;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
-constexpr int kBoxF = 16;                           // weight rows per TMA box
 constexpr int kMaxCta = 256;                        // partial records per row
 
 struct TcArgs {
@@ -57,10 +56,13 @@ struct TcArgs {
   int n_units, n_cta;
   int G, NC;
   int stages;       // TMA ring depth
-  int px;           // bytes between the X tiles of consecutive stages
-  int xregion;      // bytes of the X region (stages * px + tail)
-  int wst;          // bytes of one stage's W tile
+  int kbs;          // 64-wide k-blocks per stage (one TMA box each for X and W)
+  int px;           // bytes between consecutive k-block X tiles
+  int pxs;          // bytes of one stage's X tiles
+  int xregion;      // bytes of the X region (stages * pxs + tail)
+  int wst;          // bytes of one stage's W tiles
   int xbox;         // X rows per TMA box
+  int wh[3];        // row counts of the three W tensor maps' boxes
   int n_rgroups;
   int kind;
   void* out;
@@ -110,53 +112,91 @@ __device__ __forceinline__ void epi_store(const TcArgs& a, int row, int f0, int 
   }
 }
 
+// 8 floats -> 8 bf16 (round to nearest even) packed in 16 bytes.
+__device__ __forceinline__ uint4 pack8(const float* v) {
+  uint4 pk;
+  __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(&pk);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) p2[e] = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+  return pk;
+}
+
+// U[b, 1 + i, j] = h[b, j] + SiLU(Y[b, i d + j]); row 0 of U is a copy of h.
+// Written 16 features at a time: f0 is a multiple of 16 and d of 64, so a
+// group of 16 never straddles two heads.
 __device__ __forceinline__ void epi_heads(const TcArgs& a, int b, int f0, int nv,
                                           const float (&v)[32]) {
   __nv_bfloat16* U = static_cast<__nv_bfloat16*>(a.out);
   const __nv_bfloat16* hb = a.h + (long long)b * a.d;
   const long long ubase = (long long)b * (a.K + 1) * a.d;
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    if (j >= nv) break;
-    const int f = f0 + j;
-    const int i = f / a.d, jj = f - i * a.d;
-    const __nv_bfloat16 hraw = hb[jj];
-    const float hv = __bfloat162float(hraw);
-    U[ubase + (long long)(1 + i) * a.d + jj] = __float2bfloat16_rn(hv + silu(v[j]));
-    if (i == 0) U[ubase + jj] = hraw;
+  for (int half = 0; half < 2; ++half) {
+    const int f = f0 + 16 * half;
+    const int i = f / a.d, j0 = f - i * a.d;
+    if (nv >= 16 * (half + 1)) {
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const uint4 hraw = *reinterpret_cast<const uint4*>(hb + j0 + q * 8);
+        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&hraw);
+        float u[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 hf = __bfloat1622float2(h2[e]);
+          u[2 * e] = hf.x + silu(v[16 * half + q * 8 + 2 * e]);
+          u[2 * e + 1] = hf.y + silu(v[16 * half + q * 8 + 2 * e + 1]);
+        }
+        *reinterpret_cast<uint4*>(U + ubase + (long long)(1 + i) * a.d + j0 + q * 8) = pack8(u);
+        if (i == 0) *reinterpret_cast<uint4*>(U + ubase + j0 + q * 8) = hraw;
+      }
+    } else {
+      for (int j = 0; j < 16 && 16 * half + j < nv; ++j) {
+        const __nv_bfloat16 hraw = hb[j0 + j];
+        U[ubase + (long long)(1 + i) * a.d + j0 + j] =
+            __float2bfloat16_rn(__bfloat162float(hraw) + silu(v[16 * half + j]));
+        if (i == 0) U[ubase + j0 + j] = hraw;
+      }
+    }
   }
 }
 
+// q -> [B, Hkv, N g, dh]; k, v -> cache slot P_b + n.  Written 16 features
+// at a time (dh % 16 == 0 and f0 % 16 == 0, so 16 never straddle heads).
 __device__ __forceinline__ void epi_qkv(const TcArgs& a, int r, int f0, int nv,
                                         const float (&v)[32]) {
   const int qd = a.Hq * a.dh, kd = a.Hkv * a.dh;
   const int b = r / a.N, n = r - b * a.N;
   const int Pb = a.P[b];
   const bool cache_ok = Pb >= 0 && Pb + n < a.Pmax;
-  bool bad = false;
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    if (j >= nv) break;
-    const int f = f0 + j;
+  for (int half = 0; half < 2; ++half) {
+    const int f = f0 + 16 * half;
+    if (16 * half >= nv) break;
+    __nv_bfloat16* dst;
     if (f < qd) {
-      // q in the attention kernel's layout [B, Hkv, N * g, dh]
       const int g = a.Hq / a.Hkv;
       const int hq = f / a.dh, c = f - hq * a.dh;
       const int hk = hq / g, jj = hq - hk * g;
-      static_cast<__nv_bfloat16*>(a.out)[(((long long)b * a.Hkv + hk) * a.N * g + n * g + jj) * a.dh + c] =
-          __float2bfloat16_rn(v[j]);
-    } else if (!cache_ok) {
-      bad = true;
+      dst = static_cast<__nv_bfloat16*>(a.out) +
+            (((long long)b * a.Hkv + hk) * a.N * g + n * g + jj) * a.dh + c;
     } else {
+      if (!cache_ok) {
+        latch_error(a.ws, MDS_DEV_KV_CAPACITY);
+        continue;
+      }
       const int f2 = f - qd;
       const int which = f2 >= kd;
       const int f3 = f2 - which * kd;
       const int hk = f3 / a.dh, c = f3 - hk * a.dh;
       __nv_bfloat16* cache = which ? a.Vc : a.Kc;
-      cache[(((long long)b * a.Hkv + hk) * a.Pmax + Pb + n) * a.dh + c] = __float2bfloat16_rn(v[j]);
+      dst = cache + (((long long)b * a.Hkv + hk) * a.Pmax + Pb + n) * a.dh + c;
+    }
+    if (nv >= 16 * (half + 1)) {
+      *reinterpret_cast<uint4*>(dst) = pack8(v + 16 * half);
+      *reinterpret_cast<uint4*>(dst + 8) = pack8(v + 16 * half + 8);
+    } else {
+      for (int j = 0; 16 * half + j < nv; ++j) dst[j] = __float2bfloat16_rn(v[16 * half + j]);
     }
   }
-  if (bad) latch_error(a.ws, MDS_DEV_KV_CAPACITY);
 }
 
 struct TopList {
@@ -187,6 +227,8 @@ struct TopList {
   }
 };
 
+// Running softmax statistics of one row over 32-column blocks: maximum m,
+// its lowest column (argmax), S = sum e^(z - m), Q = sum z e^(z - m).
 struct SoftStat {
   float m, S, Q;
   int am;
@@ -197,41 +239,66 @@ struct SoftStat {
     am = 0x7fffffff;
   }
   __device__ __forceinline__ void push32(const float (&z)[32], int f0, int nv) {
-    float lm = -INFINITY;
-    int li = 0x7fffffff;
+    constexpr float kL2E = 1.4426950408889634f;
+    float zz[32];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const bool ok = j < nv;
-      if (ok && z[j] > lm) {
-        lm = z[j];
-        li = f0 + j;
-      }
-    }
-    if (lm > m) {
-      const float sc = __expf(m - lm);
+    for (int j = 0; j < 32; ++j) zz[j] = j < nv ? z[j] : -1e30f;   // never the max
+    float t[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) t[j] = fmaxf(zz[j], zz[j + 16]);
+#pragma unroll
+    for (int w = 8; w; w >>= 1)
+#pragma unroll
+      for (int j = 0; j < w; ++j) t[j] = fmaxf(t[j], t[j + w]);
+    const float cm = t[0];
+    if (cm > m) {
+      int li = 31;
+#pragma unroll
+      for (int j = 31; j >= 0; --j)
+        if (zz[j] == cm) li = j;
+      const float sc = m == -INFINITY ? 0.f : fast_exp2((m - cm) * kL2E);
       S *= sc;
       Q *= sc;
-      m = lm;
-      am = li;
+      m = cm;
+      am = f0 + li;
     }
-    if (m == -INFINITY) return;
-    float s = 0.f, q = 0.f;
+    const float nm = -m * kL2E;
+    float s4[4] = {0.f, 0.f, 0.f, 0.f}, q4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
-      if (j < nv) {
-        const float e = __expf(z[j] - m);
-        s += e;
-        q = fmaf(z[j], e, q);
-      }
+      const float e = fast_exp2(fmaf(zz[j], kL2E, nm));
+      s4[j & 3] += e;
+      q4[j & 3] = fmaf(zz[j], e, q4[j & 3]);
     }
-    S += s;
-    Q += q;
+    S += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+    Q += (q4[0] + q4[1]) + (q4[2] + q4[3]);
   }
 };
 
+// One 32-column block of a row's accumulators (raw fp32 bits in r).
+template <int KIND>
+__device__ __forceinline__ void epi_block(const TcArgs& a, int row, int g, int f0, int nv,
+                                          const uint32_t (&r)[32], TopList (&tl)[2],
+                                          SoftStat (&ss)[2]) {
+  float v[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+  if constexpr (KIND == TC_STORE) epi_store(a, row, f0, nv, v);
+  if constexpr (KIND == TC_HEADS) epi_heads(a, row, f0, nv, v);
+  if constexpr (KIND == TC_QKV) epi_qkv(a, row, f0, nv, v);
+  if constexpr (KIND == TC_DRAFT) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < nv) tl[g].push(v[j], f0 + j);
+  }
+  if constexpr (KIND == TC_VERIFY) ss[g].push32(v, f0, nv);
+}
+
 // ------------------------------------------------------------------ kernel
+template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
-    k_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW0,
+              const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmW2,
               TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -251,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cta = blockIdx.x;
   const Range rg = cta_range(a, cta);
-  const int nkb = a.Kd / 64;
+  const int nks = a.Kd / (64 * a.kbs);     // stages per chunk
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -266,11 +333,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     ptx::fence_mbar_init();
     ptx::tma_prefetch_desc(&tmX);
-    ptx::tma_prefetch_desc(&tmW);
+    ptx::tma_prefetch_desc(&tmW0);
+    ptx::tma_prefetch_desc(&tmW1);
+    ptx::tma_prefetch_desc(&tmW2);
   }
   if (warp == 1) ptx::tmem_alloc(tmem_slot, kTmemCols);
   ptx::tc_fence_before();
-  __syncthreads();
+  ptx::cta_barrier(1, kThreads);
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -292,22 +361,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int ch = 0; ch < rg.n_chunks && ok; ++ch) {
           const int fc = rg.f_begin + ch * a.NC;
           const int len = min(a.NC, rg.f_end - fc);
-          const int nbox = (len + kBoxF - 1) / kBoxF;
-          const uint32_t xbytes = a.G == 1 ? (uint32_t)a.xbox * 128 : (uint32_t)Geff * 128 * 128;
-          const uint32_t bytes = xbytes + (uint32_t)nbox * kBoxF * 128;
-          for (int kb = 0; kb < nkb; ++kb) {
+          // the W map whose box height is this chunk's rows (rounded to 16)
+          const int h16 = (len + 15) / 16 * 16;
+          const CUtensorMap* mw = h16 == a.wh[0] ? &tmW0 : (h16 == a.wh[1] ? &tmW1 : &tmW2);
+          const uint32_t xbytes = a.G == 1 ? (uint32_t)(a.kbs * a.xbox * 128)
+                                           : (uint32_t)(Geff * a.kbs * 16384);
+          const uint32_t bytes = xbytes + (uint32_t)(a.kbs * h16 * 128);
+          for (int kq = 0; kq < nks; ++kq) {
             if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, kWaitLimitNs)) {
               ok = false;
               break;
             }
-            uint8_t* sA = sXr + stage * a.px;
+            uint8_t* sA = sXr + stage * a.pxs;
             uint8_t* sB = sWr + stage * a.wst;
             ptx::mbar_arrive_expect_tx(&full[stage], bytes);
             for (int g = 0; g < Geff; ++g)
-              ptx::tma_load_2d(sA + g * 16384, &tmX, kb * 64, row0 + g * 128, &full[stage], pol_x);
-            for (int j = 0; j < nbox; ++j)
-              ptx::tma_load_2d(sB + j * kBoxF * 128, &tmW, kb * 64, fc + j * kBoxF, &full[stage],
-                               pol_w);
+              ptx::tma_load_3d(sA + g * a.kbs * 16384, &tmX, 0, row0 + g * 128, kq * a.kbs,
+                               &full[stage], pol_x);
+            ptx::tma_load_3d(sB, mw, 0, fc, kq * a.kbs, &full[stage], pol_w);
             issued[stage] = true;
             issued_phase[stage] = phase;
             if (++stage == S) {
@@ -348,21 +419,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           ptx::tc_fence_after();
-          for (int kb = 0; kb < nkb; ++kb) {
+          const int h16 = npad;
+          for (int kq = 0; kq < nks; ++kq) {
             if (!ptx::mbar_wait(&full[stage], phase, abort_flag, kWaitLimitNs)) {
               ok = false;
               break;
             }
             ptx::tc_fence_after();
-            const uint32_t sA = ptx::smem_addr(sXr + stage * a.px);
+            const uint32_t sA = ptx::smem_addr(sXr + stage * a.pxs);
             const uint32_t sB = ptx::smem_addr(sWr + stage * a.wst);
-            for (int g = 0; g < Geff; ++g) {
-              const uint32_t dcol = tmem_base + (uint32_t)(acc * a.G * a.NC + g * a.NC);
+            for (int q = 0; q < a.kbs; ++q) {
+              const uint32_t bq = sB + (uint32_t)(q * h16 * 128);
+              for (int g = 0; g < Geff; ++g) {
+                const uint32_t aq = a.G == 1 ? sA + (uint32_t)(q * a.px)
+                                             : sA + (uint32_t)((g * a.kbs + q) * 16384);
+                const uint32_t dcol = tmem_base + (uint32_t)(acc * a.G * a.NC + g * a.NC);
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const uint64_t ad = ptx::sdesc_k128(sA + g * 16384 + k * 32);
-                const uint64_t bd = ptx::sdesc_k128(sB + k * 32);
-                ptx::mma_bf16(dcol, ad, bd, idesc, (kb | k) != 0);
+                for (int k = 0; k < 4; ++k) {
+                  const uint64_t ad = ptx::sdesc_k128(aq + k * 32);
+                  const uint64_t bd = ptx::sdesc_k128(bq + k * 32);
+                  ptx::mma_bf16(dcol, ad, bd, idesc, (kq | q | k) != 0);
+                }
               }
             }
             ptx::mma_commit(&empty[stage]);
@@ -414,24 +491,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (g >= Geff) break;
           const int row = row0 + g * 128 + trow;
           const bool live = row < a.R;
-          for (int cb = 0; cb * 32 < len; ++cb) {
-            float v[32];
-            const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) +
-                                   (uint32_t)(acc * a.G * a.NC + g * a.NC + cb * 32);
-            ptx::tmem_ld32(taddr, v);
-            const int f0 = fc + cb * 32;
-            const int nv = min(32, len - cb * 32);
-            if (!live) continue;
-            switch (a.kind) {
-              case TC_STORE: epi_store(a, row, f0, nv, v); break;
-              case TC_HEADS: epi_heads(a, row, f0, nv, v); break;
-              case TC_QKV: epi_qkv(a, row, f0, nv, v); break;
-              case TC_DRAFT:
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                  if (j < nv) tl[g].push(v[j], f0 + j);
-                break;
-              case TC_VERIFY: ss[g].push32(v, f0, nv); break;
+          const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) +
+                                 (uint32_t)(acc * a.G * a.NC + g * a.NC);
+          const int ncb = (len + 31) / 32;
+          // two register buffers: the load of block cb + 1 overlaps the work on cb
+          uint32_t rb[2][32];
+          ptx::tmem_ld32_async(tbase, rb[0]);
+          ptx::tmem_wait32(rb[0]);
+#pragma unroll 1
+          for (int cb = 0; cb < ncb; cb += 2) {
+            const bool more1 = cb + 1 < ncb, more2 = cb + 2 < ncb;
+            if (more1) ptx::tmem_ld32_async(tbase + (uint32_t)(cb + 1) * 32, rb[1]);
+            if (live) epi_block<KIND>(a, row, g, fc + cb * 32, min(32, len - cb * 32), rb[0], tl, ss);
+            if (more1) {
+              ptx::tmem_wait32(rb[1]);
+              if (more2) ptx::tmem_ld32_async(tbase + (uint32_t)(cb + 2) * 32, rb[0]);
+              if (live)
+                epi_block<KIND>(a, row, g, fc + (cb + 1) * 32, min(32, len - (cb + 1) * 32), rb[1],
+                                tl, ss);
+              if (more2) ptx::tmem_wait32(rb[0]);
             }
           }
         }
@@ -440,14 +518,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) ptx::mbar_arrive(&tempty[acc]);
       }
       if (!ok) break;
-      if (rg.n_chunks > 0 && (a.kind == TC_DRAFT || a.kind == TC_VERIFY)) {
+      if (rg.n_chunks > 0 && (KIND == TC_DRAFT || KIND == TC_VERIFY)) {
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
           if (g >= Geff) break;
           const int row = row0 + g * 128 + trow;
           if (row >= a.R) continue;
           const long long rec = (long long)cta * a.R + row;
-          if (a.kind == TC_VERIFY) {
+          if (KIND == TC_VERIFY) {
             float4 o = make_float4(ss[g].m, ss[g].S, ss[g].Q, __int_as_float(ss[g].am));
             static_cast<float4*>(a.partial)[rec] = o;
           } else {
@@ -465,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   ptx::tc_fence_before();
-  __syncthreads();
+  ptx::cta_barrier(2, kThreads);
   ptx::tc_fence_after();
   if (warp == 1) ptx::tmem_dealloc(tmem_base, kTmemCols);
 }
@@ -603,7 +681,7 @@ __global__ void __launch_bounds__(256) k_draft_merge(const float2* __restrict__ 
         s_id[warp][j] = wid[j];
       }
   }
-  __syncthreads();
+  block_sync();
   if (warp != 0) return;
   // warp 0: lane l holds warp l's list (lanes >= 8 hold nothing)
 #pragma unroll
@@ -673,22 +751,27 @@ __global__ void __launch_bounds__(256) k_child_dot(const __nv_bfloat16* __restri
 }
 
 // ------------------------------------------------------------------ host
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 int g_num_sms = 0;
 
-int init_host() {
-  if (!g_encode) {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess || !fn)
-      return MDS_ECUDA;
-    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    if (cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+template <int KIND>
+int set_smem_attr() {
+  static bool done = false;
+  if (!done) {
+    if (cudaFuncSetAttribute(k_gemm_tc<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemBytes) != cudaSuccess)
       return MDS_ECUDA;
+    done = true;
   }
+  return MDS_OK;
+}
+
+int init_host() {
+  int rc = set_smem_attr<TC_STORE>();
+  if (!rc) rc = set_smem_attr<TC_HEADS>();
+  if (!rc) rc = set_smem_attr<TC_QKV>();
+  if (!rc) rc = set_smem_attr<TC_DRAFT>();
+  if (!rc) rc = set_smem_attr<TC_VERIFY>();
+  if (rc) return rc;
   if (!g_num_sms) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MDS_ECUDA;
@@ -704,16 +787,11 @@ int grid_ctas(int F) {
   return n_units < n ? n_units : n;
 }
 
-int make_map(CUtensorMap* m, const void* base, int rows, int cols, int box_rows) {
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
-  cuuint32_t es[2] = {1, 1};
-  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
-                              dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? MDS_OK : MDS_ECUDA;
+// Rows of the last chunk of a CTA range of `units` 16-row units.
+int last_chunk_rows(int units, int NC) {
+  const int len = units * 16;
+  const int n = (len + NC - 1) / NC;
+  return len - (n - 1) * NC;
 }
 
 int launch_tc(TcArgs a, const void* X, const void* W, cudaStream_t st) {
@@ -727,30 +805,57 @@ int launch_tc(TcArgs a, const void* X, const void* W, cudaStream_t st) {
   a.n_rgroups = (a.R + 128 * a.G - 1) / (128 * a.G);
   a.n_units = (a.F + 15) / 16;
   a.n_cta = grid_ctas(a.F);
-  // shared-memory plan: X stage pitch, W stage size, ring depth
+  // W box heights: full chunks of NC rows and the last chunk of a range of
+  // lo or hi units (ranges differ by at most one unit)
+  const int lo = a.n_units / a.n_cta, hi = (a.n_units + a.n_cta - 1) / a.n_cta;
+  a.wh[0] = a.NC;
+  a.wh[1] = last_chunk_rows(lo > 0 ? lo : 1, a.NC);
+  a.wh[2] = last_chunk_rows(hi, a.NC);
+  const int h_max = min(a.NC, hi * 16);
+  // shared-memory plan: k-blocks per stage, X pitch, ring depth
   int tail = 0;
   if (a.G == 1) {
     a.xbox = (a.R + 7) / 8 * 8;
     a.px = a.xbox * 128;
-    tail = 16384 - a.px;           // the last stage's 128-row read stays inside
+    tail = 16384 - a.px;           // the last tile's 128-row read stays inside
   } else {
     a.xbox = 128;
-    a.px = 2 * 16384;
+    a.px = 16384;
   }
-  const int units_max = (a.n_units + a.n_cta - 1) / a.n_cta;
-  const int nc_max = min(a.NC, units_max * 16);
-  a.wst = nc_max * 128;
   const int budget = kSmemBytes - 1024 /*alignment*/ - kBarBytes - tail;
-  a.stages = min(kMaxStages, budget / (a.px + a.wst));
-  if (a.stages < 2) return MDS_EUNSUPPORTED;
-  a.xregion = a.stages * a.px + tail;
+  a.kbs = 0;
+  for (int kbs = 4; kbs >= 1; kbs >>= 1) {
+    if (a.Kd % (64 * kbs)) continue;
+    const int pxs = a.G == 1 ? kbs * a.px : 2 * kbs * 16384;
+    const int wst = kbs * h_max * 128;
+    const int st_n = min(kMaxStages, budget / (pxs + wst));
+    if (st_n >= 3 || (kbs == 1 && st_n >= 2)) {
+      a.kbs = kbs;
+      a.pxs = pxs;
+      a.wst = wst;
+      a.stages = st_n;
+      break;
+    }
+  }
+  if (a.kbs == 0) return MDS_EUNSUPPORTED;
+  a.xregion = a.stages * a.pxs + tail;
   const int smem = 1024 + a.xregion + a.stages * a.wst + kBarBytes;
-  CUtensorMap mx, mw;
-  rc = make_map(&mx, X, a.R, a.Kd, a.xbox);
+  CUtensorMap mx, mw[3];
+  // X as (64 columns, rows, column blocks): a box of (64, rows, kbs) lands as
+  // kbs consecutive K-major tiles, one per 64-wide k-block; W likewise
+  rc = tensor_map_bf16(&mx, X, a.R, a.Kd, 3, a.xbox, a.kbs);
   if (rc) return rc;
-  rc = make_map(&mw, W, a.F, a.Kd, kBoxF);
-  if (rc) return rc;
-  k_gemm_tc<<<a.n_cta, kThreads, smem, st>>>(mx, mw, a);
+  for (int i = 0; i < 3; ++i) {
+    rc = tensor_map_bf16(&mw[i], W, a.F, a.Kd, 3, a.wh[i], a.kbs);
+    if (rc) return rc;
+  }
+  switch (a.kind) {
+    case TC_STORE: k_gemm_tc<TC_STORE><<<a.n_cta, kThreads, smem, st>>>(mx, mw[0], mw[1], mw[2], a); break;
+    case TC_HEADS: k_gemm_tc<TC_HEADS><<<a.n_cta, kThreads, smem, st>>>(mx, mw[0], mw[1], mw[2], a); break;
+    case TC_QKV: k_gemm_tc<TC_QKV><<<a.n_cta, kThreads, smem, st>>>(mx, mw[0], mw[1], mw[2], a); break;
+    case TC_DRAFT: k_gemm_tc<TC_DRAFT><<<a.n_cta, kThreads, smem, st>>>(mx, mw[0], mw[1], mw[2], a); break;
+    default: k_gemm_tc<TC_VERIFY><<<a.n_cta, kThreads, smem, st>>>(mx, mw[0], mw[1], mw[2], a); break;
+  }
   MDS_LAUNCH_CHECK();
   return MDS_OK;
 }

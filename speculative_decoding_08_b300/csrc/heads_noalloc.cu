@@ -73,6 +73,9 @@ extern "C" int mds_medusa_heads_noalloc(int B, int d, int V, int K, const void* 
     if (shortlist[i] < 1 || shortlist[i] > smax || shortlist[i] > V) return MDS_EINVAL;
     sl.s[i] = shortlist[i];
   }
+  if (((reinterpret_cast<uintptr_t>(h) | reinterpret_cast<uintptr_t>(W) |
+        reinterpret_cast<uintptr_t>(lm) | reinterpret_cast<uintptr_t>(U)) & 15) != 0)
+    return MDS_EINVAL;
   const long long rows = (long long)B * (K + 1);
   if (rows > kNoAllocMaxRows || tc_partial_bytes((int)rows, true) > kNoAllocPartialBytes)
     return MDS_EUNSUPPORTED;

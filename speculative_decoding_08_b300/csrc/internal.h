@@ -5,7 +5,17 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <cuda.h>
+
 namespace mds {
+
+// Encodes a bf16 tiled tensor map with the 128-byte swizzle, or returns a
+// cached copy of one encoded with the same arguments (the map holds only the
+// address, sizes, strides and box, so an identical request gets an identical
+// map).  rank 2: dims {cols, rows}, box {64, box_rows}; rank 3: dims
+// {64, rows, cols / 64}, strides {cols * 2, 128}, box {64, box_rows, box_kb}.
+int tensor_map_bf16(CUtensorMap* out, const void* base, long long rows, int cols, int rank,
+                    int box_rows, int box_kb);
 
 // Epilogues of the projection GEMMs  Y[r, f] = sum_k X[r, k] W[f, k].
 enum EpiKind {

@@ -44,7 +44,7 @@ __global__ void __launch_bounds__(128) k_build_tree(Shortlist sl, int max_rank_s
     }
     s_count = cnt;
   }
-  __syncthreads();
+  block_sync();
   if (s_count != N) return;   // host counted N the same way; never differs
   for (int i = threadIdx.x; i < N; i += blockDim.x) {
     parent[i] = s_parent[i];

@@ -4,6 +4,10 @@
 issues, in order: medusa_heads -> tree_attention (with the token fill) ->
 lm_verify -> verify_accept -> compact_kv.  The tree is built once at
 construction ("Medusa deep dive": the tree is chosen ahead of time).
+
+Every buffer of the step is fixed at construction, so the whole step can be
+recorded once as a CUDA graph (``capture``) and re-issued with a single
+launch (``replay``): the step's dozen kernels then cost one host call.
 """
 from __future__ import annotations
 
@@ -59,6 +63,28 @@ class MedusaStep:
         nbytes = workspace_size(dtype_code(lm), B, self.d, self.V, K, N, Hq, Hkv, self.dh,
                                 self.smax)
         self.ws = new_workspace(nbytes, dev)
+
+    def capture(self, h: torch.Tensor, mode: int = TYPICAL, eps: float = 0.09,
+                delta: float = 0.3, commit: bool = True) -> None:
+        """Record one step reading ``h`` into a CUDA graph.  Runs the step once
+        eagerly first (on a side stream, so that every lazy set-up happens
+        outside the capture); that run updates the KV cache and P like any
+        step.  ``h`` must keep its storage: replays read it in place."""
+        side = torch.cuda.Stream(device=h.device)
+        side.wait_stream(torch.cuda.current_stream(h.device))
+        with torch.cuda.stream(side):
+            self.run(h, mode, eps, delta, commit)
+        torch.cuda.current_stream(h.device).wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            self.run(h, mode, eps, delta, commit)
+        self._graph = graph
+
+    def replay(self) -> None:
+        """Enqueue the captured step on the current stream (asynchronous)."""
+        if getattr(self, "_graph", None) is None:
+            raise RuntimeError("capture() has not been called")
+        self._graph.replay()
 
     def run(self, h: torch.Tensor, mode: int = TYPICAL, eps: float = 0.09,
             delta: float = 0.3, commit: bool = True) -> None:
