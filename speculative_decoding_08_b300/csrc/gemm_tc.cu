@@ -48,6 +48,10 @@ constexpr int kThreads = 192;
 constexpr int kTmemCols = 512;
 constexpr int kSmemBytes = 232448;                  // 227 KB, the opt-in maximum
 constexpr int kBarBytes = 512;
+// Column-parallel epilogue scratch (HEADS): a 32 x 33 fp32 staging tile per
+// epilogue warp.
+constexpr int kTileFloats = 32 * 33;
+constexpr int kColParBytes = 4 * kTileFloats * 4;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
 constexpr int kMaxCta = 256;                        // partial records per row
 
@@ -275,6 +279,42 @@ struct SoftStat {
   }
 };
 
+__device__ __forceinline__ float silu_fast(float x) {
+  return __fdividef(x, 1.f + fast_exp2(-1.4426950408889634f * x));
+}
+
+// Column-parallel form of one 32-column block of the HEADS epilogue (few
+// rows: one per sequence): the warp's 32 rows (thread = row, 32 columns in
+// r) are staged in shared memory, then the warp walks its live rows with one
+// lane per column:  U[b, 1 + i, j] = h[b, j] + SiLU(Y[b, i d + j]),
+// U[b, 0, j] = h[b, j].  A row-per-thread epilogue would leave one thread
+// doing all of a CTA's columns for a batch of one.
+template <int KIND>
+__device__ __forceinline__ void colpar_block(const TcArgs& a, float* tile,
+                                             int row_base, int nlive, int f0, int nv,
+                                             const uint32_t (&r)[32]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int c = 0; c < 32; ++c) tile[lane * 33 + c] = __uint_as_float(r[c]);
+  __syncwarp();
+  const bool valid = lane < nv;
+  const int f = f0 + lane;
+  for (int rr = 0; rr < nlive; ++rr) {
+    const float x = tile[rr * 33 + lane];
+    if constexpr (KIND == TC_HEADS) {
+      if (valid) {
+        const int b = row_base + rr;
+        const int i = f / a.d, j = f - i * a.d;
+        const __nv_bfloat16 hraw = a.h[(long long)b * a.d + j];
+        __nv_bfloat16* U = static_cast<__nv_bfloat16*>(a.out) + (long long)b * (a.K + 1) * a.d;
+        U[(long long)(1 + i) * a.d + j] = __float2bfloat16_rn(__bfloat162float(hraw) + silu_fast(x));
+        if (i == 0) U[j] = hraw;
+      }
+    }
+  }
+  __syncwarp();
+}
+
 // One 32-column block of a row's accumulators (raw fp32 bits in r).
 template <int KIND>
 __device__ __forceinline__ void epi_block(const TcArgs& a, int row, int g, int f0, int nv,
@@ -287,9 +327,21 @@ __device__ __forceinline__ void epi_block(const TcArgs& a, int row, int g, int f
   if constexpr (KIND == TC_HEADS) epi_heads(a, row, f0, nv, v);
   if constexpr (KIND == TC_QKV) epi_qkv(a, row, f0, nv, v);
   if constexpr (KIND == TC_DRAFT) {
+    // skip the block when its maximum cannot enter the row's top-8 (after the
+    // first blocks nearly always): one tree maximum instead of 32 checks
+    float t[16];
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (j < nv) tl[g].push(v[j], f0 + j);
+    for (int j = 0; j < 16; ++j)
+      t[j] = fmaxf(j < nv ? v[j] : -INFINITY, j + 16 < nv ? v[j + 16] : -INFINITY);
+#pragma unroll
+    for (int w = 8; w; w >>= 1)
+#pragma unroll
+      for (int j = 0; j < w; ++j) t[j] = fmaxf(t[j], t[j + w]);
+    if (t[0] > tl[g].v[kMaxS - 1]) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < nv) tl[g].push(v[j], f0 + j);
+    }
   }
   if constexpr (KIND == TC_VERIFY) ss[g].push32(v, f0, nv);
 }
@@ -314,6 +366,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* done = bars + 2 * kMaxStages + 4;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kMaxStages + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* epi_tile = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + kBarBytes);
+  constexpr bool kColPar = KIND == TC_HEADS;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cta = blockIdx.x;
@@ -464,6 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // --------------------------------------------------------- epilogue
     const int quarter = warp & 3;
     const int trow = quarter * 32 + lane;
+    float* tile = epi_tile + quarter * kTileFloats;
     int item = 0;
     bool ok = true;
     for (int g0 = 0; g0 < a.n_rgroups && ok; ++g0) {
@@ -494,6 +549,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) +
                                  (uint32_t)(acc * a.G * a.NC + g * a.NC);
           const int ncb = (len + 31) / 32;
+          const int row_base = row0 + g * 128 + quarter * 32;
+          const int nlive = min(32, max(0, a.R - row_base));
+          if (kColPar && nlive == 0) continue;     // warp-uniform: nothing to read
           // two register buffers: the load of block cb + 1 overlaps the work on cb
           uint32_t rb[2][32];
           ptx::tmem_ld32_async(tbase, rb[0]);
@@ -502,11 +560,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int cb = 0; cb < ncb; cb += 2) {
             const bool more1 = cb + 1 < ncb, more2 = cb + 2 < ncb;
             if (more1) ptx::tmem_ld32_async(tbase + (uint32_t)(cb + 1) * 32, rb[1]);
-            if (live) epi_block<KIND>(a, row, g, fc + cb * 32, min(32, len - cb * 32), rb[0], tl, ss);
+            if constexpr (kColPar)
+              colpar_block<KIND>(a, tile, row_base, nlive, fc + cb * 32,
+                                 min(32, len - cb * 32), rb[0]);
+            else if (live)
+              epi_block<KIND>(a, row, g, fc + cb * 32, min(32, len - cb * 32), rb[0], tl, ss);
             if (more1) {
               ptx::tmem_wait32(rb[1]);
               if (more2) ptx::tmem_ld32_async(tbase + (uint32_t)(cb + 2) * 32, rb[0]);
-              if (live)
+              if constexpr (kColPar)
+                colpar_block<KIND>(a, tile, row_base, nlive, fc + (cb + 1) * 32,
+                                   min(32, len - (cb + 1) * 32), rb[1]);
+              else if (live)
                 epi_block<KIND>(a, row, g, fc + (cb + 1) * 32, min(32, len - (cb + 1) * 32), rb[1],
                                 tl, ss);
               if (more2) ptx::tmem_wait32(rb[0]);
@@ -822,7 +887,8 @@ int launch_tc(TcArgs a, const void* X, const void* W, cudaStream_t st) {
     a.xbox = 128;
     a.px = 16384;
   }
-  const int budget = kSmemBytes - 1024 /*alignment*/ - kBarBytes - tail;
+  const int colpar = a.kind == TC_HEADS ? kColParBytes : 0;
+  const int budget = kSmemBytes - 1024 /*alignment*/ - kBarBytes - colpar - tail;
   a.kbs = 0;
   for (int kbs = 4; kbs >= 1; kbs >>= 1) {
     if (a.Kd % (64 * kbs)) continue;
@@ -839,7 +905,7 @@ int launch_tc(TcArgs a, const void* X, const void* W, cudaStream_t st) {
   }
   if (a.kbs == 0) return MDS_EUNSUPPORTED;
   a.xregion = a.stages * a.pxs + tail;
-  const int smem = 1024 + a.xregion + a.stages * a.wst + kBarBytes;
+  const int smem = 1024 + a.xregion + a.stages * a.wst + kBarBytes + colpar;
   CUtensorMap mx, mw[3];
   // X as (64 columns, rows, column blocks): a box of (64, rows, kbs) lands as
   // kbs consecutive K-major tiles, one per 64-wide k-block; W likewise
