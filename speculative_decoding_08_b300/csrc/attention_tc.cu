@@ -13,17 +13,18 @@
 // m with mask(n, m) set (the ancestors of n, n itself and the root).
 //
 // Design.  One work unit is (b, h, group of up to 3 query tiles of 128 rows);
-// its keys [0, P_b + N) are cut into tiles of 64.  The tiles of all units are
+// its keys [0, P_b + N) are cut into tiles of BN = 128 (one query tile) or
+// 64 (several; tensor memory holds their accumulators).  The tiles of all units are
 // laid end to end and split evenly over the CTAs (one per SM), so ragged
 // prefixes and any batch balance across the GPU (stream-K).  A CTA streams
 // its key tiles through a TMA ring once; every query tile of the unit uses
 // each key tile while it is in shared memory:
 //
-//   S = Q K^T      tcgen05, M = 128 query rows, N = 64 keys, K = dh      -> TMEM
+//   S = Q K^T      tcgen05, M = 128 query rows, N = BN keys, K = dh      -> TMEM
 //   softmax        one thread per query row reads its S row from TMEM,
 //                  masks, keeps a running max m (log2 domain) and sum l,
 //                  writes P = 2^(S - m) as bf16 into shared memory
-//   O += P V       tcgen05, M = 128, N = dh, K = 64 keys, V read MN-major -> TMEM
+//   O += P V       tcgen05, M = 128, N = dh, K = BN keys, V read MN-major -> TMEM
 //
 // The running max is raised lazily: O is rescaled only when a row's maximum
 // grows by more than 2^8, so the accumulator in TMEM is rarely touched; the
@@ -31,8 +32,11 @@
 // several CTAs leaves one partial (O, m, l) per CTA; a second kernel, one
 // warp per (unit, row), merges them.  No CTA ever waits for another.
 //
-// Warp roles (192 threads): warp 0 TMA producer, warp 1 TMEM owner and MMA
-// issuer, warps 2..5 softmax / epilogue (thread = TMEM lane = query row).
+// Warp roles (320 threads): warp 0 TMA producer, warp 1 TMEM owner and MMA
+// issuer, warps 2..9 softmax / epilogue.  Two warps share each TMEM lane
+// quarter (thread = query row) and split a key tile's 64 columns; they
+// exchange row maxima and sums through shared memory under an mbarrier, and
+// only the first of the pair touches the O accumulator.
 // Every mbarrier wait is bounded; on timeout the CTA latches MDS_DEV_TIMEOUT,
 // drains its own copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -45,8 +49,7 @@
 namespace mds {
 namespace {
 
-constexpr int kBN = 64;                 // keys per tile
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;          // 2 role warps + 8 softmax warps
 constexpr int kMaxNM = 3;               // query tiles per unit
 constexpr int kMaxCtaAttn = 160;
 constexpr int kMaxBAttn = 256;
@@ -57,6 +60,7 @@ constexpr int kSmemLimit = 232448;      // 227 KB
 struct AttnArgs {
   int B, N, Hq, Hkv, g, Pmax;
   int Mrows;        // N * g query rows per (b, h)
+  int BN;           // keys per tile (128 with one query tile per unit, else 64)
   int NM;           // query tiles per unit
   int n_mg;         // units per (b, h)
   int stages;
@@ -110,11 +114,11 @@ __device__ __forceinline__ uint64_t sdesc_mn128(uint32_t saddr, uint32_t lbo) {
 }
 
 // --------------------------------------------------------- work partition
-// Tiles of sequence b's units: ceil((P_b + N) / 64), or 0 when P_b is out of
-// range (reported once).
+// Tiles of sequence b's units: ceil((P_b + N) / BN), or 0 when P_b is out
+// of range (reported once).
 __device__ __forceinline__ int tiles_of(const AttnArgs& a, int Pb) {
   if (Pb < 0 || Pb + a.N > a.Pmax) return 0;
-  return (Pb + a.N + kBN - 1) / kBN;
+  return (Pb + a.N + a.BN - 1) / a.BN;
 }
 
 struct Seg {
@@ -161,17 +165,19 @@ __device__ __forceinline__ long long cta_start(long long Ttot, int G, int c) {
 }
 
 // --------------------------------------------------------------- kernel
-template <int DH, int NM>
+template <int DH, int NM, int kBN>
 __global__ void __launch_bounds__(kThreads, 1)
     k_tree_attention_tc(const __grid_constant__ CUtensorMap tmQ,
                         const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, AttnArgs a) {
   constexpr int kHalves = DH / 64;
   constexpr uint32_t kQTileBytes = 128 * DH * 2;
-  constexpr uint32_t kKVHalfBytes = kBN * 128;            // 64 keys x 64 dh x 2 B
+  constexpr uint32_t kKVHalfBytes = kBN * 128;            // BN keys x 64 dh x 2 B
   constexpr uint32_t kStageBytes = 2 * kHalves * kKVHalfBytes;
-  constexpr uint32_t kPBytes = 128 * kBN * 2;
-  constexpr uint32_t kSCol0 = 0;                          // S: 2 x 64 columns
+  constexpr uint32_t kPBytes = 128 * kBN * 2;             // one P tile (kBN / 64 atoms)
+  constexpr int kNP = kBN == 128 ? 1 : 2;                 // P buffers
+  constexpr int kWC = kBN / 2;                            // keys per softmax warp
+  constexpr uint32_t kSCol0 = 0;                          // S: 2 x kBN columns
   constexpr uint32_t kOCol0 = 2 * kBN;                    // O: NM x DH columns
 
   extern __shared__ uint8_t smem_raw[];
@@ -180,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int S = a.stages;
   uint8_t* sQ = smem;
   uint8_t* sP = sQ + NM * kQTileBytes;
-  uint8_t* sKV = sP + 2 * kPBytes;
+  uint8_t* sKV = sP + kNP * kPBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + S * kStageBytes);
   uint64_t* kv_full = bars;               // [S]
   uint64_t* kv_empty = bars + 8;          // [S]
@@ -194,7 +200,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* done = bars + 31;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 32);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* pre = reinterpret_cast<int*>(bars + 34);   // [B + 1]
+  uint64_t* xbar = bars + 34;                     // [4] pair exchanges, one per lane quarter
+  float* xbuf = reinterpret_cast<float*>(bars + 38);   // [2 parity][2 half][128 rows]
+  int* pre = reinterpret_cast<int*>(xbuf + 512);  // [B + 1]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cta = blockIdx.x;
@@ -218,13 +226,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&s_full[i], 1);
-      ptx::mbar_init(&s_empty[i], 4);
-      ptx::mbar_init(&p_full[i], 4);
+      ptx::mbar_init(&s_empty[i], 8);
+      ptx::mbar_init(&p_full[i], 8);
       ptx::mbar_init(&p_empty[i], 1);
     }
     ptx::mbar_init(q_full, 1);
     ptx::mbar_init(q_empty, 1);
-    ptx::mbar_init(o_empty, 4);
+    ptx::mbar_init(o_empty, 8);
+    for (int q = 0; q < 4; ++q) ptx::mbar_init(&xbar[q], 2);
     ptx::mbar_init(done, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
@@ -303,8 +312,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     // O[m] += P[it % 2] V[stage]
     auto issue_pv = [&]() {
-      const int pb = pv_it & 1;
-      if (!wait(&p_full[pb], (pv_it >> 1) & 1)) return;
+      const int pb = pv_it % kNP;
+      if (!wait(&p_full[pb], (pv_it / kNP) & 1)) return;
       ptx::tc_fence_after();
       if (lane == 0) {
         const uint32_t aP = ptx::smem_addr(sP + pb * kPBytes);
@@ -312,7 +321,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t dO = tmem + kOCol0 + (uint32_t)(pv_m * DH);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          ptx::mma_bf16(dO, ptx::sdesc_k128(aP + kk * 32), sdesc_mn128(bV + kk * 2048, kKVHalfBytes),
+          ptx::mma_bf16(dO, ptx::sdesc_k128(aP + (kk >> 2) * 16384 + (kk & 3) * 32),
+                        sdesc_mn128(bV + kk * 2048, kKVHalfBytes),
                         idO, (pv_first && kk == 0) ? 0u : 1u);
         ptx::mma_commit(&p_empty[pb]);
         if (pv_lastm) ptx::mma_commit(&kv_empty[pv_stage]);
@@ -381,16 +391,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------- softmax and epilogue
-    const int quarter = warp & 3;
+    const int sw = warp - 2;                          // 0..7
+    const int quarter = warp & 3;                     // TMEM lane quarter
+    const int half = sw >> 2;                         // columns [32 half, 32 half + 32)
     const int t = quarter * 32 + lane;                // TMEM lane = row in tile
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     const int g = a.g;
-    int it = 0, segc = 0;
+    int it = 0, segc = 0, xc = 0;
     bool ok = true;
     auto wait = [&](uint64_t* bar, uint32_t par) {
       if (!ok) return false;
       if (!ptx::mbar_wait(bar, par, abort_flag, kWaitNs)) ok = false;
       return ok;
+    };
+    // value of this row from the other warp of the pair (exchange number xc)
+    auto exchange = [&](float mine) -> float {
+      float* slot = xbuf + (xc & 1) * 256;
+      slot[half * 128 + t] = mine;
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&xbar[quarter]);
+      const bool got = wait(&xbar[quarter], xc & 1);
+      ++xc;
+      return got ? slot[(half ^ 1) * 128 + t] : 0.f;
     };
     Seg s;
     while (ok && iter.next(a, pre, s)) {
@@ -415,45 +437,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int Pb = s.Pb;
       for (int j = s.j0; j < s.j1 && ok; ++j) {
-        const int key0 = j * kBN;
+        const int key0 = j * kBN + half * kWC;          // this warp's first key
         for (int m = 0; m < NM; ++m, ++it) {
           const int sb = it & 1;
           if (!wait(&s_full[sb], (it >> 1) & 1)) break;
           ptx::tc_fence_after();
-          float sv[kBN];
+          float sv[kWC];
           {
-            uint32_t r0[32], r1[32];
-            ptx::tmem_ld32_async(lane_base + kSCol0 + sb * kBN, r0);
-            ptx::tmem_ld32_async(lane_base + kSCol0 + sb * kBN + 32, r1);
-            ptx::tmem_wait32(r0);
-            ptx::tmem_wait32(r1);
+            uint32_t r0[32];
+            ptx::tmem_ld32_async(lane_base + kSCol0 + sb * kBN + half * kWC, r0);
+            if constexpr (kWC == 64) {
+              uint32_t r1[32];
+              ptx::tmem_ld32_async(lane_base + kSCol0 + sb * kBN + half * kWC + 32, r1);
+              ptx::tmem_wait32(r0);
+              ptx::tmem_wait32(r1);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              sv[c] = __uint_as_float(r0[c]);
-              sv[32 + c] = __uint_as_float(r1[c]);
+              for (int c = 0; c < 32; ++c) sv[32 + c] = __uint_as_float(r1[c]);
+            } else {
+              ptx::tmem_wait32(r0);
             }
+#pragma unroll
+            for (int c = 0; c < 32; ++c) sv[c] = __uint_as_float(r0[c]);
           }
           ptx::tc_fence_before();
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive(&s_empty[sb]);
           // mask; the row maximum is taken on raw scores (scale > 0)
           float mx = -INFINITY;
-          if (key0 + kBN <= Pb) {
-            // a tile inside the prefix: every key is visible to live rows
+          if (key0 + kWC <= Pb) {
+            // columns inside the prefix: every key is visible to live rows
             if (!live[m]) {
 #pragma unroll
-              for (int c = 0; c < kBN; ++c) sv[c] = -INFINITY;
+              for (int c = 0; c < kWC; ++c) sv[c] = -INFINITY;
             }
             float t8[8];
 #pragma unroll
             for (int c = 0; c < 8; ++c) t8[c] = sv[c];
 #pragma unroll
-            for (int c = 8; c < kBN; ++c) t8[c & 7] = fmaxf(t8[c & 7], sv[c]);
+            for (int c = 8; c < kWC; ++c) t8[c & 7] = fmaxf(t8[c & 7], sv[c]);
             mx = fmaxf(fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3])),
                        fmaxf(fmaxf(t8[4], t8[5]), fmaxf(t8[6], t8[7])));
           } else {
 #pragma unroll
-            for (int c = 0; c < kBN; ++c) {
+            for (int c = 0; c < kWC; ++c) {
               const int key = key0 + c;
               const int mm = key - Pb;
               const uint64_t w = mm < 64 ? mw0[m] : mw1[m];
@@ -462,27 +488,32 @@ __global__ void __launch_bounds__(kThreads, 1)
               mx = fmaxf(mx, sv[c]);
             }
           }
+          mx = fmaxf(mx, exchange(mx));                  // row maximum over all 64 keys
+          if (!ok) break;
           mx *= a.scale_log2;
           const float mold = mref[m];
           const float mnew = fmaxf(mold, mx);
+          // both warps of the pair see the same maximum and decide alike
           const bool need = mold != -INFINITY && mnew > mold + kRescaleLog2;
           if (__any_sync(0xffffffffu, need)) {
-            // rescale this tile's O: every earlier P V must be complete.  The
-            // commit on p_empty after P V (it - 1) covers all earlier MMAs;
-            // P V (it - 3) was awaited one item ago, so the phase is exact.
-            if (!wait(&p_empty[(it - 1) & 1], ((it - 1) >> 1) & 1)) break;
-            ptx::tc_fence_after();
             const float f = need ? ex2(mold - mnew) : 1.f;
-            const uint32_t ocol = lane_base + kOCol0 + (uint32_t)(m * DH);
+            if (half == 0) {
+              // rescale this tile's O: every earlier P V must be complete.  The
+              // commit on p_empty after P V (it - 1) covers all earlier MMAs;
+              // P V (it - 3) was awaited one item ago, so the phase is exact.
+              if (!wait(&p_empty[(it - 1) % kNP], ((it - 1) / kNP) & 1)) break;
+              ptx::tc_fence_after();
+              const uint32_t ocol = lane_base + kOCol0 + (uint32_t)(m * DH);
 #pragma unroll
-            for (int cb = 0; cb < DH / 32; ++cb) {
-              float ov[32];
-              ptx::tmem_ld32(ocol + cb * 32, ov);
+              for (int cb = 0; cb < DH / 32; ++cb) {
+                float ov[32];
+                ptx::tmem_ld32(ocol + cb * 32, ov);
 #pragma unroll
-              for (int c = 0; c < 32; ++c) ov[c] *= f;
-              tmem_st32(ocol + cb * 32, ov);
+                for (int c = 0; c < 32; ++c) ov[c] *= f;
+                tmem_st32(ocol + cb * 32, ov);
+              }
+              ptx::tc_fence_before();
             }
-            ptx::tc_fence_before();
             if (need) {
               lsum[m] *= f;
               mref[m] = mnew;
@@ -491,12 +522,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (mref[m] == -INFINITY) mref[m] = mnew;
           const float mr = mref[m];
           // P = 2^(s - m) rounded to bf16; l sums the rounded values
-          uint32_t pk[kBN / 2];
+          uint32_t pk[kWC / 2];
           float ls4[4] = {0.f, 0.f, 0.f, 0.f};
           const float sc = a.scale_log2;
           const float nmr = mr == -INFINITY ? 0.f : -mr;
 #pragma unroll
-          for (int c = 0; c < kBN; c += 2) {
+          for (int c = 0; c < kWC; c += 2) {
             // 2^(s * scale - m); masked keys (s = -inf) give 0
             const float p0 = mr == -INFINITY ? 0.f : ex2(fmaf(sv[c], sc, nmr));
             const float p1 = mr == -INFINITY ? 0.f : ex2(fmaf(sv[c + 1], sc, nmr));
@@ -506,39 +537,52 @@ __global__ void __launch_bounds__(kThreads, 1)
             pk[c / 2] = *reinterpret_cast<const uint32_t*>(&b2);
           }
           lsum[m] += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
-          if (!wait(&p_empty[sb], ((it >> 1) & 1) ^ 1u)) break;
-          uint8_t* prow = sP + sb * kPBytes + t * 128;
+          const int pbuf = it % kNP;
+          if (!wait(&p_empty[pbuf], ((it / kNP) & 1) ^ 1u)) break;
+          // this warp's keys [half kWC, half kWC + kWC) of the row: 16-byte
+          // chunks of the swizzled K-major P tile (64-key atoms of 16 KB)
+          uint8_t* prow = sP + pbuf * kPBytes + t * 128;
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(prow + ((c ^ (t & 7)) << 4)) =
+          for (int c = 0; c < kWC / 8; ++c) {
+            const int kl = half * kWC + c * 8;              // first key of the chunk
+            const int ch = (kl & 63) >> 3;
+            *reinterpret_cast<uint4*>(prow + (kl >> 6) * 16384 + ((ch ^ (t & 7)) << 4)) =
                 make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+          }
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(&p_full[sb]);
+          if (lane == 0) ptx::mbar_arrive(&p_full[pbuf]);
         }
       }
       if (!ok) break;
       // ---- segment epilogue: final rows, or a partial record that the
-      //      merge kernel combines with the unit's other segments
+      //      merge kernel combines with the unit's other segments.  Each warp
+      //      of the pair writes half of the O columns.
       const bool whole = s.j0 == 0 && s.j1 == s.nt;
       int slot = 0;
       if (!whole) slot = 2 * cta + (cta_start(Ttot, a.G, cta) >= s.U0 ? 0 : 1);
       const int rows_unit = NM * 128;
+      float ltot[kMaxNM];
+#pragma unroll
+      for (int m = 0; m < kMaxNM; ++m)
+        if (m < NM) ltot[m] = lsum[m] + exchange(lsum[m]);
+      if (!ok) break;
       // every P V of the segment is complete once P V (it - 1) is
-      if (!wait(&p_empty[(it - 1) & 1], ((it - 1) >> 1) & 1)) break;
+      if (!wait(&p_empty[(it - 1) % kNP], ((it - 1) / kNP) & 1)) break;
       ptx::tc_fence_after();
+      constexpr int kHalfCols = DH / 2;
       for (int m = 0; m < NM && ok; ++m) {
         const int r = (s.mg * NM + m) * 128 + t;
-        const uint32_t ocol = lane_base + kOCol0 + (uint32_t)(m * DH);
+        const uint32_t ocol = lane_base + kOCol0 + (uint32_t)(m * DH + half * kHalfCols);
         if (whole) {
-          const float inv = lsum[m] > 0.f ? 1.f / lsum[m] : 0.f;
+          const float inv = ltot[m] > 0.f ? 1.f / ltot[m] : 0.f;
           __nv_bfloat16* dst = nullptr;
           if (live[m]) {
             const int n = r / g, jj = r - n * g;
-            dst = a.o + (((long long)s.b * a.N + n) * a.Hq + s.h * g + jj) * DH;
+            dst = a.o + (((long long)s.b * a.N + n) * a.Hq + s.h * g + jj) * DH + half * kHalfCols;
           }
 #pragma unroll
-          for (int cb = 0; cb < DH / 32; ++cb) {
+          for (int cb = 0; cb < kHalfCols / 32; ++cb) {
             float ov[32];
             ptx::tmem_ld32(ocol + cb * 32, ov);
             if (dst) {
@@ -554,11 +598,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         } else {
-          float* po = a.part + ((long long)slot * rows_unit + m * 128 + t) * DH;
+          float* po = a.part + ((long long)slot * rows_unit + m * 128 + t) * DH + half * kHalfCols;
           float* pml = a.part + (long long)2 * a.G * rows_unit * DH +
                        ((long long)slot * rows_unit + m * 128 + t) * 2;
 #pragma unroll
-          for (int cb = 0; cb < DH / 32; ++cb) {
+          for (int cb = 0; cb < kHalfCols / 32; ++cb) {
             float ov[32];
             ptx::tmem_ld32(ocol + cb * 32, ov);
             if (live[m]) {
@@ -568,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     make_float4(ov[4 * q], ov[4 * q + 1], ov[4 * q + 2], ov[4 * q + 3]);
             }
           }
-          if (live[m]) *reinterpret_cast<float2*>(pml) = make_float2(mref[m], lsum[m]);
+          if (live[m] && half == 0) *reinterpret_cast<float2*>(pml) = make_float2(mref[m], ltot[m]);
         }
       }
       if (!ok) break;
@@ -674,7 +718,7 @@ __global__ void __launch_bounds__(256) k_attention_merge(AttnArgs a) {
 
 // ----------------------------------------------------------------- host
 struct Plan {
-  int NM, n_mg, stages, G;
+  int NM, n_mg, stages, G, BN;
   size_t smem;
 };
 
@@ -683,10 +727,11 @@ Plan plan(int N, int g, int dh, int num_sms) {
   const int mtiles = (N * g + 127) / 128;
   p.n_mg = (mtiles + kMaxNM - 1) / kMaxNM;
   p.NM = (mtiles + p.n_mg - 1) / p.n_mg;
+  p.BN = p.NM == 1 ? 128 : 64;
   const size_t q = (size_t)p.NM * 128 * dh * 2;
-  const size_t pbuf = 2 * (size_t)128 * kBN * 2;
-  const size_t stage = 2 * (size_t)kBN * dh * 2;
-  const size_t fixed = 1024 /*align*/ + 34 * 8 + (kMaxBAttn + 1) * 4;
+  const size_t pbuf = (p.BN == 128 ? 1 : 2) * (size_t)128 * p.BN * 2;
+  const size_t stage = 2 * (size_t)p.BN * dh * 2;
+  const size_t fixed = 1024 /*align*/ + 38 * 8 + 512 * 4 + (kMaxBAttn + 1) * 4;
   int st = (int)((kSmemLimit - q - pbuf - fixed) / stage);
   p.stages = st > 6 ? 6 : st;
   p.smem = q + pbuf + (size_t)p.stages * stage + fixed;
@@ -700,6 +745,8 @@ bool g_attr_set[2][kMaxNM + 1] = {};
 template <int DH, int NM>
 int launch_one(const Plan& p, const CUtensorMap& mq, const CUtensorMap& mk,
                const CUtensorMap& mv, const AttnArgs& a, cudaStream_t st);
+// keys per tile: 128 with one query tile per unit (S 2 x 128 + O 128 TMEM
+// columns), else 64 (S 2 x 64 + O NM x DH)
 
 template <int DH>
 int launch_nm(const Plan& p, const CUtensorMap& mq, const CUtensorMap& mk,
@@ -715,14 +762,15 @@ int launch_nm(const Plan& p, const CUtensorMap& mq, const CUtensorMap& mk,
 template <int DH, int NM>
 int launch_one(const Plan& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                const AttnArgs& a, cudaStream_t st) {
+  constexpr int BN = NM == 1 ? 128 : 64;
   bool& set = g_attr_set[DH == 128 ? 1 : 0][NM];
   if (!set) {
-    if (cudaFuncSetAttribute(k_tree_attention_tc<DH, NM>,
+    if (cudaFuncSetAttribute(k_tree_attention_tc<DH, NM, BN>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit) != cudaSuccess)
       return MDS_ECUDA;
     set = true;
   }
-  k_tree_attention_tc<DH, NM><<<p.G, kThreads, p.smem, st>>>(mq, mk, mv, a);
+  k_tree_attention_tc<DH, NM, BN><<<p.G, kThreads, p.smem, st>>>(mq, mk, mv, a);
   return MDS_OK;
 }
 
@@ -761,6 +809,7 @@ int attention_tc(int B, int N, int Hq, int Hkv, int dh, int Pmax, const int32_t*
   a.g = gq;
   a.Pmax = Pmax;
   a.Mrows = N * gq;
+  a.BN = p.BN;
   a.NM = p.NM;
   a.n_mg = p.n_mg;
   a.stages = p.stages;
@@ -775,9 +824,9 @@ int attention_tc(int B, int N, int Hq, int Hkv, int dh, int Pmax, const int32_t*
   CUtensorMap mq, mk, mv;
   int rc = tensor_map_bf16(&mq, q, (long long)B * Hkv * a.Mrows, dh, 2, 128, 1);
   if (rc) return rc;
-  rc = tensor_map_bf16(&mk, Kc, (long long)B * Hkv * Pmax, dh, 2, kBN, 1);
+  rc = tensor_map_bf16(&mk, Kc, (long long)B * Hkv * Pmax, dh, 2, p.BN, 1);
   if (rc) return rc;
-  rc = tensor_map_bf16(&mv, Vc, (long long)B * Hkv * Pmax, dh, 2, kBN, 1);
+  rc = tensor_map_bf16(&mv, Vc, (long long)B * Hkv * Pmax, dh, 2, p.BN, 1);
   if (rc) return rc;
   rc = dh == 128 ? launch_nm<128>(p, mq, mk, mv, a, st) : launch_nm<64>(p, mq, mk, mv, a, st);
   if (rc) return rc;

@@ -15,8 +15,11 @@
 // costs ceil(R/8) KB of X plus the CTA's W tile, and the ring holds 2-4x
 // more weight bytes in flight than with whole 16 KB X tiles.  One thread
 // issues tcgen05.mma with M = 128 rows (X) and N = up to 256 features (W);
-// the fp32 accumulators live in tensor memory, double-buffered so that the
-// epilogue of one feature chunk overlaps the MMAs of the next.
+// the fp32 accumulators live in tensor memory (double-buffered for up to 128
+// rows, so that the epilogue of one feature chunk overlaps the MMAs of the
+// next; single-buffered 2 x 256 columns for more rows).  N is 256 features
+// per MMA where the CTA's range allows: a tcgen05.mma costs about the same
+// for any N up to 256.
 //
 // Warp roles (192 threads): warp 0 = TMA producer, warp 1 = TMEM allocator and
 // MMA issuer, warps 2..5 = epilogue (one TMEM lane = one row per thread).
@@ -59,6 +62,7 @@ struct TcArgs {
   int R, F, Kd;
   int n_units, n_cta;
   int G, NC;
+  int nacc;         // accumulator buffers in TMEM (nacc * G * NC <= 512 columns)
   int stages;       // TMA ring depth
   int kbs;          // 64-wide k-blocks per stage (one TMA box each for X and W)
   int px;           // bytes between consecutive k-block X tiles
@@ -214,25 +218,31 @@ struct TopList {
     }
   }
   // Insert keeping (value desc, id asc); ids arrive in increasing order, so
-  // an equal value never displaces an earlier (lower) id.
+  // an equal value never displaces an earlier (lower) id.  The entries that
+  // stay ahead of x form a prefix; every slot's new content is picked with
+  // independent compares and selects (no chain of dependent swaps).
   __device__ __forceinline__ void push(float x, int i) {
     if (!(x > v[kMaxS - 1])) return;
+    bool ahead[kMaxS];
+#pragma unroll
+    for (int j = 0; j < kMaxS; ++j) ahead[j] = v[j] >= x;
+    float nvv[kMaxS];
+    int nid[kMaxS];
+    nvv[0] = ahead[0] ? v[0] : x;
+    nid[0] = ahead[0] ? id[0] : i;
+#pragma unroll
+    for (int j = 1; j < kMaxS; ++j) {
+      nvv[j] = ahead[j] ? v[j] : (ahead[j - 1] ? x : v[j - 1]);
+      nid[j] = ahead[j] ? id[j] : (ahead[j - 1] ? i : id[j - 1]);
+    }
 #pragma unroll
     for (int j = 0; j < kMaxS; ++j) {
-      if (x > v[j]) {
-        const float tv = v[j];
-        const int ti = id[j];
-        v[j] = x;
-        id[j] = i;
-        x = tv;
-        i = ti;
-      }
+      v[j] = nvv[j];
+      id[j] = nid[j];
     }
   }
 };
 
-// Running softmax statistics of one row over 32-column blocks: maximum m,
-// its lowest column (argmax), S = sum e^(z - m), Q = sum z e^(z - m).
 struct SoftStat {
   float m, S, Q;
   int am;
@@ -466,8 +476,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int len = min(a.NC, rg.f_end - fc);
           const int npad = (len + 15) / 16 * 16;
           const uint32_t idesc = ptx::idesc_bf16(128, npad);
-          const int acc = item & 1;
-          const uint32_t aphase = (item >> 1) & 1;
+          const int acc = item % a.nacc;
+          const uint32_t aphase = (item / a.nacc) & 1;
           if (!ptx::mbar_wait(&tempty[acc], aphase ^ 1u, abort_flag, kWaitLimitNs)) {
             ok = false;
             break;
@@ -534,8 +544,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int ch = 0; ch < rg.n_chunks; ++ch, ++item) {
         const int fc = rg.f_begin + ch * a.NC;
         const int len = min(a.NC, rg.f_end - fc);
-        const int acc = item & 1;
-        const uint32_t aphase = (item >> 1) & 1;
+        const int acc = item % a.nacc;
+        const uint32_t aphase = (item / a.nacc) & 1;
         if (!ptx::mbar_wait(&tfull[acc], aphase, abort_flag, kWaitLimitNs)) {
           ok = false;
           break;
@@ -866,7 +876,20 @@ int launch_tc(TcArgs a, const void* X, const void* W, cudaStream_t st) {
   if (a.Kd % 64 != 0) return MDS_EUNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(X) | reinterpret_cast<uintptr_t>(W)) & 15) return MDS_EINVAL;
   a.G = a.R <= 128 ? 1 : 2;
-  a.NC = 256 / a.G;
+  // Features per MMA (N) and accumulator buffers.  Every tcgen05.mma costs
+  // about the same up to N = 256, so N is 256 where TMEM allows: with one
+  // 128-row group, double-buffered (the epilogue of one chunk overlaps the
+  // MMAs of the next).  With two groups, the verify pass (wide CTA ranges,
+  // light epilogue) takes one 2 x 256-column accumulator; the others keep
+  // N = 128 double-buffered, since their ranges are narrow or their
+  // epilogue is heavy.
+  if (a.G == 1 || a.kind == TC_VERIFY) {
+    a.NC = 256;
+    a.nacc = a.G == 1 ? 2 : 1;
+  } else {
+    a.NC = 128;
+    a.nacc = 2;
+  }
   a.n_rgroups = (a.R + 128 * a.G - 1) / (128 * a.G);
   a.n_units = (a.F + 15) / 16;
   a.n_cta = grid_ctas(a.F);
