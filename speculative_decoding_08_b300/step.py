@@ -65,19 +65,44 @@ class MedusaStep:
         self.ws = new_workspace(nbytes, dev)
 
     def capture(self, h: torch.Tensor, mode: int = TYPICAL, eps: float = 0.09,
-                delta: float = 0.3, commit: bool = True) -> None:
+                delta: float = 0.3, commit: bool = True,
+                h_host: Optional[torch.Tensor] = None, outputs_to_host: bool = False) -> None:
         """Record one step reading ``h`` into a CUDA graph.  Runs the step once
         eagerly first (on a side stream, so that every lazy set-up happens
         outside the capture); that run updates the KV cache and P like any
-        step.  ``h`` must keep its storage: replays read it in place."""
-        side = torch.cuda.Stream(device=h.device)
-        side.wait_stream(torch.cuda.current_stream(h.device))
-        with torch.cuda.stream(side):
+        step.  ``h`` must keep its storage: replays read it in place.
+
+        ``h_host`` (pinned CPU tensor shaped like ``h``): every replay first
+        copies it into ``h``.  ``outputs_to_host``: every replay ends by
+        copying L, path, the tree tokens and next_root into pinned CPU
+        tensors, available as ``self.host_out`` once the replay's stream has
+        been synchronised.  A step then costs one graph launch."""
+        dev = h.device
+        if h_host is not None and (h_host.is_cuda or not h_host.is_pinned()):
+            raise ValueError("h_host must be a pinned CPU tensor")
+        self.host_out = None
+        if outputs_to_host:
+            self.host_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory()
+                             for k, v in (("L", self.L), ("path", self.path), ("tok", self.tok),
+                                          ("next_root", self.next_root))}
+
+        def body():
+            if h_host is not None:
+                h.copy_(h_host, non_blocking=True)
             self.run(h, mode, eps, delta, commit)
-        torch.cuda.current_stream(h.device).wait_stream(side)
+            if self.host_out is not None:
+                for k, src in (("L", self.L), ("path", self.path), ("tok", self.tok),
+                               ("next_root", self.next_root)):
+                    self.host_out[k].copy_(src, non_blocking=True)
+
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            body()
+        torch.cuda.current_stream(dev).wait_stream(side)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=side):
-            self.run(h, mode, eps, delta, commit)
+            body()
         self._graph = graph
 
     def replay(self) -> None:

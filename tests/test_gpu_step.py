@@ -134,3 +134,29 @@ def test_step_full_size(mds, cfg, sample, modes):
     w = ms.workload(cfg)
     compare_step(mds, w, sample, modes)
     torch.cuda.empty_cache()
+
+
+def test_captured_step_with_host_buffers(mds):
+    """MedusaStep.capture with a pinned host input and host outputs: one graph
+    replay reproduces the eager step (h copied in, tokens and path copied out)."""
+    w = MINI
+    x = ms.make_inputs(w)
+    step, h = make_step(mds, w, x)
+    step.run(h, mode=1, eps=w.eps, delta=w.delta, commit=False)
+    torch.cuda.synchronize()
+    want = dict(L=host(step.L), path=host(step.path), tok=host(step.tok), nr=host(step.next_root))
+    h_host = h.cpu().pin_memory()
+    h_dev = torch.zeros_like(h)
+    step.capture(h_dev, mode=1, eps=w.eps, delta=w.delta, commit=False, h_host=h_host,
+                 outputs_to_host=True)
+    for t in step.host_out.values():
+        t.zero_()
+    h_dev.zero_()
+    step.replay()
+    torch.cuda.synchronize()
+    assert mds.status_check(step.ws) == 0
+    np.testing.assert_array_equal(step.host_out["L"].numpy(), want["L"])
+    np.testing.assert_array_equal(step.host_out["path"].numpy(), want["path"])
+    np.testing.assert_array_equal(step.host_out["tok"].numpy(), want["tok"])
+    np.testing.assert_array_equal(step.host_out["next_root"].numpy(), want["nr"])
+    assert torch.equal(h_dev, h)
