@@ -1,6 +1,7 @@
 // C ABI entry points: host-side argument checks, workspace carving, and
 // dispatch to the kernels.  Every data-path operation runs in a kernel.
 #include <atomic>
+#include <stdlib.h>
 #include <string.h>
 
 #include "common.cuh"
@@ -11,6 +12,20 @@ using namespace mds;
 namespace mds {
 static std::atomic<long long> g_launches{0};
 void count_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("MDS_PDL");
+    return !(v && v[0] == '0');
+  }();
+  return on;
+}
+bool ksplit_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("MDS_KSPLIT");
+    return !(v && v[0] == '0');
+  }();
+  return on;
+}
 }  // namespace mds
 
 namespace {
@@ -53,15 +68,26 @@ char* scratch(void* ws) { return static_cast<char*>(ws) + kWsScratch; }
 bool shape_ok(int d, int dh) { return d > 0 && d % 64 == 0 && (dh == 64 || dh == 128); }
 
 size_t need_heads(int dtype, int B, int d, int V, int K) {
-  (void)d;
-  if (dtype == MDS_BF16) return kWsScratch + align_up(tc_partial_bytes(B * (K + 1), true));
+  if (dtype == MDS_BF16) {
+    // the heads pass's K-split partials and then the draft pass's candidate
+    // lists share the scratch region (the heads pass is done before the
+    // draft pass writes)
+    const size_t kp = tc_kpart_bytes(B, K * d, d);
+    const size_t dr = tc_partial_bytes(B * (K + 1), true);
+    return kWsScratch + align_up(kp > dr ? kp : dr);
+  }
   return kWsScratch + align_up((size_t)B * (K + 1) * V * 4);
 }
 size_t need_attention(int dtype, int B, int N, int d, int Hq, int Hkv, int dh) {
   const size_t rows = (size_t)B * N;
   size_t n = kWsScratch + align_up(rows * d * esize(dtype)) + 2 * align_up(rows * Hq * 128 * esize(dtype));
-  if (dtype == MDS_BF16 && Hkv > 0 && Hq % Hkv == 0)
+  if (dtype == MDS_BF16 && Hkv > 0 && Hq % Hkv == 0) {
     n += align_up(attention_tc_partial_bytes(N, Hq / Hkv, dh));
+    // K-split partials of the QKV and output projections (one at a time)
+    const size_t kq = tc_kpart_bytes((int)rows, (Hq + 2 * Hkv) * dh, d);
+    const size_t ko = tc_kpart_bytes((int)rows, d, Hq * dh);
+    n += align_up(kq > ko ? kq : ko);
+  }
   return n;
 }
 size_t need_verify(int dtype, int B, int N, int V) {
@@ -143,7 +169,7 @@ int mds_medusa_heads(int dtype, int B, int d, int V, int K, const void* h, const
   if (!aligned16(h) || !aligned16(W) || !aligned16(lm) || !aligned16(U)) return MDS_EINVAL;
   cudaStream_t st = as_stream(stream);
   if (dtype == MDS_BF16) {
-    int rc = gemm_tc_heads(h, B, W, K, d, U, ws, st);
+    int rc = gemm_tc_heads(h, B, W, K, d, U, scratch(ws), ws, st);
     if (rc) return rc;
     return lm_draft_tc(U, B, K, d, lm, V, sl, smax, root, topk_id, topk_val, scratch(ws), ws, st);
   }
@@ -194,12 +220,13 @@ int mds_tree_attention(int dtype, int B, int N, int d, int V, int Hq, int Hkv, i
                         ws, st);
   if (rc) return rc;
   if (dtype == MDS_BF16) {
-    rc = gemm_tc_qkv(x, B, N, d, wqkv, Hq, Hkv, dh, Pmax, P, q, Kc, Vc, ws, st);
-    if (rc) return rc;
     void* part = static_cast<char*>(q) + 2 * align_up(rows * Hq * 128 * esize(dtype));
+    void* kpart = static_cast<char*>(part) + align_up(attention_tc_partial_bytes(N, Hq / Hkv, dh));
+    rc = gemm_tc_qkv(x, B, N, d, wqkv, Hq, Hkv, dh, Pmax, P, q, Kc, Vc, kpart, ws, st);
+    if (rc) return rc;
     rc = attention_tc(B, N, Hq, Hkv, dh, Pmax, P, mask, words, q, Kc, Vc, o, part, ws, st);
     if (rc) return rc;
-    return gemm_tc_store(o, (int)rows, wo, d, Hq * dh, y, d, ws, st);
+    return gemm_tc_store(o, (int)rows, wo, d, Hq * dh, y, d, kpart, ws, st);
   }
   EpiArgs e;
   e.kind = EPI_QKV;

@@ -17,6 +17,7 @@ __global__ void __launch_bounds__(256) k_embed(int N, int d, int V, int K, int s
                                                const int32_t* topk_id, const int32_t* depth,
                                                const int32_t* rank, const T* __restrict__ emb,
                                                T* __restrict__ x, void* ws) {
+  grid_dep_launch();   // the QKV projection may start loading its weights
   const int r = blockIdx.x, b = r / N, n = r % N;
   __shared__ int s_tok;
   if (threadIdx.x == 0) {

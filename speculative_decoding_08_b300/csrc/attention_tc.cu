@@ -188,8 +188,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sP = sQ + NM * kQTileBytes;
   uint8_t* sKV = sP + kNP * kPBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + S * kStageBytes);
-  uint64_t* kv_full = bars;               // [S]
-  uint64_t* kv_empty = bars + 8;          // [S]
+  // K and V of a stage have their own barriers: K is free again once the S
+  // MMAs of its tile are done, V only after the P V MMAs.
+  uint64_t* k_full = bars;                // [S]
+  uint64_t* k_empty = bars + 8;           // [S]
   uint64_t* s_full = bars + 16;           // [2]
   uint64_t* s_empty = bars + 18;          // [2]
   uint64_t* p_full = bars + 20;           // [2]
@@ -201,11 +203,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 32);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   uint64_t* xbar = bars + 34;                     // [4] pair exchanges, one per lane quarter
-  float* xbuf = reinterpret_cast<float*>(bars + 38);   // [2 parity][2 half][128 rows]
+  uint64_t* v_full = bars + 38;           // [S]
+  uint64_t* v_empty = bars + 46;          // [S]
+  float* xbuf = reinterpret_cast<float*>(bars + 54);   // [2 parity][2 half][128 rows]
   int* pre = reinterpret_cast<int*>(xbuf + 512);  // [B + 1]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cta = blockIdx.x;
+  // The stream's next kernel may start its own set-up from here on.  The
+  // scan of P below may run before the previous kernel (the QKV projection,
+  // which does not write P) has finished; everything after the set-up
+  // barrier waits for it.
+  grid_dep_launch();
 
   // tile prefix over sequences (every thread reads P; thread 0 scans)
   if (threadIdx.x == 0) {
@@ -221,8 +230,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     pre[a.B] = acc;
     if (bad && cta == 0) latch_error(a.ws, MDS_DEV_KV_CAPACITY);
     for (int s = 0; s < S; ++s) {
-      ptx::mbar_init(&kv_full[s], 1);
-      ptx::mbar_init(&kv_empty[s], 1);
+      ptx::mbar_init(&k_full[s], 1);
+      ptx::mbar_init(&k_empty[s], 1);
+      ptx::mbar_init(&v_full[s], 1);
+      ptx::mbar_init(&v_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&s_full[i], 1);
@@ -245,6 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_before();
   ptx::cta_barrier(1, kThreads);
   ptx::tc_fence_after();
+  grid_dep_wait();
   const uint32_t tmem = *tmem_slot;
   const long long Ttot = (long long)pre[a.B];
   SegIter iter;
@@ -256,10 +268,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint64_t pol_kv = ptx::policy_evict_first();
       const uint64_t pol_q = ptx::policy_evict_last();
-      int kvt = 0, segc = 0;
+      // Requests in the order the slots free up: K of tile t (its slot frees
+      // when the S MMAs of tile t - S are done), then V of tile t - 1 (slot
+      // frees after the P V MMAs of tile t - 1 - S).  At a unit's first tile
+      // the pending V goes before the unit's Q: the P V MMAs of the previous
+      // tile precede that unit's last S MMA, which frees Q.
+      int kvt = 0, vt = 0, segc = 0;
+      int v_row = 0;                  // KV row of the pending V tile (vt)
       bool ok = true;
+      auto issue_v = [&]() -> bool {
+        const int st = vt % S;
+        if (!ptx::mbar_wait(&v_empty[st], ((vt / S) & 1) ^ 1u, abort_flag, kWaitNs)) return false;
+        uint8_t* sv = sKV + st * kStageBytes + kHalves * kKVHalfBytes;
+        ptx::mbar_arrive_expect_tx(&v_full[st], kHalves * kKVHalfBytes);
+        for (int hh = 0; hh < kHalves; ++hh)
+          ptx::tma_load_2d(sv + hh * kKVHalfBytes, &tmV, hh * 64, v_row, &v_full[st], pol_kv);
+        ++vt;
+        return true;
+      };
       Seg s;
       while (ok && iter.next(a, pre, s)) {
+        if (vt < kvt && !issue_v()) { ok = false; break; }
         if (!ptx::mbar_wait(q_empty, (segc & 1) ^ 1u, abort_flag, kWaitNs)) { ok = false; break; }
         const int qrow0 = (s.b * a.Hkv + s.h) * a.Mrows + s.mg * NM * 128;
         ptx::mbar_arrive_expect_tx(q_full, NM * kQTileBytes);
@@ -271,21 +300,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kvrow0 = (s.b * a.Hkv + s.h) * a.Pmax;
         for (int j = s.j0; j < s.j1; ++j, ++kvt) {
           const int st = kvt % S;
-          if (!ptx::mbar_wait(&kv_empty[st], ((kvt / S) & 1) ^ 1u, abort_flag, kWaitNs)) {
+          if (!ptx::mbar_wait(&k_empty[st], ((kvt / S) & 1) ^ 1u, abort_flag, kWaitNs)) {
             ok = false;
             break;
           }
           uint8_t* sk = sKV + st * kStageBytes;
-          uint8_t* sv = sk + kHalves * kKVHalfBytes;
-          ptx::mbar_arrive_expect_tx(&kv_full[st], kStageBytes);
-          for (int hh = 0; hh < kHalves; ++hh) {
+          ptx::mbar_arrive_expect_tx(&k_full[st], kHalves * kKVHalfBytes);
+          for (int hh = 0; hh < kHalves; ++hh)
             ptx::tma_load_2d(sk + hh * kKVHalfBytes, &tmK, hh * 64, kvrow0 + j * kBN,
-                             &kv_full[st], pol_kv);
-            ptx::tma_load_2d(sv + hh * kKVHalfBytes, &tmV, hh * 64, kvrow0 + j * kBN,
-                             &kv_full[st], pol_kv);
-          }
+                             &k_full[st], pol_kv);
+          if (vt < kvt && !issue_v()) { ok = false; break; }
+          v_row = kvrow0 + j * kBN;
         }
       }
+      if (ok && vt < kvt && !issue_v()) ok = false;
       if (!ok) {
         latch_error(a.ws, MDS_DEV_TIMEOUT);
         *abort_flag = 1;
@@ -293,7 +321,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // drain: the copies issued last into each stage and into Q have landed
       for (int i = 0; i < S && i < kvt; ++i) {
         const int t = kvt - 1 - i;
-        ptx::mbar_wait(&kv_full[t % S], (t / S) & 1, abort_flag, kWaitNs);
+        ptx::mbar_wait(&k_full[t % S], (t / S) & 1, abort_flag, kWaitNs);
+      }
+      for (int i = 0; i < S && i < vt; ++i) {
+        const int t = vt - 1 - i;
+        ptx::mbar_wait(&v_full[t % S], (t / S) & 1, abort_flag, kWaitNs);
       }
       if (segc > 0) ptx::mbar_wait(q_full, (segc - 1) & 1, abort_flag, kWaitNs);
     }
@@ -303,7 +335,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t idS = ptx::idesc_bf16(128, kBN);
     const uint32_t idO = ptx::idesc_bf16(128, DH) | (1u << 16);   // B (V) MN-major
     int it = 0, kvt = 0, segc = 0;
-    int pv_it = -1, pv_m = 0, pv_stage = 0, pv_first = 0, pv_lastm = 0;   // pending P V
+    // pending P V: item, query tile, stage, first tile of the unit, last
+    // query tile of the key tile, key-tile number, valid keys in the tile
+    int pv_it = -1, pv_m = 0, pv_stage = 0, pv_first = 0, pv_lastm = 0, pv_t = 0, pv_nv = 0;
     bool ok = true;
     auto wait = [&](uint64_t* bar, uint32_t par) {
       if (!ok) return false;
@@ -314,6 +348,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto issue_pv = [&]() {
       const int pb = pv_it % kNP;
       if (!wait(&p_full[pb], (pv_it / kNP) & 1)) return;
+      if (!wait(&v_full[pv_stage], (pv_t / S) & 1)) return;
+      if (pv_m == 0 && pv_nv < kBN) {
+        // keys past the unit's end: zero their V rows so that stale cache
+        // contents (never weighted, P = 0) cannot inject NaN into O
+        uint8_t* sv = sKV + pv_stage * kStageBytes + kHalves * kKVHalfBytes;
+        for (int hh = 0; hh < kHalves; ++hh)
+          for (int i = pv_nv * 8 + lane; i < kBN * 8; i += 32)
+            reinterpret_cast<uint4*>(sv + hh * kKVHalfBytes)[i] = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
       ptx::tc_fence_after();
       if (lane == 0) {
         const uint32_t aP = ptx::smem_addr(sP + pb * kPBytes);
@@ -325,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         sdesc_mn128(bV + kk * 2048, kKVHalfBytes),
                         idO, (pv_first && kk == 0) ? 0u : 1u);
         ptx::mma_commit(&p_empty[pb]);
-        if (pv_lastm) ptx::mma_commit(&kv_empty[pv_stage]);
+        if (pv_lastm) ptx::mma_commit(&v_empty[pv_stage]);
       }
       __syncwarp();
     };
@@ -335,18 +380,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int Lk = s.Pb + a.N;
       for (int j = s.j0; j < s.j1 && ok; ++j, ++kvt) {
         const int st = kvt % S;
-        if (!wait(&kv_full[st], (kvt / S) & 1)) break;
+        if (!wait(&k_full[st], (kvt / S) & 1)) break;
         const int nv = Lk - j * kBN;
-        if (nv < kBN) {
-          // keys past the unit's end: zero their V rows so that stale cache
-          // contents (never weighted, P = 0) cannot inject NaN into O
-          uint8_t* sv = sKV + st * kStageBytes + kHalves * kKVHalfBytes;
-          for (int hh = 0; hh < kHalves; ++hh)
-            for (int i = nv * 8 + lane; i < kBN * 8; i += 32)
-              reinterpret_cast<uint4*>(sv + hh * kKVHalfBytes)[i] = make_uint4(0, 0, 0, 0);
-          fence_proxy_async_smem();
-          __syncwarp();
-        }
         for (int m = 0; m < NM; ++m, ++it) {
           const int sb = it & 1;
           if (!wait(&s_empty[sb], ((it >> 1) & 1) ^ 1u)) break;
@@ -363,6 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             kk ? 1u : 0u);
             }
             ptx::mma_commit(&s_full[sb]);
+            if (m == NM - 1) ptx::mma_commit(&k_empty[st]);
             if (j == s.j1 - 1 && m == NM - 1) ptx::mma_commit(q_empty);
           }
           __syncwarp();
@@ -375,6 +411,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           pv_stage = st;
           pv_first = j == s.j0;
           pv_lastm = m == NM - 1;
+          pv_t = kvt;
+          pv_nv = nv;
         }
       }
       ++segc;
@@ -640,6 +678,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // The partition is recomputed from P exactly as the main kernel computes it.
 template <int DH>
 __global__ void __launch_bounds__(256) k_attention_merge(AttnArgs a) {
+  grid_dep_launch();
+  grid_dep_wait();
   __shared__ int pre[kMaxBAttn + 1];
   __shared__ long long starts[kMaxCtaAttn + 1];   // first global tile of each CTA
   for (int b = threadIdx.x; b < a.B; b += blockDim.x) pre[b + 1] = a.Hkv * a.n_mg * tiles_of(a, a.P[b]);
@@ -731,10 +771,13 @@ Plan plan(int N, int g, int dh, int num_sms) {
   const size_t q = (size_t)p.NM * 128 * dh * 2;
   const size_t pbuf = (p.BN == 128 ? 1 : 2) * (size_t)128 * p.BN * 2;
   const size_t stage = 2 * (size_t)p.BN * dh * 2;
-  const size_t fixed = 1024 /*align*/ + 38 * 8 + 512 * 4 + (kMaxBAttn + 1) * 4;
+  const size_t fixed = 1024 /*align*/ + 54 * 8 + 512 * 4 + (kMaxBAttn + 1) * 4;
   int st = (int)((kSmemLimit - q - pbuf - fixed) / stage);
   p.stages = st > 6 ? 6 : st;
   p.smem = q + pbuf + (size_t)p.stages * stage + fixed;
+  // more than half of the SM's shared memory: no two CTAs holding all 512
+  // TMEM columns (this kernel's or the projection GEMM's) share an SM
+  if (p.smem < (size_t)kSmemLimit / 2 + 1024) p.smem = (size_t)kSmemLimit / 2 + 1024;
   p.G = num_sms < kMaxCtaAttn ? num_sms : kMaxCtaAttn;
   return p;
 }
@@ -770,7 +813,10 @@ int launch_one(const Plan& p, const CUtensorMap& mq, const CUtensorMap& mk, cons
       return MDS_ECUDA;
     set = true;
   }
-  k_tree_attention_tc<DH, NM, BN><<<p.G, kThreads, p.smem, st>>>(mq, mk, mv, a);
+  // follows the QKV projection of the same call
+  if (launch_kernel(k_tree_attention_tc<DH, NM, BN>, dim3(p.G), dim3(kThreads), p.smem, st, true,
+                    mq, mk, mv, a) != cudaSuccess)
+    return MDS_ECUDA;
   return MDS_OK;
 }
 
@@ -832,11 +878,8 @@ int attention_tc(int B, int N, int Hq, int Hkv, int dh, int Pmax, const int32_t*
   if (rc) return rc;
   MDS_LAUNCH_CHECK();
   const dim3 mgrid(B * Hkv * p.n_mg, p.NM * 16);
-  if (dh == 128)
-    k_attention_merge<128><<<mgrid, 256, 0, st>>>(a);
-  else
-    k_attention_merge<64><<<mgrid, 256, 0, st>>>(a);
-  MDS_LAUNCH_CHECK();
+  MDS_LAUNCH_TRY(launch_kernel(dh == 128 ? k_attention_merge<128> : k_attention_merge<64>, mgrid,
+                               dim3(256), 0, st, true, a));
   return MDS_OK;
 }
 

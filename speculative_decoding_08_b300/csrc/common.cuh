@@ -66,6 +66,18 @@ __device__ __forceinline__ void block_sync() {
   __syncthreads();
 }
 
+// Programmatic dependent launch (griddepcontrol).  grid_dep_wait returns
+// once the grids this one depends on have completed and their memory
+// operations are visible to it; grid_dep_launch lets the stream's next grid
+// be scheduled before this one ends.  For a grid launched without the
+// programmatic-serialisation attribute, both do nothing.
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Host-side count of enqueued kernels (see mds_launch_count).
 void count_launch(int n = 1);
 
@@ -75,6 +87,13 @@ void count_launch(int n = 1);
   do {                                          \
     cudaError_t _e = (expr);                    \
     if (_e != cudaSuccess) return MDS_ECUDA;    \
+  } while (0)
+
+// For launches through cudaLaunchKernelEx, whose status is its return value.
+#define MDS_LAUNCH_TRY(expr)                                 \
+  do {                                                       \
+    if ((expr) != cudaSuccess) return MDS_ECUDA;             \
+    ::mds::count_launch();                                   \
   } while (0)
 
 #define MDS_LAUNCH_CHECK()                                   \

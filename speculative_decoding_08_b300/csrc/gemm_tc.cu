@@ -8,7 +8,15 @@
 // Wqkv, Wo).  Each CTA owns a contiguous range of weight rows (features),
 // split evenly over the SMs in units of 16, and streams it through a TMA
 // ring as deep as shared memory allows; X tiles (the rows) are re-read from
-// L2.  With at most 128 rows the MMA reads a 128-row X tile of which only
+// L2.  Above 256 rows the CTAs are also split over the 256-row groups: each
+// takes one group and a correspondingly wider feature range, the CTAs of
+// one range reading its weights together (once from HBM, the rest from L2).
+// With at most 128 rows and few features (Wo, Wqkv, the heads) the k-blocks
+// are split over ks CTAs per feature range instead, and k_split_reduce adds
+// the fp32 partial sums and runs the epilogue: every tcgen05.mma costs the
+// issuing SM about 190 cycles for any N, so a CTA's Kd / 16 MMAs per chunk
+// would otherwise outlast its share of the weight stream.
+// With at most 128 rows the MMA reads a 128-row X tile of which only
 // the first R rows matter (the other accumulator rows are never read), so the
 // X tiles of consecutive stages overlap: stage s starts ceil(R/8) KB after
 // stage s-1 and its don't-care rows are the next stages' data.  A stage then
@@ -34,8 +42,8 @@
 //           ("From top-k heads to a sparse candidate tree")
 //   VERIFY  per row running max / argmax / sum e^(z-m) / sum z e^(z-m)
 //           (entropy for "Typical acceptance, not exact rejection sampling")
-// DRAFT and VERIFY leave one partial record per (CTA, row); a merge kernel
-// combines them.
+// DRAFT and VERIFY leave one partial record per (feature range, row); a
+// merge kernel combines them.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -71,7 +79,20 @@ struct TcArgs {
   int wst;          // bytes of one stage's W tiles
   int xbox;         // X rows per TMA box
   int wh[3];        // row counts of the three W tensor maps' boxes
-  int n_rgroups;
+  int n_rgroups;    // groups of 128 G rows
+  // CTA c takes row groups c % n_rs, c % n_rs + n_rs, ... and feature range
+  // c / n_rs of n_fr.  n_rs = 1 (every CTA sweeps all rows over a range of
+  // F / n_cta features) up to 256 rows; beyond that each CTA takes one row
+  // group and a range n_rs times wider, so that a 256-wide N stays filled.
+  int n_rs, n_fr;
+  // K split (at most 128 rows, STORE / HEADS / QKV): ks CTAs share a feature
+  // range, each over 1 / ks of the k-blocks, writing fp32 partial sums to
+  // kpart [ks][R][F]; k_split_reduce then adds them in split order and runs
+  // the epilogue.  Without the split a CTA issues Kd / 16 MMAs per chunk
+  // whatever its width (about 190 SM cycles each), which bounds the narrow
+  // projections (Wo, Wqkv, the heads) at batch 1 above their HBM time.
+  int ks;
+  float* kpart;
   int kind;
   void* out;
   long long ldo;
@@ -91,10 +112,10 @@ struct Range {
   int f_begin, f_end, n_chunks;
 };
 
-__device__ __forceinline__ Range cta_range(const TcArgs& a, int c) {
+__device__ __forceinline__ Range cta_range(const TcArgs& a, int fr) {
   Range r;
-  r.f_begin = 16 * (int)(((long long)c * a.n_units) / a.n_cta);
-  const int fe = 16 * (int)(((long long)(c + 1) * a.n_units) / a.n_cta);
+  r.f_begin = 16 * (int)(((long long)fr * a.n_units) / a.n_fr);
+  const int fe = 16 * (int)(((long long)(fr + 1) * a.n_units) / a.n_fr);
   r.f_end = fe < a.F ? fe : a.F;
   r.n_chunks = r.f_end > r.f_begin ? (r.f_end - r.f_begin + a.NC - 1) / a.NC : 0;
   return r;
@@ -104,19 +125,20 @@ __device__ __forceinline__ Range cta_range(const TcArgs& a, int c) {
 __device__ __forceinline__ void epi_store(const TcArgs& a, int row, int f0, int nv,
                                           const float (&v)[32]) {
   __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out) + (long long)row * a.ldo + f0;
-  if (nv == 32 && (a.ldo % 8) == 0) {
+  const bool vec = (a.ldo % 8) == 0;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < 4; ++q) {
+    if (vec && nv >= 8 * (q + 1)) {
       uint4 pk;
       __nv_bfloat162* p2 = reinterpret_cast<__nv_bfloat162*>(&pk);
 #pragma unroll
       for (int e = 0; e < 4; ++e) p2[e] = __floats2bfloat162_rn(v[q * 8 + 2 * e], v[q * 8 + 2 * e + 1]);
       *reinterpret_cast<uint4*>(o + q * 8) = pk;
-    }
-  } else {
+    } else {
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (j < nv) o[j] = __float2bfloat16_rn(v[j]);
+      for (int e = 0; e < 8; ++e)
+        if (q * 8 + e < nv) o[q * 8 + e] = __float2bfloat16_rn(v[q * 8 + e]);
+    }
   }
 }
 
@@ -325,6 +347,23 @@ __device__ __forceinline__ void colpar_block(const TcArgs& a, float* tile,
   __syncwarp();
 }
 
+// K split: this CTA's fp32 sums of one 32-column block of a row.
+__device__ __forceinline__ void store_kpart(const TcArgs& a, int kspl, int row, int f0, int nv,
+                                            const uint32_t (&r)[32]) {
+  float* p = a.kpart + ((long long)kspl * a.R + row) * a.F + f0;
+  if (nv == 32) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      reinterpret_cast<float4*>(p)[q] =
+          make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                      __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < nv) p[j] = __uint_as_float(r[j]);
+  }
+}
+
 // One 32-column block of a row's accumulators (raw fp32 bits in r).
 template <int KIND>
 __device__ __forceinline__ void epi_block(const TcArgs& a, int row, int g, int f0, int nv,
@@ -380,9 +419,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr bool kColPar = KIND == TC_HEADS;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int cta = blockIdx.x;
-  const Range rg = cta_range(a, cta);
-  const int nks = a.Kd / (64 * a.kbs);     // stages per chunk
+  const int sub = blockIdx.x % (a.n_rs * a.ks);
+  const int rs = sub % a.n_rs;             // first row group of this CTA
+  const int kspl = sub / a.n_rs;           // K split of this CTA
+  const int fr = blockIdx.x / (a.n_rs * a.ks);   // feature range of this CTA
+  const Range rg = cta_range(a, fr);
+  // k-blocks [kb0, kb1) of this CTA (all of them without a K split, where
+  // kbs = 1 otherwise)
+  const int nkb = a.Kd / 64;
+  const int kb0 = kspl * nkb / a.ks, kb1 = (kspl + 1) * nkb / a.ks;
+  const int nks = (kb1 - kb0) / a.kbs;     // stages per chunk
+  const int kz0 = kb0 / a.kbs;             // first stage's k-block group
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -406,6 +453,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::cta_barrier(1, kThreads);
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // The stream's next kernel may start its own set-up from here on.  Every
+  // thread but the producer waits for the previous kernel now; the producer
+  // first requests weight tiles, which no kernel of the same call writes.
+  grid_dep_launch();
+  if (threadIdx.x != 0) grid_dep_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
@@ -418,31 +470,59 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool issued[kMaxStages];
       for (int s = 0; s < kMaxStages; ++s) issued[s] = false, issued_phase[s] = 0;
       bool ok = true;
-      for (int g0 = 0; g0 < a.n_rgroups && ok; ++g0) {
-        const int row0 = g0 * 128 * a.G;
-        const int rem = a.R - row0;
-        const int Geff = min(a.G, (rem + 127) / 128);
+      // Chunk geometry: the W map whose box height is this chunk's rows
+      // (rounded to 16), the first feature, and the stage's byte count.
+      struct Chunk {
+        const CUtensorMap* mw;
+        int fc, Geff, row0;
+        uint32_t bytes;
+      };
+      auto chunk = [&](int g0, int ch) {
+        Chunk c;
+        c.row0 = g0 * 128 * a.G;
+        c.Geff = min(a.G, (a.R - c.row0 + 127) / 128);
+        c.fc = rg.f_begin + ch * a.NC;
+        const int len = min(a.NC, rg.f_end - c.fc);
+        const int h16 = (len + 15) / 16 * 16;
+        c.mw = h16 == a.wh[0] ? &tmW0 : (h16 == a.wh[1] ? &tmW1 : &tmW2);
+        const uint32_t xbytes = a.G == 1 ? (uint32_t)(a.kbs * a.xbox * 128)
+                                         : (uint32_t)(c.Geff * a.kbs * 16384);
+        c.bytes = xbytes + (uint32_t)(a.kbs * h16 * 128);
+        return c;
+      };
+      // W tiles of the first S stages, before the wait (the ring is empty,
+      // so no empty-slot wait is needed); their X tiles follow the wait.
+      int pre = 0;
+      for (int g0 = rs; g0 < a.n_rgroups && pre < S; g0 += a.n_rs) {
+        for (int ch = 0; ch < rg.n_chunks && pre < S; ++ch) {
+          const Chunk c = chunk(g0, ch);
+          for (int kq = 0; kq < nks && pre < S; ++kq, ++pre) {
+            ptx::mbar_arrive_expect_tx(&full[pre], c.bytes);
+            ptx::tma_load_3d(sWr + pre * a.wst, c.mw, 0, c.fc, (kz0 + kq) * a.kbs, &full[pre],
+                             pol_w);
+            issued[pre] = true;
+          }
+        }
+      }
+      grid_dep_wait();
+      int j = 0;   // stages in issue order
+      for (int g0 = rs; g0 < a.n_rgroups && ok; g0 += a.n_rs) {
         for (int ch = 0; ch < rg.n_chunks && ok; ++ch) {
-          const int fc = rg.f_begin + ch * a.NC;
-          const int len = min(a.NC, rg.f_end - fc);
-          // the W map whose box height is this chunk's rows (rounded to 16)
-          const int h16 = (len + 15) / 16 * 16;
-          const CUtensorMap* mw = h16 == a.wh[0] ? &tmW0 : (h16 == a.wh[1] ? &tmW1 : &tmW2);
-          const uint32_t xbytes = a.G == 1 ? (uint32_t)(a.kbs * a.xbox * 128)
-                                           : (uint32_t)(Geff * a.kbs * 16384);
-          const uint32_t bytes = xbytes + (uint32_t)(a.kbs * h16 * 128);
-          for (int kq = 0; kq < nks; ++kq) {
-            if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, kWaitLimitNs)) {
-              ok = false;
-              break;
-            }
+          const Chunk c = chunk(g0, ch);
+          for (int kq = 0; kq < nks; ++kq, ++j) {
             uint8_t* sA = sXr + stage * a.pxs;
-            uint8_t* sB = sWr + stage * a.wst;
-            ptx::mbar_arrive_expect_tx(&full[stage], bytes);
-            for (int g = 0; g < Geff; ++g)
-              ptx::tma_load_3d(sA + g * a.kbs * 16384, &tmX, 0, row0 + g * 128, kq * a.kbs,
-                               &full[stage], pol_x);
-            ptx::tma_load_3d(sB, mw, 0, fc, kq * a.kbs, &full[stage], pol_w);
+            if (j >= pre) {
+              if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, kWaitLimitNs)) {
+                ok = false;
+                break;
+              }
+              ptx::mbar_arrive_expect_tx(&full[stage], c.bytes);
+              ptx::tma_load_3d(sWr + stage * a.wst, c.mw, 0, c.fc, (kz0 + kq) * a.kbs,
+                               &full[stage], pol_w);
+            }
+            for (int g = 0; g < c.Geff; ++g)
+              ptx::tma_load_3d(sA + g * a.kbs * 16384, &tmX, 0, c.row0 + g * 128,
+                               (kz0 + kq) * a.kbs, &full[stage], pol_x);
             issued[stage] = true;
             issued_phase[stage] = phase;
             if (++stage == S) {
@@ -468,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int item = 0;
       bool ok = true;
-      for (int g0 = 0; g0 < a.n_rgroups && ok; ++g0) {
+      for (int g0 = rs; g0 < a.n_rgroups && ok; g0 += a.n_rs) {
         const int rem = a.R - g0 * 128 * a.G;
         const int Geff = min(a.G, (rem + 127) / 128);
         for (int ch = 0; ch < rg.n_chunks && ok; ++ch, ++item) {
@@ -531,7 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* tile = epi_tile + quarter * kTileFloats;
     int item = 0;
     bool ok = true;
-    for (int g0 = 0; g0 < a.n_rgroups && ok; ++g0) {
+    for (int g0 = rs; g0 < a.n_rgroups && ok; g0 += a.n_rs) {
       const int row0 = g0 * 128 * a.G;
       const int rem = a.R - row0;
       const int Geff = min(a.G, (rem + 127) / 128);
@@ -570,20 +650,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int cb = 0; cb < ncb; cb += 2) {
             const bool more1 = cb + 1 < ncb, more2 = cb + 2 < ncb;
             if (more1) ptx::tmem_ld32_async(tbase + (uint32_t)(cb + 1) * 32, rb[1]);
-            if constexpr (kColPar)
+            if (a.ks > 1) {
+              if (live) store_kpart(a, kspl, row, fc + cb * 32, min(32, len - cb * 32), rb[0]);
+            } else if constexpr (kColPar) {
               colpar_block<KIND>(a, tile, row_base, nlive, fc + cb * 32,
                                  min(32, len - cb * 32), rb[0]);
-            else if (live)
+            } else if (live) {
               epi_block<KIND>(a, row, g, fc + cb * 32, min(32, len - cb * 32), rb[0], tl, ss);
+            }
             if (more1) {
               ptx::tmem_wait32(rb[1]);
               if (more2) ptx::tmem_ld32_async(tbase + (uint32_t)(cb + 2) * 32, rb[0]);
-              if constexpr (kColPar)
+              if (a.ks > 1) {
+                if (live)
+                  store_kpart(a, kspl, row, fc + (cb + 1) * 32, min(32, len - (cb + 1) * 32),
+                              rb[1]);
+              } else if constexpr (kColPar) {
                 colpar_block<KIND>(a, tile, row_base, nlive, fc + (cb + 1) * 32,
                                    min(32, len - (cb + 1) * 32), rb[1]);
-              else if (live)
+              } else if (live) {
                 epi_block<KIND>(a, row, g, fc + (cb + 1) * 32, min(32, len - (cb + 1) * 32), rb[1],
                                 tl, ss);
+              }
               if (more2) ptx::tmem_wait32(rb[0]);
             }
           }
@@ -599,7 +687,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (g >= Geff) break;
           const int row = row0 + g * 128 + trow;
           if (row >= a.R) continue;
-          const long long rec = (long long)cta * a.R + row;
+          const long long rec = (long long)fr * a.R + row;
           if (KIND == TC_VERIFY) {
             float4 o = make_float4(ss[g].m, ss[g].S, ss[g].Q, __int_as_float(ss[g].am));
             static_cast<float4*>(a.partial)[rec] = o;
@@ -623,16 +711,61 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) ptx::tmem_dealloc(tmem_base, kTmemCols);
 }
 
+// K split: one thread per (row, 16-feature group) adds the ks partial sums
+// in split order (all loads issued before the adds) and applies the pass's
+// epilogue.
+constexpr int kMaxKs = 8;
+template <int KIND>
+__global__ void __launch_bounds__(256) k_split_reduce(TcArgs a) {
+  grid_dep_launch();
+  grid_dep_wait();
+  const int ng = a.F / 16;
+  const long long item = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (item >= (long long)a.R * ng) return;
+  const int row = (int)(item / ng), f0 = (int)(item - (long long)row * ng) * 16;
+  float4 x[kMaxKs][4];
+#pragma unroll
+  for (int k = 0; k < kMaxKs; ++k) {
+    if (k < a.ks) {
+      const float4* p =
+          reinterpret_cast<const float4*>(a.kpart + ((long long)k * a.R + row) * a.F + f0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) x[k][q] = __ldcg(p + q);
+    }
+  }
+  float v[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = 0.f;
+#pragma unroll
+  for (int k = 0; k < kMaxKs; ++k) {
+    if (k < a.ks) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        v[4 * q] += x[k][q].x;
+        v[4 * q + 1] += x[k][q].y;
+        v[4 * q + 2] += x[k][q].z;
+        v[4 * q + 3] += x[k][q].w;
+      }
+    }
+  }
+  if constexpr (KIND == TC_STORE) epi_store(a, row, f0, 16, v);
+  if constexpr (KIND == TC_HEADS) epi_heads(a, row, f0, 16, v);
+  if constexpr (KIND == TC_QKV) epi_qkv(a, row, f0, 16, v);
+}
+
 // ----------------------------------------------------------- merge kernels
-// One warp per row: combine the per-CTA (m, S, Q, argmax) records.
-__global__ void __launch_bounds__(256) k_verify_merge(const float4* __restrict__ part, int n_cta,
+// One warp per row: combine the row's (m, S, Q, argmax) records, one per
+// feature range.
+__global__ void __launch_bounds__(256) k_verify_merge(const float4* __restrict__ part, int n_rec,
                                                       int R, int32_t* argmax, float* stats) {
+  grid_dep_launch();
+  grid_dep_wait();
   const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= R) return;
   float m = -INFINITY, S = 0.f, Q = 0.f;
   int am = 0x7fffffff;
-  for (int c = lane; c < n_cta; c += 32) {
+  for (int c = lane; c < n_rec; c += 32) {
     const float4 p = part[(long long)c * R + row];
     const int pam = __float_as_int(p.w);
     if (p.y == 0.f && p.x == -INFINITY) continue;   // empty range
@@ -671,7 +804,8 @@ __global__ void __launch_bounds__(256) k_verify_merge(const float4* __restrict__
   }
 }
 
-// One block per head row (b, i): top s_i of the per-CTA candidate lists.
+// One block per head row (b, i): top s_i of the candidate lists, one list per
+// feature range.
 // Each thread keeps a sorted top-8 of the entries it scans; each warp then
 // extracts its top-8 by repeated warp-wide maxima, and warp 0 extracts the
 // row's top s_i from the warps' lists.  Order: value desc, id asc.
@@ -723,10 +857,12 @@ __device__ __forceinline__ void warp_extract(const float (&v)[kMaxS], const int 
   }
 }
 
-__global__ void __launch_bounds__(256) k_draft_merge(const float2* __restrict__ part, int n_cta,
+__global__ void __launch_bounds__(256) k_draft_merge(const float2* __restrict__ part, int n_rec,
                                                      int R, int K, Shortlist sl, int smax,
                                                      int32_t* root, int32_t* topk_id,
                                                      float* topk_val) {
+  grid_dep_launch();
+  grid_dep_wait();
   __shared__ float s_v[8][kMaxS];
   __shared__ int s_id[8][kMaxS];
   const int row = blockIdx.x;
@@ -740,7 +876,7 @@ __global__ void __launch_bounds__(256) k_draft_merge(const float2* __restrict__ 
     v[j] = -INFINITY;
     id[j] = 0x7fffffff;
   }
-  for (int c = threadIdx.x; c < n_cta * kMaxS; c += blockDim.x) {
+  for (int c = threadIdx.x; c < n_rec * kMaxS; c += blockDim.x) {
     const float2 e = part[((long long)(c / kMaxS) * R + row) * kMaxS + (c % kMaxS)];
     const int eid = __float_as_int(e.y);
     if (eid != 0x7fffffff) top8_insert(v, id, e.x, eid);
@@ -788,6 +924,8 @@ __global__ void __launch_bounds__(256) k_child_dot(const __nv_bfloat16* __restri
                                                    int d, int V, const int32_t* tok,
                                                    const int32_t* parent, float* child,
                                                    void* ws) {
+  grid_dep_launch();
+  grid_dep_wait();
   const int b = blockIdx.x;
   const int lane = threadIdx.x & 31;
   {
@@ -856,10 +994,18 @@ int init_host() {
   return MDS_OK;
 }
 
-int grid_ctas(int F) {
-  const int n_units = (F + 15) / 16;
-  int n = g_num_sms < kMaxCta ? g_num_sms : kMaxCta;
-  return n_units < n ? n_units : n;
+// K splits for a pass of at most 128 rows over F features and Kd inputs:
+// enough that a CTA's MMAs (Kd / 16 / ks per chunk, about 190 SM cycles each)
+// stay below its share of the weight stream (F Kd 2 / SMs bytes), while every
+// feature range keeps at most 256 features (one chunk) and every split at
+// least two k-blocks.
+int k_splits(int F, int Kd, int sms) {
+  const int nmin = (F + 255) / 256;
+  int ks = sms / nmin;
+  ks = min(ks, (32768 + F - 1) / F);
+  ks = min(ks, Kd / 128);
+  ks = min(ks, kMaxKs);
+  return ks >= 2 ? ks : 1;
 }
 
 // Rows of the last chunk of a CTA range of `units` 16-row units.
@@ -869,7 +1015,9 @@ int last_chunk_rows(int units, int NC) {
   return len - (n - 1) * NC;
 }
 
-int launch_tc(TcArgs a, const void* X, const void* W, cudaStream_t st) {
+// Plans and launches one pass; a.n_fr (the feature ranges, i.e. the partial
+// records per row of DRAFT and VERIFY) is left in `a` for the merge kernels.
+int launch_tc(TcArgs& a, const void* X, const void* W, bool dependent, cudaStream_t st) {
   int rc = init_host();
   if (rc) return rc;
   if (a.R <= 0 || a.F <= 0) return MDS_OK;
@@ -883,19 +1031,39 @@ int launch_tc(TcArgs a, const void* X, const void* W, cudaStream_t st) {
   // light epilogue) takes one 2 x 256-column accumulator; the others keep
   // N = 128 double-buffered, since their ranges are narrow or their
   // epilogue is heavy.
-  if (a.G == 1 || a.kind == TC_VERIFY) {
+  //
+  // Above 256 rows every CTA takes one row group (n_rs partitions of the
+  // rows) and a feature range n_rs times wider: a CTA's MMAs then cost
+  // 1 / n_rs of sweeping all rows over a narrow range, whose N would be far
+  // below 256; the n_rs CTAs that share a range read its weights at about
+  // the same time, so HBM sees them once and L2 serves the rest.
+  a.n_rgroups = (a.R + 128 * a.G - 1) / (128 * a.G);
+  a.n_units = (a.F + 15) / 16;
+  const int sms = g_num_sms < kMaxCta ? g_num_sms : kMaxCta;
+  a.n_rs = (a.G == 2 && a.n_rgroups >= 2) ? min(a.n_rgroups, sms) : 1;
+  a.n_fr = max(1, min(sms / a.n_rs, a.n_units));
+  a.n_cta = a.n_rs * a.n_fr;
+  a.ks = 1;
+  if (a.G == 1 && a.kpart && ksplit_enabled() &&
+      (a.kind == TC_STORE || a.kind == TC_HEADS || a.kind == TC_QKV)) {
+    a.ks = k_splits(a.F, a.Kd, sms);
+    if (a.ks > 1) {
+      a.n_fr = min(sms / a.ks, a.n_units);   // at most 256 features each: one chunk
+      a.n_cta = a.n_fr * a.ks;
+    }
+  }
+  if (a.G == 1 || a.kind == TC_VERIFY || (a.n_rs > 1 && a.kind != TC_DRAFT)) {
     a.NC = 256;
     a.nacc = a.G == 1 ? 2 : 1;
   } else {
+    // the draft epilogue (a running top-8 per row) is heavy: it keeps two
+    // accumulators so that it overlaps the next chunk's MMAs
     a.NC = 128;
     a.nacc = 2;
   }
-  a.n_rgroups = (a.R + 128 * a.G - 1) / (128 * a.G);
-  a.n_units = (a.F + 15) / 16;
-  a.n_cta = grid_ctas(a.F);
   // W box heights: full chunks of NC rows and the last chunk of a range of
   // lo or hi units (ranges differ by at most one unit)
-  const int lo = a.n_units / a.n_cta, hi = (a.n_units + a.n_cta - 1) / a.n_cta;
+  const int lo = a.n_units / a.n_fr, hi = (a.n_units + a.n_fr - 1) / a.n_fr;
   a.wh[0] = a.NC;
   a.wh[1] = last_chunk_rows(lo > 0 ? lo : 1, a.NC);
   a.wh[2] = last_chunk_rows(hi, a.NC);
@@ -913,7 +1081,7 @@ int launch_tc(TcArgs a, const void* X, const void* W, cudaStream_t st) {
   const int colpar = a.kind == TC_HEADS ? kColParBytes : 0;
   const int budget = kSmemBytes - 1024 /*alignment*/ - kBarBytes - colpar - tail;
   a.kbs = 0;
-  for (int kbs = 4; kbs >= 1; kbs >>= 1) {
+  for (int kbs = a.ks > 1 ? 1 : 4; kbs >= 1; kbs >>= 1) {
     if (a.Kd % (64 * kbs)) continue;
     const int pxs = a.G == 1 ? kbs * a.px : 2 * kbs * 16384;
     const int wst = kbs * h_max * 128;
@@ -928,7 +1096,11 @@ int launch_tc(TcArgs a, const void* X, const void* W, cudaStream_t st) {
   }
   if (a.kbs == 0) return MDS_EUNSUPPORTED;
   a.xregion = a.stages * a.pxs + tail;
-  const int smem = 1024 + a.xregion + a.stages * a.wst + kBarBytes + colpar;
+  // more than half of the SM's shared memory, so that no two CTAs that each
+  // hold all 512 TMEM columns share an SM (this kernel's or the attention
+  // kernel's, which may start early under programmatic dependent launch)
+  const int smem = max(1024 + a.xregion + a.stages * a.wst + kBarBytes + colpar,
+                       kSmemBytes / 2 + 1024);
   CUtensorMap mx, mw[3];
   // X as (64 columns, rows, column blocks): a box of (64, rows, kbs) lands as
   // kbs consecutive K-major tiles, one per 64-wide k-block; W likewise
@@ -938,22 +1110,37 @@ int launch_tc(TcArgs a, const void* X, const void* W, cudaStream_t st) {
     rc = tensor_map_bf16(&mw[i], W, a.F, a.Kd, 3, a.wh[i], a.kbs);
     if (rc) return rc;
   }
+  void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
+               TcArgs);
   switch (a.kind) {
-    case TC_STORE: k_gemm_tc<TC_STORE><<<a.n_cta, kThreads, smem, st>>>(mx, mw[0], mw[1], mw[2], a); break;
-    case TC_HEADS: k_gemm_tc<TC_HEADS><<<a.n_cta, kThreads, smem, st>>>(mx, mw[0], mw[1], mw[2], a); break;
-    case TC_QKV: k_gemm_tc<TC_QKV><<<a.n_cta, kThreads, smem, st>>>(mx, mw[0], mw[1], mw[2], a); break;
-    case TC_DRAFT: k_gemm_tc<TC_DRAFT><<<a.n_cta, kThreads, smem, st>>>(mx, mw[0], mw[1], mw[2], a); break;
-    default: k_gemm_tc<TC_VERIFY><<<a.n_cta, kThreads, smem, st>>>(mx, mw[0], mw[1], mw[2], a); break;
+    case TC_STORE: kern = k_gemm_tc<TC_STORE>; break;
+    case TC_HEADS: kern = k_gemm_tc<TC_HEADS>; break;
+    case TC_QKV: kern = k_gemm_tc<TC_QKV>; break;
+    case TC_DRAFT: kern = k_gemm_tc<TC_DRAFT>; break;
+    default: kern = k_gemm_tc<TC_VERIFY>; break;
   }
-  MDS_LAUNCH_CHECK();
+  MDS_LAUNCH_TRY(launch_kernel(kern, dim3(a.n_cta), dim3(kThreads), smem, st, dependent, mx,
+                               mw[0], mw[1], mw[2], a));
+  if (a.ks > 1) {
+    void (*red)(TcArgs);
+    switch (a.kind) {
+      case TC_STORE: red = k_split_reduce<TC_STORE>; break;
+      case TC_HEADS: red = k_split_reduce<TC_HEADS>; break;
+      default: red = k_split_reduce<TC_QKV>; break;
+    }
+    const long long items = (long long)a.R * (a.F / 16);
+    MDS_LAUNCH_TRY(launch_kernel(red, dim3((unsigned)((items + 255) / 256)), dim3(256), 0, st,
+                                 true, a));
+  }
   return MDS_OK;
 }
 
 }  // namespace
 
-int gemm_tc_heads(const void* h, int B, const void* W, int K, int d, void* U, void* ws,
-                  cudaStream_t st) {
+int gemm_tc_heads(const void* h, int B, const void* W, int K, int d, void* U, void* kpart,
+                  void* ws, cudaStream_t st) {
   TcArgs a{};
+  a.kpart = static_cast<float*>(kpart);
   a.R = B;
   a.F = K * d;
   a.Kd = d;
@@ -963,12 +1150,13 @@ int gemm_tc_heads(const void* h, int B, const void* W, int K, int d, void* U, vo
   a.d = d;
   a.K = K;
   a.ws = ws;
-  return launch_tc(a, h, W, st);
+  return launch_tc(a, h, W, false, st);   // first kernel of the heads call
 }
 
 int gemm_tc_store(const void* X, int R, const void* W, int F, int Kd, void* out, long long ldo,
-                  void* ws, cudaStream_t st) {
+                  void* kpart, void* ws, cudaStream_t st) {
   TcArgs a{};
+  a.kpart = static_cast<float*>(kpart);
   a.R = R;
   a.F = F;
   a.Kd = Kd;
@@ -976,13 +1164,14 @@ int gemm_tc_store(const void* X, int R, const void* W, int F, int Kd, void* out,
   a.out = out;
   a.ldo = ldo;
   a.ws = ws;
-  return launch_tc(a, X, W, st);
+  return launch_tc(a, X, W, true, st);    // follows the attention merge
 }
 
 int gemm_tc_qkv(const void* x, int B, int N, int d, const void* wqkv, int Hq, int Hkv, int dh,
-                int Pmax, const int32_t* P, void* q, void* Kc, void* Vc, void* ws,
+                int Pmax, const int32_t* P, void* q, void* Kc, void* Vc, void* kpart, void* ws,
                 cudaStream_t st) {
   TcArgs a{};
+  a.kpart = static_cast<float*>(kpart);
   a.R = B * N;
   a.F = (Hq + 2 * Hkv) * dh;
   a.Kd = d;
@@ -997,7 +1186,14 @@ int gemm_tc_qkv(const void* x, int B, int N, int d, const void* wqkv, int Hq, in
   a.Kc = static_cast<__nv_bfloat16*>(Kc);
   a.Vc = static_cast<__nv_bfloat16*>(Vc);
   a.ws = ws;
-  return launch_tc(a, x, wqkv, st);
+  return launch_tc(a, x, wqkv, true, st); // follows the embedding gather
+}
+
+size_t tc_kpart_bytes(int R, int F, int Kd) {
+  // an upper bound for any SM count (k_splits only lowers ks for fewer SMs)
+  if (R > 128 || F <= 0) return 0;
+  const int ks = k_splits(F, Kd, kMaxCta * 256);
+  return ks > 1 ? (size_t)ks * R * F * 4 : 0;
 }
 
 size_t tc_partial_bytes(int R, bool draft) {
@@ -1016,12 +1212,11 @@ int lm_draft_tc(const void* U, int B, int K, int d, const void* lm, int V, Short
   a.kind = TC_DRAFT;
   a.partial = partial;
   a.ws = ws;
-  int rc = launch_tc(a, U, lm, st);
+  int rc = launch_tc(a, U, lm, true, st);   // follows the heads GEMM
   if (rc) return rc;
-  const int n_cta = grid_ctas(V);
-  k_draft_merge<<<a.R, 256, 0, st>>>(static_cast<const float2*>(partial), n_cta, a.R,
-                                                K, sl, smax, root, topk_id, topk_val);
-  MDS_LAUNCH_CHECK();
+  MDS_LAUNCH_TRY(launch_kernel(k_draft_merge, dim3(a.R), dim3(256), 0, st, true,
+                               static_cast<const float2*>(partial), a.n_fr, a.R, K, sl, smax,
+                               root, topk_id, topk_val));
   return MDS_OK;
 }
 
@@ -1035,16 +1230,15 @@ int lm_verify_tc(const void* y, int B, int N, int d, const void* lm, int V, cons
   a.kind = TC_VERIFY;
   a.partial = partial;
   a.ws = ws;
-  int rc = launch_tc(a, y, lm, st);
+  int rc = launch_tc(a, y, lm, false, st);   // first kernel of the verify call
   if (rc) return rc;
-  const int n_cta = grid_ctas(V);
-  k_verify_merge<<<(a.R + 7) / 8, 256, 0, st>>>(static_cast<const float4*>(partial), n_cta, a.R,
-                                                 argmax, stats);
-  MDS_LAUNCH_CHECK();
-  k_child_dot<<<dim3(B, (N + 7) / 8), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(y),
-                                 static_cast<const __nv_bfloat16*>(lm), N, d, V, tok, parent,
-                                 childlogit, ws);
-  MDS_LAUNCH_CHECK();
+  MDS_LAUNCH_TRY(launch_kernel(k_verify_merge, dim3((a.R + 7) / 8), dim3(256), 0, st, true,
+                               static_cast<const float4*>(partial), a.n_fr, a.R, argmax,
+                               stats));
+  MDS_LAUNCH_TRY(launch_kernel(k_child_dot, dim3(B, (N + 7) / 8), dim3(256), 0, st, true,
+                               static_cast<const __nv_bfloat16*>(y),
+                               static_cast<const __nv_bfloat16*>(lm), N, d, V, tok, parent,
+                               childlogit, ws));
   return MDS_OK;
 }
 

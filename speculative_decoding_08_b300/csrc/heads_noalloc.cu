@@ -86,7 +86,7 @@ extern "C" int mds_medusa_heads_noalloc(int B, int d, int V, int K, const void* 
   // The array keeps the previous call's contents; only the status word must
   // start at zero (every candidate list is written before it is read).
   MDS_CUDA_TRY(cudaMemsetAsync(scratch, 0, 256, st));
-  rc = gemm_tc_heads(h, B, W, K, d, U, scratch, st);
+  rc = gemm_tc_heads(h, B, W, K, d, U, nullptr, scratch, st);   // no K split here
   if (rc) return rc;
   rc = lm_draft_tc(U, B, K, d, lm, V, sl, smax, root, topk_id, topk_val,
                    static_cast<char*>(scratch) + kWsScratch, scratch, st);

@@ -7,7 +7,41 @@
 
 #include <cuda.h>
 
+#include <utility>
+
 namespace mds {
+
+// Kernel launch with optional programmatic stream serialisation.  With
+// `dependent` true, the kernel may start while the kernel before it in the
+// stream is still running (once every CTA of that kernel has executed
+// griddepcontrol.launch_dependents).  Such a kernel executes
+// griddepcontrol.wait before it touches memory the earlier kernel writes or
+// reads; before that point it may only read data that no kernel of the same
+// call writes (the weights).  Only the second and later kernels of one C-ABI
+// call are launched this way, so the first kernel of every call still starts
+// after all work enqueued before the call.  MDS_PDL=0 in the environment
+// launches every kernel without the attribute.
+bool pdl_enabled();
+
+// K-split projections at batch sizes of at most 128 rows (see gemm_tc.cu);
+// MDS_KSPLIT=0 in the environment turns them off.
+bool ksplit_enabled();
+
+template <typename... P, typename... A>
+cudaError_t launch_kernel(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t st, bool dependent, A&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = (dependent && pdl_enabled()) ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<A>(args)...);
+}
 
 // Encodes a bf16 tiled tensor map with the 128-byte swizzle, or returns a
 // cached copy of one encoded with the same arguments (the map holds only the
@@ -88,12 +122,15 @@ int attention_tc(int B, int N, int Hq, int Hkv, int dh, int Pmax, const int32_t*
 
 // Tensor-core (tcgen05) path, bf16 inputs.
 size_t tc_partial_bytes(int R, bool draft);
-int gemm_tc_heads(const void* h, int B, const void* W, int K, int d, void* U, void* ws,
-                  cudaStream_t st);
-int gemm_tc_store(const void* X, int R, const void* W, int F, int Kd, void* out, long long ldo,
+// fp32 partial sums of a K-split pass over R rows, F features, Kd inputs
+// (0 when the pass is not split); kpart arguments below may be null (no split).
+size_t tc_kpart_bytes(int R, int F, int Kd);
+int gemm_tc_heads(const void* h, int B, const void* W, int K, int d, void* U, void* kpart,
                   void* ws, cudaStream_t st);
+int gemm_tc_store(const void* X, int R, const void* W, int F, int Kd, void* out, long long ldo,
+                  void* kpart, void* ws, cudaStream_t st);
 int gemm_tc_qkv(const void* x, int B, int N, int d, const void* wqkv, int Hq, int Hkv, int dh,
-                int Pmax, const int32_t* P, void* q, void* Kc, void* Vc, void* ws,
+                int Pmax, const int32_t* P, void* q, void* Kc, void* Vc, void* kpart, void* ws,
                 cudaStream_t st);
 int lm_draft_tc(const void* U, int B, int K, int d, const void* lm, int V, Shortlist sl, int smax,
                 int32_t* root, int32_t* topk_id, float* topk_val, void* partial, void* ws,
