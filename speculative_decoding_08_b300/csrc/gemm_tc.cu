@@ -1000,6 +1000,11 @@ int init_host() {
 // feature range keeps at most 256 features (one chunk) and every split at
 // least two k-blocks.
 int k_splits(int F, int Kd, int sms) {
+  // Measured at batch 1: the split pays for its reduce kernel on Wo
+  // (F = 4096: MMA floor ~4.6x the HBM time per CTA) but not on Wqkv or the
+  // heads (F >= 12288: ~1.2-1.5x), whose time is mostly fixed per-kernel
+  // costs (ramp-up, epilogue) rather than MMA issue.
+  if (F > 8192) return 1;
   const int nmin = (F + 255) / 256;
   int ks = sms / nmin;
   ks = min(ks, (32768 + F - 1) / F);
