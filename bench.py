@@ -134,8 +134,11 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def oracle_sample(w, x, budget_s=15.0):
-    """Time the fp64 oracle's step on this host for up to ~budget_s."""
+def oracle_sample(w, x, budget_s=15.0, steps=50, warmup=0, warmup_budget_s=30.0):
+    """Time the fp64 oracle's step on this host: up to `warmup` untimed steps
+    (at most ~warmup_budget_s), then up to `steps` timed steps (at most
+    ~budget_s, at least one).  Returns (cpu_baseline dict, timed steps,
+    seconds, warm-up steps run)."""
     import oracle
     try:
         from threadpoolctl import threadpool_info
@@ -147,18 +150,23 @@ def oracle_sample(w, x, budget_s=15.0):
     f["vc"] = ms.as_f64(x["vc"][:1], w.dtype)
     f["h"] = f["h"][:1]
     mode = "greedy" if w.accept == "greedy" else "typical"
+    nw = 0
+    t0 = time.perf_counter()
+    while nw < warmup and time.perf_counter() - t0 < warmup_budget_s:
+        oracle.step(w, f, x["P"][:1], mode, batch=[0])
+        nw += 1
     t0 = time.perf_counter()
     n = 0
     while True:
         oracle.step(w, f, x["P"][:1], mode, batch=[0])
         n += 1
-        if time.perf_counter() - t0 >= budget_s or n >= 50:
+        if time.perf_counter() - t0 >= budget_s or n >= steps:
             break
     dt = time.perf_counter() - t0
     # one oracle step processes one sequence; a GPU step processes B
     return dict(value=n / dt / w.B, unit="steps/s", cores=cores, kind="oracle",
                 sample=f"{n} oracle step(s) of one sequence of {w.name} "
-                       f"(scaled by 1/B={w.B} to whole-batch steps/s)"), n, dt
+                       f"(scaled by 1/B={w.B} to whole-batch steps/s)"), n, dt, nw
 
 
 def run_reference(args, w):
@@ -166,9 +174,13 @@ def run_reference(args, w):
     if rank != 0:
         return
     x = ms.make_inputs(w)
-    cb, n, dt = oracle_sample(w, x, budget_s=max(5.0, min(60.0, 3.0 * args.steps)))
+    # W untimed warm-up steps, then K timed ones, each one oracle step of one
+    # sequence; both legs are capped in time so that the run ends within a
+    # few minutes (the line reports the counts actually run)
+    cb, n, dt, nw = oracle_sample(w, x, budget_s=180.0, steps=max(1, args.steps),
+                                  warmup=args.warmup, warmup_budget_s=30.0)
     line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "steps/s",
-            "n_gpus": args.gpus, "steps": n, "warmup": 0, "ms_per_step": 1e3 * dt / n,
+            "n_gpus": args.gpus, "steps": n, "warmup": nw, "ms_per_step": 1e3 * dt / n,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": w.name, "B": w.B, "d": w.d, "V": w.V,
                                             "K": w.K, "shortlist": list(w.shortlist),
@@ -369,7 +381,7 @@ def run_ours(args, w):
                 "d2h_bytes_per_step": d2h},
     }
     if not args.no_cpu_baseline:
-        cb, _, _ = oracle_sample(w, x, budget_s=args.cpu_budget)
+        cb, _, _, _ = oracle_sample(w, x, budget_s=args.cpu_budget)
         line["cpu_baseline"] = cb
     print(json.dumps(line), flush=True)
     if world > 1:
