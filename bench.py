@@ -190,6 +190,22 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
+def rank_max(values, dev):
+    """Element-wise maximum over the ranks of a list of times: the slowest
+    rank sets each whole-job time (a no-op without a process group)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64, device=dev)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def whole_job_rate(world, units_per_rank, seconds):
+    """Units all ranks processed per second of the slowest rank."""
+    return world * units_per_rank / seconds
+
+
 def run_ours(args, w):
     import torch
     import torch.distributed as dist
@@ -335,17 +351,14 @@ def run_ours(args, w):
     d2h = sum(o.numel() * o.element_size() for o in outs)
     L_host = step.host_out["L"].numpy().copy()
 
-    # max over ranks
-    tmax = torch.tensor([ms_total], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
-    ms_total = float(tmax.item())
+    # max over ranks (device-timed steps and the end-to-end loop)
+    ms_total, e2e_dt = rank_max([ms_total, e2e_dt], dev)
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return
     ms_step = ms_total / args.steps
-    steps_per_s = world * args.steps / (ms_total / 1e3)
+    steps_per_s = whole_job_rate(world, args.steps, ms_total / 1e3)
     mean_emit = float(np.mean(L_host + 1))
     pk = peaks()
     lmv_bytes = lm_verify_bytes(w, N)
@@ -377,7 +390,8 @@ def run_ours(args, w):
                      "peak_src": pk["src"], "algorithmic_bytes_per_launch": lmv_bytes},
         "gpu_launches": per_step_kernels * args.steps,
         "clocks": clk,
-        "e2e": {"value": e2e_steps / e2e_dt, "unit": "steps/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": whole_job_rate(world, e2e_steps, e2e_dt), "unit": "steps/s",
+                "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
     }
     if not args.no_cpu_baseline:
