@@ -43,6 +43,14 @@
  *    aligned and zero-filled once before first use.
  *  - Limits: N (tree rows incl. root) <= 128, K <= 8, s_i <= 8, d % 64 == 0,
  *    dh in {64, 128}, Hq % Hkv == 0.  Larger shapes return MDS_EUNSUPPORTED.
+ *  - Within one call, the second and later kernels are launched with
+ *    programmatic stream serialisation: they may start while the previous
+ *    kernel of the same call finishes, touching only the weights before that
+ *    kernel is complete.  The first kernel of every call starts after all
+ *    work enqueued before the call, so inputs written by earlier work on the
+ *    stream are always seen.  Environment switches, read once per process:
+ *    MDS_PDL=0 launches every kernel plainly; MDS_KSPLIT=0 turns off the
+ *    K-split form of the narrow projections (Wo at <= 128 rows).
  */
 #ifndef MEDUSA_B300_H
 #define MEDUSA_B300_H
