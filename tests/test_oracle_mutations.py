@@ -123,11 +123,11 @@ CASES = [
     ("tree: mask misses the node itself", dict(build_tree=tree_mask_no_self), [pins.check_tree_golden, pins.check_mask_is_ancestors]),
     ("tree: parent index shifted", dict(build_tree=tree_parent_shift), [pins.check_tree_golden, pins.check_mask_is_ancestors]),
     ("top-s: ties to the higher id", dict(sorted_ids=sorted_ids_high_id_first), [pins.check_topk]),
-    ("attention: mask transposed", dict(tree_attention=attention_with("mask_T")), [pins.check_attention_per_path]),
-    ("attention: GQA head map j % Hkv", dict(tree_attention=attention_with("gqa_mod")), [pins.check_attention_per_path]),
+    ("attention: mask transposed", dict(tree_attention=attention_with("mask_T")), [pins.check_attention_per_path, pins.check_attention_uniform_weights]),
+    ("attention: GQA head map j % Hkv", dict(tree_attention=attention_with("gqa_mod")), [pins.check_attention_per_path, pins.check_attention_uniform_weights]),
     ("attention: no 1/sqrt(dh)", dict(tree_attention=attention_with("no_scale")), [pins.check_attention_per_path]),
-    ("attention: prefix one short", dict(tree_attention=attention_with("prefix_short")), [pins.check_attention_per_path]),
-    ("verify: entropy in bits", dict(verify_stats=verify_entropy_log2), [pins.check_verify_stats]),
+    ("attention: prefix one short", dict(tree_attention=attention_with("prefix_short")), [pins.check_attention_per_path, pins.check_attention_uniform_weights]),
+    ("verify: entropy in bits", dict(verify_stats=verify_entropy_log2), [pins.check_verify_stats, pins.check_verify_two_level]),
     ("accept: wrong row's entropy", dict(accept_edges=accept_own_row), [pins.check_typical_direct]),
     ("path: ties to the highest index", dict(longest_path=longest_path_high_index), [pins.check_longest_path_golden, pins.check_longest_path_brute]),
     ("compaction: root row dropped", dict(compact_kv=compact_skip_root), [pins.check_compaction]),

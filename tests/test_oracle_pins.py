@@ -240,6 +240,36 @@ def test_attention_chain_is_causal():
     check_attention_per_path(oracle, shortlist=(2, 2, 2, 2), mrs=0, Hq=2, Hkv=2, seed=2)
 
 
+def check_attention_uniform_weights(orc):
+    """Closed form: with every key zero (Wk = 0 and a zero prefix K), all
+    scores are equal, so each head's output is the plain mean of the V rows
+    it may see: the prefix and the tree nodes of its mask row, V taken from
+    the query head's KV head."""
+    w, f, P = tiny(seed=4, B=2, shortlist=(3, 2, 2), Hq=6, Hkv=2, P=(3, 7))
+    tr = orc.build_tree(w.shortlist, -1)
+    tok = ms.random_tokens(4, w.B, tr["N"], w.V).astype(np.int64)
+    kc0 = np.zeros_like(f["kc"])
+    at = orc.tree_attention(tok, P, tr["mask"], f["emb"], f["wq"], np.zeros_like(f["wk"]),
+                            f["wv"], f["wo"], kc0, f["vc"], w.Hq, w.Hkv, w.dh, "f32")
+    g = w.Hq // w.Hkv
+    for b in range(w.B):
+        Pb = int(P[b])
+        v_tree = (f["emb"][tok[b]] @ f["wv"].T).reshape(tr["N"], w.Hkv, w.dh)
+        for n in range(tr["N"]):
+            vis = [m for m in range(tr["N"]) if tr["mask"][n, m]]
+            o = np.empty(w.Hq * w.dh)
+            for hq in range(w.Hq):
+                hk = hq // g
+                rows = [f["vc"][b, hk, j] for j in range(Pb)] + [v_tree[m, hk] for m in vis]
+                o[hq * w.dh:(hq + 1) * w.dh] = np.mean(rows, axis=0)
+            np.testing.assert_allclose(at["o"][b, n], o, rtol=1e-12, atol=1e-13)
+            np.testing.assert_allclose(at["y"][b, n], f["wo"] @ o, rtol=1e-11, atol=1e-12)
+
+
+def test_attention_uniform_weights():
+    check_attention_uniform_weights(oracle)
+
+
 def test_attention_root_only_is_decode():
     w, f, P = tiny(seed=9, B=1)
     tok = np.array([[5]])
@@ -281,6 +311,31 @@ def check_verify_stats(orc):
 
 def test_verify_stats():
     check_verify_stats(oracle)
+
+
+def check_verify_two_level(orc):
+    """Closed forms for logits that take two values: k ids at a, the other
+    V - k at 0.  With Z = k e^a + V - k: lse = ln Z, H = ln Z - k a e^a / Z,
+    argmax = the lowest of the k ids (a > 0) or the lowest other id (a < 0)."""
+    V, d = 50, 8
+    y = np.zeros((1, 2, d))
+    y[0, :, 0] = 1.0                     # logit of id v = lm[v, 0]
+    for a, ids in [(2.5, [7, 3, 31]), (-1.25, [0, 1, 2, 40]), (0.75, [49])]:
+        lm = np.zeros((V, d))
+        lm[:, 1:] = np.random.default_rng(1).standard_normal((V, d - 1))   # multiplied by 0
+        lm[ids, 0] = a
+        st = orc.verify_stats(y, lm, np.array([[0, 5]]), np.array([-1, 0]))
+        k = len(ids)
+        Z = k * math.exp(a) + (V - k)
+        np.testing.assert_allclose(st["lse"][0], math.log(Z), rtol=1e-13)
+        np.testing.assert_allclose(st["H"][0], math.log(Z) - k * a * math.exp(a) / Z, rtol=1e-12)
+        want = min(ids) if a > 0 else min(set(range(V)) - set(ids))
+        assert np.all(st["argmax"][0] == want)
+        np.testing.assert_allclose(st["childlogit"][0, 1], a if 5 in ids else 0.0, atol=0)
+
+
+def test_verify_two_level():
+    check_verify_two_level(oracle)
 
 
 # ---------------------------------------------------------------------------
