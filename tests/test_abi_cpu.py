@@ -68,6 +68,18 @@ def test_workspace_size_monotone(lib):
     assert mds.workspace_size(7, 1, 64, 10, 1, 2, 1, 1, 64, 1) == 0
 
 
+def test_workspace_covers_k_split_partials(lib):
+    # Wo at 89 rows (d = Hq dh = 4096) may run as 8 K-splits with fp32
+    # partial sums [8][89][4096]; with MDS_KSPLIT unset the size must hold
+    # them on top of the attention scratch (x, q, o: 3 x 89 x 4096 bf16)
+    a = mds.workspace_size(1, 1, 4096, 32000, 4, 89, 32, 32, 128, 4)
+    assert a >= 8192 + 8 * 89 * 4096 * 4 + 3 * 89 * 4096 * 2
+    # no split at more than 128 rows: 16 x 89 rows need no such region
+    per_row_small = mds.workspace_size(1, 1, 4096, 32000, 4, 89, 32, 32, 128, 4) / 89
+    per_row_big = mds.workspace_size(1, 16, 4096, 32000, 4, 89, 32, 32, 128, 4) / (16 * 89)
+    assert per_row_big < per_row_small
+
+
 def test_host_validation_rejects_before_launch(lib):
     null = None
     sl = (ctypes.c_int32 * 2)(2, 2)
