@@ -209,7 +209,10 @@ def tree_attention(tok: np.ndarray, P: np.ndarray, mask: np.ndarray,
                    wo: np.ndarray, kc: np.ndarray, vc: np.ndarray,
                    Hq: int, Hkv: int, dh: int, dtype: str) -> Dict[str, np.ndarray]:
     """Returns q, k, v [B, N, H*dh], o [B, N, Hq*dh], y [B, N, d] and the
-    caches with the tree rows written at P_b .. P_b+N-1 (copies)."""
+    caches with the tree rows written at P_b .. P_b+N-1 (copies).  For bf16
+    workloads o and y are the stored (bf16-rounded) values; ``o_exact`` and
+    ``y_exact`` are the same quantities before that final rounding (y_exact
+    is computed from the rounded o, as the next projection reads it)."""
     B, N = tok.shape
     g = Hq // Hkv
     x = emb[tok]                                         # [B, N, d]
@@ -237,9 +240,11 @@ def tree_attention(tok: np.ndarray, P: np.ndarray, mask: np.ndarray,
                 p = np.exp(s)
                 p = p / p.sum()
                 o[b, n, hq * dh:(hq + 1) * dh] = p @ vals
-    o = maybe_round(o, dtype)
-    y = maybe_round(o @ wo.T, dtype)
-    return dict(x=x, q=q, k=k, v=v, o=o, y=y, kc=kc, vc=vc)
+    o_exact = o
+    o = maybe_round(o_exact, dtype)
+    y_exact = o @ wo.T
+    y = maybe_round(y_exact, dtype)
+    return dict(x=x, q=q, k=k, v=v, o=o, y=y, o_exact=o_exact, y_exact=y_exact, kc=kc, vc=vc)
 
 
 # ----------------------------------------------------------------------------
@@ -286,8 +291,11 @@ def accept_edges(mode: str, eps: float, delta: float, tok: np.ndarray,
                  parent: np.ndarray, st: Dict[str, np.ndarray]) -> Tuple[np.ndarray, np.ndarray]:
     """ok [B, N] (entry 0 = True), margin [B, N] (entry 0 = inf).
 
-    Greedy margin: the parent row's top-1 minus top-2 logit gap.  Typical
-    margin: |ln p - ln threshold| (inf when the threshold is 0)."""
+    mode "greedy", "typical" or "sample" (R11; ``st`` then also holds
+    sample_tokens' output).  Greedy margin: the parent row's top-1 minus
+    top-2 logit gap.  Typical margin: |ln p - ln threshold| (inf when the
+    threshold is 0).  Sample margin: the parent row's best minus second-best
+    Gumbel key."""
     B, N = tok.shape
     ok = np.ones((B, N), bool)
     margin = np.full((B, N), np.inf)
@@ -297,6 +305,10 @@ def accept_edges(mode: str, eps: float, delta: float, tok: np.ndarray,
             if mode == "greedy":
                 ok[b, c] = tok[b, c] == st["argmax"][b, pa]
                 margin[b, c] = st["argmax_gap"][b, pa]
+            elif mode == "sample":
+                # R11: the child carrying the token drawn at its parent
+                ok[b, c] = tok[b, c] == st["sample"][b, pa]
+                margin[b, c] = st["sample_gap"][b, pa]
             else:
                 p = math.exp(st["childlogit"][b, c] - st["lse"][b, pa])
                 thr = min(eps, delta * math.exp(-st["H"][b, pa]))
@@ -362,10 +374,12 @@ def compact_kv(kc: np.ndarray, vc: np.ndarray, P: np.ndarray, L: np.ndarray,
 # ----------------------------------------------------------------------------
 
 def step(w, f64: Dict[str, np.ndarray], P: np.ndarray, mode: str,
-         batch: Sequence[int] = None) -> Dict[str, object]:
+         batch: Sequence[int] = None, sampling: Tuple[float, int, int] = None) -> Dict[str, object]:
     """One step on inputs ``f64`` (float64 copies of the stored inputs:
     h, W, lm, emb, wq, wk, wv, wo, kc, vc).  ``batch`` restricts the step to
-    some sequences (their rows of h, kc, vc, P).  Returns every
+    some sequences (their rows of h, kc, vc, P).  mode "sample" draws the
+    tree rows' tokens with ``sampling`` = (T, seed, offset) (R11, R12); the
+    rows are numbered b N + n over the restricted batch.  Returns every
     intermediate."""
     sel = list(range(w.B)) if batch is None else list(batch)
     h = f64["h"][sel]
@@ -379,8 +393,157 @@ def step(w, f64: Dict[str, np.ndarray], P: np.ndarray, mode: str,
     at = tree_attention(tok, Psel, tr["mask"], f64["emb"], f64["wq"], f64["wk"],
                         f64["wv"], f64["wo"], kc, vc, w.Hq, w.Hkv, w.dh, w.dtype)
     st = verify_stats(at["y"], f64["lm"], tok, tr["parent"])
+    if mode == "sample":
+        st.update(sample_tokens(at["y"], f64["lm"], *sampling))
     ok, margin = accept_edges(mode, w.eps, w.delta, tok, tr["parent"], st)
-    lp = longest_path(ok, tr["parent"], tr["depth"], st["argmax"], w.K)
+    lp = longest_path(ok, tr["parent"], tr["depth"],
+                      st["sample"] if mode == "sample" else st["argmax"], w.K)
     kc2, vc2, Pn = compact_kv(at["kc"], at["vc"], Psel, lp["L"], lp["path"])
     return dict(batch=sel, U=U, draft=dr, tree=tr, tok=tok, attn=at, stats=st,
                 ok=ok, margin=margin, path=lp, kc=kc2, vc=vc2, P=Pn)
+
+
+# ----------------------------------------------------------------------------
+# The decoding loop: consecutive steps with the caches and prefix lengths
+# carried ("Medusa Heads", "How it works": draft, verify, accept and roll
+# back, then draft again from the last accepted position).  R10 below.
+#   R10 The hidden state the next step's heads read is the verify layer's
+#       output y at the step's accepted node p_L: the base model's last hidden
+#       state at the last accepted token.  Its base-head argmax is therefore
+#       the step's next_root, which becomes the next step's root (R7), so the
+#       tokens emitted over consecutive steps are root, path tokens, then the
+#       next root, and so on.
+# ----------------------------------------------------------------------------
+
+def next_hidden(y: np.ndarray, L: np.ndarray, path: np.ndarray) -> np.ndarray:
+    """h for the next step: y[b, path[b, L_b]] for every sequence (R10)."""
+    B = y.shape[0]
+    return np.stack([y[b, int(path[b, int(L[b])])] for b in range(B)])
+
+
+def decode(w, f64: Dict[str, np.ndarray], P: np.ndarray, mode: str, n_steps: int,
+           batch: Sequence[int] = None, eps: float = None, delta: float = None,
+           sampling: Tuple[float, int, int] = None) -> List[Dict]:
+    """``n_steps`` consecutive steps from hidden state f64["h"]: each step as
+    ``step`` on the carried caches and prefix lengths, the next step reading
+    next_hidden of this one.  mode "sample": step s draws with offset
+    sampling[2] + s.  Returns each step's intermediates plus its ``emitted``
+    tokens per sequence (root and accepted path tokens, L + 1)."""
+    sel = list(range(w.B)) if batch is None else list(batch)
+    wk = w if eps is None and delta is None else w.with_(
+        eps=w.eps if eps is None else eps, delta=w.delta if delta is None else delta)
+    cur = dict(f64)
+    cur["h"] = f64["h"][sel]
+    cur["kc"] = f64["kc"][sel]
+    cur["vc"] = f64["vc"][sel]
+    Pc = np.asarray(P)[sel].astype(np.int64)
+    idx = list(range(len(sel)))
+    out = []
+    for s in range(n_steps):
+        smp = None if sampling is None else (sampling[0], sampling[1], sampling[2] + s)
+        r = step(wk, cur, Pc, mode, batch=idx, sampling=smp)
+        r["emitted"] = [[int(r["tok"][b, int(n)]) for n in r["path"]["path"][b, : int(r["path"]["L"][b]) + 1]]
+                        for b in idx]
+        out.append(r)
+        cur = dict(cur)
+        cur["h"] = next_hidden(r["attn"]["y"], r["path"]["L"], r["path"]["path"])
+        cur["kc"], cur["vc"] = r["kc"], r["vc"]
+        Pc = r["P"]
+    return out
+
+
+# ----------------------------------------------------------------------------
+# Exact (lossless) sampling acceptance.  [DD] "Typical acceptance, not exact
+# rejection sampling": classic speculative decoding accepts or rejects each
+# drafted token with a probability chosen so that the output is distributed
+# exactly as sampling from the target model; [GU] "Deep Dive": rejection
+# sampling against the base model's distribution makes Medusa lossless.
+#   R11 The drafts are deterministic (each head's top s_i), so a candidate's
+#       proposal is a point mass q = 1{x}: the accept/reject rule accepts x
+#       with probability min(1, p(x)/q(x)) = p(x), and on rejection the
+#       residual max(0, p - q), renormalised, is p with x removed.  Trying a
+#       node's children in rank order this way is the same, in distribution,
+#       as drawing one token t ~ p from the node's verify distribution and
+#       accepting the child whose token is t; when no child carries t, t is
+#       the bonus token, a draw from the residual (p without the children).
+#       That is the form computed here: t is drawn once per tree row with the
+#       Gumbel-max rule t = argmax_v (l_v / T + G_v), G_v = -ln(-ln U_v), at
+#       temperature T (p proportional to exp(l / T)); ties go to the lowest id.
+#       Acceptance is then greedy acceptance with t in place of the argmax,
+#       and next_root is t at the accepted node.
+#   R12 Random numbers: U for row r = b N + n and token v comes from
+#       Philox4x64-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers:
+#       as easy as 1, 2, 3", SC 2011) with key (seed, 0) and counter
+#       (v >> 3, r, offset, 0); of the four 64-bit words the one at position
+#       (v >> 1) & 3 is used, its top 24 bits for even v and bits 16..39 for
+#       odd v: m, and U = (m + 0.5) / 2^24.  -ln U is evaluated as
+#       -log1p(-(1 - U)) with 1 - U = (2^24 - m - 0.5) / 2^24 exact.
+# ----------------------------------------------------------------------------
+
+_PHILOX_M = (0xD2E7470EE14C6C93, 0xCA5A826395121157)
+_PHILOX_W = (0x9E3779B97F4A7C15, 0xBB67AE8584CAA73B)
+
+
+def _mulhilo64(a: np.ndarray, b: int) -> Tuple[np.ndarray, np.ndarray]:
+    """High and low 64 bits of the 128-bit product a * b (a uint64 array)."""
+    a = np.asarray(a, np.uint64)
+    m32 = np.uint64(0xFFFFFFFF)
+    s32 = np.uint64(32)
+    bl, bh = np.uint64(b & 0xFFFFFFFF), np.uint64(b >> 32)
+    al, ah = a & m32, a >> s32
+    ll, lh, hl, hh = al * bl, al * bh, ah * bl, ah * bh
+    mid = (ll >> s32) + (lh & m32) + (hl & m32)
+    hi = hh + (lh >> s32) + (hl >> s32) + (mid >> s32)
+    lo = (ll & m32) | ((mid & m32) << s32)
+    return hi, lo
+
+
+def philox4x64(counter: Sequence[np.ndarray], key: Tuple[int, int],
+               rounds: int = 10) -> List[np.ndarray]:
+    """Philox4x64 block function on uint64 counter words c0..c3 (arrays of
+    one shape) and key (k0, k1): ``rounds`` rounds, the key bumped by the
+    Weyl constants before every round but the first."""
+    with np.errstate(over="ignore"):
+        c = [np.asarray(x, np.uint64).copy() for x in counter]
+        k0, k1 = np.uint64(key[0]), np.uint64(key[1])
+        for i in range(rounds):
+            if i:
+                k0 = np.uint64((int(k0) + _PHILOX_W[0]) & 0xFFFFFFFFFFFFFFFF)
+                k1 = np.uint64((int(k1) + _PHILOX_W[1]) & 0xFFFFFFFFFFFFFFFF)
+            hi0, lo0 = _mulhilo64(c[0], _PHILOX_M[0])
+            hi1, lo1 = _mulhilo64(c[2], _PHILOX_M[1])
+            c = [hi1 ^ c[1] ^ k0, lo1, hi0 ^ c[3] ^ k1, lo0]
+    return c
+
+
+def gumbel_keys(logits: np.ndarray, T: float, seed: int, offset: int, row: int) -> np.ndarray:
+    """l_v / T + G_v for one row of logits (R11, R12)."""
+    V = logits.shape[0]
+    v = np.arange(V, dtype=np.uint64)
+    zero = np.zeros(V, np.uint64)
+    words = philox4x64([v >> np.uint64(3), zero + np.uint64(row), zero + np.uint64(offset), zero],
+                       (seed, 0))
+    sel = ((v >> np.uint64(1)) & np.uint64(3)).astype(np.int64)
+    x = np.choose(sel, words)
+    odd = (v & np.uint64(1)).astype(bool)
+    m = np.where(odd, (x >> np.uint64(16)) & np.uint64(0xFFFFFF), x >> np.uint64(40))
+    one_minus_u = (2.0 ** 24 - m.astype(np.float64) - 0.5) / 2.0 ** 24
+    neg_log_u = -np.log1p(-one_minus_u)
+    return logits / T - np.log(neg_log_u)
+
+
+def sample_tokens(y: np.ndarray, lm: np.ndarray, T: float, seed: int,
+                  offset: int) -> Dict[str, np.ndarray]:
+    """y [B, N, d] -> sample [B, N] (the token drawn at every tree row, R11)
+    and sample_gap [B, N] (best minus second-best key: the decision margin)."""
+    B, N, d = y.shape
+    sample = np.empty((B, N), np.int64)
+    gap = np.empty((B, N))
+    for b in range(B):
+        l = y[b] @ lm.T
+        for n in range(N):
+            keys = gumbel_keys(l[n], T, seed, offset, b * N + n)
+            order = sorted_ids(keys)
+            sample[b, n] = order[0]
+            gap[b, n] = keys[order[0]] - keys[order[1]]
+    return dict(sample=sample, sample_gap=gap)

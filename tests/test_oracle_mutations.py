@@ -116,6 +116,44 @@ def round_truncate(x):
     return np.ldexp(np.trunc(m * 256.0) / 256.0, e)
 
 
+def decode_with_hidden(pick):
+    """The decoding loop with another choice of the next step's hidden state."""
+    def f(*args, **kw):
+        orig = mo.next_hidden
+        try:
+            mo.next_hidden = pick
+            return mo.decode(*args, **kw)
+        finally:
+            mo.next_hidden = orig
+    return f
+
+
+def hidden_of_root(y, L, path):
+    return y[:, 0].copy()
+
+
+def hidden_of_parent(y, L, path):
+    # the accepted node's parent (the root when nothing was accepted)
+    return np.stack([y[b, int(path[b, max(int(L[b]) - 1, 0)])] for b in range(y.shape[0])])
+
+
+def philox_no_key_bump(counter, key, rounds=10):
+    # every round with the original key
+    c = [np.asarray(x, np.uint64).copy() for x in counter]
+    for _ in range(rounds):
+        c = mo.philox4x64(c, key, rounds=1)
+    return c
+
+
+def gumbel_no_temperature(logits, T, seed, offset, row):
+    return mo.gumbel_keys(logits, 1.0, seed, offset, row)
+
+
+def gumbel_sign_flipped(logits, T, seed, offset, row):
+    g = mo.gumbel_keys(logits, T, seed, offset, row) - logits / T
+    return logits / T - g
+
+
 CASES = [
     ("heads: sigmoid instead of SiLU", dict(heads_residual=heads_sigmoid_only), [pins.check_heads_torch]),
     ("heads: residual dropped", dict(heads_residual=heads_no_residual), [pins.check_zero_heads, pins.check_heads_torch]),
@@ -132,6 +170,11 @@ CASES = [
     ("path: ties to the highest index", dict(longest_path=longest_path_high_index), [pins.check_longest_path_golden, pins.check_longest_path_brute]),
     ("compaction: root row dropped", dict(compact_kv=compact_skip_root), [pins.check_compaction]),
     ("bf16: truncation instead of rounding", dict(round_bf16=round_truncate), [pins.check_round_bf16]),
+    ("philox: key not bumped between rounds", dict(philox4x64=philox_no_key_bump), [pins.check_philox_library]),
+    ("sample: temperature ignored", dict(gumbel_keys=gumbel_no_temperature), [pins.check_sampler_distribution]),
+    ("sample: Gumbel noise sign flipped", dict(gumbel_keys=gumbel_sign_flipped), [pins.check_sampler_distribution, pins.check_sampling_is_rejection_sampling]),
+    ("decode: next hidden state from the root row", dict(decode=decode_with_hidden(hidden_of_root)), [pins.check_decode_greedy_lossless]),
+    ("decode: next hidden state from the accepted node's parent", dict(decode=decode_with_hidden(hidden_of_parent)), [pins.check_decode_greedy_lossless]),
 ]
 
 

@@ -50,12 +50,15 @@ def tiny(seed=0, B=2, d=32, V=40, Hq=4, Hkv=2, dh=8, shortlist=(3, 2, 2), mrs=-1
 
 def check_tree_counts(orc):
     for ln in golden_lines("tree_counts.txt"):
-        sl, mrs, nodes, paths = [t.strip() for t in ln.split(";")]
+        sl, mrs, nodes, paths, per_depth = [t.strip() for t in ln.split(";")]
         s = tuple(int(v) for v in sl.split(","))
         tr = orc.build_tree(s, int(mrs))
         assert tr["N"] - 1 == int(nodes), (s, tr["N"])
         if paths != "-":
             assert int(np.sum(tr["depth"] == len(s))) == int(paths)
+        want = [int(v) for v in per_depth.split(",")]
+        got = [int(np.sum(tr["depth"] == dd)) for dd in range(1, len(s) + 1)]
+        assert got == want, (s, got, want)
     # closed form sum_d prod_{j<=d} s_j on random full trees
     rng = np.random.default_rng(5)
     for _ in range(20):
@@ -509,3 +512,184 @@ def test_step_config0_consistent():
     assert r["tree"]["N"] == 15
     assert r["P"][0] == x["P"][0] + r["path"]["L"][0] + 1
     assert r["tok"][0, 0] == r["draft"]["root"][0]
+
+
+# ---------------------------------------------------------------------------
+# The decoding loop: greedy acceptance over consecutive steps emits exactly
+# sequential greedy decoding, and the cache it leaves is the one sequential
+# decoding builds ("Medusa Heads": rollback to the last accepted position, the
+# next token from the base model, then draft again; "Medusa Decoding Heads",
+# "Deep Dive": the output is what the model would have produced anyway)
+# ---------------------------------------------------------------------------
+
+def check_decode_greedy_lossless(orc, seed=12, n_steps=4):
+    # a vocabulary of 8 with shortlists (3, 2, 2) makes drafts hit often, so
+    # the accepted depths over the steps range from 0 to K
+    w, f, P = tiny(seed=seed, B=3, d=64, V=8, Hq=2, Hkv=1, dh=64, shortlist=(3, 2, 2),
+                   P=(5, 12))
+    rs = orc.decode(w, f, P, "greedy", n_steps)
+    depths = set()
+    for b in range(w.B):
+        emitted = sum((r["emitted"][b] for r in rs), [])
+        depths |= {int(r["path"]["L"][b]) for r in rs}
+        Pb = int(P[b])
+        seq = brute.greedy_decode(f["kc"][b][:, :Pb], f["vc"][b][:, :Pb], emitted[0],
+                                  len(emitted), f["emb"], f["wq"], f["wk"], f["wv"], f["wo"],
+                                  f["lm"], w.Hq, w.Hkv, w.dh)
+        # every emitted token, and the last step's bonus token after them
+        assert emitted + [int(rs[-1]["path"]["next_root"][b])] == seq
+        # cache: one row per emitted token (a token's K/V depend on it alone
+        # in this one-layer verifier), the prefix untouched, P advanced
+        last = rs[-1]
+        assert int(last["P"][b]) == Pb + len(emitted)
+        _, k, v = brute.project(emitted, f["emb"], f["wq"], f["wk"], f["wv"])
+        for j in range(len(emitted)):
+            np.testing.assert_allclose(last["kc"][b][:, Pb + j].reshape(-1), k[j], rtol=1e-12,
+                                       atol=1e-12)
+            np.testing.assert_allclose(last["vc"][b][:, Pb + j].reshape(-1), v[j], rtol=1e-12,
+                                       atol=1e-12)
+        np.testing.assert_array_equal(last["kc"][b][:, :Pb], f["kc"][b][:, :Pb])
+    assert depths >= {0, 1, 2, 3}, depths
+
+
+@pytest.mark.parametrize("seed", [12, 16])
+def test_decode_greedy_lossless(seed):
+    check_decode_greedy_lossless(oracle, seed)
+
+
+# ---------------------------------------------------------------------------
+# Exact sampling acceptance: the random numbers, the draw, and the rule
+# ("Medusa deep dive", "Typical acceptance, not exact rejection sampling";
+# "Medusa Decoding Heads", "Deep Dive": rejection sampling against the base
+# model keeps its output distribution)
+# ---------------------------------------------------------------------------
+
+def check_philox_library(orc):
+    """Philox4x64-10 equals numpy's implementation of it (numpy's generator
+    advances its counter before each block, so its first block is that of
+    counter + 1)."""
+    cases = [((0, 0), (0, 0, 0, 0)), ((123456789, 0), (7, 3, 2, 1)),
+             ((2 ** 64 - 1, 2 ** 63 + 5), (2 ** 64 - 1, 0, 9, 2 ** 40))]
+    for key, ctr in cases:
+        bg = np.random.Philox(key=np.array(key, dtype=np.uint64),
+                              counter=np.array(ctr, dtype=np.uint64))
+        raw = [int(v) for v in bg.random_raw(8)]
+        c = list(ctr)
+        for blk in range(2):
+            c[0] = (c[0] + 1) % 2 ** 64
+            if c[0] == 0:
+                c[1] += 1
+            got = [int(wd[0]) for wd in orc.philox4x64([np.array([v], np.uint64) for v in c], key)]
+            assert got == raw[4 * blk:4 * blk + 4], (key, ctr, blk)
+
+
+def check_sampler_distribution(orc, rows=4000):
+    """The Gumbel-max draw at temperature T is distributed as
+    softmax(l / T): empirical frequencies over many rows (independent
+    counters) within 5 standard deviations of the exact probabilities."""
+    logits = np.array([1.0, 0.2, -0.5, 2.0, 0.0])
+    for T in (0.7, 1.3):
+        counts = np.zeros(5)
+        for r in range(rows):
+            counts[int(np.argmax(orc.gumbel_keys(logits, T, 99, 5, r)))] += 1
+        p = scipy.special.softmax(logits / T)
+        sd = np.sqrt(rows * p * (1 - p))
+        assert np.all(np.abs(counts - rows * p) < 5 * sd), (T, counts, rows * p)
+
+
+def check_sampling_is_rejection_sampling(orc, rows=4000):
+    """Accepting the child that carries the drawn token is the accept/reject
+    rule with point-mass proposals: trying the children c_1..c_m in rank order,
+    each accepted with probability p(c_j) / (1 - sum_{i<j} p(c_i)), and on
+    rejection of all a residual draw from p without the children.  The
+    outcome frequencies of the oracle's rule match that procedure's exact
+    outcome probabilities, which a direct simulation of the procedure (with
+    independent uniforms) also matches."""
+    logits = np.array([0.5, 1.5, -1.0, 0.3, 1.0, -0.2])
+    children = [1, 4, 0]                      # rank order of the drafted tokens
+    p = scipy.special.softmax(logits)
+    # exact outcome probabilities of the sequential rule
+    want = np.zeros(len(logits))
+    rest = 1.0
+    for c in children:
+        want[c] = rest * (p[c] / rest)
+        rest -= p[c]
+    others = [v for v in range(len(logits)) if v not in children]
+    for v in others:
+        want[v] = rest * p[v] / rest
+    np.testing.assert_allclose(want, p, rtol=1e-12)
+    # simulation of the sequential rule
+    rng = np.random.default_rng(0)
+    sim = np.zeros(len(logits))
+    for _ in range(rows):
+        rest, out = 1.0, None
+        for c in children:
+            if rng.random() < p[c] / rest:
+                out = c
+                break
+            rest -= p[c]
+        if out is None:
+            q = np.array([p[v] for v in others]) / rest
+            out = others[int(rng.choice(len(others), p=q))]
+        sim[out] += 1
+    # the oracle's rule: the drawn token is the accepted child or the bonus
+    got = np.zeros(len(logits))
+    for r in range(rows):
+        got[int(np.argmax(orc.gumbel_keys(logits, 1.0, 7, 0, r)))] += 1
+    sd = np.sqrt(rows * want * (1 - want))
+    assert np.all(np.abs(sim - rows * want) < 5 * sd), (sim, rows * want)
+    assert np.all(np.abs(got - rows * want) < 5 * sd), (got, rows * want)
+
+
+def check_sample_acceptance(orc):
+    """The accepted path follows the drawn tokens: plant the drawn token of
+    each node as one of its children's tokens down one branch; the accepted
+    depth is the planted depth and next_root is the token drawn at the
+    accepted node."""
+    w, f, P = tiny(seed=5, B=1, V=40, shortlist=(3, 2, 2))
+    tr = orc.build_tree(w.shortlist, -1)
+    rng = np.random.default_rng(1)
+    y = rng.standard_normal((1, tr["N"], w.d))
+    smp = orc.sample_tokens(y, f["lm"], 0.8, 11, 3)
+    for plant in range(w.K + 1):
+        tok = rng.integers(0, w.V, size=(1, tr["N"]))
+        node = 0
+        for dd in range(plant):
+            child = [c for c in range(tr["N"]) if tr["parent"][c] == node][1 if dd % 2 else 0]
+            tok[0, child] = smp["sample"][0, node]
+            node = child
+        # no other child of a node on the branch carries its draw
+        for c in range(1, tr["N"]):
+            pa = tr["parent"][c]
+            if tok[0, c] == smp["sample"][0, pa] and c not in _branch(tr, node):
+                tok[0, c] = (tok[0, c] + 1) % w.V
+        st = dict(smp)
+        ok, _ = orc.accept_edges("sample", 0, 0, tok, tr["parent"], st)
+        r = orc.longest_path(ok, tr["parent"], tr["depth"], smp["sample"], w.K)
+        assert int(r["L"][0]) == plant
+        assert int(r["path"][0, plant]) == node
+        assert int(r["next_root"][0]) == int(smp["sample"][0, node])
+
+
+def _branch(tr, node):
+    out = []
+    while node:
+        out.append(node)
+        node = int(tr["parent"][node])
+    return out
+
+
+def test_philox_library():
+    check_philox_library(oracle)
+
+
+def test_sampler_distribution():
+    check_sampler_distribution(oracle)
+
+
+def test_sampling_is_rejection_sampling():
+    check_sampling_is_rejection_sampling(oracle)
+
+
+def test_sample_acceptance():
+    check_sample_acceptance(oracle)
