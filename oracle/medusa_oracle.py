@@ -374,13 +374,13 @@ def compact_kv(kc: np.ndarray, vc: np.ndarray, P: np.ndarray, L: np.ndarray,
 # ----------------------------------------------------------------------------
 
 def step(w, f64: Dict[str, np.ndarray], P: np.ndarray, mode: str,
-         batch: Sequence[int] = None, sampling: Tuple[float, int, int] = None) -> Dict[str, object]:
+         batch: Sequence[int] = None, sampling: Tuple = None) -> Dict[str, object]:
     """One step on inputs ``f64`` (float64 copies of the stored inputs:
     h, W, lm, emb, wq, wk, wv, wo, kc, vc).  ``batch`` restricts the step to
     some sequences (their rows of h, kc, vc, P).  mode "sample" draws the
-    tree rows' tokens with ``sampling`` = (T, seed, offset) (R11, R12); the
-    rows are numbered b N + n over the restricted batch.  Returns every
-    intermediate."""
+    tree rows' tokens with ``sampling`` = (T, seed) or (T, seed, seq), seq
+    the sequences' numbers (R11, R12; default: their positions in the
+    batch).  Returns every intermediate."""
     sel = list(range(w.B)) if batch is None else list(batch)
     h = f64["h"][sel]
     kc = f64["kc"][sel]
@@ -394,7 +394,8 @@ def step(w, f64: Dict[str, np.ndarray], P: np.ndarray, mode: str,
                         f64["wv"], f64["wo"], kc, vc, w.Hq, w.Hkv, w.dh, w.dtype)
     st = verify_stats(at["y"], f64["lm"], tok, tr["parent"])
     if mode == "sample":
-        st.update(sample_tokens(at["y"], f64["lm"], *sampling))
+        seq = sampling[2] if len(sampling) > 2 else None
+        st.update(sample_tokens(at["y"], f64["lm"], sampling[0], sampling[1], Psel, seq))
     ok, margin = accept_edges(mode, w.eps, w.delta, tok, tr["parent"], st)
     lp = longest_path(ok, tr["parent"], tr["depth"],
                       st["sample"] if mode == "sample" else st["argmax"], w.K)
@@ -423,12 +424,13 @@ def next_hidden(y: np.ndarray, L: np.ndarray, path: np.ndarray) -> np.ndarray:
 
 def decode(w, f64: Dict[str, np.ndarray], P: np.ndarray, mode: str, n_steps: int,
            batch: Sequence[int] = None, eps: float = None, delta: float = None,
-           sampling: Tuple[float, int, int] = None) -> List[Dict]:
+           sampling: Tuple = None) -> List[Dict]:
     """``n_steps`` consecutive steps from hidden state f64["h"]: each step as
     ``step`` on the carried caches and prefix lengths, the next step reading
-    next_hidden of this one.  mode "sample": step s draws with offset
-    sampling[2] + s.  Returns each step's intermediates plus its ``emitted``
-    tokens per sequence (root and accepted path tokens, L + 1)."""
+    next_hidden of this one (``sampling`` as in ``step``; the draws of each
+    step are tied to its prefix lengths, R12).  Returns each step's
+    intermediates plus its ``emitted`` tokens per sequence (root and accepted
+    path tokens, L + 1)."""
     sel = list(range(w.B)) if batch is None else list(batch)
     wk = w if eps is None and delta is None else w.with_(
         eps=w.eps if eps is None else eps, delta=w.delta if delta is None else delta)
@@ -439,9 +441,8 @@ def decode(w, f64: Dict[str, np.ndarray], P: np.ndarray, mode: str, n_steps: int
     Pc = np.asarray(P)[sel].astype(np.int64)
     idx = list(range(len(sel)))
     out = []
-    for s in range(n_steps):
-        smp = None if sampling is None else (sampling[0], sampling[1], sampling[2] + s)
-        r = step(wk, cur, Pc, mode, batch=idx, sampling=smp)
+    for _ in range(n_steps):
+        r = step(wk, cur, Pc, mode, batch=idx, sampling=sampling)
         r["emitted"] = [[int(r["tok"][b, int(n)]) for n in r["path"]["path"][b, : int(r["path"]["L"][b]) + 1]]
                         for b in idx]
         out.append(r)
@@ -471,13 +472,16 @@ def decode(w, f64: Dict[str, np.ndarray], P: np.ndarray, mode: str, n_steps: int
 #       temperature T (p proportional to exp(l / T)); ties go to the lowest id.
 #       Acceptance is then greedy acceptance with t in place of the argmax,
 #       and next_root is t at the accepted node.
-#   R12 Random numbers: U for row r = b N + n and token v comes from
-#       Philox4x64-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers:
-#       as easy as 1, 2, 3", SC 2011) with key (seed, 0) and counter
-#       (v >> 3, r, offset, 0); of the four 64-bit words the one at position
-#       (v >> 1) & 3 is used, its top 24 bits for even v and bits 16..39 for
-#       odd v: m, and U = (m + 0.5) / 2^24.  -ln U is evaluated as
-#       -log1p(-(1 - U)) with 1 - U = (2^24 - m - 0.5) / 2^24 exact.
+#   R12 Random numbers: U for tree node n of sequence b, whose root sits at
+#       position P_b, and token v comes from Philox4x64-10 (Salmon, Moraes,
+#       Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3", SC 2011)
+#       with key (seed, 0) and counter (v >> 3, n, P_b, b): every draw is
+#       tied to its sequence, position and node, and P_b advances every step,
+#       so consecutive steps draw afresh with no other state.  Of the four
+#       64-bit words the one at position (v >> 1) & 3 is used, its top 24
+#       bits for even v and bits 16..39 for odd v: m, and
+#       U = (m + 0.5) / 2^24.  -ln U is evaluated as -log1p(-(1 - U)) with
+#       1 - U = (2^24 - m - 0.5) / 2^24 exact.
 # ----------------------------------------------------------------------------
 
 _PHILOX_M = (0xD2E7470EE14C6C93, 0xCA5A826395121157)
@@ -516,13 +520,13 @@ def philox4x64(counter: Sequence[np.ndarray], key: Tuple[int, int],
     return c
 
 
-def gumbel_keys(logits: np.ndarray, T: float, seed: int, offset: int, row: int) -> np.ndarray:
-    """l_v / T + G_v for one row of logits (R11, R12)."""
+def gumbel_keys(logits: np.ndarray, T: float, seed: int, words3: Tuple[int, int, int]) -> np.ndarray:
+    """l_v / T + G_v for one row of logits (R11); words3 = the counter's
+    last three words (node, position, sequence: R12)."""
     V = logits.shape[0]
     v = np.arange(V, dtype=np.uint64)
     zero = np.zeros(V, np.uint64)
-    words = philox4x64([v >> np.uint64(3), zero + np.uint64(row), zero + np.uint64(offset), zero],
-                       (seed, 0))
+    words = philox4x64([v >> np.uint64(3)] + [zero + np.uint64(c) for c in words3], (seed, 0))
     sel = ((v >> np.uint64(1)) & np.uint64(3)).astype(np.int64)
     x = np.choose(sel, words)
     odd = (v & np.uint64(1)).astype(bool)
@@ -532,18 +536,114 @@ def gumbel_keys(logits: np.ndarray, T: float, seed: int, offset: int, row: int) 
     return logits / T - np.log(neg_log_u)
 
 
-def sample_tokens(y: np.ndarray, lm: np.ndarray, T: float, seed: int,
-                  offset: int) -> Dict[str, np.ndarray]:
+def sample_tokens(y: np.ndarray, lm: np.ndarray, T: float, seed: int, P: np.ndarray,
+                  seq: Sequence[int] = None) -> Dict[str, np.ndarray]:
     """y [B, N, d] -> sample [B, N] (the token drawn at every tree row, R11)
-    and sample_gap [B, N] (best minus second-best key: the decision margin)."""
+    and sample_gap [B, N] (best minus second-best key: the decision margin).
+    P [B]: the sequences' prefix lengths; seq [B]: their sequence numbers
+    (default 0..B-1)."""
     B, N, d = y.shape
+    seq = list(range(B)) if seq is None else list(seq)
     sample = np.empty((B, N), np.int64)
     gap = np.empty((B, N))
     for b in range(B):
         l = y[b] @ lm.T
         for n in range(N):
-            keys = gumbel_keys(l[n], T, seed, offset, b * N + n)
+            keys = gumbel_keys(l[n], T, seed, (n, int(P[b]), int(seq[b])))
             order = sorted_ids(keys)
             sample[b, n] = order[0]
             gap[b, n] = keys[order[0]] - keys[order[1]]
     return dict(sample=sample, sample_gap=gap)
+
+
+# ----------------------------------------------------------------------------
+# A backbone pass over the tree: position ids applied and several layers.
+# [DD] "From top-k heads to a sparse candidate tree": the tree is laid out as
+# a flat node sequence with a matching attention mask *and position ids*, and
+# the whole tree is pushed through the backbone in one forward pass.
+#   R13b Position ids: node n of sequence b sits at position P_b + depth_n
+#       (its root at P_b, the position the next token takes), so every
+#       root-to-node path carries the positions sequential decoding would
+#       give it.  They are applied as rotary position embeddings (RoFormer,
+#       Su et al. 2021): within each head, the pair (x_{2i}, x_{2i+1}) of q
+#       and k is rotated by the angle pos * base^(-2i/dh); v is not rotated.
+#       The cache holds rotated keys (the prefix's are taken as already
+#       rotated), so a committed tree row needs no re-rotation: the j-th node
+#       of the accepted path has depth j and lands at slot P_b + j.
+#   R13c Layers: x_0 = Emb[tok]; layer l computes q, k, v from x_{l-1} (its
+#       own Wq, Wk, Wv, Wo and KV cache), attends like the single verify
+#       layer, and adds its output to the residual stream:
+#       x_l = x_{l-1} + Wo_l o_l (stored in bf16 for bf16 workloads).  The
+#       verify logits read x_L.  No norm or MLP (the pages name none).
+# ----------------------------------------------------------------------------
+
+def rope(x: np.ndarray, pos: np.ndarray, dh: int, base: float) -> np.ndarray:
+    """x [..., H*dh] at positions pos [...]: every head's pairs (2i, 2i+1)
+    rotated by pos * base^(-2i/dh) (R13b)."""
+    shp = x.shape
+    xr = x.reshape(shp[:-1] + (shp[-1] // dh, dh // 2, 2))
+    theta = base ** (-2.0 * np.arange(dh // 2) / dh)
+    ang = np.asarray(pos, np.float64)[..., None, None] * theta        # [..., 1, dh/2]
+    c, s = np.cos(ang), np.sin(ang)
+    out = np.empty_like(xr)
+    out[..., 0] = xr[..., 0] * c - xr[..., 1] * s
+    out[..., 1] = xr[..., 0] * s + xr[..., 1] * c
+    return out.reshape(shp)
+
+
+def backbone_layer(x: np.ndarray, P: np.ndarray, depth: np.ndarray, mask: np.ndarray,
+                   wq: np.ndarray, wk: np.ndarray, wv: np.ndarray, wo: np.ndarray,
+                   kc: np.ndarray, vc: np.ndarray, Hq: int, Hkv: int, dh: int, dtype: str,
+                   rope_base: float) -> Dict[str, np.ndarray]:
+    """One backbone layer over the tree rows x [B, N, d] (R13b, R13c): like
+    ``tree_attention`` from x instead of token embeddings, with q and k rotated
+    to the rows' position ids and the output added to x.  Returns q, k, v, o,
+    y (= the new residual stream) and the layer's caches with the tree rows
+    written (copies); o_exact and y_exact before their bf16 rounding."""
+    B, N, _ = x.shape
+    g = Hq // Hkv
+    pos = np.asarray(P, np.int64)[:, None] + np.asarray(depth, np.int64)[None, :]   # [B, N]
+    q = maybe_round(rope(x @ wq.T, pos, dh, rope_base), dtype)
+    k = maybe_round(rope(x @ wk.T, pos, dh, rope_base), dtype)
+    v = maybe_round(x @ wv.T, dtype)
+    kc = kc.copy()
+    vc = vc.copy()
+    o = np.empty((B, N, Hq * dh))
+    scale = 1.0 / math.sqrt(dh)
+    for b in range(B):
+        Pb = int(P[b])
+        for n in range(N):
+            kc[b, :, Pb + n, :] = k[b, n].reshape(Hkv, dh)
+            vc[b, :, Pb + n, :] = v[b, n].reshape(Hkv, dh)
+        for n in range(N):
+            slots = list(range(Pb)) + [Pb + m for m in range(N) if mask[n, m]]
+            for hq in range(Hq):
+                hk = hq // g
+                keys = kc[b, hk, slots, :]
+                vals = vc[b, hk, slots, :]
+                s = keys @ q[b, n, hq * dh:(hq + 1) * dh] * scale
+                s = s - s.max()
+                p = np.exp(s)
+                p = p / p.sum()
+                o[b, n, hq * dh:(hq + 1) * dh] = p @ vals
+    o_exact = o
+    o = maybe_round(o_exact, dtype)
+    y_exact = x + o @ wo.T
+    y = maybe_round(y_exact, dtype)
+    return dict(q=q, k=k, v=v, o=o, y=y, o_exact=o_exact, y_exact=y_exact, kc=kc, vc=vc)
+
+
+def backbone(tok: np.ndarray, P: np.ndarray, depth: np.ndarray, mask: np.ndarray,
+             emb: np.ndarray, layers: Sequence[Dict[str, np.ndarray]], kcs: Sequence[np.ndarray],
+             vcs: Sequence[np.ndarray], Hq: int, Hkv: int, dh: int, dtype: str,
+             rope_base: float) -> Dict[str, object]:
+    """The L-layer pass over the tree (R13c): x_0 = Emb[tok], then every
+    layer in turn.  Returns the per-layer results and y = x_L."""
+    x = emb[tok]
+    outs = []
+    for l, lw in enumerate(layers):
+        r = backbone_layer(x, P, depth, mask, lw["wq"], lw["wk"], lw["wv"], lw["wo"], kcs[l],
+                           vcs[l], Hq, Hkv, dh, dtype, rope_base)
+        outs.append(r)
+        x = r["y"]
+    return dict(layers=outs, y=x, y_exact=outs[-1]["y_exact"])
