@@ -17,6 +17,10 @@
  *   mds_lm_verify        verify logits -> argmax / lse / entropy  [DD] typical acceptance
  *   mds_verify_accept    per-edge test + longest accepted path    [GL], [GU], [DD]
  *   mds_compact_kv       commit the accepted path's KV            [GL] KV cache, rollback
+ *   mds_next_inputs      next step's hidden state / draft        [GL] decoding loop
+ * Fused steady-state form: mds_lm_verify_draft replaces mds_lm_verify and
+ * drafts the next step in the same LM-projection stream (the next step then
+ * skips mds_medusa_heads).
  *
  * Conventions shared by every call
  *  - Pointers marked "device" are CUDA device pointers on the current device;
@@ -50,7 +54,12 @@
  *    work enqueued before the call, so inputs written by earlier work on the
  *    stream are always seen.  Environment switches, read once per process:
  *    MDS_PDL=0 launches every kernel plainly; MDS_KSPLIT=0 turns off the
- *    K-split form of the narrow projections (Wo at <= 128 rows).
+ *    K-split form of the narrow projections (Wo at <= 128 rows).  One more
+ *    switch, read at every launch, exists to test the bounded waits:
+ *    MDS_STALL_TEST=1 makes every projection-GEMM CTA first wait (1 ms limit)
+ *    on a barrier that nothing completes, after which it gives up exactly as
+ *    a real timeout does (MDS_DEV_TIMEOUT latched, its copies and MMAs
+ *    drained, tensor memory freed); the call's outputs are then undefined.
  */
 #ifndef MEDUSA_B300_H
 #define MEDUSA_B300_H
@@ -157,11 +166,12 @@ MDS_API int mds_medusa_heads(int dtype, int B, int d, int V, int K, const void* 
  *                 code of this call (0 = none), stream-ordered.
  *   Limits: B * (K + 1) <= 64; larger returns MDS_EUNSUPPORTED before any
  *   work is enqueued.  It calls no cudaMalloc or cudaFree.
- *   The first call on a device looks up the array's device address
- *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture.  All calls share the one array: calls that
- *   overlap on the GPU (other streams, other host threads) race and must be
- *   serialised by the caller. */
+ *   Every call looks up the array's device address (cudaGetSymbolAddress)
+ *   on the current device; the first call on a device also loads the
+ *   library's module there, so make that first call before any stream
+ *   capture.  All calls share the one array: calls that overlap on the GPU
+ *   (other streams, other host threads) race and must be serialised by the
+ *   caller. */
 MDS_API int mds_medusa_heads_noalloc(int B, int d, int V, int K, const void* h, const void* W,
                              const void* lm, const int32_t* shortlist, int smax, void* U,
                              int32_t* root, int32_t* topk_id, float* topk_val,
@@ -209,6 +219,57 @@ MDS_API int mds_lm_verify(int dtype, int B, int N, int d, int V, const void* y, 
                   const int32_t* tok, const int32_t* parent, int32_t* argmax, float* stats,
                   float* childlogit, void* ws, size_t ws_bytes, void* stream);
 
+/* mds_lm_verify plus exact (lossless) sampling: a token drawn at every tree
+ * row from softmax(l / temperature) ([DD] "Typical acceptance, not exact
+ * rejection sampling": rejection sampling keeps the target model's output
+ * distribution exactly; [GU] "Deep Dive": rejection sampling against the
+ * base model makes Medusa lossless).  The drafts are deterministic (the
+ * heads' top s_i), so each candidate's proposal is a point mass: the
+ * accept/reject rule accepts candidate x with probability p(x) and, on
+ * rejection, leaves p without x.  Trying a node's children in rank order
+ * that way is, in distribution, one draw t ~ p per node with the child
+ * carrying t accepted, and t itself the bonus token when no child carries
+ * it; mds_verify_accept with mode 2 applies that rule to sample_id.
+ * The draw is the Gumbel-max rule t = argmax_v (l_v / T - ln(-ln U_v)),
+ * ties to the lowest id, with U_v from Philox4x64-10 (Salmon et al., SC
+ * 2011): key (seed, 0), counter (v >> 3, n, P_b, b) for tree row n of
+ * sequence b, word (v >> 1) & 3 of the block, its top 24 bits for even v and
+ * bits 16..39 for odd v as m, U = (m + 0.5) / 2^24.  Keying by the prefix
+ * length P_b makes consecutive steps draw afresh with no other state.
+ *   P          device [B] int32     prefix lengths (as for the step's
+ *                                   tree attention, before compaction)
+ *   temperature > 0, seed           the draw's temperature and key
+ *   sample_id  device [B, N] int32  out: the token drawn at every tree row
+ *   other arguments as in mds_lm_verify (statistics at temperature 1). */
+MDS_API int mds_lm_verify_sample(int dtype, int B, int N, int d, int V, const void* y,
+                         const void* lm, const int32_t* tok, const int32_t* parent,
+                         const int32_t* P, float temperature, uint64_t seed, int32_t* argmax,
+                         float* stats, float* childlogit, int32_t* sample_id, void* ws,
+                         size_t ws_bytes, void* stream);
+
+/* Verify pass that also drafts the next step, over one LM-projection stream
+ * ([GL] "How it works": the decoding loop drafts, verifies, accepts and rolls
+ * back, then drafts again from the last accepted position; [DD] "The heads
+ * are residual blocks": head_i(h) = LMproj(h + SiLU(W_i h))).  Which tree
+ * row is accepted is not known until mds_verify_accept runs, so the K heads
+ * are applied to every tree row's y, and the verify rows and all B N K head
+ * rows share one pass over LMproj.  The next step then takes its root
+ * (next_root) and shortlists (tree_topk at the accepted node) from this call
+ * through mds_next_inputs instead of running mds_medusa_heads.  bf16 only.
+ *   y, lm, tok, parent, argmax, stats, childlogit   as in mds_lm_verify
+ *   W         device [K, d, d]            the heads' W_i (out, in)
+ *   shortlist host [K], smax              as in mds_medusa_heads
+ *   tree_topk_id  device [B, N, K, smax]  out: head i's top s_i ids at every
+ *                                         tree row (value desc, id asc; -1 pad)
+ *   tree_topk_val device [B, N, K, smax]  out: their logits (-inf pad)
+ *   ws: at least mds_verify_draft_workspace_size(B, N, d, K) bytes. */
+MDS_API size_t mds_verify_draft_workspace_size(int B, int N, int d, int K);
+MDS_API int mds_lm_verify_draft(int dtype, int B, int N, int d, int V, int K, const void* y,
+                        const void* W, const void* lm, const int32_t* shortlist, int smax,
+                        const int32_t* tok, const int32_t* parent, int32_t* argmax,
+                        float* stats, float* childlogit, int32_t* tree_topk_id,
+                        float* tree_topk_val, void* ws, size_t ws_bytes, void* stream);
+
 /* Acceptance and the longest accepted path ([GL] verification pass: early
  * stop at the first rejection, rollback to the last accepted position, the
  * next token comes from the base model; [GU] "Deep Dive": accept the longest
@@ -217,6 +278,10 @@ MDS_API int mds_lm_verify(int dtype, int B, int N, int d, int V, const void* y, 
  *   mode 0 = greedy: child c passes iff tok_c == argmax of its parent row.
  *   mode 1 = typical: passes iff l_parent[tok_c] - lse_parent >
  *            min(ln eps, ln delta - H_parent)  (eps, delta >= 0).
+ *   mode 2 = exact sampling: `argmax` holds the tokens drawn at the rows
+ *            (sample_id of mds_lm_verify_sample); child c passes iff tok_c
+ *            is its parent's draw, and next_root is the draw at the
+ *            accepted node (the bonus token).
  *   The accepted node is the deepest node whose every edge passes, ties to
  *   the lowest breadth-first index.
  *   ok       device [B, N] uint8 or NULL   out: per-edge result (root = 1)
@@ -239,6 +304,29 @@ MDS_API int mds_verify_accept(int B, int N, int K, int mode, float eps, float de
 MDS_API int mds_compact_kv(int dtype, int B, int Hkv, int dh, int Pmax, int K, const int32_t* L,
                    const int32_t* path, void* Kc, void* Vc, int32_t* P,
                    void* ws, size_t ws_bytes, void* stream);
+
+/* Inputs of the next step of the decoding loop ([GL] "How it works":
+ * drafting resumes from the last accepted position).  With a = path[b, L_b]
+ * the accepted node of this step:
+ *   h_next    device [B, d] or NULL   out: y[b, a, :], the hidden state the
+ *                                     next step's heads read (the verify
+ *                                     layer's output at the last accepted
+ *                                     token; its base-head argmax is
+ *                                     next_root)
+ *   root_out  device [B] or NULL      out: next_root[b] (the next step's root)
+ *   topk_id_out, topk_val_out device [B, K, smax] or NULL
+ *                                     out: tree_topk_id/val[b, a] from
+ *                                     mds_lm_verify_draft (the next step's
+ *                                     shortlists)
+ *   y device [B, N, d] (dtype), L, path, next_root as produced above.
+ *   An accepted node outside [0, N) latches MDS_DEV_TREE_INDEX (L outside
+ *   [0, K]: MDS_DEV_PATH_LENGTH) and leaves that sequence's outputs as
+ *   they were. */
+MDS_API int mds_next_inputs(int dtype, int B, int N, int K, int smax, int d, const int32_t* L,
+                    const int32_t* path, const int32_t* next_root, const void* y,
+                    const int32_t* tree_topk_id, const float* tree_topk_val, void* h_next,
+                    int32_t* root_out, int32_t* topk_id_out, float* topk_val_out, void* ws,
+                    size_t ws_bytes, void* stream);
 
 /* Number of kernels this library has enqueued since it was loaded (a host
  * counter; launches captured into a CUDA graph count once, at capture). */

@@ -17,7 +17,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmedusa_b300.so")
 
 F32, BF16 = 0, 1
-GREEDY, TYPICAL = 0, 1
+GREEDY, TYPICAL, SAMPLE = 0, 1, 2
 
 _lib = None
 
@@ -37,6 +37,11 @@ _SIGS = {
     "mds_lm_verify": ([_c_int] * 5 + [_p] * 8 + [_c_size, _p], _c_int),
     "mds_verify_accept": ([_c_int] * 4 + [_c_float, _c_float] + [_p] * 11 + [_c_size, _p], _c_int),
     "mds_compact_kv": ([_c_int] * 6 + [_p] * 6 + [_c_size, _p], _c_int),
+    "mds_lm_verify_sample": ([_c_int] * 5 + [_p] * 5 + [_c_float, ctypes.c_uint64] + [_p] * 5
+                             + [_c_size, _p], _c_int),
+    "mds_verify_draft_workspace_size": ([_c_int] * 4, _c_size),
+    "mds_lm_verify_draft": ([_c_int] * 6 + [_p] * 4 + [_c_int] + [_p] * 8 + [_c_size, _p], _c_int),
+    "mds_next_inputs": ([_c_int] * 6 + [_p] * 11 + [_c_size, _p], _c_int),
     "mds_launch_count": ([], ctypes.c_longlong),
     "mds_status_check": ([_p, _p, _p], _c_int),
 }
@@ -175,6 +180,49 @@ def lm_verify(y, lm, tok, parent, argmax, stats, childlogit, ws):
                               _ptr(parent), _ptr(argmax), _ptr(stats), _ptr(childlogit),
                               _ptr(ws), ws.numel(), _stream())
     _check(rc, "lm_verify")
+
+
+def lm_verify_sample(y, lm, tok, parent, P, temperature, seed, argmax, stats, childlogit,
+                     sample_id, ws):
+    B, N, d = y.shape
+    V = lm.shape[0]
+    rc = load().mds_lm_verify_sample(dtype_code(y), B, N, d, V, _ptr(y), _ptr(lm), _ptr(tok),
+                                     _ptr(parent), _ptr(P), float(temperature),
+                                     ctypes.c_uint64(int(seed)), _ptr(argmax), _ptr(stats),
+                                     _ptr(childlogit), _ptr(sample_id), _ptr(ws), ws.numel(),
+                                     _stream())
+    _check(rc, "lm_verify_sample")
+
+
+def verify_draft_workspace_size(B: int, N: int, d: int, K: int) -> int:
+    return load().mds_verify_draft_workspace_size(B, N, d, K)
+
+
+def lm_verify_draft(y, W, lm, shortlist, smax, tok, parent, argmax, stats, childlogit,
+                    tree_topk_id, tree_topk_val, ws):
+    B, N, d = y.shape
+    V = lm.shape[0]
+    K = W.shape[0]
+    rc = load().mds_lm_verify_draft(dtype_code(y), B, N, d, V, K, _ptr(y), _ptr(W), _ptr(lm),
+                                    _i32(shortlist), smax, _ptr(tok), _ptr(parent),
+                                    _ptr(argmax), _ptr(stats), _ptr(childlogit),
+                                    _ptr(tree_topk_id), _ptr(tree_topk_val), _ptr(ws),
+                                    ws.numel(), _stream())
+    _check(rc, "lm_verify_draft")
+
+
+def next_inputs(L, path, ws, *, N, smax, next_root=None, y=None, tree_topk_id=None,
+                tree_topk_val=None, h_next=None, root_out=None, topk_id_out=None,
+                topk_val_out=None):
+    B = L.shape[0]
+    K = path.shape[1] - 1
+    d = y.shape[2] if y is not None else 1
+    dt = dtype_code(y) if y is not None else BF16
+    rc = load().mds_next_inputs(dt, B, N, K, smax, d, _ptr(L), _ptr(path), _ptr(next_root),
+                                _ptr(y), _ptr(tree_topk_id), _ptr(tree_topk_val), _ptr(h_next),
+                                _ptr(root_out), _ptr(topk_id_out), _ptr(topk_val_out),
+                                _ptr(ws), ws.numel(), _stream())
+    _check(rc, "next_inputs")
 
 
 def verify_accept(mode, eps, delta, parent, depth, tok, argmax, stats, childlogit, L, path,

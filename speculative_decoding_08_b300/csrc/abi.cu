@@ -1,6 +1,7 @@
 // C ABI entry points: host-side argument checks, workspace carving, and
 // dispatch to the kernels.  Every data-path operation runs in a kernel.
 #include <atomic>
+#include <math.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -90,9 +91,20 @@ size_t need_attention(int dtype, int B, int N, int d, int Hq, int Hkv, int dh) {
   }
   return n;
 }
+size_t need_verify_draft(int B, int N, int d, int K) {
+  const size_t R = (size_t)B * N;
+  return kWsScratch + align_up((size_t)(K + 1) * R * d * 2) +
+         align_up(tc_partial_bytes((int)R, false)) + align_up(tc_partial_bytes((int)R * K, true));
+}
 size_t need_verify(int dtype, int B, int N, int V) {
   if (dtype == MDS_BF16) return kWsScratch + align_up(tc_partial_bytes(B * N, false));
   return kWsScratch + align_up((size_t)B * N * V * 4);
+}
+// sampling form: the drawn tokens' (key, id) records after the statistics'
+size_t sample_records_bytes(int B, int N) { return tc_partial_bytes(B * N, false) / 2; }
+size_t need_verify_sample(int dtype, int B, int N, int V) {
+  if (dtype == MDS_BF16) return need_verify(dtype, B, N, V) + align_up(sample_records_bytes(B, N));
+  return need_verify(dtype, B, N, V);
 }
 
 }  // namespace
@@ -130,7 +142,7 @@ size_t mds_workspace_size(int dtype, int B, int d, int V, int K, int N, int Hq, 
   if (!valid_dtype(dtype) || B < 1 || d < 1 || V < 1 || K < 1 || N < 1 || Hq < 1) return 0;
   size_t need = need_heads(dtype, B, d, V, K);
   const size_t a = need_attention(dtype, B, N, d, Hq, Hkv, dh);
-  const size_t v = need_verify(dtype, B, N, V);
+  const size_t v = need_verify_sample(dtype, B, N, V);
   if (a > need) need = a;
   if (v > need) need = v;
   return need;
@@ -169,7 +181,7 @@ int mds_medusa_heads(int dtype, int B, int d, int V, int K, const void* h, const
   if (!aligned16(h) || !aligned16(W) || !aligned16(lm) || !aligned16(U)) return MDS_EINVAL;
   cudaStream_t st = as_stream(stream);
   if (dtype == MDS_BF16) {
-    int rc = gemm_tc_heads(h, B, W, K, d, U, scratch(ws), ws, st);
+    int rc = gemm_tc_heads(h, B, W, K, d, U, false, scratch(ws), ws, st);
     if (rc) return rc;
     return lm_draft_tc(U, B, K, d, lm, V, sl, smax, root, topk_id, topk_val, scratch(ws), ws, st);
   }
@@ -263,7 +275,7 @@ int mds_lm_verify(int dtype, int B, int N, int d, int V, const void* y, const vo
   cudaStream_t st = as_stream(stream);
   if (dtype == MDS_BF16)
     return lm_verify_tc(y, B, N, d, lm, V, tok, parent, argmax, stats, childlogit, scratch(ws),
-                        ws, st);
+                        false, 1.f, 0ull, nullptr, nullptr, nullptr, ws, st);
   float* logits = reinterpret_cast<float*>(scratch(ws));
   EpiArgs el;
   el.kind = EPI_LOGITS;
@@ -274,13 +286,96 @@ int mds_lm_verify(int dtype, int B, int N, int d, int V, const void* y, const vo
   return verify_reduce(logits, B, N, V, tok, parent, argmax, stats, childlogit, ws, st);
 }
 
+int mds_lm_verify_sample(int dtype, int B, int N, int d, int V, const void* y, const void* lm,
+                         const int32_t* tok, const int32_t* parent, const int32_t* P,
+                         float temperature, uint64_t seed, int32_t* argmax, float* stats,
+                         float* childlogit, int32_t* sample_id, void* ws, size_t ws_bytes,
+                         void* stream) {
+  if (!valid_dtype(dtype) || !y || !lm || !tok || !parent || !P || !argmax || !stats ||
+      !childlogit || !sample_id)
+    return MDS_EINVAL;
+  if (B < 1 || N < 1 || V < 2) return MDS_EINVAL;
+  if (!(temperature > 0.f) || !(temperature < INFINITY)) return MDS_EINVAL;
+  if (N > kMaxN || d % 64 != 0 || d <= 0) return MDS_EUNSUPPORTED;
+  if (!ws_ok(ws, ws_bytes, need_verify_sample(dtype, B, N, V))) return MDS_EWORKSPACE;
+  if (!aligned16(y) || !aligned16(lm)) return MDS_EINVAL;
+  cudaStream_t st = as_stream(stream);
+  if (dtype == MDS_BF16) {
+    char* part = scratch(ws);
+    char* part2 = part + align_up(tc_partial_bytes(B * N, false));
+    return lm_verify_tc(y, B, N, d, lm, V, tok, parent, argmax, stats, childlogit, part, true,
+                        temperature, (unsigned long long)seed, P, sample_id, part2, ws, st);
+  }
+  float* logits = reinterpret_cast<float*>(scratch(ws));
+  EpiArgs el;
+  el.kind = EPI_LOGITS;
+  el.out = logits;
+  el.ldo = V;
+  int rc = gemm_simple(dtype, y, B * N, lm, V, d, el, st);
+  if (rc) return rc;
+  rc = verify_reduce(logits, B, N, V, tok, parent, argmax, stats, childlogit, ws, st);
+  if (rc) return rc;
+  return sample_reduce(logits, B, N, V, temperature, (unsigned long long)seed, P, sample_id, st);
+}
+
+size_t mds_verify_draft_workspace_size(int B, int N, int d, int K) {
+  if (B < 1 || N < 1 || d < 1 || K < 1) return 0;
+  return need_verify_draft(B, N, d, K);
+}
+
+int mds_lm_verify_draft(int dtype, int B, int N, int d, int V, int K, const void* y,
+                        const void* W, const void* lm, const int32_t* shortlist, int smax,
+                        const int32_t* tok, const int32_t* parent, int32_t* argmax,
+                        float* stats, float* childlogit, int32_t* tree_topk_id,
+                        float* tree_topk_val, void* ws, size_t ws_bytes, void* stream) {
+  if (!valid_dtype(dtype) || !y || !W || !lm || !shortlist || !tok || !parent || !argmax ||
+      !stats || !childlogit || !tree_topk_id || !tree_topk_val)
+    return MDS_EINVAL;
+  if (B < 1 || N < 1 || V < 2 || K < 1 || smax < 1) return MDS_EINVAL;
+  if (dtype != MDS_BF16) return MDS_EUNSUPPORTED;
+  if (N > kMaxN || K > kMaxK || smax > kMaxS || d % 64 != 0 || d <= 0) return MDS_EUNSUPPORTED;
+  Shortlist sl{};
+  sl.K = K;
+  for (int i = 0; i < K; ++i) {
+    if (shortlist[i] < 1 || shortlist[i] > smax || shortlist[i] > V) return MDS_EINVAL;
+    sl.s[i] = shortlist[i];
+  }
+  if (!ws_ok(ws, ws_bytes, need_verify_draft(B, N, d, K))) return MDS_EWORKSPACE;
+  if (!aligned16(y) || !aligned16(W) || !aligned16(lm)) return MDS_EINVAL;
+  const size_t R = (size_t)B * N;
+  char* U2 = scratch(ws);
+  char* part = U2 + align_up((size_t)(K + 1) * R * d * 2);
+  char* part2 = part + align_up(tc_partial_bytes((int)R, false));
+  return lm_verify_draft_tc(y, B, N, d, W, K, lm, V, sl, smax, tok, parent, argmax, stats,
+                            childlogit, tree_topk_id, tree_topk_val, U2, part, part2, ws,
+                            as_stream(stream));
+}
+
+int mds_next_inputs(int dtype, int B, int N, int K, int smax, int d, const int32_t* L,
+                    const int32_t* path, const int32_t* next_root, const void* y,
+                    const int32_t* tree_topk_id, const float* tree_topk_val, void* h_next,
+                    int32_t* root_out, int32_t* topk_id_out, float* topk_val_out, void* ws,
+                    size_t ws_bytes, void* stream) {
+  if (!valid_dtype(dtype) || !L || !path) return MDS_EINVAL;
+  if (h_next && !y) return MDS_EINVAL;
+  if (root_out && !next_root) return MDS_EINVAL;
+  if (topk_id_out && !tree_topk_id) return MDS_EINVAL;
+  if (topk_val_out && (!tree_topk_val || !topk_id_out)) return MDS_EINVAL;
+  if (B < 1 || N < 1 || K < 1 || smax < 1 || d < 1) return MDS_EINVAL;
+  if (N > kMaxN || K > kMaxK || smax > kMaxS) return MDS_EUNSUPPORTED;
+  if (!ws_ok(ws, ws_bytes, kWsScratch)) return MDS_EWORKSPACE;
+  return next_inputs(dtype, B, N, K, smax, d, L, path, next_root, y, tree_topk_id,
+                     tree_topk_val, h_next, root_out, topk_id_out, topk_val_out, ws,
+                     as_stream(stream));
+}
+
 int mds_verify_accept(int B, int N, int K, int mode, float eps, float delta,
                       const int32_t* parent, const int32_t* depth, const int32_t* tok,
                       const int32_t* argmax, const float* stats, const float* childlogit,
                       uint8_t* ok, int32_t* L, int32_t* path, int32_t* next_root, void* ws,
                       size_t ws_bytes, void* stream) {
   if (!parent || !depth || !tok || !argmax || !L || !path || !next_root) return MDS_EINVAL;
-  if (mode != 0 && mode != 1) return MDS_EINVAL;
+  if (mode != 0 && mode != 1 && mode != 2) return MDS_EINVAL;
   if (mode == 1 && (!stats || !childlogit || !(eps >= 0.f) || !(delta >= 0.f)))
     return MDS_EINVAL;
   if (B < 1 || N < 1 || K < 1) return MDS_EINVAL;

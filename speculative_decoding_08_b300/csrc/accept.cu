@@ -37,7 +37,9 @@ __global__ void __launch_bounds__(32) k_accept(int N, int K, int mode, float log
       if (pa < 0 || pa >= n || dd < 1 || dd > K) {
         bad = true;
         okv = 0;
-      } else if (mode == 0) {
+      } else if (mode != 1) {
+        // greedy (argmax = the rows' argmax) or exact sampling (argmax = the
+        // tokens drawn at the rows): the child carrying its parent's token
         okv = tok[base + n] == argmax[base + pa];
       } else {
         const float lse = stats[(base + pa) * 4 + 1];
@@ -150,7 +152,73 @@ __global__ void __launch_bounds__(128) k_compact(int Hkv, int dh, int Pmax, int 
   }
 }
 
+// Inputs of the next step of the decoding loop, one block per sequence: the
+// accepted node a = path[b, L_b] of this step
+//   h_next[b, :]      = y[b, a, :]             (the next step's hidden state)
+//   root_out[b]       = next_root[b]           (argmax of a's verify logits)
+//   topk_out[b, :, :] = tree_topk[b, a, :, :]  (the heads' shortlists at a,
+//                                               from the fused verify pass)
+// Any output may be null.  "Medusa Heads", "How it works": after acceptance
+// and rollback the loop drafts again from the last accepted position.
+template <typename T>
+__global__ void __launch_bounds__(128) k_next_inputs(int N, int K, int smax, int d,
+                                                     const int32_t* L, const int32_t* path,
+                                                     const int32_t* next_root, const T* y,
+                                                     const int32_t* tree_topk_id,
+                                                     const float* tree_topk_val, T* h_next,
+                                                     int32_t* root_out, int32_t* topk_out,
+                                                     float* topk_val_out, void* ws) {
+  const int b = blockIdx.x;
+  const int Lb = L[b];
+  int a = -1;
+  if (Lb >= 0 && Lb <= K) a = path[(long long)b * (K + 1) + Lb];
+  if (a < 0 || a >= N) {
+    if (threadIdx.x == 0) latch_error(ws, (Lb < 0 || Lb > K) ? MDS_DEV_PATH_LENGTH
+                                                             : MDS_DEV_TREE_INDEX);
+    return;
+  }
+  if (h_next) {
+    const T* src = y + ((long long)b * N + a) * d;
+    T* dst = h_next + (long long)b * d;
+    if ((d * sizeof(T)) % 16 == 0) {
+      const int n16 = d * (int)sizeof(T) / 16;
+      for (int i = threadIdx.x; i < n16; i += blockDim.x)
+        reinterpret_cast<uint4*>(dst)[i] = reinterpret_cast<const uint4*>(src)[i];
+    } else {
+      for (int i = threadIdx.x; i < d; i += blockDim.x) dst[i] = src[i];
+    }
+  }
+  if (root_out && threadIdx.x == 0) root_out[b] = next_root[b];
+  if (tree_topk_id && topk_out) {
+    const long long src = ((long long)b * N + a) * K * smax;
+    for (int i = threadIdx.x; i < K * smax; i += blockDim.x) {
+      topk_out[(long long)b * K * smax + i] = tree_topk_id[src + i];
+      if (tree_topk_val && topk_val_out)
+        topk_val_out[(long long)b * K * smax + i] = tree_topk_val[src + i];
+    }
+  }
+}
+
 }  // namespace
+
+int next_inputs(int dtype, int B, int N, int K, int smax, int d, const int32_t* L,
+                const int32_t* path, const int32_t* next_root, const void* y,
+                const int32_t* tree_topk_id, const float* tree_topk_val, void* h_next,
+                int32_t* root_out, int32_t* topk_out, float* topk_val_out, void* ws,
+                cudaStream_t st) {
+  if (dtype == MDS_F32)
+    k_next_inputs<float><<<B, 128, 0, st>>>(N, K, smax, d, L, path, next_root,
+                                            static_cast<const float*>(y), tree_topk_id,
+                                            tree_topk_val, static_cast<float*>(h_next), root_out,
+                                            topk_out, topk_val_out, ws);
+  else
+    k_next_inputs<__nv_bfloat16><<<B, 128, 0, st>>>(
+        N, K, smax, d, L, path, next_root, static_cast<const __nv_bfloat16*>(y), tree_topk_id,
+        tree_topk_val, static_cast<__nv_bfloat16*>(h_next), root_out, topk_out, topk_val_out,
+        ws);
+  MDS_LAUNCH_CHECK();
+  return MDS_OK;
+}
 
 int accept_path(int B, int N, int K, int mode, float eps, float delta, const int32_t* parent,
                 const int32_t* depth, const int32_t* tok, const int32_t* argmax,

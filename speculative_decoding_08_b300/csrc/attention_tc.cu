@@ -321,13 +321,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // drain: the copies issued last into each stage and into Q have landed
       for (int i = 0; i < S && i < kvt; ++i) {
         const int t = kvt - 1 - i;
-        ptx::mbar_wait(&k_full[t % S], (t / S) & 1, abort_flag, kWaitNs);
+        ptx::mbar_wait(&k_full[t % S], (t / S) & 1, nullptr, kWaitNs);
       }
       for (int i = 0; i < S && i < vt; ++i) {
         const int t = vt - 1 - i;
-        ptx::mbar_wait(&v_full[t % S], (t / S) & 1, abort_flag, kWaitNs);
+        ptx::mbar_wait(&v_full[t % S], (t / S) & 1, nullptr, kWaitNs);
       }
-      if (segc > 0) ptx::mbar_wait(q_full, (segc - 1) & 1, abort_flag, kWaitNs);
+      if (segc > 0) ptx::mbar_wait(q_full, (segc - 1) & 1, nullptr, kWaitNs);
     }
     __syncwarp();   // the warp reaches the final barrier converged
   } else if (warp == 1) {
@@ -424,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (lane == 0) {
       ptx::mma_commit(done);
-      ptx::mbar_wait(done, 0, abort_flag, kWaitNs);
+      ptx::mbar_wait(done, 0, nullptr, kWaitNs);
     }
     __syncwarp();
   } else {

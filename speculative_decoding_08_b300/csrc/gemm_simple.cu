@@ -5,6 +5,7 @@
 // sum_k X[r, k] W[f, k] with W stored (out, in), fp32 accumulation.
 #include "common.cuh"
 #include "internal.h"
+#include "sampling.cuh"
 
 namespace mds {
 namespace {
@@ -245,6 +246,39 @@ int gemm_simple(int dtype, const void* X, int R, const void* W, int F, int Kd,
 int draft_select(const float* logits, int B, int K, int V, Shortlist sl, int smax,
                  int32_t* root, int32_t* topk_id, float* topk_val, cudaStream_t st) {
   k_draft_select<<<B * (K + 1), 256, 0, st>>>(logits, K, V, sl, smax, root, topk_id, topk_val);
+  MDS_LAUNCH_CHECK();
+  return MDS_OK;
+}
+
+// One block per tree row b N + n: the token drawn by the Gumbel-max rule,
+// argmax_v z_v / T - ln(-ln U_v), U_v from Philox4x64-10 with key (seed, 0)
+// and counter (v >> 3, n, P_b, b); ties to the lowest id.
+__global__ void __launch_bounds__(256) k_sample_reduce(const float* __restrict__ logits, int N,
+                                                       int V, float inv_T,
+                                                       unsigned long long seed,
+                                                       const int32_t* P, int32_t* sample_id) {
+  __shared__ Cand red[33];
+  const long long row = blockIdx.x;
+  const int b = (int)(row / N), n = (int)(row - (long long)b * N);
+  const float* z = logits + row * V;
+  Cand c{-INFINITY, -1};
+  for (int g = threadIdx.x; g * 8 < V; g += blockDim.x) {
+    unsigned long long w[4] = {(unsigned long long)g, (unsigned long long)n,
+                               (unsigned long long)(unsigned)P[b], (unsigned long long)b};
+    philox4x64_10(w, seed, 0ull);
+    for (int e = 0; e < 8 && g * 8 + e < V; ++e) {
+      const int v = g * 8 + e;
+      c = better(c, Cand{z[v] * inv_T + gumbel_of(gumbel_bits(w, e)), v});
+    }
+  }
+  c = block_best(c, red);
+  if (threadIdx.x == 0) sample_id[row] = c.id;
+}
+
+int sample_reduce(const float* logits, int B, int N, int V, float temperature,
+                  unsigned long long seed, const int32_t* P, int32_t* sample_id,
+                  cudaStream_t st) {
+  k_sample_reduce<<<B * N, 256, 0, st>>>(logits, N, V, 1.f / temperature, seed, P, sample_id);
   MDS_LAUNCH_CHECK();
   return MDS_OK;
 }

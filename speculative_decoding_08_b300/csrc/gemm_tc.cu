@@ -46,10 +46,12 @@
 // merge kernel combines them.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <stdlib.h>
 
 #include "common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
+#include "sampling.cuh"
 
 namespace mds {
 namespace {
@@ -98,15 +100,36 @@ struct TcArgs {
   long long ldo;
   const __nv_bfloat16* h;
   int d, K;
+  // HEADS output strides (elements): U row b, head i, feature j lives at
+  // b * u_row + i * u_head + j.  Row-major [B, K+1, d]: u_row = (K+1) d,
+  // u_head = d; head-major [K+1, R, d] (the fused verify pass): u_row = d,
+  // u_head = R d.
+  long long u_row, u_head;
+  // VDRAFT (verify rows and head rows in one pass): rows [0, Rv) take the
+  // verify statistics, rows [Rv, R) the running top-8; partial2 holds the
+  // top-8 records.
+  int Rv;
+  void* partial2;
+  // VSAMPLE (verify statistics plus the token drawn at every row, exact
+  // sampling at temperature 1 / inv_T): Philox4x64-10 key (seed, 0),
+  // counter (v >> 3, n, P_b, b) for row b N + n; partial2 holds (best key,
+  // id) records.
+  float inv_T;
+  unsigned long long seed;
   int N, Hq, Hkv, dh, Pmax;
   const int32_t* P;
   __nv_bfloat16* Kc;
   __nv_bfloat16* Vc;
   void* partial;
   void* ws;
+  // Test of the bounded-wait path (MDS_STALL_TEST=1 in the environment): the
+  // producer first waits, with a 1 ms limit, on a barrier that nothing
+  // arrives on, and then gives up the way a real timeout does.
+  int stall_test;
 };
 
-enum { TC_STORE = 0, TC_HEADS = 1, TC_QKV = 2, TC_DRAFT = 3, TC_VERIFY = 4 };
+enum { TC_STORE = 0, TC_HEADS = 1, TC_QKV = 2, TC_DRAFT = 3, TC_VERIFY = 4, TC_VDRAFT = 5,
+       TC_VSAMPLE = 6 };
 
 struct Range {
   int f_begin, f_end, n_chunks;
@@ -158,7 +181,7 @@ __device__ __forceinline__ void epi_heads(const TcArgs& a, int b, int f0, int nv
                                           const float (&v)[32]) {
   __nv_bfloat16* U = static_cast<__nv_bfloat16*>(a.out);
   const __nv_bfloat16* hb = a.h + (long long)b * a.d;
-  const long long ubase = (long long)b * (a.K + 1) * a.d;
+  const long long ubase = (long long)b * a.u_row;
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
     const int f = f0 + 16 * half;
@@ -175,13 +198,13 @@ __device__ __forceinline__ void epi_heads(const TcArgs& a, int b, int f0, int nv
           u[2 * e] = hf.x + silu(v[16 * half + q * 8 + 2 * e]);
           u[2 * e + 1] = hf.y + silu(v[16 * half + q * 8 + 2 * e + 1]);
         }
-        *reinterpret_cast<uint4*>(U + ubase + (long long)(1 + i) * a.d + j0 + q * 8) = pack8(u);
+        *reinterpret_cast<uint4*>(U + ubase + (long long)(1 + i) * a.u_head + j0 + q * 8) = pack8(u);
         if (i == 0) *reinterpret_cast<uint4*>(U + ubase + j0 + q * 8) = hraw;
       }
     } else {
       for (int j = 0; j < 16 && 16 * half + j < nv; ++j) {
         const __nv_bfloat16 hraw = hb[j0 + j];
-        U[ubase + (long long)(1 + i) * a.d + j0 + j] =
+        U[ubase + (long long)(1 + i) * a.u_head + j0 + j] =
             __float2bfloat16_rn(__bfloat162float(hraw) + silu(v[16 * half + j]));
         if (i == 0) U[ubase + j0 + j] = hraw;
       }
@@ -265,6 +288,40 @@ struct TopList {
   }
 };
 
+// Running Gumbel-max draw of one row: the best l_v / T - ln(-ln U_v) and its
+// id (ties to the lowest id), U_v from Philox word (v >> 1) & 3 of counter
+// (v >> 3, c1, c2, c3): the top 24 bits for even v, bits 16..39 for odd v,
+// m, and U = (m + 0.5) / 2^24, with -ln U = -log1p(-(1 - U)) and
+// 1 - U = (2^24 - m - 0.5) / 2^24 exact in fp32.
+struct GumbelMax {
+  float k;
+  int id;
+  __device__ __forceinline__ void init() {
+    k = -INFINITY;
+    id = 0x7fffffff;
+  }
+  // one 32-column block starting at f0 (a multiple of 8)
+  __device__ __forceinline__ void push32(const float (&z)[32], int f0, int nv,
+                                         unsigned long long c1, unsigned long long c2,
+                                         unsigned long long c3, float inv_T,
+                                         unsigned long long seed) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      unsigned long long c[4] = {(unsigned long long)((f0 >> 3) + q), c1, c2, c3};
+      philox4x64_10(c, seed, 0ull);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int j = q * 8 + e;
+        const float key = z[j] * inv_T + gumbel_of(gumbel_bits(c, e));
+        if (j < nv && key > k) {
+          k = key;
+          id = f0 + j;
+        }
+      }
+    }
+  }
+};
+
 struct SoftStat {
   float m, S, Q;
   int am;
@@ -338,8 +395,8 @@ __device__ __forceinline__ void colpar_block(const TcArgs& a, float* tile,
         const int b = row_base + rr;
         const int i = f / a.d, j = f - i * a.d;
         const __nv_bfloat16 hraw = a.h[(long long)b * a.d + j];
-        __nv_bfloat16* U = static_cast<__nv_bfloat16*>(a.out) + (long long)b * (a.K + 1) * a.d;
-        U[(long long)(1 + i) * a.d + j] = __float2bfloat16_rn(__bfloat162float(hraw) + silu_fast(x));
+        __nv_bfloat16* U = static_cast<__nv_bfloat16*>(a.out) + (long long)b * a.u_row;
+        U[(long long)(1 + i) * a.u_head + j] = __float2bfloat16_rn(__bfloat162float(hraw) + silu_fast(x));
         if (i == 0) U[j] = hraw;
       }
     }
@@ -364,35 +421,48 @@ __device__ __forceinline__ void store_kpart(const TcArgs& a, int kspl, int row, 
   }
 }
 
+// Running top-8 of one row over a 32-column block.  The block is skipped when
+// its maximum cannot enter the list (after the first blocks nearly always):
+// one tree maximum instead of 32 checks.
+__device__ __forceinline__ void top8_block(TopList& tl, const float (&v)[32], int f0, int nv) {
+  float t[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    t[j] = fmaxf(j < nv ? v[j] : -INFINITY, j + 16 < nv ? v[j + 16] : -INFINITY);
+#pragma unroll
+  for (int w = 8; w; w >>= 1)
+#pragma unroll
+    for (int j = 0; j < w; ++j) t[j] = fmaxf(t[j], t[j + w]);
+  if (t[0] > tl.v[kMaxS - 1]) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < nv) tl.push(v[j], f0 + j);
+  }
+}
+
 // One 32-column block of a row's accumulators (raw fp32 bits in r).
 template <int KIND>
 __device__ __forceinline__ void epi_block(const TcArgs& a, int row, int g, int f0, int nv,
                                           const uint32_t (&r)[32], TopList (&tl)[2],
-                                          SoftStat (&ss)[2]) {
+                                          SoftStat (&ss)[2], GumbelMax (&gm)[2]) {
   float v[32];
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
   if constexpr (KIND == TC_STORE) epi_store(a, row, f0, nv, v);
   if constexpr (KIND == TC_HEADS) epi_heads(a, row, f0, nv, v);
   if constexpr (KIND == TC_QKV) epi_qkv(a, row, f0, nv, v);
-  if constexpr (KIND == TC_DRAFT) {
-    // skip the block when its maximum cannot enter the row's top-8 (after the
-    // first blocks nearly always): one tree maximum instead of 32 checks
-    float t[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j)
-      t[j] = fmaxf(j < nv ? v[j] : -INFINITY, j + 16 < nv ? v[j + 16] : -INFINITY);
-#pragma unroll
-    for (int w = 8; w; w >>= 1)
-#pragma unroll
-      for (int j = 0; j < w; ++j) t[j] = fmaxf(t[j], t[j + w]);
-    if (t[0] > tl[g].v[kMaxS - 1]) {
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (j < nv) tl[g].push(v[j], f0 + j);
-    }
-  }
+  if constexpr (KIND == TC_DRAFT) top8_block(tl[g], v, f0, nv);
   if constexpr (KIND == TC_VERIFY) ss[g].push32(v, f0, nv);
+  if constexpr (KIND == TC_VSAMPLE) {
+    ss[g].push32(v, f0, nv);
+    const int b = row / a.N, n = row - b * a.N;
+    gm[g].push32(v, f0, nv, (unsigned long long)n, (unsigned long long)(unsigned)a.P[b],
+                 (unsigned long long)b, a.inv_T, a.seed);
+  }
+  if constexpr (KIND == TC_VDRAFT) {
+    if (row < a.Rv) ss[g].push32(v, f0, nv);
+    else top8_block(tl[g], v, f0, nv);
+  }
 }
 
 // ------------------------------------------------------------------ kernel
@@ -415,6 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* done = bars + 2 * kMaxStages + 4;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kMaxStages + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint64_t* never = bars + 2 * kMaxStages + 6;     // no thread arrives on it
   float* epi_tile = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + kBarBytes);
   constexpr bool kColPar = KIND == TC_HEADS;
 
@@ -441,6 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&tempty[s], 4);
     }
     ptx::mbar_init(done, 1);
+    ptx::mbar_init(never, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
     ptx::tma_prefetch_desc(&tmX);
@@ -470,6 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool issued[kMaxStages];
       for (int s = 0; s < kMaxStages; ++s) issued[s] = false, issued_phase[s] = 0;
       bool ok = true;
+      if (a.stall_test && !ptx::mbar_wait(never, 0, abort_flag, 1000000ull)) ok = false;
       // Chunk geometry: the W map whose box height is this chunk's rows
       // (rounded to 16), the first feature, and the stage's byte count.
       struct Chunk {
@@ -493,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // W tiles of the first S stages, before the wait (the ring is empty,
       // so no empty-slot wait is needed); their X tiles follow the wait.
       int pre = 0;
-      for (int g0 = rs; g0 < a.n_rgroups && pre < S; g0 += a.n_rs) {
+      for (int g0 = rs; ok && g0 < a.n_rgroups && pre < S; g0 += a.n_rs) {
         for (int ch = 0; ch < rg.n_chunks && pre < S; ++ch) {
           const Chunk c = chunk(g0, ch);
           for (int kq = 0; kq < nks && pre < S; ++kq, ++pre) {
@@ -538,7 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // drain: every issued copy has landed before the CTA can exit
       for (int s = 0; s < S; ++s)
-        if (issued[s]) ptx::mbar_wait(&full[s], issued_phase[s], abort_flag, kWaitLimitNs);
+        if (issued[s]) ptx::mbar_wait(&full[s], issued_phase[s], nullptr, kWaitLimitNs);
     }
     __syncwarp();   // the warp reaches the final barrier converged
   } else if (warp == 1) {
@@ -601,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // every MMA issued by this thread is complete before TMEM is freed
       ptx::mma_commit(done);
-      ptx::mbar_wait(done, 0, abort_flag, kWaitLimitNs);
+      ptx::mbar_wait(done, 0, nullptr, kWaitLimitNs);
     }
     __syncwarp();
   } else {
@@ -617,10 +690,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int Geff = min(a.G, (rem + 127) / 128);
       TopList tl[2];
       SoftStat ss[2];
+      GumbelMax gm[2];
       tl[0].init();
       tl[1].init();
       ss[0].init();
       ss[1].init();
+      gm[0].init();
+      gm[1].init();
       for (int ch = 0; ch < rg.n_chunks; ++ch, ++item) {
         const int fc = rg.f_begin + ch * a.NC;
         const int len = min(a.NC, rg.f_end - fc);
@@ -656,7 +732,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               colpar_block<KIND>(a, tile, row_base, nlive, fc + cb * 32,
                                  min(32, len - cb * 32), rb[0]);
             } else if (live) {
-              epi_block<KIND>(a, row, g, fc + cb * 32, min(32, len - cb * 32), rb[0], tl, ss);
+              epi_block<KIND>(a, row, g, fc + cb * 32, min(32, len - cb * 32), rb[0], tl, ss, gm);
             }
             if (more1) {
               ptx::tmem_wait32(rb[1]);
@@ -670,7 +746,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    min(32, len - (cb + 1) * 32), rb[1]);
               } else if (live) {
                 epi_block<KIND>(a, row, g, fc + (cb + 1) * 32, min(32, len - (cb + 1) * 32), rb[1],
-                                tl, ss);
+                                tl, ss, gm);
               }
               if (more2) ptx::tmem_wait32(rb[0]);
             }
@@ -681,18 +757,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) ptx::mbar_arrive(&tempty[acc]);
       }
       if (!ok) break;
-      if (rg.n_chunks > 0 && (KIND == TC_DRAFT || KIND == TC_VERIFY)) {
+      if (rg.n_chunks > 0 &&
+          (KIND == TC_DRAFT || KIND == TC_VERIFY || KIND == TC_VDRAFT || KIND == TC_VSAMPLE)) {
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
           if (g >= Geff) break;
           const int row = row0 + g * 128 + trow;
           if (row >= a.R) continue;
-          const long long rec = (long long)fr * a.R + row;
-          if (KIND == TC_VERIFY) {
+          // VDRAFT: verify rows [0, Rv) keep statistics records (Rv per
+          // range), head rows [Rv, R) top-8 records (R - Rv per range)
+          const bool stat = KIND == TC_VERIFY || KIND == TC_VSAMPLE ||
+                            (KIND == TC_VDRAFT && row < a.Rv);
+          if (stat) {
+            const int nr = KIND == TC_VDRAFT ? a.Rv : a.R;
             float4 o = make_float4(ss[g].m, ss[g].S, ss[g].Q, __int_as_float(ss[g].am));
-            static_cast<float4*>(a.partial)[rec] = o;
+            static_cast<float4*>(a.partial)[(long long)fr * nr + row] = o;
+            if (KIND == TC_VSAMPLE)
+              static_cast<float2*>(a.partial2)[(long long)fr * nr + row] =
+                  make_float2(gm[g].k, __int_as_float(gm[g].id));
           } else {
-            float2* p = static_cast<float2*>(a.partial) + rec * kMaxS;
+            const int nr = KIND == TC_VDRAFT ? a.R - a.Rv : a.R;
+            const int rr = KIND == TC_VDRAFT ? row - a.Rv : row;
+            float2* p = static_cast<float2*>(KIND == TC_VDRAFT ? a.partial2 : a.partial) +
+                        ((long long)fr * nr + rr) * kMaxS;
 #pragma unroll
             for (int j = 0; j < kMaxS; ++j) p[j] = make_float2(tl[g].v[j], __int_as_float(tl[g].id[j]));
           }
@@ -756,13 +843,38 @@ __global__ void __launch_bounds__(256) k_split_reduce(TcArgs a) {
 // ----------------------------------------------------------- merge kernels
 // One warp per row: combine the row's (m, S, Q, argmax) records, one per
 // feature range.
+// With spart (exact sampling), also the row's drawn token: the largest
+// Gumbel key over the ranges' (key, id) records, ties to the lowest id.
 __global__ void __launch_bounds__(256) k_verify_merge(const float4* __restrict__ part, int n_rec,
-                                                      int R, int32_t* argmax, float* stats) {
+                                                      int R, int32_t* argmax, float* stats,
+                                                      const float2* __restrict__ spart,
+                                                      int32_t* sample_out) {
   grid_dep_launch();
   grid_dep_wait();
   const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= R) return;
+  if (spart) {
+    float bk = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int c = lane; c < n_rec; c += 32) {
+      const float2 p = spart[(long long)c * R + row];
+      const int pid = __float_as_int(p.y);
+      if (p.x > bk || (p.x == bk && pid < bi)) {
+        bk = p.x;
+        bi = pid;
+      }
+    }
+    for (int o = 16; o; o >>= 1) {
+      const float k2 = __shfl_xor_sync(0xffffffffu, bk, o);
+      const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (k2 > bk || (k2 == bk && i2 < bi)) {
+        bk = k2;
+        bi = i2;
+      }
+    }
+    if (lane == 0) sample_out[row] = bi;
+  }
   float m = -INFINITY, S = 0.f, Q = 0.f;
   int am = 0x7fffffff;
   for (int c = lane; c < n_rec; c += 32) {
@@ -857,17 +969,22 @@ __device__ __forceinline__ void warp_extract(const float (&v)[kMaxS], const int 
   }
 }
 
+//   hm_rows = 0: rows are (b, i) with i = 0 the base head (root) and
+//   i = 1..K the heads, R = B (K + 1).  hm_rows > 0 (fused verify pass): rows
+//   are head-major, row = (i - 1) hm_rows + b for heads i = 1..K only, and b
+//   indexes the hm_rows tree rows.
 __global__ void __launch_bounds__(256) k_draft_merge(const float2* __restrict__ part, int n_rec,
                                                      int R, int K, Shortlist sl, int smax,
-                                                     int32_t* root, int32_t* topk_id,
-                                                     float* topk_val) {
+                                                     int hm_rows, int32_t* root,
+                                                     int32_t* topk_id, float* topk_val) {
   grid_dep_launch();
   grid_dep_wait();
   __shared__ float s_v[8][kMaxS];
   __shared__ int s_id[8][kMaxS];
   const int row = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = row / (K + 1), i = row - b * (K + 1);
+  const int b = hm_rows > 0 ? row % hm_rows : row / (K + 1);
+  const int i = hm_rows > 0 ? row / hm_rows + 1 : row - b * (K + 1);
   const int s = i == 0 ? 1 : sl.s[i - 1];
   float v[kMaxS];
   int id[kMaxS];
@@ -984,6 +1101,8 @@ int init_host() {
   if (!rc) rc = set_smem_attr<TC_QKV>();
   if (!rc) rc = set_smem_attr<TC_DRAFT>();
   if (!rc) rc = set_smem_attr<TC_VERIFY>();
+  if (!rc) rc = set_smem_attr<TC_VDRAFT>();
+  if (!rc) rc = set_smem_attr<TC_VSAMPLE>();
   if (rc) return rc;
   if (!g_num_sms) {
     int dev = 0;
@@ -1025,6 +1144,10 @@ int last_chunk_rows(int units, int NC) {
 int launch_tc(TcArgs& a, const void* X, const void* W, bool dependent, cudaStream_t st) {
   int rc = init_host();
   if (rc) return rc;
+  {
+    const char* v = getenv("MDS_STALL_TEST");   // read at every launch (a test switch)
+    a.stall_test = (v && v[0] == '1') ? 1 : 0;
+  }
   if (a.R <= 0 || a.F <= 0) return MDS_OK;
   if (a.Kd % 64 != 0) return MDS_EUNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(X) | reinterpret_cast<uintptr_t>(W)) & 15) return MDS_EINVAL;
@@ -1057,12 +1180,16 @@ int launch_tc(TcArgs& a, const void* X, const void* W, bool dependent, cudaStrea
       a.n_cta = a.n_fr * a.ks;
     }
   }
-  if (a.G == 1 || a.kind == TC_VERIFY || (a.n_rs > 1 && a.kind != TC_DRAFT)) {
+  if (a.G == 1 || a.kind == TC_VERIFY || a.kind == TC_VSAMPLE ||
+      (a.n_rs > 1 && a.kind != TC_DRAFT)) {
     a.NC = 256;
     a.nacc = a.G == 1 ? 2 : 1;
   } else {
-    // the draft epilogue (a running top-8 per row) is heavy: it keeps two
-    // accumulators so that it overlaps the next chunk's MMAs
+    // 129-256 rows in one row group (narrow feature ranges), and the draft
+    // pass above 128 rows: N = 128 with two accumulators, so that the
+    // epilogue of one chunk overlaps the MMAs of the next.  Measured on the
+    // batch-64 draft pass (320 rows): 698 us this way, 786 us with one
+    // 2 x 256-column accumulator (its top-8 epilogue then stalls the MMAs).
     a.NC = 128;
     a.nacc = 2;
   }
@@ -1122,6 +1249,8 @@ int launch_tc(TcArgs& a, const void* X, const void* W, bool dependent, cudaStrea
     case TC_HEADS: kern = k_gemm_tc<TC_HEADS>; break;
     case TC_QKV: kern = k_gemm_tc<TC_QKV>; break;
     case TC_DRAFT: kern = k_gemm_tc<TC_DRAFT>; break;
+    case TC_VDRAFT: kern = k_gemm_tc<TC_VDRAFT>; break;
+    case TC_VSAMPLE: kern = k_gemm_tc<TC_VSAMPLE>; break;
     default: kern = k_gemm_tc<TC_VERIFY>; break;
   }
   MDS_LAUNCH_TRY(launch_kernel(kern, dim3(a.n_cta), dim3(kThreads), smem, st, dependent, mx,
@@ -1142,8 +1271,8 @@ int launch_tc(TcArgs& a, const void* X, const void* W, bool dependent, cudaStrea
 
 }  // namespace
 
-int gemm_tc_heads(const void* h, int B, const void* W, int K, int d, void* U, void* kpart,
-                  void* ws, cudaStream_t st) {
+int gemm_tc_heads(const void* h, int B, const void* W, int K, int d, void* U, bool head_major,
+                  void* kpart, void* ws, cudaStream_t st) {
   TcArgs a{};
   a.kpart = static_cast<float*>(kpart);
   a.R = B;
@@ -1154,8 +1283,10 @@ int gemm_tc_heads(const void* h, int B, const void* W, int K, int d, void* U, vo
   a.h = static_cast<const __nv_bfloat16*>(h);
   a.d = d;
   a.K = K;
+  a.u_row = head_major ? d : (long long)(K + 1) * d;
+  a.u_head = head_major ? (long long)B * d : d;
   a.ws = ws;
-  return launch_tc(a, h, W, false, st);   // first kernel of the heads call
+  return launch_tc(a, h, W, false, st);   // first kernel of its call
 }
 
 int gemm_tc_store(const void* X, int R, const void* W, int F, int Kd, void* out, long long ldo,
@@ -1220,14 +1351,49 @@ int lm_draft_tc(const void* U, int B, int K, int d, const void* lm, int V, Short
   int rc = launch_tc(a, U, lm, true, st);   // follows the heads GEMM
   if (rc) return rc;
   MDS_LAUNCH_TRY(launch_kernel(k_draft_merge, dim3(a.R), dim3(256), 0, st, true,
-                               static_cast<const float2*>(partial), a.n_fr, a.R, K, sl, smax,
+                               static_cast<const float2*>(partial), a.n_fr, a.R, K, sl, smax, 0,
                                root, topk_id, topk_val));
+  return MDS_OK;
+}
+
+int lm_verify_draft_tc(const void* y, int B, int N, int d, const void* W, int K, const void* lm,
+                       int V, Shortlist sl, int smax, const int32_t* tok, const int32_t* parent,
+                       int32_t* argmax, float* stats, float* childlogit, int32_t* tree_topk_id,
+                       float* tree_topk_val, void* U2, void* partial, void* partial2, void* ws,
+                       cudaStream_t st) {
+  const int Rv = B * N;
+  // the K heads on every tree row, head-major: U2 = [y ; y + SiLU(W_1 y) ; ...]
+  int rc = gemm_tc_heads(y, Rv, W, K, d, U2, true, nullptr, ws, st);
+  if (rc) return rc;
+  TcArgs a{};
+  a.R = (K + 1) * Rv;
+  a.Rv = Rv;
+  a.F = V;
+  a.Kd = d;
+  a.kind = TC_VDRAFT;
+  a.partial = partial;
+  a.partial2 = partial2;
+  a.ws = ws;
+  rc = launch_tc(a, U2, lm, true, st);       // follows the heads GEMM
+  if (rc) return rc;
+  MDS_LAUNCH_TRY(launch_kernel(k_verify_merge, dim3((Rv + 7) / 8), dim3(256), 0, st, true,
+                               static_cast<const float4*>(partial), a.n_fr, Rv, argmax, stats,
+                               static_cast<const float2*>(nullptr), static_cast<int32_t*>(nullptr)));
+  MDS_LAUNCH_TRY(launch_kernel(k_draft_merge, dim3(K * Rv), dim3(256), 0, st, true,
+                               static_cast<const float2*>(partial2), a.n_fr, K * Rv, K, sl, smax,
+                               Rv, static_cast<int32_t*>(nullptr), tree_topk_id, tree_topk_val));
+  MDS_LAUNCH_TRY(launch_kernel(k_child_dot, dim3(B, (N + 7) / 8), dim3(256), 0, st, true,
+                               static_cast<const __nv_bfloat16*>(y),
+                               static_cast<const __nv_bfloat16*>(lm), N, d, V, tok, parent,
+                               childlogit, ws));
   return MDS_OK;
 }
 
 int lm_verify_tc(const void* y, int B, int N, int d, const void* lm, int V, const int32_t* tok,
                  const int32_t* parent, int32_t* argmax, float* stats, float* childlogit,
-                 void* partial, void* ws, cudaStream_t st) {
+                 void* partial, bool sample, float temperature, unsigned long long seed,
+                 const int32_t* P, int32_t* sample_id, void* partial2, void* ws,
+                 cudaStream_t st) {
   TcArgs a{};
   a.R = B * N;
   a.F = V;
@@ -1235,11 +1401,20 @@ int lm_verify_tc(const void* y, int B, int N, int d, const void* lm, int V, cons
   a.kind = TC_VERIFY;
   a.partial = partial;
   a.ws = ws;
+  if (sample) {
+    a.kind = TC_VSAMPLE;
+    a.partial2 = partial2;
+    a.inv_T = 1.f / temperature;
+    a.seed = seed;
+    a.N = N;
+    a.P = P;
+  }
   int rc = launch_tc(a, y, lm, false, st);   // first kernel of the verify call
   if (rc) return rc;
   MDS_LAUNCH_TRY(launch_kernel(k_verify_merge, dim3((a.R + 7) / 8), dim3(256), 0, st, true,
                                static_cast<const float4*>(partial), a.n_fr, a.R, argmax,
-                               stats));
+                               stats, static_cast<const float2*>(sample ? partial2 : nullptr),
+                               sample_id));
   MDS_LAUNCH_TRY(launch_kernel(k_child_dot, dim3(B, (N + 7) / 8), dim3(256), 0, st, true,
                                static_cast<const __nv_bfloat16*>(y),
                                static_cast<const __nv_bfloat16*>(lm), N, d, V, tok, parent,

@@ -12,10 +12,10 @@
 //
 // The array is a static __device__ symbol, so every GPU that loads this
 // library holds kNoAllocBytes of it until the process exits.  Host code
-// cannot use the symbol's name as a device address: the address is looked
-// up with cudaGetSymbolAddress once per device, with that device current,
-// on the first call made on it.
-#include <mutex>
+// cannot use the symbol's name as a device address: every call looks the
+// address up with cudaGetSymbolAddress on the current device (the first call
+// on a device also loads the module there).  The address is not cached, so a
+// device reset or a new context on the same ordinal is looked up afresh.
 
 #include "common.cuh"
 #include "internal.h"
@@ -29,28 +29,16 @@ namespace {
 constexpr int kNoAllocMaxRows = 64;
 constexpr size_t kNoAllocPartialBytes = (size_t)kNoAllocMaxRows * 256 * kMaxS * 8;
 constexpr size_t kNoAllocBytes = kWsScratch + kNoAllocPartialBytes;
-constexpr int kNoAllocMaxDevices = 64;
 
 // Layout matches a caller workspace: status word at offset 0, candidate
 // lists from kWsScratch on.
 static __device__ __align__(256) unsigned char g_heads_scratch[kNoAllocBytes];
 
-std::mutex g_scratch_mu;
-void* g_scratch_addr[kNoAllocMaxDevices] = {};
-
-// Device address of g_heads_scratch on the current device (looked up once
-// per device, under a lock).
+// Device address of g_heads_scratch in the current device's context.
 int scratch_address(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return MDS_ECUDA;
-  if (dev < 0 || dev >= kNoAllocMaxDevices) return MDS_EUNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_heads_scratch) != cudaSuccess || !p) return MDS_ECUDA;
-    g_scratch_addr[dev] = p;
-  }
-  *out = g_scratch_addr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_heads_scratch) != cudaSuccess || !p) return MDS_ECUDA;
+  *out = p;
   return MDS_OK;
 }
 
@@ -86,7 +74,7 @@ extern "C" int mds_medusa_heads_noalloc(int B, int d, int V, int K, const void* 
   // The array keeps the previous call's contents; only the status word must
   // start at zero (every candidate list is written before it is read).
   MDS_CUDA_TRY(cudaMemsetAsync(scratch, 0, 256, st));
-  rc = gemm_tc_heads(h, B, W, K, d, U, nullptr, scratch, st);   // no K split here
+  rc = gemm_tc_heads(h, B, W, K, d, U, false, nullptr, scratch, st);   // no K split here
   if (rc) return rc;
   rc = lm_draft_tc(U, B, K, d, lm, V, sl, smax, root, topk_id, topk_val,
                    static_cast<char*>(scratch) + kWsScratch, scratch, st);

@@ -109,6 +109,12 @@ int accept_path(int B, int N, int K, int mode, float eps, float delta, const int
                 const float* stats, const float* childlogit, uint8_t* ok, int32_t* L,
                 int32_t* path, int32_t* next_root, void* ws, cudaStream_t st);
 
+int next_inputs(int dtype, int B, int N, int K, int smax, int d, const int32_t* L,
+                const int32_t* path, const int32_t* next_root, const void* y,
+                const int32_t* tree_topk_id, const float* tree_topk_val, void* h_next,
+                int32_t* root_out, int32_t* topk_out, float* topk_val_out, void* ws,
+                cudaStream_t st);
+
 int compact(int dtype, int B, int Hkv, int dh, int Pmax, int K, const int32_t* L,
             const int32_t* path, void* Kc, void* Vc, int32_t* P, void* ws, cudaStream_t st);
 
@@ -125,8 +131,9 @@ size_t tc_partial_bytes(int R, bool draft);
 // fp32 partial sums of a K-split pass over R rows, F features, Kd inputs
 // (0 when the pass is not split); kpart arguments below may be null (no split).
 size_t tc_kpart_bytes(int R, int F, int Kd);
-int gemm_tc_heads(const void* h, int B, const void* W, int K, int d, void* U, void* kpart,
-                  void* ws, cudaStream_t st);
+// head_major = false: U [B, K+1, d]; true: U [K+1, B, d] (block 0 = h).
+int gemm_tc_heads(const void* h, int B, const void* W, int K, int d, void* U, bool head_major,
+                  void* kpart, void* ws, cudaStream_t st);
 int gemm_tc_store(const void* X, int R, const void* W, int F, int Kd, void* out, long long ldo,
                   void* kpart, void* ws, cudaStream_t st);
 int gemm_tc_qkv(const void* x, int B, int N, int d, const void* wqkv, int Hq, int Hkv, int dh,
@@ -135,8 +142,27 @@ int gemm_tc_qkv(const void* x, int B, int N, int d, const void* wqkv, int Hq, in
 int lm_draft_tc(const void* U, int B, int K, int d, const void* lm, int V, Shortlist sl, int smax,
                 int32_t* root, int32_t* topk_id, float* topk_val, void* partial, void* ws,
                 cudaStream_t st);
+// Fused verify pass: the K heads on all B N tree rows (into U2 [K+1, B N, d])
+// and one LM-projection stream over the verify rows and the head rows:
+// verify statistics as lm_verify_tc plus, for every tree row, each head's
+// top s_i (tree_topk [B, N, K, smax]).  partial: B N float4 records per
+// feature range; partial2: K B N top-8 records per feature range.
+int lm_verify_draft_tc(const void* y, int B, int N, int d, const void* W, int K, const void* lm,
+                       int V, Shortlist sl, int smax, const int32_t* tok, const int32_t* parent,
+                       int32_t* argmax, float* stats, float* childlogit, int32_t* tree_topk_id,
+                       float* tree_topk_val, void* U2, void* partial, void* partial2, void* ws,
+                       cudaStream_t st);
+// sample: also draw a token at every row (exact sampling at the given
+// temperature, Philox4x64-10 key (seed, 0), counter (v >> 3, n, P_b, b));
+// partial2 then holds kMaxCta float2 records per row, sample_id [B, N].
 int lm_verify_tc(const void* y, int B, int N, int d, const void* lm, int V, const int32_t* tok,
                  const int32_t* parent, int32_t* argmax, float* stats, float* childlogit,
-                 void* partial, void* ws, cudaStream_t st);
+                 void* partial, bool sample, float temperature, unsigned long long seed,
+                 const int32_t* P, int32_t* sample_id, void* partial2, void* ws,
+                 cudaStream_t st);
+// fp32 path of the draw, over materialised logits [B N, V].
+int sample_reduce(const float* logits, int B, int N, int V, float temperature,
+                  unsigned long long seed, const int32_t* P, int32_t* sample_id,
+                  cudaStream_t st);
 
 }  // namespace mds

@@ -57,14 +57,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Gives up after about limit_ns (counted in SM clock cycles at <= 2 GHz, so
 // at lower clocks the limit only grows) or when *abort becomes non-zero, and
 // returns false then.  The clock and the abort flag are read once every 256
-// unsuccessful polls, so the common case is a bare try_wait loop.
+// unsuccessful polls, so the common case is a bare try_wait loop.  With
+// abort == nullptr only the time limit ends the wait: the drains at the end
+// of a kernel use that form, so that a CTA whose pipeline gave up still
+// waits (boundedly) for the copies and MMAs it has issued before it frees
+// its tensor memory and exits.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           volatile int* abort, uint64_t limit_ns) {
   long long c0 = 0;
   for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 255u) {
-      if (*abort) return false;
+      if (abort && *abort) return false;
       const long long now = clock64();
       if (c0 == 0) c0 = now;
       else if ((unsigned long long)(now - c0) > 2ull * limit_ns) return false;

@@ -45,7 +45,19 @@ __global__ void __launch_bounds__(128) k_build_tree(Shortlist sl, int max_rank_s
     s_count = cnt;
   }
   block_sync();
-  if (s_count != N) return;   // host counted N the same way; never differs
+  if (s_count != N) {
+    // The host counts N with the same enumeration, so this does not happen;
+    // if it did, the tree is written as invalid (every parent -1, empty mask
+    // rows) rather than left unwritten, and the acceptance kernel, which
+    // checks every non-root parent, latches MDS_DEV_TREE_INDEX.
+    for (int i = threadIdx.x; i < N; i += blockDim.x) {
+      parent[i] = -1;
+      depth[i] = 0;
+      rank[i] = 0;
+      for (int w = 0; w < words; ++w) mask[(long long)i * words + w] = 0ull;
+    }
+    return;
+  }
   for (int i = threadIdx.x; i < N; i += blockDim.x) {
     parent[i] = s_parent[i];
     depth[i] = s_depth[i];

@@ -15,9 +15,10 @@ from typing import Dict, Optional, Sequence
 
 import torch
 
-from . import (BF16, F32, GREEDY, TYPICAL, build_tree_mask, compact_kv, dtype_code, lm_verify,
-               medusa_heads, new_workspace, tree_attention, tree_size, verify_accept,
-               workspace_size)
+from . import (BF16, F32, GREEDY, SAMPLE, TYPICAL, build_tree_mask, compact_kv, dtype_code,
+               lm_verify, lm_verify_draft, lm_verify_sample, medusa_heads, new_workspace,
+               next_inputs, tree_attention, tree_size, verify_accept,
+               verify_draft_workspace_size, workspace_size)
 
 
 class MedusaStep:
@@ -60,8 +61,17 @@ class MedusaStep:
         self.L = torch.empty(B, dtype=i32, device=dev)
         self.path = torch.empty((B, K + 1), dtype=i32, device=dev)
         self.next_root = torch.empty(B, dtype=i32, device=dev)
+        self.sample_id = torch.empty((B, N), dtype=i32, device=dev)
         nbytes = workspace_size(dtype_code(lm), B, self.d, self.V, K, N, Hq, Hkv, self.dh,
                                 self.smax)
+        # the fused verify pass (bf16): the next step's shortlists at every
+        # tree row; its workspace need is added to the step's
+        self.fused_ok = self.dtype == torch.bfloat16
+        if self.fused_ok:
+            self.tree_topk_id = torch.empty((B, N, K, self.smax), dtype=i32, device=dev)
+            self.tree_topk_val = torch.empty((B, N, K, self.smax), dtype=torch.float32,
+                                             device=dev)
+            nbytes = max(nbytes, verify_draft_workspace_size(B, N, self.d, K))
         self.ws = new_workspace(nbytes, dev)
 
     def capture(self, h: torch.Tensor, mode: int = TYPICAL, eps: float = 0.09,
@@ -112,18 +122,113 @@ class MedusaStep:
         self._graph.replay()
 
     def run(self, h: torch.Tensor, mode: int = TYPICAL, eps: float = 0.09,
-            delta: float = 0.3, commit: bool = True) -> None:
-        """Enqueue one step on the current stream (asynchronous)."""
+            delta: float = 0.3, commit: bool = True, temperature: float = 1.0,
+            seed: int = 0) -> None:
+        """Enqueue one step on the current stream (asynchronous).  mode GREEDY,
+        TYPICAL or SAMPLE (exact sampling at ``temperature`` with key
+        ``seed``)."""
         medusa_heads(h, self.W, self.lm, self.shortlist, self.smax, self.U, self.root,
                      self.topk_id, self.topk_val, self.ws)
         tree_attention(self.P, self.tok, self.mask, self.emb, self.wqkv, self.wo, self.Kc,
                        self.Vc, self.y, self.ws, Hq=self.Hq, Hkv=self.Hkv, K=self.K,
                        smax=self.smax, root=self.root, topk_id=self.topk_id, depth=self.depth,
                        rank=self.rank)
-        lm_verify(self.y, self.lm, self.tok, self.parent, self.argmax, self.stats,
-                  self.childlogit, self.ws)
-        verify_accept(mode, eps, delta, self.parent, self.depth, self.tok, self.argmax,
-                      self.stats, self.childlogit, self.L, self.path, self.next_root, self.ws,
-                      ok=self.ok)
+        self._verify_and_accept(mode, eps, delta, temperature, seed)
         if commit:
             compact_kv(self.L, self.path, self.Kc, self.Vc, self.P, self.ws)
+
+    def _verify_and_accept(self, mode, eps, delta, temperature, seed, fused=False):
+        if fused:
+            if mode == SAMPLE:
+                raise ValueError("exact sampling runs with the separate verify pass")
+            lm_verify_draft(self.y, self.W, self.lm, self.shortlist, self.smax, self.tok,
+                            self.parent, self.argmax, self.stats, self.childlogit,
+                            self.tree_topk_id, self.tree_topk_val, self.ws)
+        elif mode == SAMPLE:
+            lm_verify_sample(self.y, self.lm, self.tok, self.parent, self.P, temperature, seed,
+                             self.argmax, self.stats, self.childlogit, self.sample_id, self.ws)
+        else:
+            lm_verify(self.y, self.lm, self.tok, self.parent, self.argmax, self.stats,
+                      self.childlogit, self.ws)
+        verify_accept(mode, eps, delta, self.parent, self.depth, self.tok,
+                      self.sample_id if mode == SAMPLE else self.argmax, self.stats,
+                      self.childlogit, self.L, self.path, self.next_root, self.ws, ok=self.ok)
+
+    # ------------------------------------------------------------------
+    # The decoding loop ("Medusa Heads", "How it works": draft, verify,
+    # accept and roll back, then draft again from the last accepted
+    # position).  Step s + 1 reads the verify layer's output at step s's
+    # accepted node as its hidden state; its root is step s's next_root.
+    #
+    # Two forms of the steady-state step:
+    #   separate (canonical order): medusa_heads(h) -> tree_attention ->
+    #       lm_verify -> verify_accept -> compact_kv -> next_inputs(h)
+    #       (two LM-projection streams per step: draft rows, verify rows);
+    #   fused: tree_attention -> lm_verify_draft -> verify_accept ->
+    #       compact_kv -> next_inputs(root, shortlists, h): the K heads run on
+    #       every tree row and one LM-projection stream serves the verify
+    #       rows and the next step's draft rows.  The first step of a loop
+    #       drafts with medusa_heads.
+    # The fused form trades a second weight stream for (K + 1) times the
+    # verify rows in one pass; it pays while those rows keep the pass near
+    # its weight-stream time (few rows), see ``FUSED_MAX_ROWS``.
+    # ------------------------------------------------------------------
+
+    # Largest B N (K + 1) for which "auto" picks the fused form.
+    FUSED_MAX_ROWS = 512
+
+    def fused_auto(self) -> bool:
+        return self.fused_ok and self.B * self.N * (self.K + 1) <= self.FUSED_MAX_ROWS
+
+    def begin_decode(self, h: torch.Tensor, fused: bool) -> None:
+        """Before the first step of a loop: the fused form drafts the first
+        step from ``h`` (root and shortlists); the separate form needs
+        nothing."""
+        if fused:
+            if not self.fused_ok:
+                raise ValueError("the fused verify pass needs bf16 weights")
+            medusa_heads(h, self.W, self.lm, self.shortlist, self.smax, self.U, self.root,
+                         self.topk_id, self.topk_val, self.ws)
+
+    def decode_step(self, h: torch.Tensor, fused: bool, mode: int = TYPICAL, eps: float = 0.09,
+                    delta: float = 0.3, temperature: float = 1.0, seed: int = 0) -> None:
+        """Enqueue one steady-state step (asynchronous).  Updates in place:
+        the KV caches and P (the accepted path committed), ``h`` (the next
+        step's hidden state) and, in the fused form, root / topk_id /
+        topk_val (the next step's draft)."""
+        if not fused:
+            medusa_heads(h, self.W, self.lm, self.shortlist, self.smax, self.U, self.root,
+                         self.topk_id, self.topk_val, self.ws)
+        tree_attention(self.P, self.tok, self.mask, self.emb, self.wqkv, self.wo, self.Kc,
+                       self.Vc, self.y, self.ws, Hq=self.Hq, Hkv=self.Hkv, K=self.K,
+                       smax=self.smax, root=self.root, topk_id=self.topk_id, depth=self.depth,
+                       rank=self.rank)
+        self._verify_and_accept(mode, eps, delta, temperature, seed, fused)
+        compact_kv(self.L, self.path, self.Kc, self.Vc, self.P, self.ws)
+        if fused:
+            next_inputs(self.L, self.path, self.ws, N=self.N, smax=self.smax,
+                        next_root=self.next_root, y=self.y, tree_topk_id=self.tree_topk_id,
+                        tree_topk_val=self.tree_topk_val, h_next=h, root_out=self.root,
+                        topk_id_out=self.topk_id, topk_val_out=self.topk_val)
+        else:
+            next_inputs(self.L, self.path, self.ws, N=self.N, smax=self.smax, y=self.y,
+                        h_next=h)
+
+    def decode(self, h: torch.Tensor, n_steps: int, fused="auto", mode: int = TYPICAL,
+               eps: float = 0.09, delta: float = 0.3, record: bool = False,
+               temperature: float = 1.0, seed: int = 0):
+        """``n_steps`` consecutive steps from hidden state ``h`` (updated in
+        place).  ``fused``: True, False or "auto" (``fused_auto``).  With
+        ``record`` the host waits after every step and the per-step L, path,
+        tree tokens and next_root are returned (host tensors)."""
+        if fused == "auto":
+            fused = self.fused_auto() and mode != SAMPLE
+        self.begin_decode(h, fused)
+        out = []
+        for _ in range(n_steps):
+            self.decode_step(h, fused, mode, eps, delta, temperature, seed)
+            if record:
+                torch.cuda.current_stream(h.device).synchronize()
+                out.append(dict(L=self.L.cpu(), path=self.path.cpu(), tok=self.tok.cpu(),
+                                next_root=self.next_root.cpu()))
+        return out

@@ -100,8 +100,8 @@ def test_host_validation_rejects_before_launch(lib):
     sl3 = (ctypes.c_int32 * 2)(3, 2)
     assert lib.mds_medusa_heads(1, 1, 64, 100, 2, fake, fake, fake, sl3, 2, fake, fake, fake,
                                 fake, fake, 1 << 30, null) == -1
-    # verify_accept: bad mode, negative eps
-    assert lib.mds_verify_accept(1, 7, 2, 2, 0.1, 0.3, fake, fake, fake, fake, fake, fake,
+    # verify_accept: bad mode (0 greedy, 1 typical, 2 exact sampling), negative eps
+    assert lib.mds_verify_accept(1, 7, 2, 3, 0.1, 0.3, fake, fake, fake, fake, fake, fake,
                                  null, fake, fake, fake, fake, 1 << 20, null) == -1
     assert lib.mds_verify_accept(1, 7, 2, 1, -0.1, 0.3, fake, fake, fake, fake, fake, fake,
                                  null, fake, fake, fake, fake, 1 << 20, null) == -1
@@ -124,6 +124,34 @@ def test_host_validation_rejects_before_launch(lib):
                                    null) == -1
 
 
+def test_new_entry_points_validate_on_the_host(lib):
+    fake = ctypes.c_void_p(256)
+    null = None
+    big = 1 << 40
+    # exact sampling: the temperature must be positive and finite
+    for T in (0.0, -1.0, float("inf"), float("nan")):
+        assert lib.mds_lm_verify_sample(1, 1, 7, 64, 100, fake, fake, fake, fake, fake, T, 3,
+                                        fake, fake, fake, fake, fake, big, null) == -1
+    # P is required
+    assert lib.mds_lm_verify_sample(1, 1, 7, 64, 100, fake, fake, fake, fake, null, 1.0, 3,
+                                    fake, fake, fake, fake, fake, big, null) == -1
+    # the fused verify pass is bf16 only; its workspace is checked
+    sl = (ctypes.c_int32 * 2)(2, 2)
+    assert lib.mds_lm_verify_draft(0, 1, 7, 64, 100, 2, fake, fake, fake, sl, 2, fake, fake,
+                                   fake, fake, fake, fake, fake, fake, big, null) == -3
+    assert lib.mds_lm_verify_draft(1, 1, 7, 64, 100, 2, fake, fake, fake, sl, 2, fake, fake,
+                                   fake, fake, fake, fake, fake, fake, 64, null) == -2
+    need = lib.mds_verify_draft_workspace_size(1, 7, 64, 2)
+    assert need >= 8192 + 3 * 7 * 64 * 2
+    # next_inputs: an output without its source is an argument error
+    assert lib.mds_next_inputs(1, 1, 7, 2, 2, 64, fake, fake, null, null, null, null, fake, null,
+                               null, null, fake, big, null) == -1
+    assert lib.mds_next_inputs(1, 1, 7, 2, 2, 64, fake, fake, null, fake, null, null, null,
+                               fake, null, null, fake, big, null) == -1
+    assert lib.mds_next_inputs(1, 1, 7, 2, 2, 64, null, fake, null, fake, null, null, fake, null,
+                               null, null, fake, big, null) == -1
+
+
 def test_python_binding_refuses_cpu_tensors(lib):
     import torch
     with pytest.raises(mds.MedusaError):
@@ -138,3 +166,16 @@ def test_missing_library_fails_loudly(tmp_path):
             mds.load(str(tmp_path / "nope.so"))
     finally:
         mds._lib = saved
+
+
+def test_binding_argument_counts_match_header(lib):
+    """Every ctypes signature of the binding has as many arguments as the
+    header's declaration (a miscount would shift every later argument)."""
+    with open(os.path.join(ROOT, "include", "medusa.h")) as f:
+        text = f.read()
+    decls = re.findall(r"MDS_API\s+[\w\s\*]+?\b(mds_\w+)\s*\(([^)]*)\)", text)
+    assert decls
+    for name, params in decls:
+        params = params.strip()
+        n = 0 if params in ("", "void") else params.count(",") + 1
+        assert len(mds._SIGS[name][0]) == n, (name, len(mds._SIGS[name][0]), n)
