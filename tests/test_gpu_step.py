@@ -1,12 +1,19 @@
 """Whole-step parity: MedusaStep (all C-ABI calls in order) against the
 oracle's step on the same seeded workload, for the small workloads and the
 five benchmark workloads at full size (large batches sampled: the GPU runs
-the whole batch, the oracle recomputes some sequences one by one).
+the whole batch, the oracle recomputes the sampled sequences one by one).
 
-A sequence whose draft holds a near-tie (a shortlist or root decision with
-oracle margin below the logit tolerance) is compared only up to the draft:
-its tree tokens may legitimately differ.  Near-tie acceptance edges end the
-comparison of that sequence's path.  Both are counted and printed."""
+Every sampled sequence is compared through the whole step.  The draft
+(root and shortlists) is compared with the oracle's, exactly where the
+oracle's ranking margin is at least the logit tolerance and by value where it
+is smaller (a near tie: either id is correct).  The GPU's tree tokens must be
+exactly the token fill of the GPU's own (validated) draft, and the oracle's
+verify layer, statistics, acceptance, longest path and compaction are then
+recomputed from those tokens and compared.  Acceptance edges whose oracle
+margin is below the tolerance are near ties: the GPU's result on every other
+edge must equal the oracle's, and the accepted length and path must be the
+longest path of the GPU's (validated) edge results.  Near ties are counted and
+printed; every configuration asserts that paths were compared."""
 from __future__ import annotations
 
 import numpy as np
@@ -37,87 +44,154 @@ def make_step(mds, w, x):
     return step, dev(x["h"], w.dtype)
 
 
+def acceptance_runs(w, modes):
+    """(label, mode name, eps, delta, T, seed) of each acceptance run.  A mode
+    is "greedy", "typical" (the workload's eps, delta), ("typical", eps,
+    delta) or ("sample", T, seed) (exact sampling at temperature T)."""
+    runs = []
+    for m in modes:
+        if isinstance(m, tuple) and m[0] == "sample":
+            runs.append((f"sample(T={m[1]},seed={m[2]})", "sample", 0.0, 0.0, m[1], m[2]))
+        elif isinstance(m, tuple):
+            runs.append((f"typical(eps={m[1]},delta={m[2]})", "typical", m[1], m[2], 1.0, 0))
+        else:
+            runs.append((m, m, w.eps, w.delta, 1.0, 0))
+    return runs
+
+
+MODE_CODE = {"greedy": 0, "typical": 1, "sample": 2}
+
+
+def sample_stats(l, T, seed, P_b, b, N):
+    """Oracle draws of one sequence's tree rows (keys per row for the
+    near-tie checks)."""
+    keys = [oracle.gumbel_keys(l[n], T, seed, (n, int(P_b), int(b))) for n in range(N)]
+    sample = np.array([[int(np.argmax(k)) for k in keys]])
+    gap = np.array([[float(np.sort(k)[-1] - np.sort(k)[-2]) for k in keys]])
+    return keys, dict(sample=sample, sample_gap=gap)
+
+
 def compare_step(mds, w, sample, modes):
+    """Runs the step once per acceptance run on the GPU (the last one commits
+    the KV cache) and compares the sampled sequences with the oracle.
+    Returns (near ties, paths compared)."""
     x = ms.make_inputs(w)
     step, h = make_step(mds, w, x)
-    final_mode = modes[-1]
+    runs = acceptance_runs(w, modes)
     results = {}
-    for mode in modes:
-        commit = mode == final_mode
-        step.run(h, mode=0 if mode == "greedy" else 1, eps=w.eps, delta=w.delta, commit=commit)
+    for k, (label, mode, eps, delta, T, seed) in enumerate(runs):
+        commit = k == len(runs) - 1
+        step.run(h, mode=MODE_CODE[mode], eps=eps, delta=delta, commit=commit, temperature=T,
+                 seed=seed)
         torch.cuda.synchronize()
         assert mds.status_check(step.ws) == 0
-        results[mode] = dict(L=host(step.L), path=host(step.path), nr=host(step.next_root),
-                             ok=host(step.ok).astype(bool))
+        results[label] = dict(L=host(step.L), path=host(step.path), nr=host(step.next_root),
+                              ok=host(step.ok).astype(bool), sample=host(step.sample_id))
     g = dict(U=host(step.U), root=host(step.root), topk_id=host(step.topk_id),
              topk_val=host(step.topk_val), tok=host(step.tok), y=host(step.y),
              argmax=host(step.argmax), stats=host(step.stats), child=host(step.childlogit),
-             kc=None, vc=None, P=host(step.P))
-    f = f64_inputs(w, x, sample)           # h, kc, vc already restricted to the sample
-    r = oracle.step(w, f, x["P"][sample], final_mode, batch=list(range(len(sample))))
+             P=host(step.P))
+    f = f64_inputs(w, x, sample)           # h, kc, vc restricted to the sample
+    tr = oracle.build_tree(w.shortlist, w.max_rank_sum)
+    parent, depth, rank = tr["parent"], tr["depth"], tr["rank"]
+    U = oracle.heads_residual(f["h"], f["W"], w.dtype)
     ties = NearTies()
-    compared_paths = 0
+    compared, exact_paths, accepted = 0, 0, []
     for i, b in enumerate(sample):
-        U = r["U"][i]
-        close_float(g["U"][b], U, w.dtype, "stored", f"U[{b}]")
-        z = U @ f["lm"].T
+        # ---- A1/A2: residual blocks and the draft
+        close_float(g["U"][b], U[i], w.dtype, "stored", f"U[{b}]")
+        dr = oracle.draft(U[i:i + 1], f["lm"], w.shortlist)
+        z = U[i] @ f["lm"].T
         tl = tol_logit(w.dtype, float(np.abs(z).max()))
-        n_before = ties.count
-        check_ranked_ids([g["root"][b]], z[0], [r["draft"]["root"][i]], tl, ties, f"root[{b}]")
+        check_ranked_ids([g["root"][b]], z[0], [dr["root"][0]], tl, ties, f"root[{b}]")
         for k, s in enumerate(w.shortlist):
-            check_ranked_ids(g["topk_id"][b, k, :s], z[k + 1], r["draft"]["topk_id"][i, k, :s], tl,
-                             ties, f"topk[{b},{k}]")
-        if ties.count > n_before:
-            continue                       # tree tokens may differ downstream
-        np.testing.assert_array_equal(g["tok"][b], r["tok"][i])
-        close_float(g["y"][b], r["attn"]["y"][i], w.dtype, "attn", f"y[{b}]")
-        st = r["stats"]
-        l = r["attn"]["y"][i] @ f["lm"].T
+            check_ranked_ids(g["topk_id"][b, k, :s], z[k + 1], dr["topk_id"][0, k, :s], tl, ties,
+                             f"topk[{b},{k}]")
+        # ---- A3: token fill of the GPU's own draft (exact); with no near
+        # tie in the draft it is also the oracle's fill
+        tok_b = oracle.fill_tokens(g["root"][b:b + 1].astype(np.int64),
+                                   g["topk_id"][b:b + 1].astype(np.int64), depth, rank)
+        np.testing.assert_array_equal(g["tok"][b], tok_b[0])
+        # ---- A4: verify layer from those tokens
+        Pb = int(x["P"][b])
+        at = oracle.tree_attention(tok_b, x["P"][b:b + 1], tr["mask"], f["emb"], f["wq"],
+                                   f["wk"], f["wv"], f["wo"], f["kc"][i:i + 1], f["vc"][i:i + 1],
+                                   w.Hq, w.Hkv, w.dh, w.dtype)
+        close_float(g["y"][b], at["y"][0], w.dtype, "attn", f"y[{b}]", exact=at["y_exact"][0])
+        # ---- A5: verify statistics
+        st = oracle.verify_stats(at["y"], f["lm"], tok_b, parent)
+        l = at["y"][0] @ f["lm"].T
         tv = tol_logit(w.dtype, float(np.abs(l).max()))
-        for n in range(r["tree"]["N"]):
-            check_ranked_ids([g["argmax"][b, n]], l[n], [st["argmax"][i, n]], tv, ties,
+        for n in range(tr["N"]):
+            check_ranked_ids([g["argmax"][b, n]], l[n], [st["argmax"][0, n]], tv, ties,
                              f"argmax[{b},{n}]")
-        close_float(g["stats"][b, :, 1], st["lse"][i], w.dtype, "logit", "lse")
-        close_float(g["stats"][b, :, 2], st["H"][i], w.dtype, "logit", "H")
-        close_float(g["child"][b, 1:], st["childlogit"][i, 1:], w.dtype, "logit", "child")
-        for mode in modes:
-            if mode == final_mode:
-                ok, margin, lp = r["ok"], r["margin"], r["path"]
-            else:
-                ok, margin = oracle.accept_edges(mode, w.eps, w.delta, r["tok"], r["tree"]["parent"], st)
-                lp = oracle.longest_path(ok, r["tree"]["parent"], r["tree"]["depth"], st["argmax"], w.K)
-            gm = results[mode]
-            sure = margin[i] >= tv
-            np.testing.assert_array_equal(gm["ok"][b][sure], ok[i][sure])
+        close_float(g["stats"][b, :, 1], st["lse"][0], w.dtype, "logit", f"lse[{b}]")
+        close_float(g["stats"][b, :, 2], st["H"][0], w.dtype, "logit", f"H[{b}]")
+        close_float(g["child"][b, 1:], st["childlogit"][0, 1:], w.dtype, "logit", f"child[{b}]")
+        # ---- A6/A7 for every acceptance run
+        for k, (label, mode, eps, delta, T, seed) in enumerate(runs):
+            gm = results[label]
+            st_m, tm = st, tv
+            if mode == "sample":
+                # the draws: exact where the oracle's key gap clears the
+                # tolerance (logit error / T, plus the noise's fp32 error)
+                keys, smp = sample_stats(l, T, seed, Pb, b, tr["N"])
+                tm = tv / T + 1e-4
+                for n in range(tr["N"]):
+                    check_ranked_ids([gm["sample"][b, n]], keys[n], [smp["sample"][0, n]], tm,
+                                     ties, f"{label} sample[{b},{n}]")
+                st_m = dict(st, **smp)
+            ok, margin = oracle.accept_edges(mode, eps, delta, tok_b, parent, st_m)
+            sure = margin[0] >= tm
+            np.testing.assert_array_equal(gm["ok"][b][sure], ok[0][sure], err_msg=f"{label} ok[{b}]")
             if not sure.all():
-                ties.add(f"{mode} edge[{b}]")
-                continue
-            assert gm["L"][b] == lp["L"][i], (mode, b)
-            np.testing.assert_array_equal(gm["path"][b], lp["path"][i])
-            best = lp["path"][i][lp["L"][i]]
-            if st["argmax_gap"][i, best] >= tv:
-                assert gm["nr"][b] == lp["next_root"][i]
-            compared_paths += 1
-            if mode == final_mode:
-                # compaction: accepted tree rows moved to P_b..P_b+L, P advanced
-                Pb = int(x["P"][b])
-                Lb = int(lp["L"][i])
-                assert g["P"][b] == Pb + Lb + 1
+                ties.add(f"{label} edges[{b}] x{int((~sure).sum())}")
+            # the longest path of the GPU's edge results (which agree with the
+            # oracle's wherever the oracle's decision is clear)
+            lp = oracle.longest_path(gm["ok"][b][None], parent, depth, st["argmax"], w.K)
+            assert gm["L"][b] == lp["L"][0], (label, b, gm["L"][b], lp["L"][0])
+            np.testing.assert_array_equal(gm["path"][b], lp["path"][0], err_msg=f"{label} path[{b}]")
+            if sure.all():
+                lo = oracle.longest_path(ok, parent, depth,
+                                         st_m["sample"] if mode == "sample" else st["argmax"],
+                                         w.K)
+                assert gm["L"][b] == lo["L"][0] and np.array_equal(gm["path"][b], lo["path"][0])
+                exact_paths += 1
+            best = int(lp["path"][0][lp["L"][0]])
+            if mode == "sample":
+                assert gm["nr"][b] == gm["sample"][b, best], (label, b)
+            else:
+                check_ranked_ids([gm["nr"][b]], l[best], [st["argmax"][0, best]], tv, ties,
+                                 f"{label} next_root[{b}]")
+            compared += 1
+            accepted.append(int(gm["L"][b]))
+            # ---- A8: compaction of the final run's path
+            if k == len(runs) - 1:
+                Lb = int(gm["L"][b])
+                kc, vc, Pn = oracle.compact_kv(at["kc"], at["vc"], x["P"][b:b + 1],
+                                               gm["L"][b:b + 1].astype(np.int64),
+                                               gm["path"][b:b + 1].astype(np.int64))
+                assert g["P"][b] == Pn[0] == Pb + Lb + 1
                 kc_g = host(step.Kc[b])
                 vc_g = host(step.Vc[b])
-                close_float(kc_g[:, Pb:Pb + Lb + 1], r["kc"][i][:, Pb:Pb + Lb + 1], w.dtype,
-                            "stored", "kc")
-                close_float(vc_g[:, Pb:Pb + Lb + 1], r["vc"][i][:, Pb:Pb + Lb + 1], w.dtype,
-                            "stored", "vc")
+                close_float(kc_g[:, Pb:Pb + Lb + 1], kc[0][:, Pb:Pb + Lb + 1], w.dtype, "stored",
+                            f"kc[{b}]")
+                close_float(vc_g[:, Pb:Pb + Lb + 1], vc[0][:, Pb:Pb + Lb + 1], w.dtype, "stored",
+                            f"vc[{b}]")
                 np.testing.assert_array_equal(kc_g[:, :Pb], f["kc"][i][:, :Pb])
+                np.testing.assert_array_equal(vc_g[:, :Pb], f["vc"][i][:, :Pb])
     ties.report(w.name)
-    print(f"[{w.name}] sequences compared: {len(sample)}, paths compared: {compared_paths}, "
+    print(f"[{w.name}] sequences compared: {len(sample)}, paths compared: {compared} "
+          f"({exact_paths} with no near tie), accepted depths: {sorted(set(accepted))}, "
           f"near-ties: {ties.count}")
-    return ties
+    assert compared == len(sample) * len(runs)
+    return ties, compared, accepted
 
 
-SMALL = [(ms.workload(0), ["greedy"]), (MINI, ["greedy", "typical"]), (MINI_GQA, ["typical"]),
-         (MINI_F32, ["greedy", "typical"])]
+SMALL = [(ms.workload(0), ["greedy", ("sample", 1.0, 3)]),
+         (MINI, ["greedy", ("sample", 0.8, 1), "typical"]),
+         (MINI_GQA, [("sample", 1.0, 2), "typical"]),
+         (MINI_F32, ["greedy", ("sample", 1.5, 4), "typical"])]
 
 
 @pytest.mark.parametrize("w,modes", SMALL, ids=lambda p: getattr(p, "name", None))
@@ -125,14 +199,28 @@ def test_step_small(mds, w, modes):
     compare_step(mds, w, list(range(w.B)), modes)
 
 
-FULL = [(1, [0], ["typical"]), (2, [0, 15], ["typical"]), (3, [3], ["typical"]),
-        (4, [0, 63], ["greedy", "typical"])]
+# Typical acceptance with eps = 1, delta = 1.05: an edge passes iff
+# ln p > ln 1.05 - H.  With the synthetic value laws the verify distributions
+# are nearly flat (H close to ln V) and ln p + H spreads over about
+# [-0.2, 0.15], so roughly a quarter to a third of the edges pass and the
+# accepted depth lands between 0 and K (the oracle gives L = 1 for the
+# Vicuna-7B-shaped batch-1 workload and 3, 0, 1, 1 for the first sequences of
+# the batched sparse one): the longest-path logic is exercised away from the
+# all-pass and none-pass extremes.
+MID = ("typical", 1.0, 1.05)
+FULL = [(1, [0], ["typical", ("sample", 1.0, 5), MID]),
+        (2, list(range(16)), [("sample", 1.0, 6), "typical", MID]),
+        (3, list(range(8)), ["typical", MID]),
+        (4, [0, 9, 18, 27, 36, 45, 54, 63], ["greedy", ("sample", 0.7, 7), MID, "typical"])]
 
 
 @pytest.mark.parametrize("cfg,sample,modes", FULL, ids=[f"cfg{c[0]}" for c in FULL])
 def test_step_full_size(mds, cfg, sample, modes):
     w = ms.workload(cfg)
-    compare_step(mds, w, sample, modes)
+    _, compared, accepted = compare_step(mds, w, sample, modes)
+    assert compared > 0
+    # the mid-range run reaches intermediate depths somewhere in the sample
+    assert any(0 < L < w.K for L in accepted), accepted
     torch.cuda.empty_cache()
 
 

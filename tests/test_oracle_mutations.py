@@ -145,12 +145,12 @@ def philox_no_key_bump(counter, key, rounds=10):
     return c
 
 
-def gumbel_no_temperature(logits, T, seed, offset, row):
-    return mo.gumbel_keys(logits, 1.0, seed, offset, row)
+def gumbel_no_temperature(logits, T, seed, words3):
+    return mo.gumbel_keys(logits, 1.0, seed, words3)
 
 
-def gumbel_sign_flipped(logits, T, seed, offset, row):
-    g = mo.gumbel_keys(logits, T, seed, offset, row) - logits / T
+def gumbel_sign_flipped(logits, T, seed, words3):
+    g = mo.gumbel_keys(logits, T, seed, words3) - logits / T
     return logits / T - g
 
 

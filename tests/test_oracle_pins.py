@@ -591,7 +591,7 @@ def check_sampler_distribution(orc, rows=4000):
     for T in (0.7, 1.3):
         counts = np.zeros(5)
         for r in range(rows):
-            counts[int(np.argmax(orc.gumbel_keys(logits, T, 99, 5, r)))] += 1
+            counts[int(np.argmax(orc.gumbel_keys(logits, T, 99, (r, 5, 0))))] += 1
         p = scipy.special.softmax(logits / T)
         sd = np.sqrt(rows * p * (1 - p))
         assert np.all(np.abs(counts - rows * p) < 5 * sd), (T, counts, rows * p)
@@ -635,7 +635,7 @@ def check_sampling_is_rejection_sampling(orc, rows=4000):
     # the oracle's rule: the drawn token is the accepted child or the bonus
     got = np.zeros(len(logits))
     for r in range(rows):
-        got[int(np.argmax(orc.gumbel_keys(logits, 1.0, 7, 0, r)))] += 1
+        got[int(np.argmax(orc.gumbel_keys(logits, 1.0, 7, (3, r, 1))))] += 1
     sd = np.sqrt(rows * want * (1 - want))
     assert np.all(np.abs(sim - rows * want) < 5 * sd), (sim, rows * want)
     assert np.all(np.abs(got - rows * want) < 5 * sd), (got, rows * want)
@@ -650,7 +650,7 @@ def check_sample_acceptance(orc):
     tr = orc.build_tree(w.shortlist, -1)
     rng = np.random.default_rng(1)
     y = rng.standard_normal((1, tr["N"], w.d))
-    smp = orc.sample_tokens(y, f["lm"], 0.8, 11, 3)
+    smp = orc.sample_tokens(y, f["lm"], 0.8, 11, P)
     for plant in range(w.K + 1):
         tok = rng.integers(0, w.V, size=(1, tr["N"]))
         node = 0
