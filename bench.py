@@ -2,28 +2,36 @@
 """Benchmark: one Medusa draft-and-verify step on one B300 (per rank).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload vicuna7b-b1]
+                    [--workload llama3-8b-gqa-b64] [--also vicuna7b-b1,...|none]
 
 A step = medusa_heads -> tree_attention -> lm_verify -> verify_accept ->
-compact_kv on the seeded synthetic workload (default: the Vicuna-7B-shaped
-batch-1 workload, d=4096, V=32000, 32 heads x 128, K=4, tree (4,3,2,2),
-prefix 2048, typical acceptance).  Inputs are resident in HBM; each step's
-bytes (about 0.8 GB) exceed the 126 MB L2, so no L2 flush is inserted.  The
-prefix length is restored before every step (one 4-byte device copy), so
-every timed step verifies against the same prefix length.
+compact_kv on a seeded synthetic workload.  The headline (``value``) is the
+largest single-GPU workload: the Llama-3-8B-shaped GQA batch of 64
+(d=4096, V=128256, 32/8 heads x 128, K=4, tree (4,3,2,2), prefix 4096,
+typical acceptance).  The other benchmark workloads (batch 1, 16 and 8) are
+measured in the same run and reported under ``workloads`` with their own
+per-pass rooflines (``--also none`` skips them).
+
+Inputs are resident in HBM; every step's bytes (0.8-3.5 GB) exceed the
+126 MB L2, so no L2 flush is inserted.  The prefix length is restored before
+every step (one small device copy), so every timed step verifies against the
+same prefix length.
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the fp64 CPU
-oracle on this host instead (a bounded sample of the same workload).
+oracle on this host instead (a bounded sample of the same workload).  With
+``--gpus N`` and no WORLD_SIZE in the environment, the script starts N ranks
+itself (torch.distributed.run, one replica per GPU).
 """
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
 import subprocess
-import tempfile
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -34,6 +42,10 @@ sys.path.insert(0, ROOT)
 import medusa_synth as ms  # noqa: E402
 
 METRIC = "Medusa draft+verify steps/s"
+HEADLINE = "llama3-8b-gqa-b64"
+ALSO = ("vicuna7b-b1", "sparse-b16", "vicuna13b-b8")
+CSRC = os.path.join(ROOT, "speculative_decoding_08_b300", "csrc")
+TRAFFIC_JSON = os.path.join(ROOT, "profiles", "dram_traffic.json")
 
 
 def peaks():
@@ -47,42 +59,80 @@ def peaks():
     return dict(hbm=6400.0, bf16=1800.0, bf16_sustained=1400.0, src="fallback")
 
 
-def step_bytes(w, N):
-    """Algorithmic HBM bytes of one step (bf16): each weight and the prefix
-    KV read once, small activations and outputs added."""
+# ---------------------------------------------------------------------------
+# Algorithmic work of each C-ABI call (bytes that must cross HBM at least once,
+# and multiply-add flops), bf16 element size e.
+# ---------------------------------------------------------------------------
+
+def pass_work(w, N, P):
     e = 2 if w.dtype == "bf16" else 4
-    d, V, K, B = w.d, w.V, w.K, w.B
-    qkv = (w.Hq + 2 * w.Hkv) * w.dh * d * e
-    wo = d * w.Hq * w.dh * e
-    return dict(heads=K * d * d * e, lm=V * d * e, qkv=qkv, wo=wo)
+    B, d, V, K = w.B, w.d, w.V, w.K
+    rows = B * N
+    qkv_w = (w.Hq + 2 * w.Hkv) * w.dh * d * e
+    wo_w = d * w.Hq * w.dh * e
+    prefix_kv = int(np.sum(P)) * w.Hkv * w.dh * 2 * e
+    keys = int(np.sum(np.asarray(P, np.int64) + N))
+    heads = dict(
+        bytes=K * d * d * e + V * d * e + B * d * e + B * (K + 1) * d * e + B * K * 8 * 8,
+        flops=2 * B * K * d * d + 2 * B * (K + 1) * d * V)
+    # tree attention: the weights, the prefix K/V read once, the embedding
+    # rows gathered, the tree rows' K/V written and y written; flops of the
+    # QKV and output projections plus q.k and p.v over the keys a query row
+    # may see (its sequence's prefix and, as an upper bound, the whole tree)
+    attn = dict(
+        bytes=qkv_w + wo_w + prefix_kv + rows * d * e + rows * w.Hkv * w.dh * 2 * e + rows * d * e,
+        flops=2 * rows * d * (w.Hq + 2 * w.Hkv) * w.dh + 2 * rows * w.Hq * w.dh * d
+        + 4 * N * w.Hq * w.dh * keys)
+    verify = dict(bytes=V * d * e + rows * d * e + rows * 24, flops=2 * rows * d * V)
+    small = dict(bytes=rows * 28 + B * (K + 1) * w.Hkv * w.dh * 2 * e * 2, flops=0)
+    return {"medusa_heads": heads, "tree_attention": attn, "lm_verify": verify,
+            "verify_accept+compact_kv": small}
 
 
-PROFILE_VERIFY = os.path.join(ROOT, "profiles", "gemm_verify_vicuna7b-b1.md")
-GEMM_SOURCE = os.path.join(ROOT, "speculative_decoding_08_b300", "csrc", "gemm_tc.cu")
+def roofline_entry(work, seconds, pk):
+    """Time-based roofline of one pass: the bound is the larger of bytes / HBM
+    and flops / tensor peak (the sustained figure: every pass is timed inside
+    a long replay); frac = achieved rate of that resource / its peak."""
+    t_hbm = work["bytes"] / (pk["hbm"] * 1e9)
+    t_tc = work["flops"] / (pk["bf16_sustained"] * 1e12)
+    gbs = work["bytes"] / seconds / 1e9
+    tfs = work["flops"] / seconds / 1e12
+    if t_tc > t_hbm:
+        bound, achieved, peak, unit = "tensor", tfs, pk["bf16_sustained"], "TFLOP/s"
+    else:
+        bound, achieved, peak, unit = "hbm", gbs, pk["hbm"], "GB/s"
+    return {"us": seconds * 1e6, "bound": bound, "achieved": achieved, "peak": peak,
+            "unit": unit, "frac": achieved / peak, "hbm_gbs": gbs, "hbm_frac": gbs / pk["hbm"],
+            "tflops": tfs, "tensor_frac": tfs / pk["bf16_sustained"],
+            "algorithmic_bytes": work["bytes"], "flops": work["flops"]}
 
 
-def profiled_traffic():
-    """DRAM bytes (read + write) per launch of the verify-pass GEMM from the
-    committed ncu summary, or None when the summary is missing or was taken
-    on another version of the kernel source (its sha256 is recorded there)."""
-    import hashlib
-    import re
+def source_hash(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(CSRC, n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(workload, call):
+    """DRAM bytes (read + write) per launch of a call's dominant kernel from
+    the committed ncu record, or None when there is no record for this
+    workload and call or it was taken on other kernel sources."""
     try:
-        text = open(PROFILE_VERIFY).read()
-        src = hashlib.sha256(open(GEMM_SOURCE, "rb").read()).hexdigest()
-    except OSError:
+        with open(TRAFFIC_JSON) as f:
+            recs = json.load(f)["records"]
+    except (OSError, ValueError, KeyError):
         return None
-    m_hash = re.search(r"gemm_tc\.cu sha256:\s*([0-9a-f]{64})", text)
-    m_bytes = re.search(r"DRAM bytes per launch \(read \+ write\):\s*([0-9]+)", text)
-    if not m_hash or not m_bytes or m_hash.group(1) != src:
-        return None
-    return int(m_bytes.group(1))
-
-
-def lm_verify_bytes(w, N):
-    e = 2 if w.dtype == "bf16" else 4
-    rows = w.B * N
-    return w.V * w.d * e + rows * w.d * e + rows * (4 * 4 + 4 + 4) + rows * 4
+    for r in recs:
+        if r.get("workload") == workload and r.get("call") == call:
+            try:
+                if source_hash(*r["sources"]) != r["sources_sha256"]:
+                    return None
+            except OSError:
+                return None
+            return int(r["dram_bytes_per_launch"])
+    return None
 
 
 class Clocks:
@@ -140,17 +190,28 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+_THREAD_VARS = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
+
+
+def blas_threads():
+    """Threads the BLAS library of this process uses."""
+    try:
+        from threadpoolctl import threadpool_info
+        return max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    except Exception:
+        for v in _THREAD_VARS:
+            if os.environ.get(v, "").isdigit():
+                return int(os.environ[v])
+        return os.cpu_count() or 1
+
+
 def oracle_sample(w, x, budget_s=15.0, steps=50, warmup=0, warmup_budget_s=30.0):
     """Time the fp64 oracle's step on this host: up to `warmup` untimed steps
     (at most ~warmup_budget_s), then up to `steps` timed steps (at most
     ~budget_s, at least one).  Returns (cpu_baseline dict, timed steps,
     seconds, warm-up steps run)."""
     import oracle
-    try:
-        from threadpoolctl import threadpool_info
-        cores = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
-    except Exception:
-        cores = os.cpu_count() or 1
+    cores = blas_threads()
     f = {k: ms.as_f64(x[k], w.dtype) for k in ("h", "W", "lm", "emb", "wq", "wk", "wv", "wo")}
     f["kc"] = ms.as_f64(x["kc"][:1], w.dtype)
     f["vc"] = ms.as_f64(x["vc"][:1], w.dtype)
@@ -170,9 +231,10 @@ def oracle_sample(w, x, budget_s=15.0, steps=50, warmup=0, warmup_budget_s=30.0)
             break
     dt = time.perf_counter() - t0
     # one oracle step processes one sequence; a GPU step processes B
-    return dict(value=n / dt / w.B, unit="steps/s", cores=cores, kind="oracle",
-                sample=f"{n} oracle step(s) of one sequence of {w.name} "
-                       f"(scaled by 1/B={w.B} to whole-batch steps/s)"), n, dt, nw
+    return dict(value=n / dt / w.B, unit="steps/s", cores=cores, nproc=os.cpu_count(),
+                kind="oracle",
+                sample=f"{n} oracle step(s) of one sequence of {w.name} on {cores} BLAS "
+                       f"thread(s) (scaled by 1/B={w.B} to whole-batch steps/s)"), n, dt, nw
 
 
 def run_reference(args, w):
@@ -212,25 +274,12 @@ def whole_job_rate(world, units_per_rank, seconds):
     return world * units_per_rank / seconds
 
 
-def run_ours(args, w):
+def measure(w, args, dev, world, e2e=True):
+    """Device-timed steps, per-call times, end-to-end steps of one workload on
+    this rank.  Returns a dict of raw results (times of this rank)."""
     import torch
     import torch.distributed as dist
     import speculative_decoding_08_b300 as mds
-    from speculative_decoding_08_b300 import build as mbuild
-
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    if rank == 0 or world == 1:
-        mbuild.build()
-    if world > 1:
-        dist.barrier()
-    mds.load()
-    dev = torch.device("cuda", local if world > 1 else 0)
-    torch.cuda.set_device(dev)
 
     x = ms.make_inputs(w)
 
@@ -258,7 +307,7 @@ def run_ours(args, w):
         for _ in range(max(args.warmup, 3)):
             one()
     s.synchronize()
-    # capture the step in a CUDA graph
+    # the step as one CUDA graph
     g = torch.cuda.CUDAGraph()
     n0 = mds.launch_count()
     with torch.cuda.graph(g, stream=s):
@@ -269,9 +318,6 @@ def run_ours(args, w):
     torch.cuda.synchronize()
     assert mds.status_check(step.ws) == 0, "device latched a data error"
 
-    clocks = Clocks(dev.index)
-    clocks.start()
-    time.sleep(0.3)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
@@ -285,10 +331,10 @@ def run_ours(args, w):
     if world > 1:
         dist.barrier()
     ms_total = e0.elapsed_time(e1)
+    L_host = step.L.cpu().numpy().copy()
 
     # per-call device time: each C-ABI call alone, captured 10 times back to
     # back in a CUDA graph and replayed; CUDA events on the launching stream
-    calls = ["medusa_heads", "tree_attention", "lm_verify", "verify_accept", "compact_kv"]
     fns = {
         "medusa_heads": lambda: mds.medusa_heads(h, step.W, step.lm, step.shortlist, step.smax,
                                                  step.U, step.root, step.topk_id,
@@ -299,23 +345,22 @@ def run_ours(args, w):
             root=step.root, topk_id=step.topk_id, depth=step.depth, rank=step.rank),
         "lm_verify": lambda: mds.lm_verify(step.y, step.lm, step.tok, step.parent, step.argmax,
                                            step.stats, step.childlogit, step.ws),
-        "verify_accept": lambda: mds.verify_accept(mode, w.eps, w.delta, step.parent,
-                                                   step.depth, step.tok, step.argmax,
-                                                   step.stats, step.childlogit, step.L,
-                                                   step.path, step.next_root, step.ws,
-                                                   ok=step.ok),
-        "compact_kv": lambda: (P.copy_(P0), mds.compact_kv(step.L, step.path, step.Kc,
-                                                           step.Vc, step.P, step.ws)),
+        "verify_accept+compact_kv": lambda: (
+            mds.verify_accept(mode, w.eps, w.delta, step.parent, step.depth, step.tok,
+                              step.argmax, step.stats, step.childlogit, step.L, step.path,
+                              step.next_root, step.ws, ok=step.ok),
+            P.copy_(P0),
+            mds.compact_kv(step.L, step.path, step.Kc, step.Vc, step.P, step.ws)),
     }
     per = {}
     reps = 10
     with torch.cuda.stream(s):
         P.copy_(P0)
-        for c in calls:
+        for c, fn in fns.items():
             gc = torch.cuda.CUDAGraph()
             with torch.cuda.graph(gc, stream=s):
                 for _ in range(reps):
-                    fns[c]()
+                    fn()
             gc.replay()
             s.synchronize()
             ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -324,105 +369,212 @@ def run_ours(args, w):
                 gc.replay()
             ev1.record(s)
             s.synchronize()
-            per[c] = ev0.elapsed_time(ev1) / (3 * reps)
+            per[c] = ev0.elapsed_time(ev1) / (3 * reps) / 1e3      # seconds
             P.copy_(P0)
-    clk = clocks.stop()
-
-    # end to end through the public API with host buffers: every step copies
-    # h in from pinned host memory, runs the step and copies the emitted
-    # tokens (L, path, tree tokens, next_root) back to pinned host memory,
-    # all inside the captured step (MedusaStep.capture with h_host and
-    # outputs_to_host); the host waits for the step every time.  The prefix
-    # length is restored before each step (one 4-byte device copy) so that
-    # every step verifies against the same prefix.
-    h_host = torch.empty_like(h, device="cpu").pin_memory()
-    h_host.copy_(h.cpu())
-    h_dev = torch.empty_like(h)
-    with torch.cuda.stream(s):
-        P.copy_(P0)
-        step.capture(h_dev, mode=mode, eps=w.eps, delta=w.delta, h_host=h_host,
-                     outputs_to_host=True)
-    s.synchronize()
-    outs = list(step.host_out.values())
-    e2e_steps = max(args.steps, 10)
     torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(e2e_steps):
+    assert mds.status_check(step.ws) == 0, "device latched a data error"
+
+    out = dict(w=w, x=x, N=N, ms_total=ms_total, per=per, L=L_host,
+               per_step_kernels=per_step_kernels)
+    if e2e:
+        # end to end through the public API with host buffers: every step
+        # copies h in from pinned host memory, runs the step and copies the
+        # emitted tokens (L, path, tree tokens, next_root) back to pinned host
+        # memory, all inside the captured step (MedusaStep.capture with h_host
+        # and outputs_to_host); the host waits for the step every time.  The
+        # prefix length is restored before each step (a small device copy) so
+        # that every step verifies against the same prefix.
+        h_host = torch.empty_like(h, device="cpu").pin_memory()
+        h_host.copy_(h.cpu())
+        h_dev = torch.empty_like(h)
         with torch.cuda.stream(s):
             P.copy_(P0)
-            step.replay()
+            step.capture(h_dev, mode=mode, eps=w.eps, delta=w.delta, h_host=h_host,
+                         outputs_to_host=True)
         s.synchronize()
-    e2e_dt = time.perf_counter() - t0
-    h2d = h.numel() * h.element_size()
-    d2h = sum(o.numel() * o.element_size() for o in outs)
-    L_host = step.host_out["L"].numpy().copy()
+        outs = list(step.host_out.values())
+        e2e_steps = max(args.steps, 10)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            with torch.cuda.stream(s):
+                P.copy_(P0)
+                step.replay()
+            s.synchronize()
+        out["e2e_dt"] = time.perf_counter() - t0
+        out["e2e_steps"] = e2e_steps
+        out["h2d"] = h.numel() * h.element_size()
+        out["d2h"] = sum(o.numel() * o.element_size() for o in outs)
+    del step, wt, h
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
+def summarise(r, world, steps, pk):
+    """Whole-job numbers and per-pass rooflines of one measured workload."""
+    w = r["w"]
+    ms_step = r["ms_total"] / steps
+    steps_per_s = whole_job_rate(world, steps, r["ms_total"] / 1e3)
+    mean_emit = float(np.mean(r["L"] + 1))
+    work = pass_work(w, r["N"], r["x"]["P"])
+    passes = {c: roofline_entry(work[c], r["per"][c], pk) for c in work}
+    total = dict(bytes=sum(v["bytes"] for v in work.values()),
+                 flops=sum(v["flops"] for v in work.values()))
+    step_rf = roofline_entry(total, ms_step / 1e3, pk)
+    dominant = max(r["per"], key=lambda c: r["per"][c])
+    return dict(steps_per_s=steps_per_s, ms_per_step=ms_step,
+                accepted_tok_per_s=steps_per_s * w.B * mean_emit,
+                mean_tokens_per_step=mean_emit, passes=passes, step=step_rf,
+                dominant=dominant)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    import speculative_decoding_08_b300 as mds
+    from speculative_decoding_08_b300 import build as mbuild
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}: launch one rank per GPU")
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    if rank == 0 or world == 1:
+        mbuild.build()
+    if world > 1:
+        dist.barrier()
+    mds.load()
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    pk = peaks()
+
+    head_w = ms.workload(args.workload)
+    also = [] if args.also == "none" else [n for n in args.also.split(",") if n != head_w.name]
+    clocks = Clocks(dev.index)
+    clocks.start()
+    time.sleep(0.3)
+    results = {}
+    for name in also:
+        results[name] = measure(ms.workload(name), args, dev, world, e2e=False)
+    head = measure(head_w, args, dev, world, e2e=True)
+    clk = clocks.stop()
 
     # max over ranks (device-timed steps and the end-to-end loop)
-    ms_total, e2e_dt = rank_max([ms_total, e2e_dt], dev)
+    keys = [head["ms_total"], head["e2e_dt"]] + [results[n]["ms_total"] for n in also]
+    keys = rank_max(keys, dev)
+    head["ms_total"], head["e2e_dt"] = keys[0], keys[1]
+    for n, v in zip(also, keys[2:]):
+        results[n]["ms_total"] = v
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return
-    ms_step = ms_total / args.steps
-    steps_per_s = whole_job_rate(world, args.steps, ms_total / 1e3)
-    mean_emit = float(np.mean(L_host + 1))
-    pk = peaks()
-    lmv_bytes = lm_verify_bytes(w, N)
-    lmv_s = per["lm_verify"] / 1e3
-    achieved = lmv_bytes / lmv_s / 1e9
-    sb = step_bytes(w, N)
-    prefix_bytes = int(np.sum(x["P"])) * w.Hkv * w.dh * 2 * (2 if w.dtype == "bf16" else 4)
-    total_bytes = sb["heads"] + 2 * sb["lm"] + sb["qkv"] + sb["wo"] + prefix_bytes
+    sh = summarise(head, world, args.steps, pk)
+    dom = sh["dominant"]
+    rf = dict(sh["passes"][dom])
+    roofline = {"kernel": f"{dom} call at {head_w.name}", "bound": rf["bound"],
+                "achieved": rf["achieved"], "peak": rf["peak"], "unit": rf["unit"],
+                "frac": rf["frac"], "traffic": profiled_traffic(head_w.name, dom),
+                "peak_src": pk["src"] + (" bf16_tflops_sustained" if rf["bound"] == "tensor"
+                                         else " hbm_gbs"),
+                "algorithmic_bytes_per_launch": rf["algorithmic_bytes"],
+                "flops_per_launch": rf["flops"], "us_per_launch": rf["us"]}
+    w = head_w
+    N = head["N"]
     line = {
-        "metric": METRIC, "value": steps_per_s, "unit": "steps/s", "n_gpus": world,
-        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_step,
+        "metric": METRIC, "value": sh["steps_per_s"], "unit": "steps/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": sh["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic (seeded; value laws of the workload description)",
         "config": {"workload": w.name, "B": w.B, "d": w.d, "V": w.V, "Hq": w.Hq, "Hkv": w.Hkv,
-                   "dh": w.dh, "K": w.K, "shortlist": list(w.shortlist),
-                   "max_rank_sum": w.max_rank_sum, "prefix": list(w.P), "accept": w.accept,
+                   "dh": w.dh, "K": w.K, "shortlist": list(w.shortlist), "N": N,
+                   "max_rank_sum": w.max_rank_sum, "prefix": list(w.P), "accept": "typical",
                    "parallelism": f"replicas x{world}", "cuda_graph": True,
-                   "l2": "per-step bytes (~%.0f MB) exceed the 126 MB L2; no flush" % (total_bytes / 1e6)},
-        "accepted_tok_per_s": steps_per_s * w.B * mean_emit,
-        "mean_tokens_per_step": mean_emit,
-        "step_hbm_gbs": total_bytes / (ms_step / 1e3) / 1e9,
-        "step_hbm_frac": total_bytes / (ms_step / 1e3) / 1e9 / pk["hbm"],
-        "per_call_us": {c: 1e3 * v for c, v in per.items()},
-        "roofline": {"kernel": "lm_verify call: k_gemm_tc<VERIFY> LM-projection stream over the "
-                               "verify rows + its statistics merge and child-logit gather",
-                     "bound": "hbm",
-                     "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
-                     "frac": achieved / pk["hbm"], "traffic": profiled_traffic(),
-                     "peak_src": pk["src"], "algorithmic_bytes_per_launch": lmv_bytes},
-        "gpu_launches": per_step_kernels * args.steps,
+                   "l2": "per-step bytes (~%.0f MB) exceed the 126 MB L2; no flush"
+                         % (sh["step"]["algorithmic_bytes"] / 1e6)},
+        "accepted_tok_per_s": sh["accepted_tok_per_s"],
+        "mean_tokens_per_step": sh["mean_tokens_per_step"],
+        "step_roofline": sh["step"],
+        "per_call_us": {c: 1e6 * v for c, v in head["per"].items()},
+        "passes": sh["passes"],
+        "roofline": roofline,
+        "gpu_launches": head["per_step_kernels"] * args.steps,
         "clocks": clk,
-        "e2e": {"value": whole_job_rate(world, e2e_steps, e2e_dt), "unit": "steps/s",
-                "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+        "e2e": {"value": whole_job_rate(world, head["e2e_steps"], head["e2e_dt"]),
+                "unit": "steps/s", "h2d_bytes_per_step": head["h2d"],
+                "d2h_bytes_per_step": head["d2h"]},
     }
+    wl = {}
+    for n in also:
+        s2 = summarise(results[n], world, args.steps, pk)
+        wl[n] = {"steps_per_s": s2["steps_per_s"], "ms_per_step": s2["ms_per_step"],
+                 "accepted_tok_per_s": s2["accepted_tok_per_s"],
+                 "mean_tokens_per_step": s2["mean_tokens_per_step"],
+                 "per_call_us": {c: 1e6 * v for c, v in results[n]["per"].items()},
+                 "passes": s2["passes"], "step_roofline": s2["step"], "dominant": s2["dominant"]}
+    if wl:
+        line["workloads"] = wl
     if not args.no_cpu_baseline:
-        cb, _, _, _ = oracle_sample(w, x, budget_s=args.cpu_budget)
+        cb, _, _, _ = oracle_sample(w, head["x"], budget_s=args.cpu_budget)
+        cb["one_core"] = one_core_baseline(w)
         line["cpu_baseline"] = cb
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
 
 
+def one_core_baseline(w):
+    """The oracle on one core: one timed oracle step in a child process whose
+    BLAS is limited to one thread (the limit must be set before numpy loads)."""
+    env = dict(os.environ)
+    for v in _THREAD_VARS:
+        env[v] = "1"
+    cmd = [sys.executable, os.path.abspath(__file__), "--impl", "reference", "--workload",
+           w.name, "--steps", "1", "--warmup", "0"]
+    try:
+        out = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=600)
+        j = json.loads(out.stdout.strip().splitlines()[-1])
+        return {"value": j["value"], "cores": j["cpu_baseline"]["cores"],
+                "sample": j["cpu_baseline"]["sample"]}
+    except Exception as e:  # reported, not fatal: the GPU numbers stand alone
+        return {"value": None, "error": f"{type(e).__name__}: {e}"[:200]}
+
+
+def relaunch(args):
+    """Start args.gpus ranks of this script (one replica per GPU)."""
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={args.gpus}", "--master-addr", "127.0.0.1",
+           f"--master-port={port}", os.path.abspath(__file__)] + sys.argv[1:]
+    return subprocess.call(cmd)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="vicuna7b-b1")
-    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--also", default=",".join(ALSO),
+                    help="other workloads measured in the same run (comma list, or none)")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        raise SystemExit(relaunch(args))
     w = ms.workload(args.workload)
     if args.impl == "reference":
         run_reference(args, w)
     else:
-        run_ours(args, w)
+        run_ours(args)
 
 
 if __name__ == "__main__":
