@@ -74,3 +74,51 @@ def paths_from_parents(parent):
             chain.append(int(parent[chain[-1]]))
         out.append(chain[::-1])
     return out
+
+
+def rope_complex(x, pos, dh, base):
+    """Rotary embedding in RoFormer's complex form: each head's pair
+    (x_{2i}, x_{2i+1}) is the complex number x_{2i} + i x_{2i+1}, multiplied
+    by exp(i pos theta_i), theta_i = base^(-2i/dh).  x [T, H*dh], pos [T]."""
+    T, HD = x.shape
+    z = x.reshape(T, HD // dh, dh // 2, 2)
+    zc = z[..., 0] + 1j * z[..., 1]
+    theta = np.array([base ** (-2.0 * i / dh) for i in range(dh // 2)])
+    rot = np.exp(1j * np.outer(np.asarray(pos, np.float64), theta))[:, None, :]
+    out = zc * rot
+    return np.stack([out.real, out.imag], axis=-1).reshape(T, HD)
+
+
+def causal_stack(prefix_ks, prefix_vs, P, tokens, emb, layers, Hq, Hkv, dh, base, kv=False):
+    """Sequential decoding's view of a token sequence placed at positions
+    P, P+1, ...: every layer rotates q and k to those positions, attends
+    causally over [its prefix ; the sequence] with a dense masked score matrix,
+    and adds Wo o to the residual stream.  Returns x_L [T, d]; with
+    ``kv=True`` also every layer's rotated k and v rows ([T, Hkv*dh] each)."""
+    x = emb[np.asarray(tokens)]
+    T = len(tokens)
+    pos = P + np.arange(T)
+    g = Hq // Hkv
+    ks, vs = [], []
+    for l, lw in enumerate(layers):
+        q = rope_complex(x @ lw["wq"].T, pos, dh, base)
+        k = rope_complex(x @ lw["wk"].T, pos, dh, base)
+        v = x @ lw["wv"].T
+        ks.append(k)
+        vs.append(v)
+        Pl = prefix_ks[l].shape[1]
+        S = Pl + T
+        o = np.zeros((T, Hq * dh))
+        for hq in range(Hq):
+            hk = hq // g
+            Kall = np.concatenate([prefix_ks[l][hk], k[:, hk * dh:(hk + 1) * dh]], axis=0)
+            Vall = np.concatenate([prefix_vs[l][hk], v[:, hk * dh:(hk + 1) * dh]], axis=0)
+            scores = np.full((T, S), -np.inf)
+            for t in range(T):
+                scores[t, :Pl + t + 1] = Kall[:Pl + t + 1] @ q[t, hq * dh:(hq + 1) * dh] / np.sqrt(dh)
+            scores -= scores.max(axis=1, keepdims=True)
+            wgt = np.exp(scores)
+            wgt /= wgt.sum(axis=1, keepdims=True)
+            o[:, hq * dh:(hq + 1) * dh] = wgt @ Vall
+        x = x + o @ lw["wo"].T
+    return (x, ks, vs) if kv else x

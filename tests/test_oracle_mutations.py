@@ -154,6 +154,39 @@ def gumbel_sign_flipped(logits, T, seed, words3):
     return logits / T - g
 
 
+def patched(name, repl, target):
+    """``target`` of the oracle module run with its ``name`` replaced."""
+    def f(*args, **kw):
+        orig = getattr(mo, name)
+        try:
+            setattr(mo, name, repl)
+            return getattr(mo, target)(*args, **kw)
+        finally:
+            setattr(mo, name, orig)
+    return f
+
+
+_backbone_layer = mo.backbone_layer
+
+
+def layer_positions_by_index(x, P, depth, *rest):
+    # position ids P_b + n (the node's index) instead of P_b + depth_n
+    return _backbone_layer(x, P, np.arange(len(depth)), *rest)
+
+
+def layer_no_residual(x, *rest):
+    r = _backbone_layer(x, *rest)
+    return dict(r, y=r["y"] - x)
+
+
+def rope_half_pairs(x, pos, dh, base):
+    # pairs (i, i + dh/2) instead of (2i, 2i + 1)
+    shp = x.shape
+    xr = x.reshape(shp[:-1] + (shp[-1] // dh, 2, dh // 2)).swapaxes(-1, -2)
+    y = mo.rope(xr.reshape(shp), pos, dh, base)
+    return y.reshape(shp[:-1] + (shp[-1] // dh, dh // 2, 2)).swapaxes(-1, -2).reshape(shp)
+
+
 CASES = [
     ("heads: sigmoid instead of SiLU", dict(heads_residual=heads_sigmoid_only), [pins.check_heads_torch]),
     ("heads: residual dropped", dict(heads_residual=heads_no_residual), [pins.check_zero_heads, pins.check_heads_torch]),
@@ -173,6 +206,9 @@ CASES = [
     ("philox: key not bumped between rounds", dict(philox4x64=philox_no_key_bump), [pins.check_philox_library]),
     ("sample: temperature ignored", dict(gumbel_keys=gumbel_no_temperature), [pins.check_sampler_distribution]),
     ("sample: Gumbel noise sign flipped", dict(gumbel_keys=gumbel_sign_flipped), [pins.check_sampler_distribution, pins.check_sampling_is_rejection_sampling]),
+    ("rope: pairs (i, i + dh/2)", dict(rope=rope_half_pairs), [pins.check_rope]),
+    ("backbone: position ids by node index", dict(backbone=patched("backbone_layer", layer_positions_by_index, "backbone")), [pins.check_backbone_per_path]),
+    ("backbone: residual stream dropped", dict(backbone=patched("backbone_layer", layer_no_residual, "backbone")), [pins.check_backbone_per_path]),
     ("decode: next hidden state from the root row", dict(decode=decode_with_hidden(hidden_of_root)), [pins.check_decode_greedy_lossless]),
     ("decode: next hidden state from the accepted node's parent", dict(decode=decode_with_hidden(hidden_of_parent)), [pins.check_decode_greedy_lossless]),
 ]

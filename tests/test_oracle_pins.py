@@ -693,3 +693,107 @@ def test_sampling_is_rejection_sampling():
 
 def test_sample_acceptance():
     check_sample_acceptance(oracle)
+
+
+# ---------------------------------------------------------------------------
+# The backbone pass over the tree: position ids as rotary embeddings and
+# several layers ("Medusa deep dive", From top-k heads to a sparse candidate
+# tree: a flat node sequence with an attention mask and position ids, pushed
+# through the backbone in one pass)
+# ---------------------------------------------------------------------------
+
+def check_rope(orc):
+    """RoFormer's complex form, norms preserved, and scores that depend only
+    on the distance between positions."""
+    rng = np.random.default_rng(4)
+    dh, H = 16, 3
+    x = rng.standard_normal((5, H * dh))
+    pos = np.array([0, 1, 7, 130, 4099])
+    np.testing.assert_allclose(orc.rope(x, pos, dh, 10000.0),
+                               brute.rope_complex(x, pos, dh, 10000.0), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(orc.rope(x, np.zeros(5), dh, 10000.0), x, rtol=0, atol=0)
+    r = orc.rope(x, pos, dh, 500.0)
+    np.testing.assert_allclose(np.linalg.norm(r.reshape(5, H, dh), axis=-1),
+                               np.linalg.norm(x.reshape(5, H, dh), axis=-1), rtol=1e-12)
+    q, k = rng.standard_normal((1, dh)), rng.standard_normal((1, dh))
+    for m, n, s in [(3, 1, 10), (100, 40, 7), (5, 5, 1000)]:
+        a = orc.rope(q, [m], dh, 10000.0) @ orc.rope(k, [n], dh, 10000.0).T
+        b = orc.rope(q, [m + s], dh, 10000.0) @ orc.rope(k, [n + s], dh, 10000.0).T
+        np.testing.assert_allclose(a, b, rtol=1e-9)
+
+
+def _backbone_case(seed, n_layers, shortlist=(3, 2, 2), mrs=-1, Hq=4, Hkv=2):
+    w, f, P = tiny(seed=seed, B=2, d=32, V=40, Hq=Hq, Hkv=Hkv, dh=8, shortlist=shortlist,
+                   mrs=mrs, P=(3, 9))
+    rng = np.random.default_rng(seed)
+    d, qd, kd = w.d, w.Hq * w.dh, w.Hkv * w.dh
+    layers = [dict(wq=rng.standard_normal((qd, d)) / np.sqrt(d),
+                   wk=rng.standard_normal((kd, d)) / np.sqrt(d),
+                   wv=rng.standard_normal((kd, d)) / np.sqrt(d),
+                   wo=rng.standard_normal((d, qd)) / np.sqrt(qd)) for _ in range(n_layers)]
+    kcs = [rng.standard_normal(f["kc"].shape) for _ in range(n_layers)]
+    vcs = [rng.standard_normal(f["vc"].shape) for _ in range(n_layers)]
+    return w, f, P, layers, kcs, vcs
+
+
+def check_backbone_per_path(orc, n_layers=3, base=10000.0):
+    """Every tree row of the L-layer pass equals sequential decoding's last
+    row for its root-to-node path placed at positions P_b, P_b + 1, ...
+    (brute force: a dense causal stack per path)."""
+    for seed, sl, mrs in [(1, (3, 2, 2), -1), (2, (8, 4, 2, 2, 1), 3)]:
+        w, f, P, layers, kcs, vcs = _backbone_case(seed, n_layers, sl, mrs)
+        tr = orc.build_tree(w.shortlist, w.max_rank_sum)
+        tok = ms.random_tokens(seed, w.B, tr["N"], w.V).astype(np.int64)
+        r = orc.backbone(tok, P, tr["depth"], tr["mask"], f["emb"], layers, kcs, vcs,
+                         w.Hq, w.Hkv, w.dh, "f32", base)
+        for b in range(w.B):
+            Pb = int(P[b])
+            pks = [kc[b][:, :Pb] for kc in kcs]
+            pvs = [vc[b][:, :Pb] for vc in vcs]
+            for n, chain in enumerate(brute.paths_from_parents(tr["parent"])):
+                xs = brute.causal_stack(pks, pvs, Pb, [int(tok[b, c]) for c in chain], f["emb"],
+                                        layers, w.Hq, w.Hkv, w.dh, base)
+                np.testing.assert_allclose(r["y"][b, n], xs[-1], rtol=1e-9, atol=1e-9)
+
+
+def check_backbone_compaction(orc, n_layers=2, base=10000.0):
+    """Committing an accepted path in every layer's cache leaves the rows
+    sequential decoding writes: the j-th node of the path has depth j, so its
+    key, rotated at P_b + j, lands in slot P_b + j unchanged."""
+    w, f, P, layers, kcs, vcs = _backbone_case(6, n_layers)
+    tr = orc.build_tree(w.shortlist, w.max_rank_sum)
+    tok = ms.random_tokens(6, w.B, tr["N"], w.V).astype(np.int64)
+    r = orc.backbone(tok, P, tr["depth"], tr["mask"], f["emb"], layers, kcs, vcs, w.Hq, w.Hkv,
+                     w.dh, "f32", base)
+    chains = brute.paths_from_parents(tr["parent"])
+    picks = [tr["tuples"].index((2, 1, 0)), tr["tuples"].index((1,))]
+    L = np.array([len(chains[n]) - 1 for n in picks])
+    path = np.full((w.B, w.K + 1), -1)
+    for b, n in enumerate(picks):
+        path[b, :L[b] + 1] = chains[n]
+    for b in range(w.B):
+        Pb = int(P[b])
+        _, ks, vs = brute.causal_stack([kc[b][:, :Pb] for kc in kcs], [vc[b][:, :Pb] for vc in vcs],
+                                       Pb, [int(tok[b, c]) for c in chains[picks[b]]], f["emb"],
+                                       layers, w.Hq, w.Hkv, w.dh, base, kv=True)
+        for l in range(n_layers):
+            lr = r["layers"][l]
+            kc, vc, Pn = orc.compact_kv(lr["kc"], lr["vc"], P, L, path)
+            assert Pn[b] == Pb + L[b] + 1
+            for j in range(L[b] + 1):
+                np.testing.assert_allclose(kc[b][:, Pb + j].reshape(-1), ks[l][j], rtol=1e-9,
+                                           atol=1e-9)
+                np.testing.assert_allclose(vc[b][:, Pb + j].reshape(-1), vs[l][j], rtol=1e-9,
+                                           atol=1e-9)
+
+
+def test_backbone_compaction():
+    check_backbone_compaction(oracle)
+
+
+def test_rope():
+    check_rope(oracle)
+
+
+def test_backbone_per_path():
+    check_backbone_per_path(oracle)
