@@ -185,6 +185,31 @@ def make_inputs(w: Workload, zero_heads: bool = False,
     return out
 
 
+def make_layers(w: Workload, n_layers: int, x: Optional[Dict[str, np.ndarray]] = None):
+    """Weights and KV caches of an n_layers-deep verifier backbone: layer 0 is
+    the single verify layer of make_inputs (``x``, drawn if not given);
+    layer l >= 1 draws its Wq, Wk, Wv, Wo, K-prefix and V-prefix with the same
+    laws from tensor ids 100 l + (4..9).  Returns a list of dicts with wq, wk,
+    wv, wo, wqkv, kc, vc (stored values, like make_inputs)."""
+    if x is None:
+        x = make_inputs(w, only=("wq", "wk", "wv", "wo", "kc", "vc"))
+    d, qd, kd = w.d, w.Hq * w.dh, w.Hkv * w.dh
+    shapes = {
+        "wq": ((qd, d), 1.0 / np.sqrt(d)), "wk": ((kd, d), 1.0 / np.sqrt(d)),
+        "wv": ((kd, d), 1.0 / np.sqrt(d)), "wo": ((d, qd), 1.0 / np.sqrt(qd)),
+        "kc": ((w.B, w.Hkv, w.pmax, w.dh), 1.0), "vc": ((w.B, w.Hkv, w.pmax, w.dh), 1.0),
+    }
+    layers = [{k: x[k] for k in ("wq", "wk", "wv", "wo", "wqkv", "kc", "vc")}]
+    for l in range(1, n_layers):
+        lw = {}
+        for name, (shape, scale) in shapes.items():
+            v = _normal(w.seed, 100 * l + TENSOR_IDS[name], shape, scale)
+            lw[name] = bf16_bits(v) if w.dtype == "bf16" else v
+        lw["wqkv"] = np.concatenate([lw["wq"], lw["wk"], lw["wv"]], axis=0)
+        layers.append(lw)
+    return layers
+
+
 def as_f64(x: np.ndarray, dtype: str) -> np.ndarray:
     """Stored input values as float64 (exact)."""
     if dtype == "bf16":

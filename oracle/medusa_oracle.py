@@ -390,8 +390,17 @@ def step(w, f64: Dict[str, np.ndarray], P: np.ndarray, mode: str,
     dr = draft(U, f64["lm"], w.shortlist)
     tr = build_tree(w.shortlist, w.max_rank_sum)
     tok = fill_tokens(dr["root"], dr["topk_id"], tr["depth"], tr["rank"])
-    at = tree_attention(tok, Psel, tr["mask"], f64["emb"], f64["wq"], f64["wk"],
-                        f64["wv"], f64["wo"], kc, vc, w.Hq, w.Hkv, w.dh, w.dtype)
+    if "layers" in f64:
+        # the backbone form of the verify pass (R13b, R13c): f64["layers"] =
+        # per-layer dicts wq, wk, wv, wo, kc, vc; f64["rope_base"]
+        lay = f64["layers"]
+        bb = backbone(tok, Psel, tr["depth"], tr["mask"], f64["emb"], lay,
+                      [lw["kc"][sel] for lw in lay], [lw["vc"][sel] for lw in lay],
+                      w.Hq, w.Hkv, w.dh, w.dtype, f64["rope_base"])
+        at = dict(bb["layers"][-1], layers=bb["layers"])
+    else:
+        at = tree_attention(tok, Psel, tr["mask"], f64["emb"], f64["wq"], f64["wk"],
+                            f64["wv"], f64["wo"], kc, vc, w.Hq, w.Hkv, w.dh, w.dtype)
     st = verify_stats(at["y"], f64["lm"], tok, tr["parent"])
     if mode == "sample":
         seq = sampling[2] if len(sampling) > 2 else None
@@ -400,8 +409,12 @@ def step(w, f64: Dict[str, np.ndarray], P: np.ndarray, mode: str,
     lp = longest_path(ok, tr["parent"], tr["depth"],
                       st["sample"] if mode == "sample" else st["argmax"], w.K)
     kc2, vc2, Pn = compact_kv(at["kc"], at["vc"], Psel, lp["L"], lp["path"])
-    return dict(batch=sel, U=U, draft=dr, tree=tr, tok=tok, attn=at, stats=st,
-                ok=ok, margin=margin, path=lp, kc=kc2, vc=vc2, P=Pn)
+    out = dict(batch=sel, U=U, draft=dr, tree=tr, tok=tok, attn=at, stats=st,
+               ok=ok, margin=margin, path=lp, kc=kc2, vc=vc2, P=Pn)
+    if "layers" in f64:
+        out["layers_kv"] = [compact_kv(r["kc"], r["vc"], Psel, lp["L"], lp["path"])[:2]
+                            for r in at["layers"]]
+    return out
 
 
 # ----------------------------------------------------------------------------
@@ -438,6 +451,8 @@ def decode(w, f64: Dict[str, np.ndarray], P: np.ndarray, mode: str, n_steps: int
     cur["h"] = f64["h"][sel]
     cur["kc"] = f64["kc"][sel]
     cur["vc"] = f64["vc"][sel]
+    if "layers" in f64:
+        cur["layers"] = [dict(lw, kc=lw["kc"][sel], vc=lw["vc"][sel]) for lw in f64["layers"]]
     Pc = np.asarray(P)[sel].astype(np.int64)
     idx = list(range(len(sel)))
     out = []
@@ -449,6 +464,9 @@ def decode(w, f64: Dict[str, np.ndarray], P: np.ndarray, mode: str, n_steps: int
         cur = dict(cur)
         cur["h"] = next_hidden(r["attn"]["y"], r["path"]["L"], r["path"]["path"])
         cur["kc"], cur["vc"] = r["kc"], r["vc"]
+        if "layers" in cur:
+            cur["layers"] = [dict(lw, kc=kv[0], vc=kv[1])
+                             for lw, kv in zip(cur["layers"], r["layers_kv"])]
         Pc = r["P"]
     return out
 
@@ -647,3 +665,59 @@ def backbone(tok: np.ndarray, P: np.ndarray, depth: np.ndarray, mask: np.ndarray
         outs.append(r)
         x = r["y"]
     return dict(layers=outs, y=x, y_exact=outs[-1]["y_exact"])
+
+
+# ----------------------------------------------------------------------------
+# MTP-style draft heads.  [SD2] "MTP": the same layout as Medusa (a shared
+# trunk, n parallel heads on h_t, one shared unembedding f_u), with
+# P(x_{t+i} | x_<=t) = softmax(f_u(f_{h_i}(h_t))), where the heads f_{h_i}
+# are transformer layers instead of a single MLP; decoding then uses them
+# with Medusa's tree and verification.
+#   R22 Head i is one transformer layer with its own weights and KV cache:
+#       attention as a backbone layer (R13b, R13c: rotary positions, residual
+#       stream) followed by an MLP with a residual, u = a + W2_i SiLU(W1_i a)
+#       (no norm; the pages name none); f_u is the shared LM projection.
+#       Its attention needs the trunk's hidden states at earlier positions:
+#       each step hands the heads the hidden states of the last step's
+#       accepted tokens (y at the accepted path nodes, positions
+#       P_b .. P_b + L) as a chain; their keys and values enter each head's
+#       cache at those positions, and the output at the last of them (the
+#       position of h) drafts head i.  The first step of a loop hands them h
+#       alone, at position P_b - 1 (the last committed position).  Row 0 of
+#       the draft is h itself (the base head), as for Medusa.
+# ----------------------------------------------------------------------------
+
+def mtp_heads(xrows: np.ndarray, L: np.ndarray, P0: np.ndarray,
+              heads: Sequence[Dict[str, np.ndarray]], Hq: int, Hkv: int, dh: int,
+              dtype: str, rope_base: float) -> Dict[str, object]:
+    """xrows [B, R, d]: hidden states at positions P0_b + j, valid for
+    j <= L_b (later rows are padding, their outputs unused).  heads: per head
+    wq, wk, wv, wo, w1 [dff, d], w2 [d, dff], kc, vc.  Returns U [B, K+1, d]
+    (U[b, 0] = xrows[b, L_b]; U[b, i] = head i's output at row L_b) and the
+    heads' caches with rows P0_b .. P0_b + R - 1 written (R22)."""
+    B, R, d = xrows.shape
+    K = len(heads)
+    depth = np.arange(R)
+    chain = np.tril(np.ones((R, R), bool))
+    U = np.empty((B, K + 1, d))
+    U[:, 0] = xrows[np.arange(B), np.asarray(L, np.int64)]
+    caches = []
+    for i, hw in enumerate(heads):
+        r = backbone_layer(xrows, P0, depth, chain, hw["wq"], hw["wk"], hw["wv"], hw["wo"],
+                           hw["kc"], hw["vc"], Hq, Hkv, dh, dtype, rope_base)
+        a = r["y"][np.arange(B), np.asarray(L, np.int64)]             # [B, d]
+        t = maybe_round(silu(a @ hw["w1"].T), dtype)
+        U[:, i + 1] = maybe_round(a + t @ hw["w2"].T, dtype)
+        caches.append((r["kc"], r["vc"]))
+    return dict(U=U, caches=caches)
+
+
+def accepted_rows(y: np.ndarray, L: np.ndarray, path: np.ndarray, K: int) -> np.ndarray:
+    """[B, K+1, d]: y at the accepted path's nodes, the last one repeated
+    past L (padding rows)."""
+    B = y.shape[0]
+    out = np.empty((B, K + 1, y.shape[2]))
+    for b in range(B):
+        for j in range(K + 1):
+            out[b, j] = y[b, int(path[b, min(j, int(L[b]))])]
+    return out

@@ -89,14 +89,17 @@ def rope_complex(x, pos, dh, base):
     return np.stack([out.real, out.imag], axis=-1).reshape(T, HD)
 
 
-def causal_stack(prefix_ks, prefix_vs, P, tokens, emb, layers, Hq, Hkv, dh, base, kv=False):
+def causal_stack(prefix_ks, prefix_vs, P, tokens, emb, layers, Hq, Hkv, dh, base, kv=False,
+                 x_rows=None):
     """Sequential decoding's view of a token sequence placed at positions
     P, P+1, ...: every layer rotates q and k to those positions, attends
     causally over [its prefix ; the sequence] with a dense masked score matrix,
     and adds Wo o to the residual stream.  Returns x_L [T, d]; with
     ``kv=True`` also every layer's rotated k and v rows ([T, Hkv*dh] each)."""
-    x = emb[np.asarray(tokens)]
-    T = len(tokens)
+    # x_rows: the sequence's input rows given directly (hidden states rather
+    # than token embeddings)
+    x = emb[np.asarray(tokens)] if x_rows is None else np.asarray(x_rows, np.float64)
+    T = x.shape[0]
     pos = P + np.arange(T)
     g = Hq // Hkv
     ks, vs = [], []
@@ -122,3 +125,20 @@ def causal_stack(prefix_ks, prefix_vs, P, tokens, emb, layers, Hq, Hkv, dh, base
             o[:, hq * dh:(hq + 1) * dh] = wgt @ Vall
         x = x + o @ lw["wo"].T
     return (x, ks, vs) if kv else x
+
+
+def greedy_decode_stack(prefix_ks, prefix_vs, P, first, steps, emb, layers, lm, Hq, Hkv, dh,
+                        base):
+    """Sequential greedy decoding with the layered verifier: x_0 = first,
+    x_{t+1} = argmax(LMproj . stack(x_0..x_t)[-1]), the whole stack recomputed
+    from scratch at every step."""
+    seq = [int(first)]
+    for _ in range(steps):
+        xs = causal_stack(prefix_ks, prefix_vs, P, seq, emb, layers, Hq, Hkv, dh, base)
+        logits = lm @ xs[-1]
+        best = 0
+        for t in range(1, logits.shape[0]):
+            if logits[t] > logits[best]:
+                best = t
+        seq.append(best)
+    return seq

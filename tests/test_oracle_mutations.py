@@ -187,6 +187,21 @@ def rope_half_pairs(x, pos, dh, base):
     return y.reshape(shp[:-1] + (shp[-1] // dh, dh // 2, 2)).swapaxes(-1, -2).reshape(shp)
 
 
+_mtp_heads = mo.mtp_heads
+
+
+def mtp_row_zero(xrows, L, P0, *rest):
+    # every head's output taken at the first row instead of the last accepted
+    return _mtp_heads(xrows, np.zeros_like(L), P0, *rest)
+
+
+def mtp_mlp_no_residual(xrows, L, P0, heads, *rest):
+    r = _mtp_heads(xrows, L, P0, heads, *rest)
+    zero_w2 = [dict(hw, w2=np.zeros_like(hw["w2"])) for hw in heads]
+    a = _mtp_heads(xrows, L, P0, zero_w2, *rest)["U"]
+    return dict(r, U=np.concatenate([r["U"][:, :1], r["U"][:, 1:] - a[:, 1:]], axis=1))
+
+
 CASES = [
     ("heads: sigmoid instead of SiLU", dict(heads_residual=heads_sigmoid_only), [pins.check_heads_torch]),
     ("heads: residual dropped", dict(heads_residual=heads_no_residual), [pins.check_zero_heads, pins.check_heads_torch]),
@@ -209,6 +224,8 @@ CASES = [
     ("rope: pairs (i, i + dh/2)", dict(rope=rope_half_pairs), [pins.check_rope]),
     ("backbone: position ids by node index", dict(backbone=patched("backbone_layer", layer_positions_by_index, "backbone")), [pins.check_backbone_per_path]),
     ("backbone: residual stream dropped", dict(backbone=patched("backbone_layer", layer_no_residual, "backbone")), [pins.check_backbone_per_path]),
+    ("mtp: output at the first row, not the last accepted", dict(mtp_heads=mtp_row_zero), [pins.check_mtp_heads]),
+    ("mtp: residual around the MLP dropped", dict(mtp_heads=mtp_mlp_no_residual), [pins.check_mtp_heads, pins.check_mtp_zero_heads]),
     ("decode: next hidden state from the root row", dict(decode=decode_with_hidden(hidden_of_root)), [pins.check_decode_greedy_lossless]),
     ("decode: next hidden state from the accepted node's parent", dict(decode=decode_with_hidden(hidden_of_parent)), [pins.check_decode_greedy_lossless]),
 ]

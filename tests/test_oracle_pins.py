@@ -797,3 +797,102 @@ def test_rope():
 
 def test_backbone_per_path():
     check_backbone_per_path(oracle)
+
+
+def check_decode_backbone_lossless(orc, seed=12, n_layers=2, n_steps=3):
+    """The decoding loop with a 2-layer backbone and greedy acceptance emits
+    exactly sequential greedy decoding of that backbone (positions and both
+    layers' caches carried across steps)."""
+    w, f, P = tiny(seed=seed, B=2, d=64, V=8, Hq=2, Hkv=1, dh=64, shortlist=(3, 2, 2),
+                   P=(5, 12))
+    x = ms.make_inputs(w)
+    f["layers"] = [{k: ms.as_f64(v, w.dtype) for k, v in lw.items()}
+                   for lw in ms.make_layers(w, n_layers, x)]
+    f["rope_base"] = 500.0
+    rs = orc.decode(w, f, P, "greedy", n_steps)
+    for b in range(w.B):
+        emitted = sum((r["emitted"][b] for r in rs), [])
+        Pb = int(P[b])
+        seq = brute.greedy_decode_stack([lw["kc"][b][:, :Pb] for lw in f["layers"]],
+                                        [lw["vc"][b][:, :Pb] for lw in f["layers"]], Pb,
+                                        emitted[0], len(emitted), f["emb"], f["layers"], f["lm"],
+                                        w.Hq, w.Hkv, w.dh, f["rope_base"])
+        assert emitted + [int(rs[-1]["path"]["next_root"][b])] == seq
+
+
+def test_decode_backbone_lossless():
+    check_decode_backbone_lossless(oracle)
+
+
+# ---------------------------------------------------------------------------
+# MTP-style draft heads ("Speculative Decoding Deep Dive II: Medusa, MTP",
+# section "MTP": transformer-layer heads on h_t with a shared unembedding)
+# ---------------------------------------------------------------------------
+
+def _mtp_case(seed, K=3, d=32, dff=48, Hq=4, Hkv=2, dh=8, B=2, zero=False):
+    rng = np.random.default_rng(seed)
+    qd, kd = Hq * dh, Hkv * dh
+    heads = []
+    for _ in range(K):
+        hw = dict(wq=rng.standard_normal((qd, d)) / np.sqrt(d),
+                  wk=rng.standard_normal((kd, d)) / np.sqrt(d),
+                  wv=rng.standard_normal((kd, d)) / np.sqrt(d),
+                  wo=rng.standard_normal((d, qd)) / np.sqrt(qd),
+                  w1=rng.standard_normal((dff, d)) / np.sqrt(d),
+                  w2=rng.standard_normal((d, dff)) / np.sqrt(dff),
+                  kc=rng.standard_normal((B, Hkv, 64, dh)),
+                  vc=rng.standard_normal((B, Hkv, 64, dh)))
+        if zero:
+            hw["wo"] = np.zeros_like(hw["wo"])
+            hw["w2"] = np.zeros_like(hw["w2"])
+        heads.append(hw)
+    xrows = rng.standard_normal((B, K + 1, d))
+    L = np.array([2, 0][:B] + [1] * max(0, B - 2))
+    P0 = np.array([5, 11][:B] + [7] * max(0, B - 2))
+    return heads, xrows, L, P0, Hq, Hkv, dh
+
+
+def check_mtp_heads(orc, base=10000.0):
+    """Head i's output at the last accepted row equals a dense causal
+    attention layer over its cache's prefix and the accepted rows (positions
+    P0_b, P0_b + 1, ...), with the residual, followed by x + W2 SiLU(W1 x)
+    computed with torch; the rows' rotated keys and values are in the cache."""
+    heads, xrows, L, P0, Hq, Hkv, dh = _mtp_case(3)
+    r = orc.mtp_heads(xrows, L, P0, heads, Hq, Hkv, dh, "f32", base)
+    for b in range(xrows.shape[0]):
+        Lb, Pb = int(L[b]), int(P0[b])
+        np.testing.assert_array_equal(r["U"][b, 0], xrows[b, Lb])
+        for i, hw in enumerate(heads):
+            lay = [dict(wq=hw["wq"], wk=hw["wk"], wv=hw["wv"], wo=hw["wo"])]
+            a, ks, vs = brute.causal_stack([hw["kc"][b][:, :Pb]], [hw["vc"][b][:, :Pb]], Pb, None,
+                                           None, lay, Hq, Hkv, dh, base, kv=True,
+                                           x_rows=xrows[b, :Lb + 1])
+            at = torch.from_numpy(a[-1])
+            u = at + torch.nn.functional.silu(at @ torch.from_numpy(hw["w1"]).T) @ \
+                torch.from_numpy(hw["w2"]).T
+            np.testing.assert_allclose(r["U"][b, i + 1], u.numpy(), rtol=1e-9, atol=1e-9)
+            kc, vc = r["caches"][i]
+            for j in range(Lb + 1):
+                np.testing.assert_allclose(kc[b][:, Pb + j].reshape(-1), ks[0][j], rtol=1e-9,
+                                           atol=1e-9)
+                np.testing.assert_allclose(vc[b][:, Pb + j].reshape(-1), vs[0][j], rtol=1e-9,
+                                           atol=1e-9)
+            np.testing.assert_array_equal(kc[b][:, :Pb], hw["kc"][b][:, :Pb])
+
+
+def check_mtp_zero_heads(orc):
+    """With Wo = 0 and W2 = 0 a head passes its input through: every head's
+    output is h (the input at the last accepted row)."""
+    heads, xrows, L, P0, Hq, Hkv, dh = _mtp_case(4, zero=True)
+    r = orc.mtp_heads(xrows, L, P0, heads, Hq, Hkv, dh, "f32", 500.0)
+    for b in range(xrows.shape[0]):
+        for i in range(len(heads) + 1):
+            np.testing.assert_array_equal(r["U"][b, i], xrows[b, int(L[b])])
+
+
+def test_mtp_heads():
+    check_mtp_heads(oracle)
+
+
+def test_mtp_zero_heads():
+    check_mtp_zero_heads(oracle)
