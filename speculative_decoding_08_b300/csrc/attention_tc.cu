@@ -179,6 +179,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kWC = kBN / 2;                            // keys per softmax warp
   constexpr uint32_t kSCol0 = 0;                          // S: 2 x kBN columns
   constexpr uint32_t kOCol0 = 2 * kBN;                    // O: NM x DH columns
+  // One query tile per unit: each warp of a pair keeps its own running
+  // maximum, sum and accumulator for its half of every key tile (O_0 for
+  // keys [0, 64), O_1 = the next DH columns for keys [64, 128)), so the pair
+  // never waits on each other inside the tile loop; the two halves are
+  // combined once per segment.  Several query tiles have no TMEM room for a
+  // second accumulator and exchange the row maximum every tile instead.
+  constexpr bool kSplitO = NM == 1;
+  static_assert(!kSplitO || 2 * kBN + 2 * DH <= 512, "TMEM columns");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -365,10 +373,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t bV = ptx::smem_addr(sKV + pv_stage * kStageBytes + kHalves * kKVHalfBytes);
         const uint32_t dO = tmem + kOCol0 + (uint32_t)(pv_m * DH);
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          ptx::mma_bf16(dO, ptx::sdesc_k128(aP + (kk >> 2) * 16384 + (kk & 3) * 32),
-                        sdesc_mn128(bV + kk * 2048, kKVHalfBytes),
-                        idO, (pv_first && kk == 0) ? 0u : 1u);
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          // split accumulators: keys [0, 64) into O_0, [64, 128) into O_1
+          const bool second = kSplitO && kk >= 4;
+          const bool fresh = pv_first && (kk == 0 || (kSplitO && kk == 4));
+          ptx::mma_bf16(dO + (second ? (uint32_t)DH : 0u),
+                        ptx::sdesc_k128(aP + (kk >> 2) * 16384 + (kk & 3) * 32),
+                        sdesc_mn128(bV + kk * 2048, kKVHalfBytes), idO, fresh ? 0u : 1u);
+        }
         ptx::mma_commit(&p_empty[pb]);
         if (pv_lastm) ptx::mma_commit(&v_empty[pv_stage]);
       }
@@ -526,22 +538,26 @@ __global__ void __launch_bounds__(kThreads, 1)
               mx = fmaxf(mx, sv[c]);
             }
           }
-          mx = fmaxf(mx, exchange(mx));                  // row maximum over all 64 keys
-          if (!ok) break;
+          if constexpr (!kSplitO) {
+            mx = fmaxf(mx, exchange(mx));                // row maximum over both halves
+            if (!ok) break;
+          }
           mx *= a.scale_log2;
           const float mold = mref[m];
           const float mnew = fmaxf(mold, mx);
-          // both warps of the pair see the same maximum and decide alike
+          // shared accumulator: both warps of the pair see the same maximum
+          // and decide alike; split accumulators: each warp for its own
           const bool need = mold != -INFINITY && mnew > mold + kRescaleLog2;
           if (__any_sync(0xffffffffu, need)) {
             const float f = need ? ex2(mold - mnew) : 1.f;
-            if (half == 0) {
+            if (kSplitO || half == 0) {
               // rescale this tile's O: every earlier P V must be complete.  The
               // commit on p_empty after P V (it - 1) covers all earlier MMAs;
               // P V (it - 3) was awaited one item ago, so the phase is exact.
               if (!wait(&p_empty[(it - 1) % kNP], ((it - 1) / kNP) & 1)) break;
               ptx::tc_fence_after();
-              const uint32_t ocol = lane_base + kOCol0 + (uint32_t)(m * DH);
+              const uint32_t ocol =
+                  lane_base + kOCol0 + (uint32_t)((kSplitO ? half : m) * DH);
 #pragma unroll
               for (int cb = 0; cb < DH / 32; ++cb) {
                 float ov[32];
@@ -601,10 +617,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!whole) slot = 2 * cta + (cta_start(Ttot, a.G, cta) >= s.U0 ? 0 : 1);
       const int rows_unit = NM * 128;
       float ltot[kMaxNM];
+      // split accumulators: weights of O_0 and O_1 relative to the combined
+      // maximum mcomb (a half that saw no visible key has weight 0)
+      float w_o[2] = {1.f, 0.f}, mcomb = mref[0];
+      if constexpr (kSplitO) {
+        const float mo = exchange(mref[0]);
+        const float lo = exchange(lsum[0]);
+        if (!ok) break;
+        mcomb = fmaxf(mref[0], mo);
+        const float ws = mref[0] == -INFINITY ? 0.f : ex2(mref[0] - mcomb);
+        const float wo = mo == -INFINITY ? 0.f : ex2(mo - mcomb);
+        ltot[0] = lsum[0] * ws + lo * wo;
+        w_o[half] = ws;
+        w_o[half ^ 1] = wo;
+      } else {
 #pragma unroll
-      for (int m = 0; m < kMaxNM; ++m)
-        if (m < NM) ltot[m] = lsum[m] + exchange(lsum[m]);
-      if (!ok) break;
+        for (int m = 0; m < kMaxNM; ++m)
+          if (m < NM) ltot[m] = lsum[m] + exchange(lsum[m]);
+        if (!ok) break;
+      }
       // every P V of the segment is complete once P V (it - 1) is
       if (!wait(&p_empty[(it - 1) % kNP], ((it - 1) / kNP) & 1)) break;
       ptx::tc_fence_after();
@@ -623,6 +654,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int cb = 0; cb < kHalfCols / 32; ++cb) {
             float ov[32];
             ptx::tmem_ld32(ocol + cb * 32, ov);
+            if constexpr (kSplitO) {
+              float o1[32];
+              ptx::tmem_ld32(ocol + DH + cb * 32, o1);
+#pragma unroll
+              for (int c = 0; c < 32; ++c) ov[c] = ov[c] * w_o[0] + o1[c] * w_o[1];
+            }
             if (dst) {
 #pragma unroll
               for (int q = 0; q < 4; ++q) {
@@ -643,6 +680,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int cb = 0; cb < kHalfCols / 32; ++cb) {
             float ov[32];
             ptx::tmem_ld32(ocol + cb * 32, ov);
+            if constexpr (kSplitO) {
+              float o1[32];
+              ptx::tmem_ld32(ocol + DH + cb * 32, o1);
+#pragma unroll
+              for (int c = 0; c < 32; ++c) ov[c] = ov[c] * w_o[0] + o1[c] * w_o[1];
+            }
             if (live[m]) {
 #pragma unroll
               for (int q = 0; q < 8; ++q)
@@ -650,7 +693,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     make_float4(ov[4 * q], ov[4 * q + 1], ov[4 * q + 2], ov[4 * q + 3]);
             }
           }
-          if (live[m] && half == 0) *reinterpret_cast<float2*>(pml) = make_float2(mref[m], ltot[m]);
+          if (live[m] && half == 0)
+            *reinterpret_cast<float2*>(pml) = make_float2(kSplitO ? mcomb : mref[m], ltot[m]);
         }
       }
       if (!ok) break;
