@@ -18,6 +18,11 @@
  *   mds_verify_accept    per-edge test + longest accepted path    [GL], [GU], [DD]
  *   mds_compact_kv       commit the accepted path's KV            [GL] KV cache, rollback
  *   mds_next_inputs      next step's hidden state / draft        [GL] decoding loop
+ *   mds_mtp_heads        transformer-layer draft heads            [SD2] "MTP"
+ *                        (in place of mds_medusa_heads)
+ * Backbone form of the verify pass (several layers with position ids):
+ * mds_embed_tokens, then mds_backbone_layer once per layer, in place of
+ * mds_tree_attention ([DD] tree with mask and position ids).
  * Fused steady-state form: mds_lm_verify_draft replaces mds_lm_verify and
  * drafts the next step in the same LM-projection stream (the next step then
  * skips mds_medusa_heads).
@@ -87,6 +92,7 @@ typedef enum {
 } mds_status;
 
 typedef enum { MDS_F32 = 0, MDS_BF16 = 1 } mds_dtype;
+
 
 /* Device error codes latched in the workspace status word. */
 enum {
@@ -205,6 +211,42 @@ MDS_API int mds_tree_attention(int dtype, int B, int N, int d, int V, int Hq, in
                        void* Kc, void* Vc, void* o_out, void* y,
                        void* ws, size_t ws_bytes, void* stream);
 
+/* Token fill and embedding gather alone (the first step of
+ * mds_tree_attention): when root != NULL, tok[b,0] = root[b] and
+ * tok[b,n] = topk_id[b, depth[n]-1, rank[n]] are written first; then
+ * x[b,n,:] = emb[tok[b,n],:].  A token outside [0, V) latches
+ * MDS_DEV_TOKEN_RANGE and leaves its row unwritten.
+ *   x  device [B, N, d] (dtype)  out.  Other arguments as in
+ *      mds_tree_attention; ws needs no scratch (8192 bytes suffice). */
+MDS_API int mds_embed_tokens(int dtype, int B, int N, int d, int V, int K, int smax, int32_t* tok,
+                     const int32_t* root, const int32_t* topk_id, const int32_t* depth,
+                     const int32_t* rank, const void* emb, void* x, void* ws, size_t ws_bytes,
+                     void* stream);
+
+/* One backbone layer over the tree rows, with their position ids ([DD]
+ * "From top-k heads to a sparse candidate tree": the tree is a flat node
+ * sequence with an attention mask and position ids, pushed through the
+ * backbone in one forward pass).  Node n of sequence b sits at position
+ * P_b + depth[n]; q and k are rotated to it (rotary embedding, RoFormer: the
+ * pair (2i, 2i+1) of every head turns by pos * rope_base^(-2i/dh)), k and v
+ * are written to cache slots P_b + n (the cache holds rotated keys; a
+ * committed path's j-th node has depth j and lands at P_b + j, where its
+ * rotation is already right), the attention is that of mds_tree_attention,
+ * and the output is added to the residual stream:
+ *   y = x + (o Wo^T)             (bf16; no norm or MLP)
+ *   x     device [B, N, d]       the layer's input rows (x_0 = the tree
+ *                                tokens' embeddings, mds_embed_tokens)
+ *   y     device [B, N, d]       out; must not alias x
+ *   depth device [N]             from mds_build_tree_mask
+ *   Kc, Vc, wqkv, wo, mask, P, o_out   as in mds_tree_attention, per layer
+ *   ws: mds_backbone_workspace_size(B, N, d, Hq, Hkv, dh) bytes.  bf16 only. */
+MDS_API size_t mds_backbone_workspace_size(int B, int N, int d, int Hq, int Hkv, int dh);
+MDS_API int mds_backbone_layer(int dtype, int B, int N, int d, int Hq, int Hkv, int dh, int Pmax,
+                       const int32_t* P, const int32_t* depth, const uint64_t* mask, int words,
+                       const void* x, const void* wqkv, const void* wo, double rope_base,
+                       void* Kc, void* Vc, void* o_out, void* y, void* ws, size_t ws_bytes,
+                       void* stream);
+
 /* Verify logits l = LMproj y for every tree row and the statistics the
  * acceptance test needs ([DD] "Typical acceptance": entropy H of the model's
  * distribution at the step; temperature 1, natural log).
@@ -318,6 +360,10 @@ MDS_API int mds_compact_kv(int dtype, int B, int Hkv, int dh, int Pmax, int K, c
  *                                     out: tree_topk_id/val[b, a] from
  *                                     mds_lm_verify_draft (the next step's
  *                                     shortlists)
+ *   rows_out  device [B, K+1, d] or NULL  out: y[b, path[b, j]] for
+ *                                     j = 0..K, the last accepted row
+ *                                     repeated past L (the accepted tokens'
+ *                                     hidden states, for mds_mtp_heads)
  *   y device [B, N, d] (dtype), L, path, next_root as produced above.
  *   An accepted node outside [0, N) latches MDS_DEV_TREE_INDEX (L outside
  *   [0, K]: MDS_DEV_PATH_LENGTH) and leaves that sequence's outputs as
@@ -325,8 +371,41 @@ MDS_API int mds_compact_kv(int dtype, int B, int Hkv, int dh, int Pmax, int K, c
 MDS_API int mds_next_inputs(int dtype, int B, int N, int K, int smax, int d, const int32_t* L,
                     const int32_t* path, const int32_t* next_root, const void* y,
                     const int32_t* tree_topk_id, const float* tree_topk_val, void* h_next,
-                    int32_t* root_out, int32_t* topk_id_out, float* topk_val_out, void* ws,
-                    size_t ws_bytes, void* stream);
+                    int32_t* root_out, int32_t* topk_id_out, float* topk_val_out,
+                    void* rows_out, void* ws, size_t ws_bytes, void* stream);
+
+/* MTP-style draft heads ([SD2] "MTP": n heads on h_t that are transformer
+ * layers, with one shared unembedding, used with Medusa's tree and
+ * verification).  Head i is one transformer layer with its own weights and
+ * KV cache: the attention of mds_backbone_layer (rotary positions, residual)
+ * followed by an MLP with a residual, u = a + W2_i SiLU(W1_i a); the shared
+ * LM projection then drafts from u as mds_medusa_heads does from its
+ * residual blocks.  The layer's attention needs the trunk's hidden states at
+ * earlier positions, so each call takes the hidden states of the last
+ * step's accepted tokens as a chain:
+ *   xrows  device [B, K+1, d]  rows at positions P0_b + j; rows past L_b
+ *                              are padding (mds_next_inputs rows_out)
+ *   L      device [B]          index of the last valid row (h itself)
+ *   P0     device [B]          position of row 0 (the step's prefix length
+ *                              before compaction; P_b - 1 with h alone)
+ *   chain_depth device [K+1], chain_mask device [K+1] uint64: the chain tree
+ *                              (mds_build_tree_mask with shortlist 1,...,1)
+ *   wqkv, wo, w1 [dff, d], w2 [d, dff], Kc, Vc: HOST arrays of K device
+ *                              pointers, one per head (caches as in
+ *                              mds_tree_attention; the rows' keys and values
+ *                              are written at slots P0_b + j)
+ *   lm, shortlist, smax, U, root, topk_id, topk_val: as in mds_medusa_heads
+ *                              (U row 0 = xrows[b, L_b], row i = u_i)
+ *   ws: mds_mtp_workspace_size(B, K, d, dff, Hq, Hkv, dh) bytes.  bf16 only;
+ *   dff % 64 == 0. */
+MDS_API size_t mds_mtp_workspace_size(int B, int K, int d, int dff, int Hq, int Hkv, int dh);
+MDS_API int mds_mtp_heads(int dtype, int B, int K, int d, int dff, int V, int Hq, int Hkv, int dh,
+                  int Pmax, const void* xrows, const int32_t* L, const int32_t* P0,
+                  const int32_t* chain_depth, const uint64_t* chain_mask,
+                  const void* const* wqkv, const void* const* wo, const void* const* w1,
+                  const void* const* w2, void* const* Kc, void* const* Vc, double rope_base,
+                  const void* lm, const int32_t* shortlist, int smax, void* U, int32_t* root,
+                  int32_t* topk_id, float* topk_val, void* ws, size_t ws_bytes, void* stream);
 
 /* Number of kernels this library has enqueued since it was loaded (a host
  * counter; launches captured into a CUDA graph count once, at capture). */

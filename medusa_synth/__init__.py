@@ -210,6 +210,28 @@ def make_layers(w: Workload, n_layers: int, x: Optional[Dict[str, np.ndarray]] =
     return layers
 
 
+def make_mtp_heads(w: Workload, dff: int):
+    """Weights and KV caches of K MTP-style draft heads (one transformer layer
+    each): head i draws Wq, Wk, Wv, Wo with the verify layer's laws, W1
+    [dff, d] ~ N(0, 1/d), W2 [d, dff] ~ N(0, 1/dff) and its K/V prefix
+    ~ N(0, 1), from tensor ids 300 + 10 i + (0..7).  Returns a list of dicts
+    with wq, wk, wv, wo, wqkv, w1, w2, kc, vc (stored values)."""
+    d, qd, kd = w.d, w.Hq * w.dh, w.Hkv * w.dh
+    shapes = [("wq", (qd, d), 1.0 / np.sqrt(d)), ("wk", (kd, d), 1.0 / np.sqrt(d)),
+              ("wv", (kd, d), 1.0 / np.sqrt(d)), ("wo", (d, qd), 1.0 / np.sqrt(qd)),
+              ("w1", (dff, d), 1.0 / np.sqrt(d)), ("w2", (d, dff), 1.0 / np.sqrt(dff)),
+              ("kc", (w.B, w.Hkv, w.pmax, w.dh), 1.0), ("vc", (w.B, w.Hkv, w.pmax, w.dh), 1.0)]
+    heads = []
+    for i in range(w.K):
+        hw = {}
+        for t, (name, shape, scale) in enumerate(shapes):
+            v = _normal(w.seed, 300 + 10 * i + t, shape, scale)
+            hw[name] = bf16_bits(v) if w.dtype == "bf16" else v
+        hw["wqkv"] = np.concatenate([hw["wq"], hw["wk"], hw["wv"]], axis=0)
+        heads.append(hw)
+    return heads
+
+
 def as_f64(x: np.ndarray, dtype: str) -> np.ndarray:
     """Stored input values as float64 (exact)."""
     if dtype == "bf16":

@@ -386,7 +386,15 @@ def step(w, f64: Dict[str, np.ndarray], P: np.ndarray, mode: str,
     kc = f64["kc"][sel]
     vc = f64["vc"][sel]
     Psel = np.asarray(P)[sel]
-    U = heads_residual(h, f64["W"], w.dtype)
+    mtp = None
+    if "mtp" in f64:
+        # MTP-style heads (R22): f64["mtp"] = dict(heads, rows, L, P0, rope_base)
+        m = f64["mtp"]
+        mtp = mtp_heads(m["rows"], m["L"], m["P0"], m["heads"], w.Hq, w.Hkv, w.dh, w.dtype,
+                        m["rope_base"])
+        U = mtp["U"]
+    else:
+        U = heads_residual(h, f64["W"], w.dtype)
     dr = draft(U, f64["lm"], w.shortlist)
     tr = build_tree(w.shortlist, w.max_rank_sum)
     tok = fill_tokens(dr["root"], dr["topk_id"], tr["depth"], tr["rank"])
@@ -414,6 +422,8 @@ def step(w, f64: Dict[str, np.ndarray], P: np.ndarray, mode: str,
     if "layers" in f64:
         out["layers_kv"] = [compact_kv(r["kc"], r["vc"], Psel, lp["L"], lp["path"])[:2]
                             for r in at["layers"]]
+    if mtp is not None:
+        out["mtp"] = mtp
     return out
 
 
@@ -453,6 +463,15 @@ def decode(w, f64: Dict[str, np.ndarray], P: np.ndarray, mode: str, n_steps: int
     cur["vc"] = f64["vc"][sel]
     if "layers" in f64:
         cur["layers"] = [dict(lw, kc=lw["kc"][sel], vc=lw["vc"][sel]) for lw in f64["layers"]]
+    if "mtp" in f64:
+        # the first step hands the MTP heads h alone, at position P_b - 1 (the
+        # rows past it are padding: copies of h)
+        m = f64["mtp"]
+        cur["mtp"] = dict(m, heads=[dict(hw, kc=hw["kc"][sel], vc=hw["vc"][sel])
+                                    for hw in m["heads"]],
+                          rows=np.repeat(cur["h"][:, None, :], w.K + 1, axis=1),
+                          L=np.zeros(len(sel), np.int64),
+                          P0=np.asarray(P)[sel].astype(np.int64) - 1)
     Pc = np.asarray(P)[sel].astype(np.int64)
     idx = list(range(len(sel)))
     out = []
@@ -467,6 +486,13 @@ def decode(w, f64: Dict[str, np.ndarray], P: np.ndarray, mode: str, n_steps: int
         if "layers" in cur:
             cur["layers"] = [dict(lw, kc=kv[0], vc=kv[1])
                              for lw, kv in zip(cur["layers"], r["layers_kv"])]
+        if "mtp" in cur:
+            cur["mtp"] = dict(cur["mtp"],
+                              heads=[dict(hw, kc=kv[0], vc=kv[1]) for hw, kv in
+                                     zip(cur["mtp"]["heads"], r["mtp"]["caches"])],
+                              rows=accepted_rows(r["attn"]["y"], r["path"]["L"],
+                                                 r["path"]["path"], w.K),
+                              L=r["path"]["L"].copy(), P0=Pc.copy())
         Pc = r["P"]
     return out
 
@@ -701,15 +727,17 @@ def mtp_heads(xrows: np.ndarray, L: np.ndarray, P0: np.ndarray,
     chain = np.tril(np.ones((R, R), bool))
     U = np.empty((B, K + 1, d))
     U[:, 0] = xrows[np.arange(B), np.asarray(L, np.int64)]
+    U_exact = U.copy()
     caches = []
     for i, hw in enumerate(heads):
         r = backbone_layer(xrows, P0, depth, chain, hw["wq"], hw["wk"], hw["wv"], hw["wo"],
                            hw["kc"], hw["vc"], Hq, Hkv, dh, dtype, rope_base)
         a = r["y"][np.arange(B), np.asarray(L, np.int64)]             # [B, d]
         t = maybe_round(silu(a @ hw["w1"].T), dtype)
-        U[:, i + 1] = maybe_round(a + t @ hw["w2"].T, dtype)
+        U_exact[:, i + 1] = a + t @ hw["w2"].T
+        U[:, i + 1] = maybe_round(U_exact[:, i + 1], dtype)
         caches.append((r["kc"], r["vc"]))
-    return dict(U=U, caches=caches)
+    return dict(U=U, U_exact=U_exact, caches=caches)
 
 
 def accepted_rows(y: np.ndarray, L: np.ndarray, path: np.ndarray, K: int) -> np.ndarray:

@@ -34,6 +34,10 @@ _SIGS = {
     "mds_medusa_heads_noalloc": ([_c_int] * 4 + [_p] * 4 + [_c_int] + [_p] * 6, _c_int),
     "mds_tree_attention": ([_c_int] * 11 + [_p] * 7 + [_c_int] + [_p] * 8 + [_c_size, _p],
                            _c_int),
+    "mds_embed_tokens": ([_c_int] * 7 + [_p] * 8 + [_c_size, _p], _c_int),
+    "mds_backbone_workspace_size": ([_c_int] * 6, _c_size),
+    "mds_backbone_layer": ([_c_int] * 8 + [_p] * 3 + [_c_int] + [_p] * 3 + [ctypes.c_double]
+                           + [_p] * 5 + [_c_size, _p], _c_int),
     "mds_lm_verify": ([_c_int] * 5 + [_p] * 8 + [_c_size, _p], _c_int),
     "mds_verify_accept": ([_c_int] * 4 + [_c_float, _c_float] + [_p] * 11 + [_c_size, _p], _c_int),
     "mds_compact_kv": ([_c_int] * 6 + [_p] * 6 + [_c_size, _p], _c_int),
@@ -41,7 +45,10 @@ _SIGS = {
                              + [_c_size, _p], _c_int),
     "mds_verify_draft_workspace_size": ([_c_int] * 4, _c_size),
     "mds_lm_verify_draft": ([_c_int] * 6 + [_p] * 4 + [_c_int] + [_p] * 8 + [_c_size, _p], _c_int),
-    "mds_next_inputs": ([_c_int] * 6 + [_p] * 11 + [_c_size, _p], _c_int),
+    "mds_next_inputs": ([_c_int] * 6 + [_p] * 12 + [_c_size, _p], _c_int),
+    "mds_mtp_workspace_size": ([_c_int] * 7, _c_size),
+    "mds_mtp_heads": ([_c_int] * 10 + [_p] * 11 + [ctypes.c_double] + [_p] * 2 + [_c_int]
+                      + [_p] * 5 + [_c_size, _p], _c_int),
     "mds_launch_count": ([], ctypes.c_longlong),
     "mds_status_check": ([_p, _p, _p], _c_int),
 }
@@ -173,6 +180,32 @@ def tree_attention(P, tok, mask, emb, wqkv, wo, Kc, Vc, y, ws, *, Hq, Hkv, K, sm
     _check(rc, "tree_attention")
 
 
+def embed_tokens(tok, emb, x, ws, *, K, smax, root=None, topk_id=None, depth=None, rank=None):
+    B, N = tok.shape
+    V, d = emb.shape
+    rc = load().mds_embed_tokens(dtype_code(emb), B, N, d, V, K, smax, _ptr(tok), _ptr(root),
+                                 _ptr(topk_id), _ptr(depth), _ptr(rank), _ptr(emb), _ptr(x),
+                                 _ptr(ws), ws.numel(), _stream())
+    _check(rc, "embed_tokens")
+
+
+def backbone_workspace_size(B, N, d, Hq, Hkv, dh) -> int:
+    return load().mds_backbone_workspace_size(B, N, d, Hq, Hkv, dh)
+
+
+def backbone_layer(P, depth, mask, x, wqkv, wo, Kc, Vc, y, ws, *, Hq, Hkv, rope_base=10000.0,
+                   o_out=None):
+    B, N, d = x.shape
+    dh = Kc.shape[3]
+    Pmax = Kc.shape[2]
+    words = mask.numel() // N if mask.dim() == 1 else mask.shape[-1]
+    rc = load().mds_backbone_layer(dtype_code(x), B, N, d, Hq, Hkv, dh, Pmax, _ptr(P),
+                                   _ptr(depth), _ptr(mask), words, _ptr(x), _ptr(wqkv), _ptr(wo),
+                                   float(rope_base), _ptr(Kc), _ptr(Vc), _ptr(o_out), _ptr(y),
+                                   _ptr(ws), ws.numel(), _stream())
+    _check(rc, "backbone_layer")
+
+
 def lm_verify(y, lm, tok, parent, argmax, stats, childlogit, ws):
     B, N, d = y.shape
     V = lm.shape[0]
@@ -213,7 +246,7 @@ def lm_verify_draft(y, W, lm, shortlist, smax, tok, parent, argmax, stats, child
 
 def next_inputs(L, path, ws, *, N, smax, next_root=None, y=None, tree_topk_id=None,
                 tree_topk_val=None, h_next=None, root_out=None, topk_id_out=None,
-                topk_val_out=None):
+                topk_val_out=None, rows_out=None):
     B = L.shape[0]
     K = path.shape[1] - 1
     d = y.shape[2] if y is not None else 1
@@ -221,8 +254,35 @@ def next_inputs(L, path, ws, *, N, smax, next_root=None, y=None, tree_topk_id=No
     rc = load().mds_next_inputs(dt, B, N, K, smax, d, _ptr(L), _ptr(path), _ptr(next_root),
                                 _ptr(y), _ptr(tree_topk_id), _ptr(tree_topk_val), _ptr(h_next),
                                 _ptr(root_out), _ptr(topk_id_out), _ptr(topk_val_out),
-                                _ptr(ws), ws.numel(), _stream())
+                                _ptr(rows_out), _ptr(ws), ws.numel(), _stream())
     _check(rc, "next_inputs")
+
+
+def mtp_workspace_size(B, K, d, dff, Hq, Hkv, dh) -> int:
+    return load().mds_mtp_workspace_size(B, K, d, dff, Hq, Hkv, dh)
+
+
+def _ptr_array(ts):
+    return (ctypes.c_void_p * len(ts))(*[_ptr(t).value for t in ts])
+
+
+def mtp_heads(xrows, L, P0, chain_depth, chain_mask, heads, lm, shortlist, smax, U, root,
+              topk_id, topk_val, ws, *, Hq, Hkv, rope_base=10000.0):
+    """heads: list of K dicts with wqkv, wo, w1, w2, Kc, Vc (device tensors)."""
+    B, R, d = xrows.shape
+    K = R - 1
+    dff = heads[0]["w1"].shape[0]
+    V = lm.shape[0]
+    dh = heads[0]["Kc"].shape[3]
+    Pmax = heads[0]["Kc"].shape[2]
+    arr = {k: _ptr_array([hw[k] for hw in heads]) for k in ("wqkv", "wo", "w1", "w2", "Kc", "Vc")}
+    rc = load().mds_mtp_heads(dtype_code(xrows), B, K, d, dff, V, Hq, Hkv, dh, Pmax, _ptr(xrows),
+                              _ptr(L), _ptr(P0), _ptr(chain_depth), _ptr(chain_mask),
+                              arr["wqkv"], arr["wo"], arr["w1"], arr["w2"], arr["Kc"], arr["Vc"],
+                              float(rope_base), _ptr(lm), _i32(shortlist), smax, _ptr(U),
+                              _ptr(root), _ptr(topk_id), _ptr(topk_val), _ptr(ws), ws.numel(),
+                              _stream())
+    _check(rc, "mtp_heads")
 
 
 def verify_accept(mode, eps, delta, parent, depth, tok, argmax, stats, childlogit, L, path,
@@ -257,4 +317,4 @@ def status_check(ws) -> int:
     return out.value
 
 
-from .step import MedusaStep  # noqa: E402,F401
+from .step import BackboneStep, MedusaStep, MTPStep  # noqa: E402,F401

@@ -234,11 +234,11 @@ int mds_tree_attention(int dtype, int B, int N, int d, int V, int Hq, int Hkv, i
   if (dtype == MDS_BF16) {
     void* part = static_cast<char*>(q) + 2 * align_up(rows * Hq * 128 * esize(dtype));
     void* kpart = static_cast<char*>(part) + align_up(attention_tc_partial_bytes(N, Hq / Hkv, dh));
-    rc = gemm_tc_qkv(x, B, N, d, wqkv, Hq, Hkv, dh, Pmax, P, q, Kc, Vc, kpart, ws, st);
+    rc = gemm_tc_qkv(x, B, N, d, wqkv, Hq, Hkv, dh, Pmax, P, nullptr, q, Kc, Vc, kpart, ws, st);
     if (rc) return rc;
     rc = attention_tc(B, N, Hq, Hkv, dh, Pmax, P, mask, words, q, Kc, Vc, o, part, ws, st);
     if (rc) return rc;
-    return gemm_tc_store(o, (int)rows, wo, d, Hq * dh, y, d, kpart, ws, st);
+    return gemm_tc_store(o, (int)rows, wo, d, Hq * dh, y, d, nullptr, kpart, ws, st);
   }
   EpiArgs e;
   e.kind = EPI_QKV;
@@ -261,6 +261,62 @@ int mds_tree_attention(int dtype, int B, int N, int d, int V, int Hq, int Hkv, i
   eo.out = y;
   eo.ldo = d;
   return gemm_simple(dtype, o, (int)rows, wo, d, Hq * dh, eo, st);
+}
+
+int mds_embed_tokens(int dtype, int B, int N, int d, int V, int K, int smax, int32_t* tok,
+                     const int32_t* root, const int32_t* topk_id, const int32_t* depth,
+                     const int32_t* rank, const void* emb, void* x, void* ws, size_t ws_bytes,
+                     void* stream) {
+  if (!valid_dtype(dtype) || !tok || !emb || !x) return MDS_EINVAL;
+  if (root && (!topk_id || !depth || !rank)) return MDS_EINVAL;
+  if (B < 1 || N < 1 || d < 1 || V < 1 || K < 1 || smax < 1) return MDS_EINVAL;
+  if (N > kMaxN || K > kMaxK || smax > kMaxS) return MDS_EUNSUPPORTED;
+  if (!ws_ok(ws, ws_bytes, kWsScratch)) return MDS_EWORKSPACE;
+  return embed_gather(dtype, B, N, d, V, K, smax, tok, root, topk_id, depth, rank, emb, x, ws,
+                      as_stream(stream));
+}
+
+size_t mds_backbone_workspace_size(int B, int N, int d, int Hq, int Hkv, int dh) {
+  if (B < 1 || N < 1 || d < 1 || Hq < 1 || Hkv < 1 || dh < 2) return 0;
+  return need_attention(MDS_BF16, B, N, d, Hq, Hkv, dh) +
+         align_up((size_t)B * N * (dh / 2) * 8);
+}
+
+int mds_backbone_layer(int dtype, int B, int N, int d, int Hq, int Hkv, int dh, int Pmax,
+                       const int32_t* P, const int32_t* depth, const uint64_t* mask, int words,
+                       const void* x, const void* wqkv, const void* wo, double rope_base,
+                       void* Kc, void* Vc, void* o_out, void* y, void* ws, size_t ws_bytes,
+                       void* stream) {
+  if (!valid_dtype(dtype) || !P || !depth || !mask || !x || !wqkv || !wo || !Kc || !Vc || !y)
+    return MDS_EINVAL;
+  if (B < 1 || N < 1 || Hq < 1 || Hkv < 1 || Pmax < N) return MDS_EINVAL;
+  if (Hq % Hkv != 0 || !(rope_base > 1.0) || !(rope_base < 1e300)) return MDS_EINVAL;
+  if (x == y) return MDS_EINVAL;       // the residual is read while y is written
+  if (dtype != MDS_BF16) return MDS_EUNSUPPORTED;
+  if (N > kMaxN || !shape_ok(d, dh)) return MDS_EUNSUPPORTED;
+  if (words < (N + 63) / 64) return MDS_EINVAL;
+  if (!attention_tc_supported(B, N, Hq / Hkv, dh)) return MDS_EUNSUPPORTED;
+  if (!ws_ok(ws, ws_bytes, mds_backbone_workspace_size(B, N, d, Hq, Hkv, dh)))
+    return MDS_EWORKSPACE;
+  if (!aligned16(x) || !aligned16(wqkv) || !aligned16(wo) || !aligned16(Kc) || !aligned16(Vc) ||
+      !aligned16(y) || (o_out && !aligned16(o_out)))
+    return MDS_EINVAL;
+  cudaStream_t st = as_stream(stream);
+  const size_t rows = (size_t)B * N;
+  // scratch as for mds_tree_attention (its x region unused), then the table
+  char* base = scratch(ws);
+  void* q = base + align_up(rows * d * 2);
+  void* o = o_out ? o_out : static_cast<void*>(static_cast<char*>(q) + align_up(rows * Hq * 128 * 2));
+  void* part = static_cast<char*>(q) + 2 * align_up(rows * Hq * 128 * 2);
+  void* kpart = static_cast<char*>(part) + align_up(attention_tc_partial_bytes(N, Hq / Hkv, dh));
+  void* table = static_cast<char*>(ws) + need_attention(MDS_BF16, B, N, d, Hq, Hkv, dh);
+  int rc = rope_table(B, N, dh, P, depth, rope_base, table, st);
+  if (rc) return rc;
+  rc = gemm_tc_qkv(x, B, N, d, wqkv, Hq, Hkv, dh, Pmax, P, table, q, Kc, Vc, kpart, ws, st);
+  if (rc) return rc;
+  rc = attention_tc(B, N, Hq, Hkv, dh, Pmax, P, mask, words, q, Kc, Vc, o, part, ws, st);
+  if (rc) return rc;
+  return gemm_tc_store(o, (int)rows, wo, d, Hq * dh, y, d, x, kpart, ws, st);
 }
 
 int mds_lm_verify(int dtype, int B, int N, int d, int V, const void* y, const void* lm,
@@ -354,10 +410,10 @@ int mds_lm_verify_draft(int dtype, int B, int N, int d, int V, int K, const void
 int mds_next_inputs(int dtype, int B, int N, int K, int smax, int d, const int32_t* L,
                     const int32_t* path, const int32_t* next_root, const void* y,
                     const int32_t* tree_topk_id, const float* tree_topk_val, void* h_next,
-                    int32_t* root_out, int32_t* topk_id_out, float* topk_val_out, void* ws,
-                    size_t ws_bytes, void* stream) {
+                    int32_t* root_out, int32_t* topk_id_out, float* topk_val_out,
+                    void* rows_out, void* ws, size_t ws_bytes, void* stream) {
   if (!valid_dtype(dtype) || !L || !path) return MDS_EINVAL;
-  if (h_next && !y) return MDS_EINVAL;
+  if ((h_next || rows_out) && !y) return MDS_EINVAL;
   if (root_out && !next_root) return MDS_EINVAL;
   if (topk_id_out && !tree_topk_id) return MDS_EINVAL;
   if (topk_val_out && (!tree_topk_val || !topk_id_out)) return MDS_EINVAL;
@@ -365,8 +421,76 @@ int mds_next_inputs(int dtype, int B, int N, int K, int smax, int d, const int32
   if (N > kMaxN || K > kMaxK || smax > kMaxS) return MDS_EUNSUPPORTED;
   if (!ws_ok(ws, ws_bytes, kWsScratch)) return MDS_EWORKSPACE;
   return next_inputs(dtype, B, N, K, smax, d, L, path, next_root, y, tree_topk_id,
-                     tree_topk_val, h_next, root_out, topk_id_out, topk_val_out, ws,
+                     tree_topk_val, h_next, root_out, topk_id_out, topk_val_out, rows_out, ws,
                      as_stream(stream));
+}
+
+size_t mds_mtp_workspace_size(int B, int K, int d, int dff, int Hq, int Hkv, int dh) {
+  if (B < 1 || K < 1 || d < 1 || dff < 1 || Hq < 1 || Hkv < 1 || dh < 2) return 0;
+  const size_t R = (size_t)B * (K + 1);
+  return mds_backbone_workspace_size(B, K + 1, d, Hq, Hkv, dh) + align_up(R * d * 2) +
+         align_up((size_t)B * d * 2) + align_up((size_t)B * dff * 2) +
+         align_up(tc_partial_bytes(B * (K + 1), true));
+}
+
+int mds_mtp_heads(int dtype, int B, int K, int d, int dff, int V, int Hq, int Hkv, int dh,
+                  int Pmax, const void* xrows, const int32_t* L, const int32_t* P0,
+                  const int32_t* chain_depth, const uint64_t* chain_mask,
+                  const void* const* wqkv, const void* const* wo, const void* const* w1,
+                  const void* const* w2, void* const* Kc, void* const* Vc, double rope_base,
+                  const void* lm, const int32_t* shortlist, int smax, void* U, int32_t* root,
+                  int32_t* topk_id, float* topk_val, void* ws, size_t ws_bytes, void* stream) {
+  if (!valid_dtype(dtype) || !xrows || !L || !P0 || !chain_depth || !chain_mask || !wqkv ||
+      !wo || !w1 || !w2 || !Kc || !Vc || !lm || !shortlist || !U || !root || !topk_id ||
+      !topk_val)
+    return MDS_EINVAL;
+  if (B < 1 || K < 1 || dff < 1 || V < 2 || Hq < 1 || Hkv < 1 || smax < 1) return MDS_EINVAL;
+  if (Hq % Hkv != 0 || !(rope_base > 1.0) || !(rope_base < 1e300)) return MDS_EINVAL;
+  if (dtype != MDS_BF16) return MDS_EUNSUPPORTED;
+  if (K + 1 > kMaxN || K > kMaxK || smax > kMaxS || !shape_ok(d, dh) || dff % 64 != 0)
+    return MDS_EUNSUPPORTED;
+  if (!attention_tc_supported(B, K + 1, Hq / Hkv, dh)) return MDS_EUNSUPPORTED;
+  Shortlist sl{};
+  sl.K = K;
+  for (int i = 0; i < K; ++i) {
+    if (!wqkv[i] || !wo[i] || !w1[i] || !w2[i] || !Kc[i] || !Vc[i]) return MDS_EINVAL;
+    if (shortlist[i] < 1 || shortlist[i] > smax || shortlist[i] > V) return MDS_EINVAL;
+    if (!aligned16(wqkv[i]) || !aligned16(wo[i]) || !aligned16(w1[i]) || !aligned16(w2[i]) ||
+        !aligned16(Kc[i]) || !aligned16(Vc[i]))
+      return MDS_EINVAL;
+    sl.s[i] = shortlist[i];
+  }
+  if (!aligned16(xrows) || !aligned16(lm) || !aligned16(U)) return MDS_EINVAL;
+  const size_t need = mds_mtp_workspace_size(B, K, d, dff, Hq, Hkv, dh);
+  if (!ws_ok(ws, ws_bytes, need)) return MDS_EWORKSPACE;
+  cudaStream_t st = as_stream(stream);
+  const int N = K + 1;
+  const size_t bb = mds_backbone_workspace_size(B, N, d, Hq, Hkv, dh);
+  char* arows = static_cast<char*>(ws) + bb;                        // [B, K+1, d]
+  char* asel = arows + align_up((size_t)B * N * d * 2);             // [B, d]
+  char* tmid = asel + align_up((size_t)B * d * 2);                 // [B, dff]
+  char* part = tmid + align_up((size_t)B * dff * 2);               // draft records
+  __nv_bfloat16* Ub = static_cast<__nv_bfloat16*>(U);
+  const long long ustride = (long long)(K + 1) * d;
+  // row 0 of the draft: h, the input at the last accepted row
+  int rc = select_rows(B, N, d, L, xrows, Ub, ustride, ws, st);
+  if (rc) return rc;
+  for (int i = 0; i < K; ++i) {
+    // head i: attention over its cache and the accepted rows (a chain),
+    // then u = a + W2 SiLU(W1 a) at the last accepted row
+    rc = mds_backbone_layer(dtype, B, N, d, Hq, Hkv, dh, Pmax, P0, chain_depth, chain_mask, 1,
+                            xrows, wqkv[i], wo[i], rope_base, Kc[i], Vc[i], nullptr, arows, ws,
+                            bb, stream);
+    if (rc) return rc;
+    rc = select_rows(B, N, d, L, arows, asel, d, ws, st);
+    if (rc) return rc;
+    rc = gemm_tc_store(asel, B, w1[i], dff, d, tmid, dff, nullptr, nullptr, ws, st, true, false);
+    if (rc) return rc;
+    rc = gemm_tc_store(tmid, B, w2[i], d, dff, Ub + (long long)(1 + i) * d, ustride, asel,
+                       nullptr, ws, st, false, true, d);
+    if (rc) return rc;
+  }
+  return lm_draft_tc(U, B, K, d, lm, V, sl, smax, root, topk_id, topk_val, part, ws, st);
 }
 
 int mds_verify_accept(int B, int N, int K, int mode, float eps, float delta,

@@ -167,7 +167,8 @@ __global__ void __launch_bounds__(128) k_next_inputs(int N, int K, int smax, int
                                                      const int32_t* tree_topk_id,
                                                      const float* tree_topk_val, T* h_next,
                                                      int32_t* root_out, int32_t* topk_out,
-                                                     float* topk_val_out, void* ws) {
+                                                     float* topk_val_out, T* rows_out,
+                                                     void* ws) {
   const int b = blockIdx.x;
   const int Lb = L[b];
   int a = -1;
@@ -189,6 +190,20 @@ __global__ void __launch_bounds__(128) k_next_inputs(int N, int K, int smax, int
     }
   }
   if (root_out && threadIdx.x == 0) root_out[b] = next_root[b];
+  if (rows_out) {
+    // the accepted path's rows y[b, path[b, j]], j = 0..K, the last one
+    // repeated past L (the hidden states of the accepted tokens, in order)
+    for (int j = 0; j <= K; ++j) {
+      const int pj = path[(long long)b * (K + 1) + (j <= Lb ? j : Lb)];
+      if (pj < 0 || pj >= N) {
+        if (threadIdx.x == 0) latch_error(ws, MDS_DEV_TREE_INDEX);
+        continue;
+      }
+      const T* src = y + ((long long)b * N + pj) * d;
+      T* dst = rows_out + ((long long)b * (K + 1) + j) * d;
+      for (int i = threadIdx.x; i < d; i += blockDim.x) dst[i] = src[i];
+    }
+  }
   if (tree_topk_id && topk_out) {
     const long long src = ((long long)b * N + a) * K * smax;
     for (int i = threadIdx.x; i < K * smax; i += blockDim.x) {
@@ -204,18 +219,44 @@ __global__ void __launch_bounds__(128) k_next_inputs(int N, int K, int smax, int
 int next_inputs(int dtype, int B, int N, int K, int smax, int d, const int32_t* L,
                 const int32_t* path, const int32_t* next_root, const void* y,
                 const int32_t* tree_topk_id, const float* tree_topk_val, void* h_next,
-                int32_t* root_out, int32_t* topk_out, float* topk_val_out, void* ws,
-                cudaStream_t st) {
+                int32_t* root_out, int32_t* topk_out, float* topk_val_out, void* rows_out,
+                void* ws, cudaStream_t st) {
   if (dtype == MDS_F32)
     k_next_inputs<float><<<B, 128, 0, st>>>(N, K, smax, d, L, path, next_root,
                                             static_cast<const float*>(y), tree_topk_id,
                                             tree_topk_val, static_cast<float*>(h_next), root_out,
-                                            topk_out, topk_val_out, ws);
+                                            topk_out, topk_val_out,
+                                            static_cast<float*>(rows_out), ws);
   else
     k_next_inputs<__nv_bfloat16><<<B, 128, 0, st>>>(
         N, K, smax, d, L, path, next_root, static_cast<const __nv_bfloat16*>(y), tree_topk_id,
         tree_topk_val, static_cast<__nv_bfloat16*>(h_next), root_out, topk_out, topk_val_out,
-        ws);
+        static_cast<__nv_bfloat16*>(rows_out), ws);
+  MDS_LAUNCH_CHECK();
+  return MDS_OK;
+}
+
+namespace {
+__global__ void __launch_bounds__(128) k_select_rows(int R, int d, const int32_t* sel,
+                                                     const __nv_bfloat16* src,
+                                                     __nv_bfloat16* dst, long long stride,
+                                                     void* ws) {
+  const int b = blockIdx.x;
+  const int r = sel[b];
+  if (r < 0 || r >= R) {
+    if (threadIdx.x == 0) latch_error(ws, MDS_DEV_PATH_LENGTH);
+    return;
+  }
+  const __nv_bfloat16* s = src + ((long long)b * R + r) * d;
+  __nv_bfloat16* o = dst + (long long)b * stride;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) o[i] = s[i];
+}
+}  // namespace
+
+int select_rows(int B, int R, int d, const int32_t* sel, const void* src, void* dst,
+                long long dst_stride, void* ws, cudaStream_t st) {
+  k_select_rows<<<B, 128, 0, st>>>(R, d, sel, static_cast<const __nv_bfloat16*>(src),
+                                    static_cast<__nv_bfloat16*>(dst), dst_stride, ws);
   MDS_LAUNCH_CHECK();
   return MDS_OK;
 }

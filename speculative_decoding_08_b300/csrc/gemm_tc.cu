@@ -118,6 +118,16 @@ struct TcArgs {
   unsigned long long seed;
   int N, Hq, Hkv, dh, Pmax;
   const int32_t* P;
+  // QKV of a backbone layer: (cos, sin) of every tree row's rotation angles,
+  // [rows][dh / 2]; q and k pairs (2i, 2i+1) of each head are rotated
+  const float2* rope;
+  // STORE of a backbone layer: out = resid + Y (resid with row stride ldr,
+  // 0 = ldo; it may be out itself: every element is read by the thread that
+  // writes it)
+  const __nv_bfloat16* resid;
+  long long ldr;
+  // STORE: out = SiLU(Y) (the first projection of an MLP)
+  int act_silu;
   __nv_bfloat16* Kc;
   __nv_bfloat16* Vc;
   void* partial;
@@ -146,9 +156,18 @@ __device__ __forceinline__ Range cta_range(const TcArgs& a, int fr) {
 
 // ------------------------------------------------------------- epilogues
 __device__ __forceinline__ void epi_store(const TcArgs& a, int row, int f0, int nv,
-                                          const float (&v)[32]) {
+                                          const float (&vin)[32]) {
   __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out) + (long long)row * a.ldo + f0;
   const bool vec = (a.ldo % 8) == 0;
+  float v[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = a.act_silu ? silu(vin[j]) : vin[j];
+  if (a.resid) {
+    const __nv_bfloat16* x = a.resid + (long long)row * (a.ldr ? a.ldr : a.ldo) + f0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < nv) v[j] += __bfloat162float(x[j]);
+  }
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     if (vec && nv >= 8 * (q + 1)) {
@@ -243,11 +262,27 @@ __device__ __forceinline__ void epi_qkv(const TcArgs& a, int r, int f0, int nv,
       __nv_bfloat16* cache = which ? a.Vc : a.Kc;
       dst = cache + (((long long)b * a.Hkv + hk) * a.Pmax + Pb + n) * a.dh + c;
     }
+    float w[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) w[j] = v[16 * half + j];
+    if (a.rope && f < qd + kd) {
+      // rotary position: pair (c, c + 1) of the head, c = f mod dh even,
+      // rotated by the row's angle for pair index c / 2
+      const int c0 = (f < qd ? f : f - qd) % a.dh;
+      const float2* cs = a.rope + (long long)r * (a.dh / 2) + c0 / 2;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float2 t = cs[j];
+        const float x0 = w[2 * j], x1 = w[2 * j + 1];
+        w[2 * j] = x0 * t.x - x1 * t.y;
+        w[2 * j + 1] = x0 * t.y + x1 * t.x;
+      }
+    }
     if (nv >= 16 * (half + 1)) {
-      *reinterpret_cast<uint4*>(dst) = pack8(v + 16 * half);
-      *reinterpret_cast<uint4*>(dst + 8) = pack8(v + 16 * half + 8);
+      *reinterpret_cast<uint4*>(dst) = pack8(w);
+      *reinterpret_cast<uint4*>(dst + 8) = pack8(w + 8);
     } else {
-      for (int j = 0; 16 * half + j < nv; ++j) dst[j] = __float2bfloat16_rn(v[16 * half + j]);
+      for (int j = 0; 16 * half + j < nv; ++j) dst[j] = __float2bfloat16_rn(w[j]);
     }
   }
 }
@@ -1290,8 +1325,12 @@ int gemm_tc_heads(const void* h, int B, const void* W, int K, int d, void* U, bo
 }
 
 int gemm_tc_store(const void* X, int R, const void* W, int F, int Kd, void* out, long long ldo,
-                  void* kpart, void* ws, cudaStream_t st) {
+                  const void* resid, void* kpart, void* ws, cudaStream_t st, bool act_silu,
+                  bool dependent, long long ldr) {
   TcArgs a{};
+  a.resid = static_cast<const __nv_bfloat16*>(resid);
+  a.ldr = ldr;
+  a.act_silu = act_silu ? 1 : 0;
   a.kpart = static_cast<float*>(kpart);
   a.R = R;
   a.F = F;
@@ -1300,13 +1339,14 @@ int gemm_tc_store(const void* X, int R, const void* W, int F, int Kd, void* out,
   a.out = out;
   a.ldo = ldo;
   a.ws = ws;
-  return launch_tc(a, X, W, true, st);    // follows the attention merge
+  return launch_tc(a, X, W, dependent, st);
 }
 
 int gemm_tc_qkv(const void* x, int B, int N, int d, const void* wqkv, int Hq, int Hkv, int dh,
-                int Pmax, const int32_t* P, void* q, void* Kc, void* Vc, void* kpart, void* ws,
-                cudaStream_t st) {
+                int Pmax, const int32_t* P, const void* rope, void* q, void* Kc, void* Vc,
+                void* kpart, void* ws, cudaStream_t st) {
   TcArgs a{};
+  a.rope = static_cast<const float2*>(rope);
   a.kpart = static_cast<float*>(kpart);
   a.R = B * N;
   a.F = (Hq + 2 * Hkv) * dh;

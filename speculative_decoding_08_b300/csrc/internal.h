@@ -48,6 +48,7 @@ cudaError_t launch_kernel(void (*kernel)(P...), dim3 grid, dim3 block, size_t sm
 // address, sizes, strides and box, so an identical request gets an identical
 // map).  rank 2: dims {cols, rows}, box {64, box_rows}; rank 3: dims
 // {64, rows, cols / 64}, strides {cols * 2, 128}, box {64, box_rows, box_kb}.
+
 int tensor_map_bf16(CUtensorMap* out, const void* base, long long rows, int cols, int rank,
                     int box_rows, int box_kb);
 
@@ -112,8 +113,13 @@ int accept_path(int B, int N, int K, int mode, float eps, float delta, const int
 int next_inputs(int dtype, int B, int N, int K, int smax, int d, const int32_t* L,
                 const int32_t* path, const int32_t* next_root, const void* y,
                 const int32_t* tree_topk_id, const float* tree_topk_val, void* h_next,
-                int32_t* root_out, int32_t* topk_out, float* topk_val_out, void* ws,
-                cudaStream_t st);
+                int32_t* root_out, int32_t* topk_out, float* topk_val_out, void* rows_out,
+                void* ws, cudaStream_t st);
+
+// dst[b * dst_stride + :] = src[b, sel[b], :] for rows of d elements (bf16),
+// src [B, R, d]; sel outside [0, R) latches MDS_DEV_PATH_LENGTH.
+int select_rows(int B, int R, int d, const int32_t* sel, const void* src, void* dst,
+                long long dst_stride, void* ws, cudaStream_t st);
 
 int compact(int dtype, int B, int Hkv, int dh, int Pmax, int K, const int32_t* L,
             const int32_t* path, void* Kc, void* Vc, int32_t* P, void* ws, cudaStream_t st);
@@ -134,11 +140,19 @@ size_t tc_kpart_bytes(int R, int F, int Kd);
 // head_major = false: U [B, K+1, d]; true: U [K+1, B, d] (block 0 = h).
 int gemm_tc_heads(const void* h, int B, const void* W, int K, int d, void* U, bool head_major,
                   void* kpart, void* ws, cudaStream_t st);
+// resid (or null): out = resid + X W^T, resid with row stride ldr (0: ldo;
+// it may be out).  act_silu: out = SiLU(X W^T).  dependent: launched with
+// programmatic stream serialisation (never for the first kernel of a call).
 int gemm_tc_store(const void* X, int R, const void* W, int F, int Kd, void* out, long long ldo,
-                  void* kpart, void* ws, cudaStream_t st);
+                  const void* resid, void* kpart, void* ws, cudaStream_t st,
+                  bool act_silu = false, bool dependent = true, long long ldr = 0);
+// rope (or null): float2 (cos, sin) [B N][dh / 2]; q and k rows rotated.
 int gemm_tc_qkv(const void* x, int B, int N, int d, const void* wqkv, int Hq, int Hkv, int dh,
-                int Pmax, const int32_t* P, void* q, void* Kc, void* Vc, void* kpart, void* ws,
-                cudaStream_t st);
+                int Pmax, const int32_t* P, const void* rope, void* q, void* Kc, void* Vc,
+                void* kpart, void* ws, cudaStream_t st);
+// (cos, sin) of (P_b + depth_n) base^(-2i/dh) for every tree row, in fp64.
+int rope_table(int B, int N, int dh, const int32_t* P, const int32_t* depth, double base,
+               void* table, cudaStream_t st);
 int lm_draft_tc(const void* U, int B, int K, int d, const void* lm, int V, Shortlist sl, int smax,
                 int32_t* root, int32_t* topk_id, float* topk_val, void* partial, void* ws,
                 cudaStream_t st);

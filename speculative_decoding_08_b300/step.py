@@ -15,9 +15,10 @@ from typing import Dict, Optional, Sequence
 
 import torch
 
-from . import (BF16, F32, GREEDY, SAMPLE, TYPICAL, build_tree_mask, compact_kv, dtype_code,
-               lm_verify, lm_verify_draft, lm_verify_sample, medusa_heads, new_workspace,
-               next_inputs, tree_attention, tree_size, verify_accept,
+from . import (BF16, F32, GREEDY, SAMPLE, TYPICAL, backbone_layer, backbone_workspace_size,
+               build_tree_mask, compact_kv, dtype_code, embed_tokens, lm_verify,
+               lm_verify_draft, lm_verify_sample, medusa_heads, mtp_heads, mtp_workspace_size,
+               new_workspace, next_inputs, tree_attention, tree_size, verify_accept,
                verify_draft_workspace_size, workspace_size)
 
 
@@ -127,15 +128,41 @@ class MedusaStep:
         """Enqueue one step on the current stream (asynchronous).  mode GREEDY,
         TYPICAL or SAMPLE (exact sampling at ``temperature`` with key
         ``seed``)."""
+        self._draft(h)
+        self._verify_layers()
+        self._verify_and_accept(mode, eps, delta, temperature, seed)
+        if commit:
+            self._commit()
+
+    def _draft(self, h):
+        """The step's draft from hidden state h: U, root and shortlists."""
         medusa_heads(h, self.W, self.lm, self.shortlist, self.smax, self.U, self.root,
                      self.topk_id, self.topk_val, self.ws)
+
+    def _before_commit(self):
+        pass
+
+    def _next(self, h, fused):
+        """The next step's inputs (after the commit)."""
+        if fused:
+            next_inputs(self.L, self.path, self.ws, N=self.N, smax=self.smax,
+                        next_root=self.next_root, y=self.y, tree_topk_id=self.tree_topk_id,
+                        tree_topk_val=self.tree_topk_val, h_next=h, root_out=self.root,
+                        topk_id_out=self.topk_id, topk_val_out=self.topk_val)
+        else:
+            next_inputs(self.L, self.path, self.ws, N=self.N, smax=self.smax, y=self.y,
+                        h_next=h)
+
+    def _verify_layers(self):
+        """Token fill and the verify layer(s): y for every tree row."""
         tree_attention(self.P, self.tok, self.mask, self.emb, self.wqkv, self.wo, self.Kc,
                        self.Vc, self.y, self.ws, Hq=self.Hq, Hkv=self.Hkv, K=self.K,
                        smax=self.smax, root=self.root, topk_id=self.topk_id, depth=self.depth,
                        rank=self.rank)
-        self._verify_and_accept(mode, eps, delta, temperature, seed)
-        if commit:
-            compact_kv(self.L, self.path, self.Kc, self.Vc, self.P, self.ws)
+
+    def _commit(self):
+        """Commit the accepted path's KV and advance P."""
+        compact_kv(self.L, self.path, self.Kc, self.Vc, self.P, self.ws)
 
     def _verify_and_accept(self, mode, eps, delta, temperature, seed, fused=False):
         if fused:
@@ -178,7 +205,8 @@ class MedusaStep:
     FUSED_MAX_ROWS = 512
 
     def fused_auto(self) -> bool:
-        return self.fused_ok and self.B * self.N * (self.K + 1) <= self.FUSED_MAX_ROWS
+        return (self.fused_ok and self.W is not None
+                and self.B * self.N * (self.K + 1) <= self.FUSED_MAX_ROWS)
 
     def begin_decode(self, h: torch.Tensor, fused: bool) -> None:
         """Before the first step of a loop: the fused form drafts the first
@@ -187,8 +215,7 @@ class MedusaStep:
         if fused:
             if not self.fused_ok:
                 raise ValueError("the fused verify pass needs bf16 weights")
-            medusa_heads(h, self.W, self.lm, self.shortlist, self.smax, self.U, self.root,
-                         self.topk_id, self.topk_val, self.ws)
+            self._draft(h)
 
     def decode_step(self, h: torch.Tensor, fused: bool, mode: int = TYPICAL, eps: float = 0.09,
                     delta: float = 0.3, temperature: float = 1.0, seed: int = 0) -> None:
@@ -197,22 +224,12 @@ class MedusaStep:
         step's hidden state) and, in the fused form, root / topk_id /
         topk_val (the next step's draft)."""
         if not fused:
-            medusa_heads(h, self.W, self.lm, self.shortlist, self.smax, self.U, self.root,
-                         self.topk_id, self.topk_val, self.ws)
-        tree_attention(self.P, self.tok, self.mask, self.emb, self.wqkv, self.wo, self.Kc,
-                       self.Vc, self.y, self.ws, Hq=self.Hq, Hkv=self.Hkv, K=self.K,
-                       smax=self.smax, root=self.root, topk_id=self.topk_id, depth=self.depth,
-                       rank=self.rank)
+            self._draft(h)
+        self._verify_layers()
         self._verify_and_accept(mode, eps, delta, temperature, seed, fused)
-        compact_kv(self.L, self.path, self.Kc, self.Vc, self.P, self.ws)
-        if fused:
-            next_inputs(self.L, self.path, self.ws, N=self.N, smax=self.smax,
-                        next_root=self.next_root, y=self.y, tree_topk_id=self.tree_topk_id,
-                        tree_topk_val=self.tree_topk_val, h_next=h, root_out=self.root,
-                        topk_id_out=self.topk_id, topk_val_out=self.topk_val)
-        else:
-            next_inputs(self.L, self.path, self.ws, N=self.N, smax=self.smax, y=self.y,
-                        h_next=h)
+        self._before_commit()
+        self._commit()
+        self._next(h, fused)
 
     def decode(self, h: torch.Tensor, n_steps: int, fused="auto", mode: int = TYPICAL,
                eps: float = 0.09, delta: float = 0.3, record: bool = False,
@@ -232,3 +249,119 @@ class MedusaStep:
                 out.append(dict(L=self.L.cpu(), path=self.path.cpu(), tok=self.tok.cpu(),
                                 next_root=self.next_root.cpu()))
         return out
+
+
+class BackboneStep(MedusaStep):
+    """A Medusa step whose verify pass is a backbone of several layers with
+    the tree's position ids ("Medusa deep dive", "From top-k heads to a
+    sparse candidate tree": the tree is a flat node sequence with an attention
+    mask and position ids, pushed through the backbone in one pass).
+
+    ``layers``: one dict per layer with ``wqkv`` [(Hq + 2 Hkv) dh, d], ``wo``
+    [d, Hq dh], ``Kc``, ``Vc`` [B, Hkv, Pmax, dh] (each layer's own cache).
+    x_0 = Emb[tok]; layer l: q, k rotated to P_b + depth_n, attention, and
+    x_l = x_{l-1} + Wo_l o_l; the verify logits read x_L.  Every layer's
+    cache gets the accepted path committed.  bf16 only."""
+
+    def __init__(self, *, layers, rope_base: float = 10000.0, **kw):
+        l0 = layers[0]
+        super().__init__(wqkv=l0["wqkv"], wo=l0["wo"], Kc=l0["Kc"], Vc=l0["Vc"], **kw)
+        if self.dtype != torch.bfloat16:
+            raise ValueError("the backbone form of the verify pass is bf16 only")
+        self.layers = list(layers)
+        self.rope_base = float(rope_base)
+        dev = self.lm.device
+        shape = (self.B, self.N, self.d)
+        self.xbuf = [torch.empty(shape, dtype=self.dtype, device=dev) for _ in range(2)]
+        self.P_scratch = torch.empty_like(self.P)
+        need = backbone_workspace_size(self.B, self.N, self.d, self.Hq, self.Hkv, self.dh)
+        if need > self.ws.numel():
+            self.ws = new_workspace(need, dev)
+
+    def _verify_layers(self):
+        embed_tokens(self.tok, self.emb, self.xbuf[0], self.ws, K=self.K, smax=self.smax,
+                     root=self.root, topk_id=self.topk_id, depth=self.depth, rank=self.rank)
+        L = len(self.layers)
+        for l, lw in enumerate(self.layers):
+            src = self.xbuf[l % 2]
+            dst = self.y if l == L - 1 else self.xbuf[(l + 1) % 2]
+            backbone_layer(self.P, self.depth, self.mask, src, lw["wqkv"], lw["wo"], lw["Kc"],
+                           lw["Vc"], dst, self.ws, Hq=self.Hq, Hkv=self.Hkv,
+                           rope_base=self.rope_base)
+
+    def _commit(self):
+        # every layer's cache takes the path at the same P; P advances once
+        for lw in self.layers[:-1]:
+            self.P_scratch.copy_(self.P)
+            compact_kv(self.L, self.path, lw["Kc"], lw["Vc"], self.P_scratch, self.ws)
+        last = self.layers[-1]
+        compact_kv(self.L, self.path, last["Kc"], last["Vc"], self.P, self.ws)
+
+
+class MTPStep(MedusaStep):
+    """A Medusa step drafted by MTP-style heads ("Speculative Decoding Deep
+    Dive II: Medusa, MTP", section "MTP": n heads on h_t that are transformer
+    layers, one shared unembedding, used with Medusa's tree and verification).
+
+    ``heads``: K dicts with ``wqkv``, ``wo`` (attention, as a backbone layer),
+    ``w1`` [dff, d], ``w2`` [d, dff] (the MLP) and ``Kc``, ``Vc`` (the head's
+    own cache).  Each draft hands the heads the hidden states of the last
+    step's accepted tokens (h alone, at position P_b - 1, for the first step
+    of a loop).  The separate form of the loop only (the fused verify pass
+    drafts with residual-block heads)."""
+
+    def __init__(self, *, heads, rope_base: float = 10000.0, **kw):
+        kw.setdefault("W", None)
+        super().__init__(**kw)
+        if self.dtype != torch.bfloat16:
+            raise ValueError("MTP heads are bf16 only")
+        if len(heads) != self.K:
+            raise ValueError("one MTP head per shortlist entry")
+        self.heads = list(heads)
+        self.rope_base = float(rope_base)
+        dev = self.lm.device
+        K, i32 = self.K, torch.int32
+        chain = (1,) * K
+        self.chain_parent = torch.empty(K + 1, dtype=i32, device=dev)
+        self.chain_depth = torch.empty(K + 1, dtype=i32, device=dev)
+        self.chain_rank = torch.empty(K + 1, dtype=i32, device=dev)
+        self.chain_mask = torch.empty((K + 1, 1), dtype=torch.int64, device=dev)
+        build_tree_mask(chain, -1, self.chain_parent, self.chain_depth, self.chain_rank,
+                        self.chain_mask)
+        self.xrows = torch.empty((self.B, K + 1, self.d), dtype=self.dtype, device=dev)
+        self.Lm = torch.zeros(self.B, dtype=i32, device=dev)
+        self.P0 = torch.empty_like(self.P)
+        dff = heads[0]["w1"].shape[0]
+        need = mtp_workspace_size(self.B, K, self.d, dff, self.Hq, self.Hkv, self.dh)
+        if need > self.ws.numel():
+            self.ws = new_workspace(need, dev)
+        self.fused_ok = False
+
+    def _start(self, h):
+        """The heads' rows from h alone: row 0 = h at position P_b - 1, the
+        others padding (copies of h)."""
+        self.xrows.copy_(h[:, None, :].expand_as(self.xrows))
+        self.Lm.zero_()
+        torch.sub(self.P, 1, out=self.P0)
+
+    def run(self, h, *args, **kw):
+        self._start(h)
+        super().run(h, *args, **kw)
+
+    def begin_decode(self, h, fused):
+        if fused:
+            raise ValueError("MTP heads run with the separate form of the loop")
+        self._start(h)
+
+    def _draft(self, h):
+        mtp_heads(self.xrows, self.Lm, self.P0, self.chain_depth, self.chain_mask, self.heads,
+                  self.lm, self.shortlist, self.smax, self.U, self.root, self.topk_id,
+                  self.topk_val, self.ws, Hq=self.Hq, Hkv=self.Hkv, rope_base=self.rope_base)
+
+    def _before_commit(self):
+        self.P0.copy_(self.P)            # position of the accepted rows' first
+
+    def _next(self, h, fused):
+        next_inputs(self.L, self.path, self.ws, N=self.N, smax=self.smax, y=self.y, h_next=h,
+                    rows_out=self.xrows)
+        self.Lm.copy_(self.L)

@@ -102,6 +102,21 @@ def close_float(got: np.ndarray, want: np.ndarray, dtype: str, kind: str, what: 
     return float(np.max(np.abs(got - want) / np.maximum(np.abs(want), 1e-30)))
 
 
+def close_chain(got, want_exact, what: str = "", roundings: int = 2):
+    """bf16 values produced through a chain of roundings (an attention output
+    stored in bf16, then further residual steps stored again): within 1e-2 of
+    the oracle's unrounded value plus one bf16 unit per rounding point of the
+    chain.  A rounding flip at an earlier point passes unchanged through a
+    residual connection, so each rounding point adds up to one unit."""
+    got = np.asarray(got, np.float64)
+    want_exact = np.asarray(want_exact, np.float64)
+    assert got.shape == want_exact.shape, (what, got.shape, want_exact.shape)
+    err = np.abs(got - want_exact)
+    lim = BF16_ATTN_ATOL + roundings * bf16_ulp(want_exact)
+    assert not (err > lim).any(), (what, float(err.max()), float((err - lim).max()))
+    return float(err.max())
+
+
 def tol_logit(dtype: str, scale: float = 1.0) -> float:
     return BF16_LOGIT_ATOL if dtype == "bf16" else FP32_RTOL * max(scale, 1.0)
 

@@ -145,11 +145,27 @@ def test_new_entry_points_validate_on_the_host(lib):
     assert need >= 8192 + 3 * 7 * 64 * 2
     # next_inputs: an output without its source is an argument error
     assert lib.mds_next_inputs(1, 1, 7, 2, 2, 64, fake, fake, null, null, null, null, fake, null,
-                               null, null, fake, big, null) == -1
+                               null, null, null, fake, big, null) == -1
     assert lib.mds_next_inputs(1, 1, 7, 2, 2, 64, fake, fake, null, fake, null, null, null,
-                               fake, null, null, fake, big, null) == -1
+                               fake, null, null, null, fake, big, null) == -1
     assert lib.mds_next_inputs(1, 1, 7, 2, 2, 64, null, fake, null, fake, null, null, fake, null,
-                               null, null, fake, big, null) == -1
+                               null, null, null, fake, big, null) == -1
+    # accepted rows without y
+    assert lib.mds_next_inputs(1, 1, 7, 2, 2, 64, fake, fake, null, null, null, null, null, null,
+                               null, null, fake, fake, big, null) == -1
+    # MTP heads: bf16 only, dff a multiple of 64, a null head pointer
+    arr = (ctypes.c_void_p * 2)(256, 256)
+    bad = (ctypes.c_void_p * 2)(256, None)
+    sl = (ctypes.c_int32 * 2)(2, 2)
+    args = [fake] * 5 + [arr, arr, arr, arr, arr, arr, 10000.0, fake, sl, 2, fake, fake, fake, fake,
+                         fake, big, null]
+    assert lib.mds_mtp_heads(0, 1, 2, 64, 64, 100, 2, 2, 64, 256, *args) == -3
+    assert lib.mds_mtp_heads(1, 1, 2, 64, 96, 100, 2, 2, 64, 256, *args) == -3
+    args_bad = list(args)
+    args_bad[5] = bad
+    assert lib.mds_mtp_heads(1, 1, 2, 64, 64, 100, 2, 2, 64, 256, *args_bad) == -1
+    assert lib.mds_mtp_workspace_size(1, 2, 64, 64, 2, 2, 64) > \
+        lib.mds_backbone_workspace_size(1, 3, 64, 2, 2, 64)
 
 
 def test_python_binding_refuses_cpu_tensors(lib):
