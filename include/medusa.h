@@ -59,7 +59,10 @@
  *    work enqueued before the call, so inputs written by earlier work on the
  *    stream are always seen.  Environment switches, read once per process:
  *    MDS_PDL=0 launches every kernel plainly; MDS_KSPLIT=0 turns off the
- *    K-split form of the narrow projections (Wo at <= 128 rows).  One more
+ *    K-split form of the narrow projections (Wo at <= 128 rows);
+ *    MDS_ATTN_GROUPED=0 keeps up to three query tiles per tree-attention
+ *    work unit (64-key tiles) instead of one tile per unit with one CTA
+ *    group per query tile, above 128 query rows per KV head.  One more
  *    switch, read at every launch, exists to test the bounded waits:
  *    MDS_STALL_TEST=1 makes every projection-GEMM CTA first wait (1 ms limit)
  *    on a barrier that nothing completes, after which it gives up exactly as

@@ -18,7 +18,16 @@
 // laid end to end and split evenly over the CTAs (one per SM), so ragged
 // prefixes and any batch balance across the GPU (stream-K).  A CTA streams
 // its key tiles through a TMA ring once; every query tile of the unit uses
-// each key tile while it is in shared memory:
+// each key tile while it is in shared memory.
+//
+// With more than 128 query rows per KV head (grouped-query attention: g
+// query heads per KV head) the units hold one query tile each and the CTAs
+// form n_mg groups: group i takes the units of query tile i of every (b, h),
+// laid end to end and split evenly over its CTAs.  CTA c of every group then
+// covers the same keys at about the same time, so the K/V tile that one of
+// them reads from HBM the others find in L2.  With BN = 128 keys a tile
+// costs 16 tcgen05.mma per query tile, against 24 with three query tiles
+// over 64-key tiles (S at N = 64 costs a full MMA issue).
 //
 //   S = Q K^T      tcgen05, M = 128 query rows, N = BN keys, K = dh      -> TMEM
 //   softmax        one thread per query row reads its S row from TMEM,
@@ -64,7 +73,9 @@ struct AttnArgs {
   int NM;           // query tiles per unit
   int n_mg;         // units per (b, h)
   int stages;
-  int G;            // CTAs
+  int G;            // CTAs (n_grp groups of Gg)
+  int n_grp, Gg;    // CTA groups, CTAs per group
+  int mpg;          // units per (b, h) in one group: n_mg / n_grp
   float scale_log2; // log2(e) / sqrt(dh)
   const int32_t* P;
   const uint64_t* mask;
@@ -129,10 +140,12 @@ struct Seg {
   long long U0;     // first global tile of the unit
 };
 
-// Walks the segments of the CTA's global tile range [t, end).  pre[b] =
-// first global tile of sequence b (shared memory, B + 1 entries).
+// Walks the segments of the CTA's tile range [t, end) within its group.
+// pre[b] = first tile of sequence b in a group's layout (shared memory,
+// B + 1 entries).
 struct SegIter {
   long long t, end;
+  int grp;          // CTA group: units of query tiles [grp mpg, grp mpg + mpg)
   __device__ __forceinline__ bool next(const AttnArgs& a, const int* pre, Seg& s) {
     if (t >= end) return false;
     int lo = 0, hi = a.B;          // largest b with pre[b] <= t
@@ -146,8 +159,8 @@ struct SegIter {
     const long long off = t - (long long)pre[b];
     const int idx = (int)(off / nt);
     s.b = b;
-    s.h = idx / a.n_mg;
-    s.mg = idx - s.h * a.n_mg;
+    s.h = idx / a.mpg;
+    s.mg = grp * a.mpg + (idx - s.h * a.mpg);
     s.unit = (b * a.Hkv + s.h) * a.n_mg + s.mg;
     s.Pb = Pb;
     s.nt = nt;
@@ -233,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int Pb = a.P[b];
       const int nt = tiles_of(a, Pb);
       if (nt == 0) bad = true;
-      acc += a.Hkv * a.n_mg * nt;
+      acc += a.Hkv * a.mpg * nt;
     }
     pre[a.B] = acc;
     if (bad && cta == 0) latch_error(a.ws, MDS_DEV_KV_CAPACITY);
@@ -266,15 +279,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   grid_dep_wait();
   const uint32_t tmem = *tmem_slot;
-  const long long Ttot = (long long)pre[a.B];
+  const long long Ttot = (long long)pre[a.B];     // tiles of one group
+  const int cgrp = cta / a.Gg, cidx = cta - cgrp * a.Gg;
   SegIter iter;
-  iter.t = cta_start(Ttot, a.G, cta);
-  iter.end = cta_start(Ttot, a.G, cta + 1);
+  iter.t = cta_start(Ttot, a.Gg, cidx);
+  iter.end = cta_start(Ttot, a.Gg, cidx + 1);
+  iter.grp = cgrp;
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
-      const uint64_t pol_kv = ptx::policy_evict_first();
+      // K/V read by one CTA per group: kept in L2 at normal priority for the
+      // other groups' CTAs, which read the same tiles at about the same time
+      const uint64_t pol_kv = a.n_grp > 1 ? ptx::policy_evict_normal() : ptx::policy_evict_first();
       const uint64_t pol_q = ptx::policy_evict_last();
       // Requests in the order the slots free up: K of tile t (its slot frees
       // when the S MMAs of tile t - S are done), then V of tile t - 1 (slot
@@ -614,7 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       //      of the pair writes half of the O columns.
       const bool whole = s.j0 == 0 && s.j1 == s.nt;
       int slot = 0;
-      if (!whole) slot = 2 * cta + (cta_start(Ttot, a.G, cta) >= s.U0 ? 0 : 1);
+      if (!whole) slot = 2 * cta + (cta_start(Ttot, a.Gg, cidx) >= s.U0 ? 0 : 1);
       const int rows_unit = NM * 128;
       float ltot[kMaxNM];
       // split accumulators: weights of O_0 and O_1 relative to the combined
@@ -725,15 +742,15 @@ __global__ void __launch_bounds__(256) k_attention_merge(AttnArgs a) {
   grid_dep_launch();
   grid_dep_wait();
   __shared__ int pre[kMaxBAttn + 1];
-  __shared__ long long starts[kMaxCtaAttn + 1];   // first global tile of each CTA
-  for (int b = threadIdx.x; b < a.B; b += blockDim.x) pre[b + 1] = a.Hkv * a.n_mg * tiles_of(a, a.P[b]);
+  __shared__ long long starts[kMaxCtaAttn + 1];   // first tile of each CTA of a group
+  for (int b = threadIdx.x; b < a.B; b += blockDim.x) pre[b + 1] = a.Hkv * a.mpg * tiles_of(a, a.P[b]);
   block_sync();
   if (threadIdx.x == 0) {
     pre[0] = 0;
     for (int b = 0; b < a.B; ++b) pre[b + 1] += pre[b];
   }
   block_sync();
-  for (int c = threadIdx.x; c <= a.G; c += blockDim.x) starts[c] = cta_start(pre[a.B], a.G, c);
+  for (int c = threadIdx.x; c <= a.Gg; c += blockDim.x) starts[c] = cta_start(pre[a.B], a.Gg, c);
   block_sync();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int u = blockIdx.x;
@@ -745,13 +762,15 @@ __global__ void __launch_bounds__(256) k_attention_merge(AttnArgs a) {
   const int r = mg * rows_unit + rloc;
   if (nt == 0 || rloc >= rows_unit || r >= a.Mrows) return;
   const long long Ttot = pre[a.B];
-  const long long U0 = (long long)pre[b] + (long long)(h * a.n_mg + mg) * nt;
+  // the unit's tiles in its group's layout; c indexes the group's CTAs
+  const int grp = mg / a.mpg;
+  const long long U0 = (long long)pre[b] + (long long)(h * a.mpg + (mg - grp * a.mpg)) * nt;
   const long long U1 = U0 + nt;
-  int c0 = (int)((U0 * a.G) / Ttot);
-  while (c0 + 1 < a.G && starts[c0 + 1] <= U0) ++c0;
+  int c0 = (int)((U0 * a.Gg) / Ttot);
+  while (c0 + 1 < a.Gg && starts[c0 + 1] <= U0) ++c0;
   while (c0 > 0 && starts[c0] > U0) --c0;
   int c1 = c0;
-  while (c1 < a.G && starts[c1] < U1) ++c1;
+  while (c1 < a.Gg && starts[c1] < U1) ++c1;
   int nseg = 0;
   for (int c = c0; c < c1; ++c)
     if (starts[c + 1] > starts[c]) ++nseg;
@@ -760,7 +779,7 @@ __global__ void __launch_bounds__(256) k_attention_merge(AttnArgs a) {
   float M = -INFINITY;
   for (int c = c0; c < c1; ++c) {
     if (starts[c + 1] == starts[c]) continue;
-    const int sl = 2 * c + (starts[c] >= U0 ? 0 : 1);
+    const int sl = 2 * (grp * a.Gg + c) + (starts[c] >= U0 ? 0 : 1);
     M = fmaxf(M, __ldcg(reinterpret_cast<const float2*>(pml) + (long long)sl * rows_unit + rloc).x);
   }
   constexpr int E = DH / 32;                 // elements per lane
@@ -770,7 +789,7 @@ __global__ void __launch_bounds__(256) k_attention_merge(AttnArgs a) {
   float L = 0.f;
   for (int c = c0; c < c1; ++c) {
     if (starts[c + 1] == starts[c]) continue;
-    const int sl = 2 * c + (starts[c] >= U0 ? 0 : 1);
+    const int sl = 2 * (grp * a.Gg + c) + (starts[c] >= U0 ? 0 : 1);
     const float2 ml = __ldcg(reinterpret_cast<const float2*>(pml) + (long long)sl * rows_unit + rloc);
     const float* po = a.part + ((long long)sl * rows_unit + rloc) * DH + lane * E;
     float v[E];
@@ -801,16 +820,37 @@ __global__ void __launch_bounds__(256) k_attention_merge(AttnArgs a) {
 }
 
 // ----------------------------------------------------------------- host
+// MDS_ATTN_GROUPED=0 keeps several query tiles per unit (64-key tiles) above
+// 128 query rows per KV head; read once per process.
+bool grouped_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("MDS_ATTN_GROUPED");
+    return !(v && v[0] == '0');
+  }();
+  return on;
+}
+
 struct Plan {
-  int NM, n_mg, stages, G, BN;
+  int NM, n_mg, stages, G, BN, n_grp, Gg;
   size_t smem;
 };
 
 Plan plan(int N, int g, int dh, int num_sms) {
   Plan p{};
   const int mtiles = (N * g + 127) / 128;
-  p.n_mg = (mtiles + kMaxNM - 1) / kMaxNM;
-  p.NM = (mtiles + p.n_mg - 1) / p.n_mg;
+  const int G = num_sms < kMaxCtaAttn ? num_sms : kMaxCtaAttn;
+  if (grouped_enabled() && mtiles > 1 && 2 * mtiles <= G) {
+    // one query tile per unit, one CTA group per query tile
+    p.n_mg = mtiles;
+    p.NM = 1;
+    p.n_grp = mtiles;
+  } else {
+    p.n_mg = (mtiles + kMaxNM - 1) / kMaxNM;
+    p.NM = (mtiles + p.n_mg - 1) / p.n_mg;
+    p.n_grp = 1;
+  }
+  p.Gg = G / p.n_grp;
+  p.G = p.Gg * p.n_grp;
   p.BN = p.NM == 1 ? 128 : 64;
   const size_t q = (size_t)p.NM * 128 * dh * 2;
   const size_t pbuf = (p.BN == 128 ? 1 : 2) * (size_t)128 * p.BN * 2;
@@ -822,7 +862,6 @@ Plan plan(int N, int g, int dh, int num_sms) {
   // more than half of the SM's shared memory: no two CTAs holding all 512
   // TMEM columns (this kernel's or the projection GEMM's) share an SM
   if (p.smem < (size_t)kSmemLimit / 2 + 1024) p.smem = (size_t)kSmemLimit / 2 + 1024;
-  p.G = num_sms < kMaxCtaAttn ? num_sms : kMaxCtaAttn;
   return p;
 }
 
@@ -867,8 +906,10 @@ int launch_one(const Plan& p, const CUtensorMap& mq, const CUtensorMap& mk, cons
 }  // namespace
 
 size_t attention_tc_partial_bytes(int N, int g, int dh) {
-  const Plan p = plan(N, g, dh, kMaxCtaAttn);
-  const size_t rows = (size_t)p.NM * 128;
+  // rows per unit of the ungrouped plan: at least those of any plan
+  const int mtiles = (N * g + 127) / 128;
+  const int n_mg = (mtiles + kMaxNM - 1) / kMaxNM;
+  const size_t rows = (size_t)((mtiles + n_mg - 1) / n_mg) * 128;
   return 2 * (size_t)kMaxCtaAttn * rows * (dh + 2) * 4;
 }
 
@@ -904,6 +945,9 @@ int attention_tc(int B, int N, int Hq, int Hkv, int dh, int Pmax, const int32_t*
   a.n_mg = p.n_mg;
   a.stages = p.stages;
   a.G = p.G;
+  a.n_grp = p.n_grp;
+  a.Gg = p.Gg;
+  a.mpg = p.n_mg / p.n_grp;
   a.scale_log2 = 1.4426950408889634f / sqrtf((float)dh);
   a.P = P;
   a.mask = mask;

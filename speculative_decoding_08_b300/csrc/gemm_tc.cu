@@ -1186,7 +1186,12 @@ int launch_tc(TcArgs& a, const void* X, const void* W, bool dependent, cudaStrea
   if (a.R <= 0 || a.F <= 0) return MDS_OK;
   if (a.Kd % 64 != 0) return MDS_EUNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(X) | reinterpret_cast<uintptr_t>(W)) & 15) return MDS_EINVAL;
-  a.G = a.R <= 128 ? 1 : 2;
+  // Row tiles of 128 per CTA.  The draft pass keeps one tile per CTA at any
+  // row count: with 2.5 tiles of rows (batch 64 x 5 head rows) a pair per CTA
+  // leaves half the CTAs a single live tile while the others issue two MMAs
+  // per k-step over N = 128; one tile per CTA at N = 256 issues a quarter of
+  // the MMAs of the busiest such CTA and keeps every CTA equally loaded.
+  a.G = (a.R <= 128 || a.kind == TC_DRAFT) ? 1 : 2;
   // Features per MMA (N) and accumulator buffers.  Every tcgen05.mma costs
   // about the same up to N = 256, so N is 256 where TMEM allows: with one
   // 128-row group, double-buffered (the epilogue of one chunk overlaps the
@@ -1195,15 +1200,15 @@ int launch_tc(TcArgs& a, const void* X, const void* W, bool dependent, cudaStrea
   // N = 128 double-buffered, since their ranges are narrow or their
   // epilogue is heavy.
   //
-  // Above 256 rows every CTA takes one row group (n_rs partitions of the
-  // rows) and a feature range n_rs times wider: a CTA's MMAs then cost
+  // With more than one row group every CTA takes one (n_rs partitions of
+  // the rows) and a feature range n_rs times wider: a CTA's MMAs then cost
   // 1 / n_rs of sweeping all rows over a narrow range, whose N would be far
   // below 256; the n_rs CTAs that share a range read its weights at about
   // the same time, so HBM sees them once and L2 serves the rest.
   a.n_rgroups = (a.R + 128 * a.G - 1) / (128 * a.G);
   a.n_units = (a.F + 15) / 16;
   const int sms = g_num_sms < kMaxCta ? g_num_sms : kMaxCta;
-  a.n_rs = (a.G == 2 && a.n_rgroups >= 2) ? min(a.n_rgroups, sms) : 1;
+  a.n_rs = a.n_rgroups >= 2 ? min(a.n_rgroups, sms) : 1;
   a.n_fr = max(1, min(sms / a.n_rs, a.n_units));
   a.n_cta = a.n_rs * a.n_fr;
   a.ks = 1;
@@ -1220,11 +1225,9 @@ int launch_tc(TcArgs& a, const void* X, const void* W, bool dependent, cudaStrea
     a.NC = 256;
     a.nacc = a.G == 1 ? 2 : 1;
   } else {
-    // 129-256 rows in one row group (narrow feature ranges), and the draft
-    // pass above 128 rows: N = 128 with two accumulators, so that the
-    // epilogue of one chunk overlaps the MMAs of the next.  Measured on the
-    // batch-64 draft pass (320 rows): 698 us this way, 786 us with one
-    // 2 x 256-column accumulator (its top-8 epilogue then stalls the MMAs).
+    // 129-256 rows in one row group (narrow feature ranges): N = 128 with
+    // two accumulators, so that the epilogue of one chunk overlaps the MMAs
+    // of the next.
     a.NC = 128;
     a.nacc = 2;
   }
@@ -1237,7 +1240,7 @@ int launch_tc(TcArgs& a, const void* X, const void* W, bool dependent, cudaStrea
   const int h_max = min(a.NC, hi * 16);
   // shared-memory plan: k-blocks per stage, X pitch, ring depth
   int tail = 0;
-  if (a.G == 1) {
+  if (a.R <= 128) {
     a.xbox = (a.R + 7) / 8 * 8;
     a.px = a.xbox * 128;
     tail = 16384 - a.px;           // the last tile's 128-row read stays inside

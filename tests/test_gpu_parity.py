@@ -206,7 +206,7 @@ def test_tree_attention_token_fill(mds, w):
 # the tree (never weighted, must not reach the output), and prefix keys whose
 # scores grow along the sequence (the running maximum rises by far more than
 # the lazy-rescale threshold).  One shape per query-tile count: g = 1 (one
-# tile), g = 2 with dh = 64 (two tiles), g = 4 (three tiles).
+# tile), g = 2 with dh = 64 (two tiles), g = 4 (three tiles), g = 8 (six).
 EDGE = [
     ms.Workload("edge-g1", "bf16", B=3, d=256, V=500, Hq=2, Hkv=2, dh=128, K=4,
                 shortlist=(4, 3, 2, 2), max_rank_sum=-1, P=(0, 900), accept="typical", seed=21),
@@ -214,6 +214,10 @@ EDGE = [
                 shortlist=(4, 3, 2, 2), max_rank_sum=-1, P=(0, 900), accept="typical", seed=22),
     ms.Workload("edge-g4", "bf16", B=3, d=512, V=500, Hq=8, Hkv=2, dh=128, K=5,
                 shortlist=(8, 4, 2, 2, 1), max_rank_sum=3, P=(0, 900), accept="typical", seed=23),
+    # g = 8: six query tiles, so six CTA groups of 24 (one query tile per
+    # unit); a group's 2-3 tiles per CTA make segments that cross units
+    ms.Workload("edge-g8-six-tiles", "bf16", B=4, d=512, V=500, Hq=16, Hkv=2, dh=128, K=4,
+                shortlist=(4, 3, 2, 2), max_rank_sum=-1, P=(0, 900), accept="typical", seed=25),
     # about 8 key tiles per CTA: segments that span several tiles
     ms.Workload("edge-multitile", "bf16", B=4, d=256, V=500, Hq=8, Hkv=8, dh=128, K=4,
                 shortlist=(4, 3, 2, 2), max_rank_sum=-1, P=(3000, 4000), accept="typical",
