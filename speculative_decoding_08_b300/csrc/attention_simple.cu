@@ -11,17 +11,22 @@
 namespace mds {
 namespace {
 
+// One warp per tree row: lane 0 resolves the row's token (tree position ->
+// head shortlist), the warp copies the embedding row with 16-byte accesses,
+// eight loads of a lane in flight.
 template <typename T>
-__global__ void __launch_bounds__(256) k_embed(int N, int d, int V, int K, int smax,
+__global__ void __launch_bounds__(256) k_embed(int R, int N, int d, int V, int K, int smax,
                                                int32_t* tok, const int32_t* root,
                                                const int32_t* topk_id, const int32_t* depth,
                                                const int32_t* rank, const T* __restrict__ emb,
                                                T* __restrict__ x, void* ws) {
   grid_dep_launch();   // the QKV projection may start loading its weights
-  const int r = blockIdx.x, b = r / N, n = r % N;
-  __shared__ int s_tok;
-  if (threadIdx.x == 0) {
-    int t;
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (r >= R) return;
+  const int b = r / N, n = r % N;
+  int t = 0;
+  if (lane == 0) {
     if (root) {
       if (n == 0) {
         t = root[b];
@@ -42,17 +47,37 @@ __global__ void __launch_bounds__(256) k_embed(int N, int d, int V, int K, int s
       latch_error(ws, MDS_DEV_TOKEN_RANGE);
       t = -1;
     }
-    s_tok = t;
   }
-  block_sync();
-  const int t = s_tok;
+  t = __shfl_sync(0xffffffffu, t, 0);
   T* xr = x + (long long)r * d;
-  if (t < 0) {
-    for (int c = threadIdx.x; c < d; c += blockDim.x) st(xr + c, 0.f);
-    return;
+  const long long row_bytes = (long long)d * (long long)sizeof(T);
+  const bool vec = row_bytes % 16 == 0 &&
+                   ((reinterpret_cast<uintptr_t>(emb) | reinterpret_cast<uintptr_t>(x)) & 15) == 0;
+  if (vec) {
+    const int nv = (int)(row_bytes / 16);
+    uint4* xv = reinterpret_cast<uint4*>(xr);
+    if (t < 0) {
+      for (int c = lane; c < nv; c += 32) xv[c] = make_uint4(0, 0, 0, 0);
+      return;
+    }
+    const uint4* ev = reinterpret_cast<const uint4*>(emb + (long long)t * d);
+    for (int c0 = lane; c0 < nv; c0 += 32 * 8) {
+      uint4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (c0 + 32 * u < nv) v[u] = __ldg(ev + c0 + 32 * u);
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (c0 + 32 * u < nv) xv[c0 + 32 * u] = v[u];
+    }
+  } else {
+    if (t < 0) {
+      for (int c = lane; c < d; c += 32) st(xr + c, 0.f);
+      return;
+    }
+    const T* er = emb + (long long)t * d;
+    for (int c = lane; c < d; c += 32) xr[c] = er[c];
   }
-  const T* er = emb + (long long)t * d;
-  for (int c = threadIdx.x; c < d; c += blockDim.x) xr[c] = er[c];
 }
 
 template <typename T>
@@ -116,13 +141,15 @@ __global__ void __launch_bounds__(256) k_attention_simple(int B, int N, int Hq, 
 int embed_gather(int dtype, int B, int N, int d, int V, int K, int smax, int32_t* tok,
                  const int32_t* root, const int32_t* topk_id, const int32_t* depth,
                  const int32_t* rank, const void* emb, void* x, void* ws, cudaStream_t st) {
+  const int R = B * N, blocks = (R + 7) / 8;
+  if (R <= 0) return MDS_OK;
   if (dtype == MDS_F32)
-    k_embed<float><<<B * N, 256, 0, st>>>(N, d, V, K, smax, tok, root, topk_id, depth, rank,
-                                          static_cast<const float*>(emb),
-                                          static_cast<float*>(x), ws);
+    k_embed<float><<<blocks, 256, 0, st>>>(R, N, d, V, K, smax, tok, root, topk_id, depth, rank,
+                                           static_cast<const float*>(emb),
+                                           static_cast<float*>(x), ws);
   else
-    k_embed<__nv_bfloat16><<<B * N, 256, 0, st>>>(
-        N, d, V, K, smax, tok, root, topk_id, depth, rank,
+    k_embed<__nv_bfloat16><<<blocks, 256, 0, st>>>(
+        R, N, d, V, K, smax, tok, root, topk_id, depth, rank,
         static_cast<const __nv_bfloat16*>(emb), static_cast<__nv_bfloat16*>(x), ws);
   MDS_LAUNCH_CHECK();
   return MDS_OK;

@@ -177,6 +177,21 @@ __device__ __forceinline__ long long cta_start(long long Ttot, int G, int c) {
   return (Ttot * c) / G;
 }
 
+// Written by every CTA for the merge kernel: the unit whose last tile lies in
+// the CTA's range while its first tile lies in an earlier CTA's (each unit
+// split over several CTAs has exactly one such CTA), or unit = -1.
+struct MergeDesc {
+  int unit, pad;
+  long long U0;      // first tile of the unit in its group's layout
+  long long Ttot;    // tiles of one group
+};
+
+// Partial records: O [2 G][rows][DH] fp32, then (m, l) [2 G][rows], then
+// one MergeDesc per CTA.
+__device__ __forceinline__ MergeDesc* merge_descs(const AttnArgs& a, int rows_unit, int dh) {
+  return reinterpret_cast<MergeDesc*>(a.part + (long long)2 * a.G * rows_unit * (dh + 2));
+}
+
 // --------------------------------------------------------------- kernel
 template <int DH, int NM, int kBN>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -285,6 +300,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   iter.t = cta_start(Ttot, a.Gg, cidx);
   iter.end = cta_start(Ttot, a.Gg, cidx + 1);
   iter.grp = cgrp;
+  if (threadIdx.x == 64) {
+    SegIter it0 = iter;
+    Seg s0;
+    MergeDesc md{-1, 0, 0, 0};
+    if (it0.next(a, pre, s0) && s0.j0 > 0 && s0.j1 == s0.nt) {
+      md.unit = s0.unit;
+      md.U0 = s0.U0;
+      md.Ttot = Ttot;
+    }
+    merge_descs(a, NM * 128, DH)[cta] = md;
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
@@ -733,53 +759,40 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // --------------------------------------------------------------- merge
-// One warp per (unit, query row) of the units whose key tiles were split over
-// several CTAs (units covered by one CTA were written by the main kernel):
-//   o = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s,   M = max_s m_s.
-// The partition is recomputed from P exactly as the main kernel computes it.
+// Block (c, y): the unit that CTA c's descriptor names (if any), query rows
+// [8 y, 8 y + 8) of it, one warp per row:
+//   o = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s,   M = max_s m_s
+// over the unit's segments, one per CTA of its group from the one holding
+// its first tile to c.  Units covered by one CTA were written by the main
+// kernel.
 template <int DH>
 __global__ void __launch_bounds__(256) k_attention_merge(AttnArgs a) {
   grid_dep_launch();
   grid_dep_wait();
-  __shared__ int pre[kMaxBAttn + 1];
-  __shared__ long long starts[kMaxCtaAttn + 1];   // first tile of each CTA of a group
-  for (int b = threadIdx.x; b < a.B; b += blockDim.x) pre[b + 1] = a.Hkv * a.mpg * tiles_of(a, a.P[b]);
-  block_sync();
-  if (threadIdx.x == 0) {
-    pre[0] = 0;
-    for (int b = 0; b < a.B; ++b) pre[b + 1] += pre[b];
-  }
-  block_sync();
-  for (int c = threadIdx.x; c <= a.Gg; c += blockDim.x) starts[c] = cta_start(pre[a.B], a.Gg, c);
-  block_sync();
+  const int rows_unit = a.NM * 128;
+  const int c = blockIdx.x;
+  const MergeDesc md = merge_descs(a, rows_unit, DH)[c];
+  if (md.unit < 0) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int u = blockIdx.x;
+  const int u = md.unit;
   const int mg = u % a.n_mg, bh = u / a.n_mg;
   const int h = bh % a.Hkv, b = bh / a.Hkv;
-  const int nt = tiles_of(a, a.P[b]);
-  const int rows_unit = a.NM * 128;
   const int rloc = blockIdx.y * 8 + warp;
   const int r = mg * rows_unit + rloc;
-  if (nt == 0 || rloc >= rows_unit || r >= a.Mrows) return;
-  const long long Ttot = pre[a.B];
-  // the unit's tiles in its group's layout; c indexes the group's CTAs
-  const int grp = mg / a.mpg;
-  const long long U0 = (long long)pre[b] + (long long)(h * a.mpg + (mg - grp * a.mpg)) * nt;
-  const long long U1 = U0 + nt;
-  int c0 = (int)((U0 * a.Gg) / Ttot);
-  while (c0 + 1 < a.Gg && starts[c0 + 1] <= U0) ++c0;
-  while (c0 > 0 && starts[c0] > U0) --c0;
-  int c1 = c0;
-  while (c1 < a.Gg && starts[c1] < U1) ++c1;
-  int nseg = 0;
-  for (int c = c0; c < c1; ++c)
-    if (starts[c + 1] > starts[c]) ++nseg;
-  if (nseg <= 1) return;
+  if (rloc >= rows_unit || r >= a.Mrows) return;
+  const int grp = c / a.Gg, ci = c - grp * a.Gg;   // c within its group
+  const long long U0 = md.U0, Ttot = md.Ttot;
+  // group CTA holding tile U0
+  int i0 = (int)((U0 * a.Gg) / Ttot);
+  if (i0 > ci) i0 = ci;
+  while (i0 < ci && cta_start(Ttot, a.Gg, i0 + 1) <= U0) ++i0;
+  while (i0 > 0 && cta_start(Ttot, a.Gg, i0) > U0) --i0;
   const float* pml = a.part + (long long)2 * a.G * rows_unit * DH;
   float M = -INFINITY;
-  for (int c = c0; c < c1; ++c) {
-    if (starts[c + 1] == starts[c]) continue;
-    const int sl = 2 * (grp * a.Gg + c) + (starts[c] >= U0 ? 0 : 1);
+  for (int i = i0; i <= ci; ++i) {
+    const long long st = cta_start(Ttot, a.Gg, i);
+    if (cta_start(Ttot, a.Gg, i + 1) == st) continue;     // empty range
+    const int sl = 2 * (grp * a.Gg + i) + (st >= U0 ? 0 : 1);
     M = fmaxf(M, __ldcg(reinterpret_cast<const float2*>(pml) + (long long)sl * rows_unit + rloc).x);
   }
   constexpr int E = DH / 32;                 // elements per lane
@@ -787,9 +800,10 @@ __global__ void __launch_bounds__(256) k_attention_merge(AttnArgs a) {
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
   float L = 0.f;
-  for (int c = c0; c < c1; ++c) {
-    if (starts[c + 1] == starts[c]) continue;
-    const int sl = 2 * (grp * a.Gg + c) + (starts[c] >= U0 ? 0 : 1);
+  for (int i = i0; i <= ci; ++i) {
+    const long long st = cta_start(Ttot, a.Gg, i);
+    if (cta_start(Ttot, a.Gg, i + 1) == st) continue;
+    const int sl = 2 * (grp * a.Gg + i) + (st >= U0 ? 0 : 1);
     const float2 ml = __ldcg(reinterpret_cast<const float2*>(pml) + (long long)sl * rows_unit + rloc);
     const float* po = a.part + ((long long)sl * rows_unit + rloc) * DH + lane * E;
     float v[E];
@@ -910,7 +924,7 @@ size_t attention_tc_partial_bytes(int N, int g, int dh) {
   const int mtiles = (N * g + 127) / 128;
   const int n_mg = (mtiles + kMaxNM - 1) / kMaxNM;
   const size_t rows = (size_t)((mtiles + n_mg - 1) / n_mg) * 128;
-  return 2 * (size_t)kMaxCtaAttn * rows * (dh + 2) * 4;
+  return 2 * (size_t)kMaxCtaAttn * rows * (dh + 2) * 4 + (size_t)kMaxCtaAttn * sizeof(MergeDesc);
 }
 
 int attention_tc_supported(int B, int N, int g, int dh) {
@@ -965,7 +979,7 @@ int attention_tc(int B, int N, int Hq, int Hkv, int dh, int Pmax, const int32_t*
   rc = dh == 128 ? launch_nm<128>(p, mq, mk, mv, a, st) : launch_nm<64>(p, mq, mk, mv, a, st);
   if (rc) return rc;
   MDS_LAUNCH_CHECK();
-  const dim3 mgrid(B * Hkv * p.n_mg, p.NM * 16);
+  const dim3 mgrid(p.G, p.NM * 16);
   MDS_LAUNCH_TRY(launch_kernel(dh == 128 ? k_attention_merge<128> : k_attention_merge<64>, mgrid,
                                dim3(256), 0, st, true, a));
   return MDS_OK;
