@@ -571,15 +571,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             mx = fmaxf(fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3])),
                        fmaxf(fmaxf(t8[4], t8[5]), fmaxf(t8[6], t8[7])));
           } else {
+            // validity of this warp's keys [key0, key0 + kWC) as a bit mask:
+            // prefix keys (below Pb), then the tree keys the row's ancestor
+            // mask allows, nothing from Pb + N on.  s0 = Pb - key0 < kWC here.
+            uint64_t vm = 0ull;
+            if (live[m]) {
+              const int s0 = Pb - key0;
+              if (s0 > 0) {
+                vm = ((1ull << s0) - 1ull) | (mw0[m] << s0);   // tree key c - s0 at bit c
+              } else {
+                const int t0 = -s0;                            // first tree key of the warp
+                vm = t0 == 0    ? mw0[m]
+                     : t0 < 64  ? (mw0[m] >> t0) | (mw1[m] << (64 - t0))
+                     : t0 < 128 ? mw1[m] >> (t0 - 64)
+                                : 0ull;
+              }
+              const int lim = s0 + a.N;                        // keys past the tree
+              vm = lim <= 0 ? 0ull : lim < 64 ? vm & ((1ull << lim) - 1ull) : vm;
+            }
+            const uint32_t vlo = (uint32_t)vm, vhi = (uint32_t)(vm >> 32);
 #pragma unroll
             for (int c = 0; c < kWC; ++c) {
-              const int key = key0 + c;
-              const int mm = key - Pb;
-              const uint64_t w = mm < 64 ? mw0[m] : mw1[m];
-              const bool valid = live[m] && (key < Pb || (mm < a.N && ((w >> (mm & 63)) & 1ull)));
-              sv[c] = valid ? sv[c] : -INFINITY;
-              mx = fmaxf(mx, sv[c]);
+              const uint32_t wv = c < 32 ? vlo : vhi;
+              sv[c] = (wv >> (c & 31)) & 1u ? sv[c] : -INFINITY;
             }
+            float t8[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) t8[c] = sv[c];
+#pragma unroll
+            for (int c = 8; c < kWC; ++c) t8[c & 7] = fmaxf(t8[c & 7], sv[c]);
+            mx = fmaxf(fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3])),
+                       fmaxf(fmaxf(t8[4], t8[5]), fmaxf(t8[6], t8[7])));
           }
           if constexpr (!kSplitO) {
             mx = fmaxf(mx, exchange(mx));                // row maximum over both halves
@@ -625,9 +647,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float nmr = mr == -INFINITY ? 0.f : -mr;
 #pragma unroll
           for (int c = 0; c < kWC; c += 2) {
-            // 2^(s * scale - m); masked keys (s = -inf) give 0
-            const float p0 = mr == -INFINITY ? 0.f : ex2(fmaf(sv[c], sc, nmr));
-            const float p1 = mr == -INFINITY ? 0.f : ex2(fmaf(sv[c + 1], sc, nmr));
+            // 2^(s * scale - m); masked keys (s = -inf) give 0, and so does
+            // every key of a row whose maximum is still -inf (all its keys
+            // so far were masked, these included)
+            const float p0 = ex2(fmaf(sv[c], sc, nmr));
+            const float p1 = ex2(fmaf(sv[c + 1], sc, nmr));
             const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
             const float2 r2 = __bfloat1622float2(b2);
             ls4[(c >> 1) & 3] += r2.x + r2.y;

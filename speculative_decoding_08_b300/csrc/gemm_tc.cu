@@ -57,7 +57,12 @@ namespace mds {
 namespace {
 
 constexpr int kMaxStages = 16;
-constexpr int kThreads = 192;
+// Warps: 0 TMA producer, 1 TMEM owner and MMA issuer, then the epilogue
+// warps, one or two per TMEM lane quarter (with two, each takes every other
+// 32-column block of a chunk).  A pass whose accumulator is single-buffered
+// (the verify pass above 128 rows) waits for its epilogue between chunks, so
+// two warps per quarter halve that wait; the sampling and fused kinds keep
+// one per quarter (their larger per-row state needs the registers).
 constexpr int kTmemCols = 512;
 constexpr int kSmemBytes = 232448;                  // 227 KB, the opt-in maximum
 constexpr int kBarBytes = 512;
@@ -66,7 +71,8 @@ constexpr int kBarBytes = 512;
 constexpr int kTileFloats = 32 * 33;
 constexpr int kColParBytes = 4 * kTileFloats * 4;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
-constexpr int kMaxCta = 256;                        // partial records per row
+constexpr int kMaxCta = 256;                        // CTAs of one pass
+constexpr int kMaxRec = 2 * kMaxCta;                // partial records per row
 
 struct TcArgs {
   int R, F, Kd;
@@ -87,6 +93,7 @@ struct TcArgs {
   // F / n_cta features) up to 256 rows; beyond that each CTA takes one row
   // group and a range n_rs times wider, so that a 256-wide N stays filled.
   int n_rs, n_fr;
+  int n_rec;        // partial records per row: n_fr times the epilogue warps per quarter
   // K split (at most 128 rows, STORE / HEADS / QKV): ks CTAs share a feature
   // range, each over 1 / ks of the k-blocks, writing fp32 partial sums to
   // kpart [ks][R][F]; k_split_reduce then adds them in split order and runs
@@ -117,6 +124,14 @@ struct TcArgs {
   float inv_T;
   unsigned long long seed;
   int N, Hq, Hkv, dh, Pmax;
+  // VERIFY, VSAMPLE and the verify rows of VDRAFT: child logits.  Row
+  // b N + n stores its logit at tok[b N + c] into child[b N + c] for every
+  // tree node c with parent[c] = n (the candidates' scores under their
+  // parents' distributions).
+  const int32_t* tok;
+  const int32_t* parent;
+  float* child;
+  int V;
   const int32_t* P;
   // QKV of a backbone layer: (cos, sin) of every tree row's rotation angles,
   // [rows][dh / 2]; q and k pairs (2i, 2i+1) of each head are rotated
@@ -140,6 +155,11 @@ struct TcArgs {
 
 enum { TC_STORE = 0, TC_HEADS = 1, TC_QKV = 2, TC_DRAFT = 3, TC_VERIFY = 4, TC_VDRAFT = 5,
        TC_VSAMPLE = 6 };
+
+__host__ __device__ constexpr int epi_warps(int kind) {
+  return (kind == TC_VSAMPLE || kind == TC_VDRAFT) ? 4 : 8;
+}
+__host__ __device__ constexpr int threads_of(int kind) { return 64 + 32 * epi_warps(kind); }
 
 struct Range {
   int f_begin, f_end, n_chunks;
@@ -475,14 +495,81 @@ __device__ __forceinline__ void top8_block(TopList& tl, const float (&v)[32], in
   }
 }
 
+// Child logits in the verify epilogue.  A row walks the children of its tree
+// node in (token, index) order over the CTA's feature range [.., f_end); the
+// next one is found by a scan of the N parents, which happens once per
+// child in range (rarely more than once per row and CTA).
+struct ChildNext {
+  int tok, c;       // tok = INT_MAX: no child left in the range
+};
+
+__device__ __forceinline__ ChildNext child_after(const TcArgs& a, int row, int t0, int c0,
+                                                 int f_end) {
+  const int b = row / a.N, n = row - b * a.N;
+  const int32_t* tk = a.tok + (long long)b * a.N;
+  ChildNext r{0x7fffffff, 0};
+  for (int c = 1; c < a.N; ++c) {
+    if (__ldg(a.parent + c) != n) continue;
+    const int t = __ldg(tk + c);
+    if (t >= f_end || t < t0 || (t == t0 && c <= c0)) continue;
+    if (t < r.tok || (t == r.tok && c < r.c)) {
+      r.tok = t;
+      r.c = c;
+    }
+  }
+  return r;
+}
+
+__device__ __forceinline__ void child_pick(const TcArgs& a, int row, ChildNext& cn, int f0,
+                                           int nv, int f_end, const float (&v)[32]) {
+  // blocks are visited in increasing order; a child whose token lies in a
+  // block this warp skips (another warp's) is passed over
+  while (cn.tok < f0 + nv) {
+    if (cn.tok >= f0) {
+      const int k = cn.tok - f0;
+      float pick = 0.f;
+#pragma unroll
+      for (int q = 0; q < 32; ++q) pick = q == k ? v[q] : pick;
+      const int b = row / a.N;
+      a.child[(long long)b * a.N + cn.c] = pick;
+    }
+    cn = child_after(a, row, cn.tok, cn.c, f_end);
+  }
+}
+
+// Row (b, 0) in the first feature range checks the tree once per sequence:
+// child[b N] = 0 (the root has no parent), and every node with a parent out
+// of range or a token out of the vocabulary gets 0 and latches its error
+// (such a node is picked by no row).
+__device__ __forceinline__ void child_check(const TcArgs& a, int row) {
+  const int b = row / a.N;
+  a.child[(long long)b * a.N] = 0.f;
+  for (int c = 1; c < a.N; ++c) {
+    const int pa = __ldg(a.parent + c);
+    const int t = __ldg(a.tok + (long long)b * a.N + c);
+    if (pa < 0 || pa >= a.N) {
+      latch_error(a.ws, MDS_DEV_TREE_INDEX);
+      a.child[(long long)b * a.N + c] = 0.f;
+    } else if (t < 0 || t >= a.V) {
+      latch_error(a.ws, MDS_DEV_TOKEN_RANGE);
+      a.child[(long long)b * a.N + c] = 0.f;
+    }
+  }
+}
+
 // One 32-column block of a row's accumulators (raw fp32 bits in r).
 template <int KIND>
 __device__ __forceinline__ void epi_block(const TcArgs& a, int row, int g, int f0, int nv,
                                           const uint32_t (&r)[32], TopList (&tl)[2],
-                                          SoftStat (&ss)[2], GumbelMax (&gm)[2]) {
+                                          SoftStat (&ss)[2], GumbelMax (&gm)[2],
+                                          ChildNext (&cn)[2], int f_end) {
   float v[32];
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+  if constexpr (KIND == TC_VERIFY || KIND == TC_VSAMPLE) child_pick(a, row, cn[g], f0, nv, f_end, v);
+  if constexpr (KIND == TC_VDRAFT) {
+    if (row < a.Rv) child_pick(a, row, cn[g], f0, nv, f_end, v);
+  }
   if constexpr (KIND == TC_STORE) epi_store(a, row, f0, nv, v);
   if constexpr (KIND == TC_HEADS) epi_heads(a, row, f0, nv, v);
   if constexpr (KIND == TC_QKV) epi_qkv(a, row, f0, nv, v);
@@ -502,7 +589,7 @@ __device__ __forceinline__ void epi_block(const TcArgs& a, int row, int g, int f
 
 // ------------------------------------------------------------------ kernel
 template <int KIND>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_of(KIND), 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW0,
               const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmW2,
               TcArgs a) {
@@ -544,7 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(&tfull[s], 1);
-      ptx::mbar_init(&tempty[s], 4);
+      ptx::mbar_init(&tempty[s], epi_warps(KIND));
     }
     ptx::mbar_init(done, 1);
     ptx::mbar_init(never, 1);
@@ -557,7 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == 1) ptx::tmem_alloc(tmem_slot, kTmemCols);
   ptx::tc_fence_before();
-  ptx::cta_barrier(1, kThreads);
+  ptx::cta_barrier(1, threads_of(KIND));
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   // The stream's next kernel may start its own set-up from here on.  Every
@@ -714,9 +801,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // --------------------------------------------------------- epilogue
+    constexpr int kHalves = epi_warps(KIND) / 4;   // epilogue warps per lane quarter
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int trow = quarter * 32 + lane;
     float* tile = epi_tile + quarter * kTileFloats;
+    // blocks cb0, cb0 + cstride, ... of every chunk; the column-parallel
+    // HEADS form stages blocks in a per-quarter tile, so one warp per quarter
+    const bool active = !(kColPar && half > 0);
+    const int cstride = kColPar ? 1 : kHalves;
+    const int cb0 = kColPar ? 0 : half;
+    const int rec = fr * kHalves + half;            // this warp's partial record
     int item = 0;
     bool ok = true;
     for (int g0 = rs; g0 < a.n_rgroups && ok; g0 += a.n_rs) {
@@ -732,6 +827,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       ss[1].init();
       gm[0].init();
       gm[1].init();
+      ChildNext cn[2] = {{0x7fffffff, 0}, {0x7fffffff, 0}};
+      if constexpr (KIND == TC_VERIFY || KIND == TC_VSAMPLE || KIND == TC_VDRAFT) {
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          const int row = row0 + g * 128 + trow;
+          const int nstat = KIND == TC_VDRAFT ? a.Rv : a.R;
+          if (g < Geff && row < nstat && a.child) {
+            cn[g] = child_after(a, row, rg.f_begin, 0, rg.f_end);
+            if (fr == 0 && half == 0 && row % a.N == 0) child_check(a, row);
+          }
+        }
+      }
       for (int ch = 0; ch < rg.n_chunks; ++ch, ++item) {
         const int fc = rg.f_begin + ch * a.NC;
         const int len = min(a.NC, rg.f_end - fc);
@@ -744,7 +851,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
-          if (g >= Geff) break;
+          if (g >= Geff || !active) break;
           const int row = row0 + g * 128 + trow;
           const bool live = row < a.R;
           const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) +
@@ -753,36 +860,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int row_base = row0 + g * 128 + quarter * 32;
           const int nlive = min(32, max(0, a.R - row_base));
           if (kColPar && nlive == 0) continue;     // warp-uniform: nothing to read
-          // two register buffers: the load of block cb + 1 overlaps the work on cb
-          uint32_t rb[2][32];
-          ptx::tmem_ld32_async(tbase, rb[0]);
-          ptx::tmem_wait32(rb[0]);
-#pragma unroll 1
-          for (int cb = 0; cb < ncb; cb += 2) {
-            const bool more1 = cb + 1 < ncb, more2 = cb + 2 < ncb;
-            if (more1) ptx::tmem_ld32_async(tbase + (uint32_t)(cb + 1) * 32, rb[1]);
+          auto work = [&](int cb, const uint32_t (&rv)[32]) {
+            const int f0 = fc + cb * 32, nv = min(32, len - cb * 32);
             if (a.ks > 1) {
-              if (live) store_kpart(a, kspl, row, fc + cb * 32, min(32, len - cb * 32), rb[0]);
+              if (live) store_kpart(a, kspl, row, f0, nv, rv);
             } else if constexpr (kColPar) {
-              colpar_block<KIND>(a, tile, row_base, nlive, fc + cb * 32,
-                                 min(32, len - cb * 32), rb[0]);
+              colpar_block<KIND>(a, tile, row_base, nlive, f0, nv, rv);
             } else if (live) {
-              epi_block<KIND>(a, row, g, fc + cb * 32, min(32, len - cb * 32), rb[0], tl, ss, gm);
+              epi_block<KIND>(a, row, g, f0, nv, rv, tl, ss, gm, cn, rg.f_end);
             }
+          };
+          // two register buffers: the load of the next block overlaps the
+          // work on this one
+          uint32_t rb[2][32];
+          if (cb0 < ncb) {
+            ptx::tmem_ld32_async(tbase + (uint32_t)cb0 * 32, rb[0]);
+            ptx::tmem_wait32(rb[0]);
+          }
+#pragma unroll 1
+          for (int cb = cb0; cb < ncb; cb += 2 * cstride) {
+            const int c1 = cb + cstride, c2 = cb + 2 * cstride;
+            const bool more1 = c1 < ncb, more2 = c2 < ncb;
+            if (more1) ptx::tmem_ld32_async(tbase + (uint32_t)c1 * 32, rb[1]);
+            work(cb, rb[0]);
             if (more1) {
               ptx::tmem_wait32(rb[1]);
-              if (more2) ptx::tmem_ld32_async(tbase + (uint32_t)(cb + 2) * 32, rb[0]);
-              if (a.ks > 1) {
-                if (live)
-                  store_kpart(a, kspl, row, fc + (cb + 1) * 32, min(32, len - (cb + 1) * 32),
-                              rb[1]);
-              } else if constexpr (kColPar) {
-                colpar_block<KIND>(a, tile, row_base, nlive, fc + (cb + 1) * 32,
-                                   min(32, len - (cb + 1) * 32), rb[1]);
-              } else if (live) {
-                epi_block<KIND>(a, row, g, fc + (cb + 1) * 32, min(32, len - (cb + 1) * 32), rb[1],
-                                tl, ss, gm);
-              }
+              if (more2) ptx::tmem_ld32_async(tbase + (uint32_t)c2 * 32, rb[0]);
+              work(c1, rb[1]);
               if (more2) ptx::tmem_wait32(rb[0]);
             }
           }
@@ -799,22 +903,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (g >= Geff) break;
           const int row = row0 + g * 128 + trow;
           if (row >= a.R) continue;
-          // VDRAFT: verify rows [0, Rv) keep statistics records (Rv per
-          // range), head rows [Rv, R) top-8 records (R - Rv per range)
+          // records [row][n_rec]; VDRAFT: verify rows [0, Rv) keep
+          // statistics records, head rows [Rv, R) top-8 records (in partial2,
+          // indexed from Rv)
           const bool stat = KIND == TC_VERIFY || KIND == TC_VSAMPLE ||
                             (KIND == TC_VDRAFT && row < a.Rv);
           if (stat) {
-            const int nr = KIND == TC_VDRAFT ? a.Rv : a.R;
             float4 o = make_float4(ss[g].m, ss[g].S, ss[g].Q, __int_as_float(ss[g].am));
-            static_cast<float4*>(a.partial)[(long long)fr * nr + row] = o;
+            static_cast<float4*>(a.partial)[(long long)row * a.n_rec + rec] = o;
             if (KIND == TC_VSAMPLE)
-              static_cast<float2*>(a.partial2)[(long long)fr * nr + row] =
+              static_cast<float2*>(a.partial2)[(long long)row * a.n_rec + rec] =
                   make_float2(gm[g].k, __int_as_float(gm[g].id));
           } else {
-            const int nr = KIND == TC_VDRAFT ? a.R - a.Rv : a.R;
             const int rr = KIND == TC_VDRAFT ? row - a.Rv : row;
             float2* p = static_cast<float2*>(KIND == TC_VDRAFT ? a.partial2 : a.partial) +
-                        ((long long)fr * nr + rr) * kMaxS;
+                        ((long long)rr * a.n_rec + rec) * kMaxS;
 #pragma unroll
             for (int j = 0; j < kMaxS; ++j) p[j] = make_float2(tl[g].v[j], __int_as_float(tl[g].id[j]));
           }
@@ -828,7 +931,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   ptx::tc_fence_before();
-  ptx::cta_barrier(2, kThreads);
+  ptx::cta_barrier(2, threads_of(KIND));
   ptx::tc_fence_after();
   if (warp == 1) ptx::tmem_dealloc(tmem_base, kTmemCols);
 }
@@ -889,14 +992,23 @@ __global__ void __launch_bounds__(256) k_verify_merge(const float4* __restrict__
   const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= R) return;
+  // a row's records are contiguous; every lane's loads are issued before
+  // any is used
+  constexpr int kPer = kMaxRec / 32;
   if (spart) {
+    float2 sp[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int c = lane + 32 * i;
+      sp[i] = c < n_rec ? spart[(long long)row * n_rec + c] : make_float2(-INFINITY, __int_as_float(0x7fffffff));
+    }
     float bk = -INFINITY;
     int bi = 0x7fffffff;
-    for (int c = lane; c < n_rec; c += 32) {
-      const float2 p = spart[(long long)c * R + row];
-      const int pid = __float_as_int(p.y);
-      if (p.x > bk || (p.x == bk && pid < bi)) {
-        bk = p.x;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int pid = __float_as_int(sp[i].y);
+      if (sp[i].x > bk || (sp[i].x == bk && pid < bi)) {
+        bk = sp[i].x;
         bi = pid;
       }
     }
@@ -910,10 +1022,17 @@ __global__ void __launch_bounds__(256) k_verify_merge(const float4* __restrict__
     }
     if (lane == 0) sample_out[row] = bi;
   }
+  float4 pr[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int c = lane + 32 * i;
+    pr[i] = c < n_rec ? part[(long long)row * n_rec + c] : make_float4(-INFINITY, 0.f, 0.f, 0.f);
+  }
   float m = -INFINITY, S = 0.f, Q = 0.f;
   int am = 0x7fffffff;
-  for (int c = lane; c < n_rec; c += 32) {
-    const float4 p = part[(long long)c * R + row];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const float4 p = pr[i];
     const int pam = __float_as_int(p.w);
     if (p.y == 0.f && p.x == -INFINITY) continue;   // empty range
     if (p.x > m || (p.x == m && pam < am)) {
@@ -977,7 +1096,9 @@ __device__ __forceinline__ void warp_extract(const float (&v)[kMaxS], const int 
                                              int count, float* out_v, int* out_id) {
   int pos = 0;
   const int lane = threadIdx.x & 31;
-  for (int t = 0; t < count; ++t) {
+#pragma unroll
+  for (int t = 0; t < kMaxS; ++t) {
+    if (t >= count) break;
     float hv = -INFINITY;
     int hid = 0x7fffffff;
 #pragma unroll
@@ -1028,20 +1149,41 @@ __global__ void __launch_bounds__(256) k_draft_merge(const float2* __restrict__ 
     v[j] = -INFINITY;
     id[j] = 0x7fffffff;
   }
-  for (int c = threadIdx.x; c < n_rec * kMaxS; c += blockDim.x) {
-    const float2 e = part[((long long)(c / kMaxS) * R + row) * kMaxS + (c % kMaxS)];
-    const int eid = __float_as_int(e.y);
-    if (eid != 0x7fffffff) top8_insert(v, id, e.x, eid);
+  // every record is sorted (value desc, id asc): the row's best s are among
+  // the first s entries of the records; a row's records are contiguous, and
+  // every thread's loads are issued before any is used
+  constexpr int kPer = kMaxRec * kMaxS / 256;
+  const int ne = n_rec * s;
+  float2 ev[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int c = threadIdx.x + 256 * i;
+    if (c < ne) {
+      const int rec = c / s, j = c - rec * s;
+      ev[i] = part[((long long)row * n_rec + rec) * kMaxS + j];
+    } else {
+      ev[i] = make_float2(-INFINITY, __int_as_float(0x7fffffff));
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int eid = __float_as_int(ev[i].y);
+    if (eid != 0x7fffffff) top8_insert(v, id, ev[i].x, eid);
   }
   float wv[kMaxS];
   int wid[kMaxS];
-  warp_extract(v, id, kMaxS, wv, wid);
+#pragma unroll
+  for (int j = 0; j < kMaxS; ++j) {
+    wv[j] = -INFINITY;
+    wid[j] = 0x7fffffff;
+  }
+  warp_extract(v, id, s, wv, wid);
   if (lane < kMaxS) {
 #pragma unroll
     for (int j = 0; j < kMaxS; ++j)
       if (j == lane) {
-        s_v[warp][j] = wv[j];
-        s_id[warp][j] = wid[j];
+        s_v[warp][j] = j < s ? wv[j] : -INFINITY;
+        s_id[warp][j] = j < s ? wid[j] : 0x7fffffff;
       }
   }
   block_sync();
@@ -1069,51 +1211,6 @@ __global__ void __launch_bounds__(256) k_draft_merge(const float2* __restrict__ 
   }
 }
 
-// childlogit[b, c] = y[b, parent(c)] . lm[tok[b, c]], one warp per child
-// (grid: sequences x groups of 8 children).
-__global__ void __launch_bounds__(256) k_child_dot(const __nv_bfloat16* __restrict__ y,
-                                                   const __nv_bfloat16* __restrict__ lm, int N,
-                                                   int d, int V, const int32_t* tok,
-                                                   const int32_t* parent, float* child,
-                                                   void* ws) {
-  grid_dep_launch();
-  grid_dep_wait();
-  const int b = blockIdx.x;
-  const int lane = threadIdx.x & 31;
-  {
-    const int c = blockIdx.y * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (c >= N) return;
-    float acc = 0.f;
-    bool valid = false;
-    if (c > 0) {
-      const int pa = parent[c];
-      const int t = tok[(long long)b * N + c];
-      if (pa < 0 || pa >= N) {
-        if (lane == 0) latch_error(ws, MDS_DEV_TREE_INDEX);
-      } else if (t < 0 || t >= V) {
-        if (lane == 0) latch_error(ws, MDS_DEV_TOKEN_RANGE);
-      } else {
-        valid = true;
-        const uint4* yr = reinterpret_cast<const uint4*>(y + ((long long)b * N + pa) * d);
-        const uint4* lr = reinterpret_cast<const uint4*>(lm + (long long)t * d);
-        for (int k = lane; k < d / 8; k += 32) {
-          const uint4 ya = yr[k], la = lr[k];
-          const __nv_bfloat162* y2 = reinterpret_cast<const __nv_bfloat162*>(&ya);
-          const __nv_bfloat162* l2 = reinterpret_cast<const __nv_bfloat162*>(&la);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 yf = __bfloat1622float2(y2[e]);
-            const float2 lf = __bfloat1622float2(l2[e]);
-            acc = fmaf(yf.x, lf.x, acc);
-            acc = fmaf(yf.y, lf.y, acc);
-          }
-        }
-      }
-    }
-    for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) child[(long long)b * N + c] = valid ? acc : 0.f;
-  }
-}
 
 // ------------------------------------------------------------------ host
 int g_num_sms = 0;
@@ -1174,8 +1271,9 @@ int last_chunk_rows(int units, int NC) {
   return len - (n - 1) * NC;
 }
 
-// Plans and launches one pass; a.n_fr (the feature ranges, i.e. the partial
-// records per row of DRAFT and VERIFY) is left in `a` for the merge kernels.
+// Plans and launches one pass; a.n_rec (the partial records per row of the
+// DRAFT and VERIFY kinds: feature ranges times epilogue warps per quarter)
+// is left in `a` for the merge kernels.
 int launch_tc(TcArgs& a, const void* X, const void* W, bool dependent, cudaStream_t st) {
   int rc = init_host();
   if (rc) return rc;
@@ -1220,6 +1318,7 @@ int launch_tc(TcArgs& a, const void* X, const void* W, bool dependent, cudaStrea
       a.n_cta = a.n_fr * a.ks;
     }
   }
+  a.n_rec = a.n_fr * (epi_warps(a.kind) / 4);
   if (a.G == 1 || a.kind == TC_VERIFY || a.kind == TC_VSAMPLE ||
       (a.n_rs > 1 && a.kind != TC_DRAFT)) {
     a.NC = 256;
@@ -1291,8 +1390,8 @@ int launch_tc(TcArgs& a, const void* X, const void* W, bool dependent, cudaStrea
     case TC_VSAMPLE: kern = k_gemm_tc<TC_VSAMPLE>; break;
     default: kern = k_gemm_tc<TC_VERIFY>; break;
   }
-  MDS_LAUNCH_TRY(launch_kernel(kern, dim3(a.n_cta), dim3(kThreads), smem, st, dependent, mx,
-                               mw[0], mw[1], mw[2], a));
+  MDS_LAUNCH_TRY(launch_kernel(kern, dim3(a.n_cta), dim3(threads_of(a.kind)), smem, st, dependent,
+                               mx, mw[0], mw[1], mw[2], a));
   if (a.ks > 1) {
     void (*red)(TcArgs);
     switch (a.kind) {
@@ -1376,9 +1475,9 @@ size_t tc_kpart_bytes(int R, int F, int Kd) {
 }
 
 size_t tc_partial_bytes(int R, bool draft) {
-  // one record per (CTA, row), at most kMaxCta CTAs
+  // at most kMaxRec records per row (feature ranges x epilogue warps per quarter)
   const size_t per = draft ? (size_t)kMaxS * 8 : 16;
-  return (size_t)kMaxCta * R * per;
+  return (size_t)kMaxRec * R * per;
 }
 
 int lm_draft_tc(const void* U, int B, int K, int d, const void* lm, int V, Shortlist sl, int smax,
@@ -1394,7 +1493,7 @@ int lm_draft_tc(const void* U, int B, int K, int d, const void* lm, int V, Short
   int rc = launch_tc(a, U, lm, true, st);   // follows the heads GEMM
   if (rc) return rc;
   MDS_LAUNCH_TRY(launch_kernel(k_draft_merge, dim3(a.R), dim3(256), 0, st, true,
-                               static_cast<const float2*>(partial), a.n_fr, a.R, K, sl, smax, 0,
+                               static_cast<const float2*>(partial), a.n_rec, a.R, K, sl, smax, 0,
                                root, topk_id, topk_val));
   return MDS_OK;
 }
@@ -1417,18 +1516,19 @@ int lm_verify_draft_tc(const void* y, int B, int N, int d, const void* W, int K,
   a.partial = partial;
   a.partial2 = partial2;
   a.ws = ws;
+  a.N = N;
+  a.V = V;
+  a.tok = tok;
+  a.parent = parent;
+  a.child = childlogit;
   rc = launch_tc(a, U2, lm, true, st);       // follows the heads GEMM
   if (rc) return rc;
   MDS_LAUNCH_TRY(launch_kernel(k_verify_merge, dim3((Rv + 7) / 8), dim3(256), 0, st, true,
-                               static_cast<const float4*>(partial), a.n_fr, Rv, argmax, stats,
+                               static_cast<const float4*>(partial), a.n_rec, Rv, argmax, stats,
                                static_cast<const float2*>(nullptr), static_cast<int32_t*>(nullptr)));
   MDS_LAUNCH_TRY(launch_kernel(k_draft_merge, dim3(K * Rv), dim3(256), 0, st, true,
-                               static_cast<const float2*>(partial2), a.n_fr, K * Rv, K, sl, smax,
+                               static_cast<const float2*>(partial2), a.n_rec, K * Rv, K, sl, smax,
                                Rv, static_cast<int32_t*>(nullptr), tree_topk_id, tree_topk_val));
-  MDS_LAUNCH_TRY(launch_kernel(k_child_dot, dim3(B, (N + 7) / 8), dim3(256), 0, st, true,
-                               static_cast<const __nv_bfloat16*>(y),
-                               static_cast<const __nv_bfloat16*>(lm), N, d, V, tok, parent,
-                               childlogit, ws));
   return MDS_OK;
 }
 
@@ -1444,6 +1544,11 @@ int lm_verify_tc(const void* y, int B, int N, int d, const void* lm, int V, cons
   a.kind = TC_VERIFY;
   a.partial = partial;
   a.ws = ws;
+  a.N = N;
+  a.V = V;
+  a.tok = tok;
+  a.parent = parent;
+  a.child = childlogit;
   if (sample) {
     a.kind = TC_VSAMPLE;
     a.partial2 = partial2;
@@ -1455,13 +1560,9 @@ int lm_verify_tc(const void* y, int B, int N, int d, const void* lm, int V, cons
   int rc = launch_tc(a, y, lm, false, st);   // first kernel of the verify call
   if (rc) return rc;
   MDS_LAUNCH_TRY(launch_kernel(k_verify_merge, dim3((a.R + 7) / 8), dim3(256), 0, st, true,
-                               static_cast<const float4*>(partial), a.n_fr, a.R, argmax,
+                               static_cast<const float4*>(partial), a.n_rec, a.R, argmax,
                                stats, static_cast<const float2*>(sample ? partial2 : nullptr),
                                sample_id));
-  MDS_LAUNCH_TRY(launch_kernel(k_child_dot, dim3(B, (N + 7) / 8), dim3(256), 0, st, true,
-                               static_cast<const __nv_bfloat16*>(y),
-                               static_cast<const __nv_bfloat16*>(lm), N, d, V, tok, parent,
-                               childlogit, ws));
   return MDS_OK;
 }
 

@@ -24,10 +24,11 @@ namespace mds {
 namespace {
 
 // Rows B * (K + 1) one call may draft.  Each row needs one candidate list of
-// kMaxS (value, id) pairs per CTA of the LM-projection pass (at most 256
-// CTAs): 256 * 8 * 8 bytes = 16 KiB per row, 1 MiB for 64 rows.
+// kMaxS (value, id) pairs per partial record of the LM-projection pass (at
+// most 512: 256 CTAs, two epilogue warps per TMEM lane quarter):
+// 512 * 8 * 8 bytes = 32 KiB per row, 2 MiB for 64 rows.
 constexpr int kNoAllocMaxRows = 64;
-constexpr size_t kNoAllocPartialBytes = (size_t)kNoAllocMaxRows * 256 * kMaxS * 8;
+constexpr size_t kNoAllocPartialBytes = (size_t)kNoAllocMaxRows * 512 * kMaxS * 8;
 constexpr size_t kNoAllocBytes = kWsScratch + kNoAllocPartialBytes;
 
 // Layout matches a caller workspace: status word at offset 0, candidate

@@ -168,7 +168,7 @@ int lm_verify_draft_tc(const void* y, int B, int N, int d, const void* W, int K,
                        cudaStream_t st);
 // sample: also draw a token at every row (exact sampling at the given
 // temperature, Philox4x64-10 key (seed, 0), counter (v >> 3, n, P_b, b));
-// partial2 then holds kMaxCta float2 records per row, sample_id [B, N].
+// partial2 then holds one float2 record per row and feature range, sample_id [B, N].
 int lm_verify_tc(const void* y, int B, int N, int d, const void* lm, int V, const int32_t* tok,
                  const int32_t* parent, int32_t* argmax, float* stats, float* childlogit,
                  void* partial, bool sample, float temperature, unsigned long long seed,

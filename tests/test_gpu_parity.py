@@ -295,6 +295,51 @@ def test_lm_verify(mds, w):
     ties.report(w.name)
 
 
+@pytest.mark.parametrize("w", [MINI, MINI_F32], ids=lambda w: w.name)
+def test_lm_verify_bad_child_inputs(mds, w):
+    """A child token outside the vocabulary, or a parent outside the tree,
+    latches its error and leaves that child's logit 0; every other child
+    logit is still its parent row's logit at its token."""
+    x = ms.make_inputs(w, only=("lm",))
+    tr = oracle.build_tree(w.shortlist, w.max_rank_sum)
+    N = tr["N"]
+    y32 = ms.random_normal(w.seed, (w.B, N, w.d), scale=0.3, tag=5)
+    y_np = ms.bf16_bits(y32) if w.dtype == "bf16" else y32
+    tok = ms.random_tokens(w.seed, w.B, N, w.V, tag=6)
+    y64, lm = ms.as_f64(y_np, w.dtype), ms.as_f64(x["lm"], w.dtype)
+    want = oracle.verify_stats(y64, lm, tok.astype(np.int64), tr["parent"])["childlogit"]
+    cases = [("token", 1, (1, 5)), ("negative token", 1, (0, 9)), ("parent", 2, (None, 7))]
+    for what, code, (bb, c) in cases:
+        t2, p2 = tok.copy(), tr["parent"].copy()
+        if what == "token":
+            t2[bb, c] = w.V + 3
+        elif what == "negative token":
+            t2[bb, c] = -2
+        else:
+            p2[c] = N + 2
+        yd = dev(y_np, w.dtype)
+        argmax = torch.empty((w.B, N), dtype=torch.int32, device="cuda")
+        stats = torch.empty((w.B, N, 4), dtype=torch.float32, device="cuda")
+        child = torch.full((w.B, N), 7.0, dtype=torch.float32, device="cuda")
+        ws = mds.new_workspace(mds.workspace_size(1 if w.dtype == "bf16" else 0, w.B, w.d, w.V,
+                                                  w.K, N, w.Hq, w.Hkv, w.dh, w.smax))
+        mds.lm_verify(yd, dev(x["lm"], w.dtype), dev(t2, "i32"), dev(p2, "i32"), argmax, stats,
+                      child, ws)
+        torch.cuda.synchronize()
+        assert mds.status_check(ws) == code, what
+        g = host(child)
+        bad = np.zeros((w.B, N), bool)
+        if bb is None:
+            bad[:, c] = True
+        else:
+            bad[bb, c] = True
+        assert (g[bad] == 0.0).all(), what
+        assert (g[:, 0] == 0.0).all(), what
+        keep = ~bad
+        keep[:, 0] = False
+        close_float(g[keep], want[keep], w.dtype, "logit", f"childlogit ({what})")
+
+
 # ---------------------------------------------------------------------------
 # verify_accept
 # ---------------------------------------------------------------------------
