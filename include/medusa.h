@@ -62,7 +62,12 @@
  *    K-split form of the narrow projections (Wo at <= 128 rows);
  *    MDS_ATTN_GROUPED=0 keeps up to three query tiles per tree-attention
  *    work unit (64-key tiles) instead of one tile per unit with one CTA
- *    group per query tile, above 128 query rows per KV head.  One more
+ *    group per query tile, above 128 query rows per KV head;
+ *    MDS_GEMM_ROWTILES=1 or 2 forces the 128-row tiles per CTA of the
+ *    projections above 128 rows (normally chosen by MMA count);
+ *    MDS_ATTN_SEGCOST=n (one digit) sets the fixed cost, in key tiles, that
+ *    the tree-attention work split charges per unit (default 2; 0 splits
+ *    tiles evenly).  One more
  *    switch, read at every launch, exists to test the bounded waits:
  *    MDS_STALL_TEST=1 makes every projection-GEMM CTA first wait (1 ms limit)
  *    on a barrier that nothing completes, after which it gives up exactly as

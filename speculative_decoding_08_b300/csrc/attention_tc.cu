@@ -75,6 +75,7 @@ struct AttnArgs {
   int stages;
   int G;            // CTAs (n_grp groups of Gg)
   int n_grp, Gg;    // CTA groups, CTAs per group
+  int seg_cost;     // fixed cost of a work unit, in key tiles, for the split
   int mpg;          // units per (b, h) in one group: n_mg / n_grp
   float scale_log2; // log2(e) / sqrt(dh)
   const int32_t* P;
@@ -173,17 +174,41 @@ struct SegIter {
   }
 };
 
-__device__ __forceinline__ long long cta_start(long long Ttot, int G, int c) {
-  return (Ttot * c) / G;
+// Weighted stream-K.  Each unit also costs a.seg_cost tiles (its Q load and
+// its epilogue, which stall the pipeline), so the CTA boundaries are placed
+// evenly on an extended axis where unit u spans seg_cost + nt_u slots, then
+// moved to real tiles: a boundary inside a unit's fixed-cost slots goes to the
+// unit's first tile.  A CTA's range is thus a contiguous run of real tiles, as
+// in plain stream-K, and CTAs that cover many short units get fewer tiles.
+// pre[b] / pex[b] = first real / extended slot of sequence b in a group's
+// layout.
+__device__ __forceinline__ long long cta_start(const AttnArgs& a, const int* pre, const int* pex,
+                                               int c) {
+  const long long Text = pex[a.B];
+  if (c >= a.Gg) return pre[a.B];
+  const long long X = (Text * c) / a.Gg;
+  int lo = 0, hi = a.B;            // largest b with pex[b] <= X
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (pex[mid] <= X) lo = mid; else hi = mid;
+  }
+  const int nt = tiles_of(a, a.P[lo]);
+  if (nt == 0) return pre[lo];
+  const long long off = X - pex[lo];
+  const long long per = nt + a.seg_cost;
+  const long long idx = off / per;
+  const long long r = off - idx * per - a.seg_cost;
+  return pre[lo] + idx * nt + (r > 0 ? r : 0);
 }
 
-// Written by every CTA for the merge kernel: the unit whose last tile lies in
-// the CTA's range while its first tile lies in an earlier CTA's (each unit
-// split over several CTAs has exactly one such CTA), or unit = -1.
+// Written by every CTA for the merge kernel: its tile range, and the unit
+// whose last tile lies in the range while its first tile lies in an earlier
+// CTA's (each unit split over several CTAs has exactly one such CTA), or
+// unit = -1.
 struct MergeDesc {
   int unit, pad;
   long long U0;      // first tile of the unit in its group's layout
-  long long Ttot;    // tiles of one group
+  long long t0, t1;  // the CTA's tile range [t0, t1)
 };
 
 // Partial records: O [2 G][rows][DH] fp32, then (m, l) [2 G][rows], then
@@ -243,6 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* v_empty = bars + 46;          // [S]
   float* xbuf = reinterpret_cast<float*>(bars + 54);   // [2 parity][2 half][128 rows]
   int* pre = reinterpret_cast<int*>(xbuf + 512);  // [B + 1]
+  int* pex = pre + kMaxBAttn + 1;                  // [B + 1]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cta = blockIdx.x;
@@ -254,16 +280,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // tile prefix over sequences (every thread reads P; thread 0 scans)
   if (threadIdx.x == 0) {
-    int acc = 0;
+    int acc = 0, ext = 0;
     bool bad = false;
     for (int b = 0; b < a.B; ++b) {
       pre[b] = acc;
+      pex[b] = ext;
       const int Pb = a.P[b];
       const int nt = tiles_of(a, Pb);
       if (nt == 0) bad = true;
       acc += a.Hkv * a.mpg * nt;
+      ext += nt > 0 ? a.Hkv * a.mpg * (nt + a.seg_cost) : 0;
     }
     pre[a.B] = acc;
+    pex[a.B] = ext;
     if (bad && cta == 0) latch_error(a.ws, MDS_DEV_KV_CAPACITY);
     for (int s = 0; s < S; ++s) {
       ptx::mbar_init(&k_full[s], 1);
@@ -294,20 +323,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   grid_dep_wait();
   const uint32_t tmem = *tmem_slot;
-  const long long Ttot = (long long)pre[a.B];     // tiles of one group
   const int cgrp = cta / a.Gg, cidx = cta - cgrp * a.Gg;
   SegIter iter;
-  iter.t = cta_start(Ttot, a.Gg, cidx);
-  iter.end = cta_start(Ttot, a.Gg, cidx + 1);
+  iter.t = cta_start(a, pre, pex, cidx);
+  iter.end = cta_start(a, pre, pex, cidx + 1);
   iter.grp = cgrp;
+  const long long my_start = iter.t;
   if (threadIdx.x == 64) {
     SegIter it0 = iter;
     Seg s0;
-    MergeDesc md{-1, 0, 0, 0};
+    MergeDesc md{-1, 0, 0, iter.t, iter.end};
     if (it0.next(a, pre, s0) && s0.j0 > 0 && s0.j1 == s0.nt) {
       md.unit = s0.unit;
       md.U0 = s0.U0;
-      md.Ttot = Ttot;
     }
     merge_descs(a, NM * 128, DH)[cta] = md;
   }
@@ -681,7 +709,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       //      of the pair writes half of the O columns.
       const bool whole = s.j0 == 0 && s.j1 == s.nt;
       int slot = 0;
-      if (!whole) slot = 2 * cta + (cta_start(Ttot, a.Gg, cidx) >= s.U0 ? 0 : 1);
+      if (!whole) slot = 2 * cta + (my_start >= s.U0 ? 0 : 1);
       const int rows_unit = NM * 128;
       float ltot[kMaxNM];
       // split accumulators: weights of O_0 and O_1 relative to the combined
@@ -805,17 +833,16 @@ __global__ void __launch_bounds__(256) k_attention_merge(AttnArgs a) {
   const int r = mg * rows_unit + rloc;
   if (rloc >= rows_unit || r >= a.Mrows) return;
   const int grp = c / a.Gg, ci = c - grp * a.Gg;   // c within its group
-  const long long U0 = md.U0, Ttot = md.Ttot;
+  const long long U0 = md.U0;
+  const MergeDesc* gd = merge_descs(a, rows_unit, DH) + grp * a.Gg;   // the group's CTAs
   // group CTA holding tile U0
-  int i0 = (int)((U0 * a.Gg) / Ttot);
-  if (i0 > ci) i0 = ci;
-  while (i0 < ci && cta_start(Ttot, a.Gg, i0 + 1) <= U0) ++i0;
-  while (i0 > 0 && cta_start(Ttot, a.Gg, i0) > U0) --i0;
+  int i0 = ci;
+  while (i0 > 0 && gd[i0].t0 > U0) --i0;
   const float* pml = a.part + (long long)2 * a.G * rows_unit * DH;
   float M = -INFINITY;
   for (int i = i0; i <= ci; ++i) {
-    const long long st = cta_start(Ttot, a.Gg, i);
-    if (cta_start(Ttot, a.Gg, i + 1) == st) continue;     // empty range
+    const long long st = gd[i].t0;
+    if (gd[i].t1 == st) continue;     // empty range
     const int sl = 2 * (grp * a.Gg + i) + (st >= U0 ? 0 : 1);
     M = fmaxf(M, __ldcg(reinterpret_cast<const float2*>(pml) + (long long)sl * rows_unit + rloc).x);
   }
@@ -825,8 +852,8 @@ __global__ void __launch_bounds__(256) k_attention_merge(AttnArgs a) {
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
   float L = 0.f;
   for (int i = i0; i <= ci; ++i) {
-    const long long st = cta_start(Ttot, a.Gg, i);
-    if (cta_start(Ttot, a.Gg, i + 1) == st) continue;
+    const long long st = gd[i].t0;
+    if (gd[i].t1 == st) continue;
     const int sl = 2 * (grp * a.Gg + i) + (st >= U0 ? 0 : 1);
     const float2 ml = __ldcg(reinterpret_cast<const float2*>(pml) + (long long)sl * rows_unit + rloc);
     const float* po = a.part + ((long long)sl * rows_unit + rloc) * DH + lane * E;
@@ -868,6 +895,18 @@ bool grouped_enabled() {
   return on;
 }
 
+// Fixed cost of a work unit in key tiles (its Q load and epilogue): about
+// 4 us against 1.5-1.8 us per 128-key tile.  MDS_ATTN_SEGCOST=n overrides it
+// (0 gives plain stream-K); read once per process.
+int seg_cost() {
+  static const int v = [] {
+    const char* e = getenv("MDS_ATTN_SEGCOST");
+    if (e && e[0] >= '0' && e[0] <= '9' && e[1] == 0) return e[0] - '0';
+    return 2;
+  }();
+  return v;
+}
+
 struct Plan {
   int NM, n_mg, stages, G, BN, n_grp, Gg;
   size_t smem;
@@ -893,7 +932,7 @@ Plan plan(int N, int g, int dh, int num_sms) {
   const size_t q = (size_t)p.NM * 128 * dh * 2;
   const size_t pbuf = (p.BN == 128 ? 1 : 2) * (size_t)128 * p.BN * 2;
   const size_t stage = 2 * (size_t)p.BN * dh * 2;
-  const size_t fixed = 1024 /*align*/ + 54 * 8 + 512 * 4 + (kMaxBAttn + 1) * 4;
+  const size_t fixed = 1024 /*align*/ + 54 * 8 + 512 * 4 + 2 * (kMaxBAttn + 1) * 4;
   int st = (int)((kSmemLimit - q - pbuf - fixed) / stage);
   p.stages = st > 6 ? 6 : st;
   p.smem = q + pbuf + (size_t)p.stages * stage + fixed;
@@ -986,6 +1025,7 @@ int attention_tc(int B, int N, int Hq, int Hkv, int dh, int Pmax, const int32_t*
   a.n_grp = p.n_grp;
   a.Gg = p.Gg;
   a.mpg = p.n_mg / p.n_grp;
+  a.seg_cost = seg_cost();
   a.scale_log2 = 1.4426950408889634f / sqrtf((float)dh);
   a.P = P;
   a.mask = mask;

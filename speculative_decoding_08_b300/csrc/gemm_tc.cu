@@ -1250,6 +1250,16 @@ int init_host() {
 // stay below its share of the weight stream (F Kd 2 / SMs bytes), while every
 // feature range keeps at most 256 features (one chunk) and every split at
 // least two k-blocks.
+// MDS_GEMM_ROWTILES=1 or 2 forces the row tiles per CTA of the passes above
+// 128 rows (the draft pass excepted); read once per process.
+int rowtiles_override() {
+  static const int v = [] {
+    const char* e = getenv("MDS_GEMM_ROWTILES");
+    return (e && (e[0] == '1' || e[0] == '2') && e[1] == 0) ? e[0] - '0' : 0;
+  }();
+  return v;
+}
+
 int k_splits(int F, int Kd, int sms) {
   // Measured at batch 1: the split pays for its reduce kernel on Wo
   // (F = 4096: MMA floor ~4.6x the HBM time per CTA) but not on Wqkv or the
@@ -1284,12 +1294,35 @@ int launch_tc(TcArgs& a, const void* X, const void* W, bool dependent, cudaStrea
   if (a.R <= 0 || a.F <= 0) return MDS_OK;
   if (a.Kd % 64 != 0) return MDS_EUNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(X) | reinterpret_cast<uintptr_t>(W)) & 15) return MDS_EINVAL;
-  // Row tiles of 128 per CTA.  The draft pass keeps one tile per CTA at any
-  // row count: with 2.5 tiles of rows (batch 64 x 5 head rows) a pair per CTA
-  // leaves half the CTAs a single live tile while the others issue two MMAs
-  // per k-step over N = 128; one tile per CTA at N = 256 issues a quarter of
-  // the MMAs of the busiest such CTA and keeps every CTA equally loaded.
-  a.G = (a.R <= 128 || a.kind == TC_DRAFT) ? 1 : 2;
+  // Row tiles per CTA (G).  Up to 128 rows: one.  Above, G = 2 pairs two
+  // row tiles on each W tile (half the W reads from L2) but can leave CTAs a
+  // short last chunk; G = 1 spreads the row tiles over more CTAs and
+  // double-buffers its accumulator.  Every tcgen05.mma costs about the same
+  // up to N = 256, so the MMA count of the busiest CTA bounds these passes;
+  // G = 1 is taken when it issues at least 1/8 fewer.  At equal counts G = 2
+  // wins: the batch-64 verify pass ran 4.67 ms with G = 2 and 5.29 ms with
+  // G = 1 (twice the W traffic from L2), while G = 1 took the batch-8 QKV
+  // and output projections from 4 and 2 chunks per CTA to 3 and 1.  The draft
+  // pass keeps G = 1 at any row count: with 2.5 tiles of rows (batch 64 x 5
+  // head rows) a pair per CTA leaves half the CTAs a single live tile.
+  const int sms = g_num_sms < kMaxCta ? g_num_sms : kMaxCta;
+  a.n_units = (a.F + 15) / 16;
+  if (a.R <= 128 || a.kind == TC_DRAFT) {
+    a.G = 1;
+  } else {
+    auto mmas = [&](int G) -> long long {
+      const int nrg = (a.R + 128 * G - 1) / (128 * G);
+      const int nrs = min(nrg, sms);
+      const int nfr = max(1, min(sms / nrs, a.n_units));
+      const int NC = (G == 1 || a.kind == TC_VERIFY || a.kind == TC_VSAMPLE || nrs > 1) ? 256 : 128;
+      const long long units = (a.n_units + nfr - 1) / nfr;
+      const long long chunks = (units * 16 + NC - 1) / NC;
+      const long long groups = (nrg + nrs - 1) / nrs;
+      return groups * chunks * G;
+    };
+    const int forced = rowtiles_override();
+    a.G = forced ? forced : (8 * mmas(1) <= 7 * mmas(2) ? 1 : 2);
+  }
   // Features per MMA (N) and accumulator buffers.  Every tcgen05.mma costs
   // about the same up to N = 256, so N is 256 where TMEM allows: with one
   // 128-row group, double-buffered (the epilogue of one chunk overlaps the
@@ -1304,13 +1337,11 @@ int launch_tc(TcArgs& a, const void* X, const void* W, bool dependent, cudaStrea
   // below 256; the n_rs CTAs that share a range read its weights at about
   // the same time, so HBM sees them once and L2 serves the rest.
   a.n_rgroups = (a.R + 128 * a.G - 1) / (128 * a.G);
-  a.n_units = (a.F + 15) / 16;
-  const int sms = g_num_sms < kMaxCta ? g_num_sms : kMaxCta;
   a.n_rs = a.n_rgroups >= 2 ? min(a.n_rgroups, sms) : 1;
   a.n_fr = max(1, min(sms / a.n_rs, a.n_units));
   a.n_cta = a.n_rs * a.n_fr;
   a.ks = 1;
-  if (a.G == 1 && a.kpart && ksplit_enabled() &&
+  if (a.R <= 128 && a.kpart && ksplit_enabled() &&
       (a.kind == TC_STORE || a.kind == TC_HEADS || a.kind == TC_QKV)) {
     a.ks = k_splits(a.F, a.Kd, sms);
     if (a.ks > 1) {
