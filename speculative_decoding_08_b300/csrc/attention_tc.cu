@@ -142,11 +142,12 @@ struct Seg {
 };
 
 // Walks the segments of the CTA's tile range [t, end) within its group.
-// pre[b] = first tile of sequence b in a group's layout (shared memory,
-// B + 1 entries).
+// pre[b] = first tile of sequence b in a group's layout, sp[b] = P_b (both in
+// shared memory, read from P once in the prologue).
 struct SegIter {
   long long t, end;
   int grp;          // CTA group: units of query tiles [grp mpg, grp mpg + mpg)
+  const int* sp;
   __device__ __forceinline__ bool next(const AttnArgs& a, const int* pre, Seg& s) {
     if (t >= end) return false;
     int lo = 0, hi = a.B;          // largest b with pre[b] <= t
@@ -155,7 +156,7 @@ struct SegIter {
       if (pre[mid] <= t) lo = mid; else hi = mid;
     }
     const int b = lo;
-    const int Pb = a.P[b];
+    const int Pb = sp[b];
     const int nt = tiles_of(a, Pb);
     const long long off = t - (long long)pre[b];
     const int idx = (int)(off / nt);
@@ -183,7 +184,7 @@ struct SegIter {
 // pre[b] / pex[b] = first real / extended slot of sequence b in a group's
 // layout.
 __device__ __forceinline__ long long cta_start(const AttnArgs& a, const int* pre, const int* pex,
-                                               int c) {
+                                               const int* sp, int c) {
   const long long Text = pex[a.B];
   if (c >= a.Gg) return pre[a.B];
   const long long X = (Text * c) / a.Gg;
@@ -192,7 +193,7 @@ __device__ __forceinline__ long long cta_start(const AttnArgs& a, const int* pre
     const int mid = (lo + hi) >> 1;
     if (pex[mid] <= X) lo = mid; else hi = mid;
   }
-  const int nt = tiles_of(a, a.P[lo]);
+  const int nt = tiles_of(a, sp[lo]);
   if (nt == 0) return pre[lo];
   const long long off = X - pex[lo];
   const long long per = nt + a.seg_cost;
@@ -269,6 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* xbuf = reinterpret_cast<float*>(bars + 54);   // [2 parity][2 half][128 rows]
   int* pre = reinterpret_cast<int*>(xbuf + 512);  // [B + 1]
   int* pex = pre + kMaxBAttn + 1;                  // [B + 1]
+  int* sp = pex + kMaxBAttn + 1;                   // [B]: P_b
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cta = blockIdx.x;
@@ -286,6 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       pre[b] = acc;
       pex[b] = ext;
       const int Pb = a.P[b];
+      sp[b] = Pb;
       const int nt = tiles_of(a, Pb);
       if (nt == 0) bad = true;
       acc += a.Hkv * a.mpg * nt;
@@ -325,9 +328,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const int cgrp = cta / a.Gg, cidx = cta - cgrp * a.Gg;
   SegIter iter;
-  iter.t = cta_start(a, pre, pex, cidx);
-  iter.end = cta_start(a, pre, pex, cidx + 1);
+  iter.t = cta_start(a, pre, pex, sp, cidx);
+  iter.end = cta_start(a, pre, pex, sp, cidx + 1);
   iter.grp = cgrp;
+  iter.sp = sp;
   const long long my_start = iter.t;
   if (threadIdx.x == 64) {
     SegIter it0 = iter;
@@ -932,7 +936,7 @@ Plan plan(int N, int g, int dh, int num_sms) {
   const size_t q = (size_t)p.NM * 128 * dh * 2;
   const size_t pbuf = (p.BN == 128 ? 1 : 2) * (size_t)128 * p.BN * 2;
   const size_t stage = 2 * (size_t)p.BN * dh * 2;
-  const size_t fixed = 1024 /*align*/ + 54 * 8 + 512 * 4 + 2 * (kMaxBAttn + 1) * 4;
+  const size_t fixed = 1024 /*align*/ + 54 * 8 + 512 * 4 + 3 * (kMaxBAttn + 1) * 4;
   int st = (int)((kSmemLimit - q - pbuf - fixed) / stage);
   p.stages = st > 6 ? 6 : st;
   p.smem = q + pbuf + (size_t)p.stages * stage + fixed;

@@ -443,16 +443,27 @@ __device__ __forceinline__ void colpar_block(const TcArgs& a, float* tile,
   __syncwarp();
   const bool valid = lane < nv;
   const int f = f0 + lane;
-  for (int rr = 0; rr < nlive; ++rr) {
-    const float x = tile[rr * 33 + lane];
-    if constexpr (KIND == TC_HEADS) {
-      if (valid) {
-        const int b = row_base + rr;
-        const int i = f / a.d, j = f - i * a.d;
-        const __nv_bfloat16 hraw = a.h[(long long)b * a.d + j];
-        __nv_bfloat16* U = static_cast<__nv_bfloat16*>(a.out) + (long long)b * a.u_row;
-        U[(long long)(1 + i) * a.u_head + j] = __float2bfloat16_rn(__bfloat162float(hraw) + silu_fast(x));
-        if (i == 0) U[j] = hraw;
+  if constexpr (KIND == TC_HEADS) {
+    if (valid) {
+      const int i = f / a.d, j = f - i * a.d;
+      // eight rows at a time, their h loads all issued before the first
+      // store (the compiler cannot move a load of h above a store to U)
+      for (int r0 = 0; r0 < nlive; r0 += 8) {
+        __nv_bfloat16 hraw[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (r0 + q < nlive) hraw[q] = __ldg(a.h + (long long)(row_base + r0 + q) * a.d + j);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          if (r0 + q < nlive) {
+            const int b = row_base + r0 + q;
+            const float x = tile[(r0 + q) * 33 + lane];
+            __nv_bfloat16* U = static_cast<__nv_bfloat16*>(a.out) + (long long)b * a.u_row;
+            U[(long long)(1 + i) * a.u_head + j] =
+                __float2bfloat16_rn(__bfloat162float(hraw[q]) + silu_fast(x));
+            if (i == 0) U[j] = hraw[q];
+          }
+        }
       }
     }
   }
@@ -508,13 +519,23 @@ __device__ __forceinline__ ChildNext child_after(const TcArgs& a, int row, int t
   const int b = row / a.N, n = row - b * a.N;
   const int32_t* tk = a.tok + (long long)b * a.N;
   ChildNext r{0x7fffffff, 0};
-  for (int c = 1; c < a.N; ++c) {
-    if (__ldg(a.parent + c) != n) continue;
-    const int t = __ldg(tk + c);
-    if (t >= f_end || t < t0 || (t == t0 && c <= c0)) continue;
-    if (t < r.tok || (t == r.tok && c < r.c)) {
-      r.tok = t;
-      r.c = c;
+  // 16 nodes at a time, all their parent and token loads in flight together
+  for (int cb = 1; cb < a.N; cb += 16) {
+    int pa[16], tv[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const int c = cb + q;
+      pa[q] = c < a.N ? __ldg(a.parent + c) : -1;
+      tv[q] = c < a.N ? __ldg(tk + c) : 0;
+    }
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const int c = cb + q, t = tv[q];
+      if (pa[q] != n || t >= f_end || t < t0 || (t == t0 && c <= c0)) continue;
+      if (t < r.tok || (t == r.tok && c < r.c)) {
+        r.tok = t;
+        r.c = c;
+      }
     }
   }
   return r;
@@ -544,15 +565,25 @@ __device__ __forceinline__ void child_pick(const TcArgs& a, int row, ChildNext& 
 __device__ __forceinline__ void child_check(const TcArgs& a, int row) {
   const int b = row / a.N;
   a.child[(long long)b * a.N] = 0.f;
-  for (int c = 1; c < a.N; ++c) {
-    const int pa = __ldg(a.parent + c);
-    const int t = __ldg(a.tok + (long long)b * a.N + c);
-    if (pa < 0 || pa >= a.N) {
-      latch_error(a.ws, MDS_DEV_TREE_INDEX);
-      a.child[(long long)b * a.N + c] = 0.f;
-    } else if (t < 0 || t >= a.V) {
-      latch_error(a.ws, MDS_DEV_TOKEN_RANGE);
-      a.child[(long long)b * a.N + c] = 0.f;
+  for (int cb = 1; cb < a.N; cb += 16) {
+    int pa[16], tv[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const int c = cb + q;
+      pa[q] = c < a.N ? __ldg(a.parent + c) : 0;
+      tv[q] = c < a.N ? __ldg(a.tok + (long long)b * a.N + c) : 0;
+    }
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const int c = cb + q;
+      if (c >= a.N) break;
+      if (pa[q] < 0 || pa[q] >= a.N) {
+        latch_error(a.ws, MDS_DEV_TREE_INDEX);
+        a.child[(long long)b * a.N + c] = 0.f;
+      } else if (tv[q] < 0 || tv[q] >= a.V) {
+        latch_error(a.ws, MDS_DEV_TOKEN_RANGE);
+        a.child[(long long)b * a.N + c] = 0.f;
+      }
     }
   }
 }
