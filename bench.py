@@ -411,6 +411,131 @@ def measure(w, args, dev, world, e2e=True):
     return out
 
 
+def measure_next_rows(w, dev, pk, reps=20):
+    """One step of each widened form of the path on workload w, each captured
+    as a CUDA graph and replayed (prefix length restored inside the graph):
+    the decoding loop's steady-state step in its separate and fused forms,
+    the verify call with exact sampling against the plain verify call, a
+    two-layer backbone verify pass, and MTP-style transformer-layer draft
+    heads.  Returns microseconds per step (or call) with the step's
+    algorithmic bytes against the measured HBM bandwidth."""
+    import torch
+    import speculative_decoding_08_b300 as mds
+
+    x = ms.make_inputs(w)
+
+    def t(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(a).to(dev)
+
+    s = torch.cuda.Stream(device=dev)
+
+    def timed(fn):
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                fn()
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                g.replay()
+            e0.record(s)
+            for _ in range(reps):
+                g.replay()
+            e1.record(s)
+        s.synchronize()
+        return 1e3 * e0.elapsed_time(e1) / reps
+
+    e = 2 if w.dtype == "bf16" else 4
+    lm_b, heads_b = w.V * w.d * e, w.K * w.d * w.d * e
+    attn_w = ((w.Hq + 2 * w.Hkv) * w.dh * w.d + w.d * w.Hq * w.dh) * e
+    kv_b = int(np.sum(x["P"])) * w.Hkv * w.dh * 2 * e
+
+    def entry(us, nbytes):
+        return {"us": us, "algorithmic_bytes": nbytes,
+                "hbm_frac": nbytes / (us * 1e-6) / (pk["hbm"] * 1e9)}
+
+    out = {"workload": w.name}
+    wt = {k: t(x[k]) for k in ("W", "lm", "emb", "wqkv", "wo", "kc", "vc")}
+    P0 = torch.from_numpy(x["P"]).to(dev)
+    P = P0.clone()
+    h = t(x["h"])
+    step = mds.MedusaStep(W=wt["W"], lm=wt["lm"], emb=wt["emb"], wqkv=wt["wqkv"], wo=wt["wo"],
+                          Kc=wt["kc"], Vc=wt["vc"], P=P, shortlist=w.shortlist,
+                          max_rank_sum=w.max_rank_sum, Hq=w.Hq, Hkv=w.Hkv, B=w.B)
+
+    def sep():
+        P.copy_(P0)
+        step.decode_step(h, False, mds.TYPICAL, w.eps, w.delta)
+    out["loop_separate"] = entry(timed(sep), heads_b + 2 * lm_b + attn_w + kv_b)
+    if step.fused_ok:
+        step.begin_decode(h, True)
+
+        def fus():
+            P.copy_(P0)
+            step.decode_step(h, True, mds.TYPICAL, w.eps, w.delta)
+        out["loop_fused"] = entry(timed(fus), heads_b + lm_b + attn_w + kv_b)
+    step.run(h, mode=mds.TYPICAL, eps=w.eps, delta=w.delta, commit=False)
+
+    def ver():
+        mds.lm_verify(step.y, step.lm, step.tok, step.parent, step.argmax, step.stats,
+                      step.childlogit, step.ws)
+
+    def ver_s():
+        mds.lm_verify_sample(step.y, step.lm, step.tok, step.parent, step.P, 1.0, 7,
+                             step.argmax, step.stats, step.childlogit, step.sample_id, step.ws)
+    out["verify"] = entry(timed(ver), lm_b)
+    out["verify_sampling"] = entry(timed(ver_s), lm_b)
+    assert mds.status_check(step.ws) == 0, "device latched a data error"
+    del step
+    torch.cuda.empty_cache()
+
+    if w.dtype == "bf16":
+        n_layers = 2
+        lays = ms.make_layers(w, n_layers, x)
+        layers = [dict(wqkv=t(lw["wqkv"]), wo=t(lw["wo"]), Kc=t(lw["kc"]), Vc=t(lw["vc"]))
+                  for lw in lays]
+        P.copy_(P0)
+        bstep = mds.BackboneStep(layers=layers, rope_base=10000.0, W=wt["W"], lm=wt["lm"],
+                                 emb=wt["emb"], P=P, shortlist=w.shortlist,
+                                 max_rank_sum=w.max_rank_sum, Hq=w.Hq, Hkv=w.Hkv, B=w.B)
+
+        def bb():
+            P.copy_(P0)
+            bstep.run(h, mode=mds.TYPICAL, eps=w.eps, delta=w.delta)
+        out["backbone_2_layers"] = entry(timed(bb), heads_b + 2 * lm_b + n_layers * (attn_w + kv_b))
+        assert mds.status_check(bstep.ws) == 0, "device latched a data error"
+        del bstep, layers
+        torch.cuda.empty_cache()
+
+        dff = 2 * w.d
+        hs = ms.make_mtp_heads(w, dff)
+        heads = [dict(wqkv=t(hw["wqkv"]), wo=t(hw["wo"]), w1=t(hw["w1"]), w2=t(hw["w2"]),
+                      Kc=t(hw["kc"]), Vc=t(hw["vc"])) for hw in hs]
+        P.copy_(P0)
+        mstep = mds.MTPStep(heads=heads, rope_base=10000.0, lm=wt["lm"], emb=wt["emb"],
+                            wqkv=wt["wqkv"], wo=wt["wo"], Kc=wt["kc"], Vc=wt["vc"], P=P,
+                            shortlist=w.shortlist, max_rank_sum=w.max_rank_sum, Hq=w.Hq,
+                            Hkv=w.Hkv, B=w.B)
+        mstep.begin_decode(h, False)
+
+        def mt():
+            P.copy_(P0)
+            mstep.decode_step(h, False, mds.TYPICAL, w.eps, w.delta)
+        head_w = w.K * (attn_w + 2 * dff * w.d * e)
+        out["mtp_heads_loop"] = entry(timed(mt), head_w + 2 * lm_b + attn_w + kv_b)
+        assert mds.status_check(mstep.ws) == 0, "device latched a data error"
+        del mstep, heads
+    del wt, h
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
 def summarise(r, world, steps, pk):
     """Whole-job numbers and per-pass rooflines of one measured workload."""
     w = r["w"]
@@ -462,6 +587,9 @@ def run_ours(args):
         results[name] = measure(ms.workload(name), args, dev, world, e2e=False)
     head = measure(head_w, args, dev, world, e2e=True)
     clk = clocks.stop()
+    nxt = None
+    if args.next_rows != "none" and rank == 0:
+        nxt = measure_next_rows(ms.workload(args.next_rows), dev, pk)
 
     # max over ranks (device-timed steps and the end-to-end loop)
     keys = [head["ms_total"], head["e2e_dt"]] + [results[n]["ms_total"] for n in also]
@@ -518,6 +646,8 @@ def run_ours(args):
                  "passes": s2["passes"], "step_roofline": s2["step"], "dominant": s2["dominant"]}
     if wl:
         line["workloads"] = wl
+    if nxt is not None:
+        line["next_rows"] = nxt
     if not args.no_cpu_baseline:
         cb, _, _, _ = oracle_sample(w, head["x"], budget_s=args.cpu_budget)
         cb["one_core"] = one_core_baseline(w)
@@ -567,6 +697,9 @@ def main():
                     help="other workloads measured in the same run (comma list, or none)")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--next-rows", default="vicuna7b-b1",
+                    help="workload on which the widened forms (loop, sampling, backbone "
+                         "layers, MTP heads) are timed, or none")
     args = ap.parse_args()
     if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
         raise SystemExit(relaunch(args))
