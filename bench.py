@@ -48,6 +48,12 @@ CSRC = os.path.join(ROOT, "speculative_decoding_08_b300", "csrc")
 TRAFFIC_JSON = os.path.join(ROOT, "profiles", "dram_traffic.json")
 
 
+# Nominal B300 figures (HBM3e bandwidth, dense bf16 tensor rate), reported
+# beside the measured-peak fractions.
+NOMINAL_HBM_GBS = 7700.0
+NOMINAL_BF16_TFLOPS = 2250.0
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -103,7 +109,9 @@ def roofline_entry(work, seconds, pk):
         bound, achieved, peak, unit = "hbm", gbs, pk["hbm"], "GB/s"
     return {"us": seconds * 1e6, "bound": bound, "achieved": achieved, "peak": peak,
             "unit": unit, "frac": achieved / peak, "hbm_gbs": gbs, "hbm_frac": gbs / pk["hbm"],
+            "hbm_frac_nominal": gbs / NOMINAL_HBM_GBS,
             "tflops": tfs, "tensor_frac": tfs / pk["bf16_sustained"],
+            "tensor_frac_nominal": tfs / NOMINAL_BF16_TFLOPS,
             "algorithmic_bytes": work["bytes"], "flops": work["flops"]}
 
 
