@@ -32,8 +32,11 @@
 //   S = Q K^T      tcgen05, M = 128 query rows, N = BN keys, K = dh      -> TMEM
 //   softmax        one thread per query row reads its S row from TMEM,
 //                  masks, keeps a running max m (log2 domain) and sum l,
-//                  writes P = 2^(S - m) as bf16 into shared memory
-//   O += P V       tcgen05, M = 128, N = dh, K = BN keys, V read MN-major -> TMEM
+//                  writes P = 2^(S - m) as bf16 back into TMEM over the S
+//                  tile it came from (one query tile per unit) or into
+//                  shared memory (several)
+//   O += P V       tcgen05, M = 128, N = dh, K = BN keys, P from TMEM or
+//                  shared memory, V read MN-major                          -> TMEM
 //
 // The running max is raised lazily: O is rescaled only when a row's maximum
 // grows by more than 2^8, so the accumulator in TMEM is rarely touched; the
@@ -72,7 +75,7 @@ struct AttnArgs {
   int BN;           // keys per tile (128 with one query tile per unit, else 64)
   int NM;           // query tiles per unit
   int n_mg;         // units per (b, h)
-  int stages;
+  int sk, sv;       // K and V ring depths
   int G;            // CTAs (n_grp groups of Gg)
   int n_grp, Gg;    // CTA groups, CTAs per group
   int seg_cost;     // fixed cost of a work unit, in key tiles, for the split
@@ -103,6 +106,34 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
       "f"(v[15]), "f"(v[16]), "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]),
       "f"(v[22]), "f"(v[23]), "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]),
       "f"(v[29]), "f"(v[30]), "f"(v[31])
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// tcgen05.mma with A read from tensor memory: M = 128 rows in lanes 0..127,
+// the K = 16 bf16 values of a row packed two per 32-bit column (8 columns,
+// the lower-indexed value in the low half) from column a_tmem on.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
+          taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
+      "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
+      "r"(v[29]), "r"(v[30]), "r"(v[31])
       : "memory");
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -227,9 +258,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kHalves = DH / 64;
   constexpr uint32_t kQTileBytes = 128 * DH * 2;
   constexpr uint32_t kKVHalfBytes = kBN * 128;            // BN keys x 64 dh x 2 B
-  constexpr uint32_t kStageBytes = 2 * kHalves * kKVHalfBytes;
+  constexpr uint32_t kSlotBytes = kHalves * kKVHalfBytes; // one K or V tile
   constexpr uint32_t kPBytes = 128 * kBN * 2;             // one P tile (kBN / 64 atoms)
-  constexpr int kNP = kBN == 128 ? 1 : 2;                 // P buffers
+  constexpr int kNP = kBN == 128 ? 1 : 2;                 // P buffers in shared memory
+  // One query tile per unit: P is written into tensor memory over the S tile
+  // it came from (each warp over the first half of its own S columns) and the
+  // P V MMAs read it from there; shared memory then holds only Q and the K
+  // and V rings.  Several query tiles keep P in shared memory.
+  constexpr bool kPT = NM == 1;
   constexpr int kWC = kBN / 2;                            // keys per softmax warp
   constexpr uint32_t kSCol0 = 0;                          // S: 2 x kBN columns
   constexpr uint32_t kOCol0 = 2 * kBN;                    // O: NM x DH columns
@@ -245,15 +281,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  const int S = a.stages;
+  const int SK = a.sk, SV = a.sv;
   uint8_t* sQ = smem;
   uint8_t* sP = sQ + NM * kQTileBytes;
-  uint8_t* sKV = sP + kNP * kPBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + S * kStageBytes);
-  // K and V of a stage have their own barriers: K is free again once the S
-  // MMAs of its tile are done, V only after the P V MMAs.
-  uint64_t* k_full = bars;                // [S]
-  uint64_t* k_empty = bars + 8;           // [S]
+  uint8_t* sK = sP + (kPT ? 0 : kNP * kPBytes);
+  uint8_t* sV = sK + SK * kSlotBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + SV * kSlotBytes);
+  // K and V rings with their own depths and barriers: a K slot is free again
+  // once the S MMAs of its tile are done, a V slot only after the P V MMAs.
+  // p_empty[i] completes when the P V MMAs of an item i mod 2 (tensor-memory
+  // P) or i mod kNP (shared-memory P) are done.
+  uint64_t* k_full = bars;                // [SK]
+  uint64_t* k_empty = bars + 8;           // [SK]
   uint64_t* s_full = bars + 16;           // [2]
   uint64_t* s_empty = bars + 18;          // [2]
   uint64_t* p_full = bars + 20;           // [2]
@@ -265,8 +304,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 32);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   uint64_t* xbar = bars + 34;                     // [4] pair exchanges, one per lane quarter
-  uint64_t* v_full = bars + 38;           // [S]
-  uint64_t* v_empty = bars + 46;          // [S]
+  uint64_t* v_full = bars + 38;           // [SV]
+  uint64_t* v_empty = bars + 46;          // [SV]
   float* xbuf = reinterpret_cast<float*>(bars + 54);   // [2 parity][2 half][128 rows]
   int* pre = reinterpret_cast<int*>(xbuf + 512);  // [B + 1]
   int* pex = pre + kMaxBAttn + 1;                  // [B + 1]
@@ -297,9 +336,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     pre[a.B] = acc;
     pex[a.B] = ext;
     if (bad && cta == 0) latch_error(a.ws, MDS_DEV_KV_CAPACITY);
-    for (int s = 0; s < S; ++s) {
+    for (int s = 0; s < SK; ++s) {
       ptx::mbar_init(&k_full[s], 1);
       ptx::mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < SV; ++s) {
       ptx::mbar_init(&v_full[s], 1);
       ptx::mbar_init(&v_empty[s], 1);
     }
@@ -352,17 +393,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_kv = a.n_grp > 1 ? ptx::policy_evict_normal() : ptx::policy_evict_first();
       const uint64_t pol_q = ptx::policy_evict_last();
       // Requests in the order the slots free up: K of tile t (its slot frees
-      // when the S MMAs of tile t - S are done), then V of tile t - 1 (slot
-      // frees after the P V MMAs of tile t - 1 - S).  At a unit's first tile
+      // when the S MMAs of tile t - SK are done), then V of tile t - 1 (slot
+      // frees after the P V MMAs of tile t - 1 - SV).  At a unit's first tile
       // the pending V goes before the unit's Q: the P V MMAs of the previous
       // tile precede that unit's last S MMA, which frees Q.
       int kvt = 0, vt = 0, segc = 0;
       int v_row = 0;                  // KV row of the pending V tile (vt)
       bool ok = true;
       auto issue_v = [&]() -> bool {
-        const int st = vt % S;
-        if (!ptx::mbar_wait(&v_empty[st], ((vt / S) & 1) ^ 1u, abort_flag, kWaitNs)) return false;
-        uint8_t* sv = sKV + st * kStageBytes + kHalves * kKVHalfBytes;
+        const int st = vt % SV;
+        if (!ptx::mbar_wait(&v_empty[st], ((vt / SV) & 1) ^ 1u, abort_flag, kWaitNs)) return false;
+        uint8_t* sv = sV + st * kSlotBytes;
         ptx::mbar_arrive_expect_tx(&v_full[st], kHalves * kKVHalfBytes);
         for (int hh = 0; hh < kHalves; ++hh)
           ptx::tma_load_2d(sv + hh * kKVHalfBytes, &tmV, hh * 64, v_row, &v_full[st], pol_kv);
@@ -382,12 +423,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++segc;
         const int kvrow0 = (s.b * a.Hkv + s.h) * a.Pmax;
         for (int j = s.j0; j < s.j1; ++j, ++kvt) {
-          const int st = kvt % S;
-          if (!ptx::mbar_wait(&k_empty[st], ((kvt / S) & 1) ^ 1u, abort_flag, kWaitNs)) {
+          const int st = kvt % SK;
+          if (!ptx::mbar_wait(&k_empty[st], ((kvt / SK) & 1) ^ 1u, abort_flag, kWaitNs)) {
             ok = false;
             break;
           }
-          uint8_t* sk = sKV + st * kStageBytes;
+          uint8_t* sk = sK + st * kSlotBytes;
           ptx::mbar_arrive_expect_tx(&k_full[st], kHalves * kKVHalfBytes);
           for (int hh = 0; hh < kHalves; ++hh)
             ptx::tma_load_2d(sk + hh * kKVHalfBytes, &tmK, hh * 64, kvrow0 + j * kBN,
@@ -402,13 +443,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 1;
       }
       // drain: the copies issued last into each stage and into Q have landed
-      for (int i = 0; i < S && i < kvt; ++i) {
+      for (int i = 0; i < SK && i < kvt; ++i) {
         const int t = kvt - 1 - i;
-        ptx::mbar_wait(&k_full[t % S], (t / S) & 1, nullptr, kWaitNs);
+        ptx::mbar_wait(&k_full[t % SK], (t / SK) & 1, nullptr, kWaitNs);
       }
-      for (int i = 0; i < S && i < vt; ++i) {
+      for (int i = 0; i < SV && i < vt; ++i) {
         const int t = vt - 1 - i;
-        ptx::mbar_wait(&v_full[t % S], (t / S) & 1, nullptr, kWaitNs);
+        ptx::mbar_wait(&v_full[t % SV], (t / SV) & 1, nullptr, kWaitNs);
       }
       if (segc > 0) ptx::mbar_wait(q_full, (segc - 1) & 1, nullptr, kWaitNs);
     }
@@ -418,24 +459,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t idS = ptx::idesc_bf16(128, kBN);
     const uint32_t idO = ptx::idesc_bf16(128, DH) | (1u << 16);   // B (V) MN-major
     int it = 0, kvt = 0, segc = 0;
-    // pending P V: item, query tile, stage, first tile of the unit, last
-    // query tile of the key tile, key-tile number, valid keys in the tile
-    int pv_it = -1, pv_m = 0, pv_stage = 0, pv_first = 0, pv_lastm = 0, pv_t = 0, pv_nv = 0;
+    // pending P V: item, query tile, first tile of the unit, last query tile
+    // of the key tile, key-tile number (its V slot is pv_t mod SV), valid
+    // keys in the tile
+    int pv_it = -1, pv_m = 0, pv_first = 0, pv_lastm = 0, pv_t = 0, pv_nv = 0;
     bool ok = true;
     auto wait = [&](uint64_t* bar, uint32_t par) {
       if (!ok) return false;
       if (!ptx::mbar_wait(bar, par, abort_flag, kWaitNs)) ok = false;
       return ok;
     };
-    // O[m] += P[it % 2] V[stage]
+    // O[m] += P V[slot]: P of item pv_it read from its S buffer in tensor
+    // memory, or from shared-memory P buffer pv_it mod kNP
     auto issue_pv = [&]() {
-      const int pb = pv_it % kNP;
-      if (!wait(&p_full[pb], (pv_it / kNP) & 1)) return;
-      if (!wait(&v_full[pv_stage], (pv_t / S) & 1)) return;
+      const int pb = kPT ? (pv_it & 1) : pv_it % kNP;
+      if (!wait(&p_full[pb], kPT ? ((pv_it >> 1) & 1) : ((pv_it / kNP) & 1))) return;
+      const int vs = pv_t % SV;
+      if (!wait(&v_full[vs], (pv_t / SV) & 1)) return;
+      uint8_t* sv = sV + vs * kSlotBytes;
       if (pv_m == 0 && pv_nv < kBN) {
         // keys past the unit's end: zero their V rows so that stale cache
         // contents (never weighted, P = 0) cannot inject NaN into O
-        uint8_t* sv = sKV + pv_stage * kStageBytes + kHalves * kKVHalfBytes;
         for (int hh = 0; hh < kHalves; ++hh)
           for (int i = pv_nv * 8 + lane; i < kBN * 8; i += 32)
             reinterpret_cast<uint4*>(sv + hh * kKVHalfBytes)[i] = make_uint4(0, 0, 0, 0);
@@ -444,20 +488,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ptx::tc_fence_after();
       if (lane == 0) {
-        const uint32_t aP = ptx::smem_addr(sP + pb * kPBytes);
-        const uint32_t bV = ptx::smem_addr(sKV + pv_stage * kStageBytes + kHalves * kKVHalfBytes);
+        const uint32_t bV = ptx::smem_addr(sv);
         const uint32_t dO = tmem + kOCol0 + (uint32_t)(pv_m * DH);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
           // split accumulators: keys [0, 64) into O_0, [64, 128) into O_1
           const bool second = kSplitO && kk >= 4;
           const bool fresh = pv_first && (kk == 0 || (kSplitO && kk == 4));
-          ptx::mma_bf16(dO + (second ? (uint32_t)DH : 0u),
-                        ptx::sdesc_k128(aP + (kk >> 2) * 16384 + (kk & 3) * 32),
-                        sdesc_mn128(bV + kk * 2048, kKVHalfBytes), idO, fresh ? 0u : 1u);
+          const uint64_t bd = sdesc_mn128(bV + kk * 2048, kKVHalfBytes);
+          if constexpr (kPT) {
+            // P of keys [16 kk, 16 kk + 16): the warp of keys [0, 64) wrote
+            // columns [0, 32) of the S buffer, the other columns [64, 96)
+            const uint32_t aT = tmem + kSCol0 + (uint32_t)(pb * kBN) +
+                                (uint32_t)(kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
+            mma_bf16_ts(dO + (second ? (uint32_t)DH : 0u), aT, bd, idO, fresh ? 0u : 1u);
+          } else {
+            const uint32_t aP = ptx::smem_addr(sP + pb * kPBytes);
+            ptx::mma_bf16(dO + (second ? (uint32_t)DH : 0u),
+                          ptx::sdesc_k128(aP + (kk >> 2) * 16384 + (kk & 3) * 32), bd, idO,
+                          fresh ? 0u : 1u);
+          }
         }
         ptx::mma_commit(&p_empty[pb]);
-        if (pv_lastm) ptx::mma_commit(&v_empty[pv_stage]);
+        if (pv_lastm) ptx::mma_commit(&v_empty[vs]);
       }
       __syncwarp();
     };
@@ -466,16 +519,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!wait(q_full, segc & 1)) break;
       const int Lk = s.Pb + a.N;
       for (int j = s.j0; j < s.j1 && ok; ++j, ++kvt) {
-        const int st = kvt % S;
-        if (!wait(&k_full[st], (kvt / S) & 1)) break;
+        const int st = kvt % SK;
+        if (!wait(&k_full[st], (kvt / SK) & 1)) break;
         const int nv = Lk - j * kBN;
         for (int m = 0; m < NM; ++m, ++it) {
           const int sb = it & 1;
           if (!wait(&s_empty[sb], ((it >> 1) & 1) ^ 1u)) break;
+          // tensor-memory P: the buffer also holds P(it - 2) until its P V
+          // MMAs are done
+          if (kPT && it >= 2 && !wait(&p_empty[sb], ((it - 2) >> 1) & 1)) break;
           ptx::tc_fence_after();
           if (lane == 0) {
             const uint32_t aQ = ptx::smem_addr(sQ + m * kQTileBytes);
-            const uint32_t bK = ptx::smem_addr(sKV + st * kStageBytes);
+            const uint32_t bK = ptx::smem_addr(sK + st * kSlotBytes);
             const uint32_t dS = tmem + kSCol0 + (uint32_t)(sb * kBN);
 #pragma unroll
             for (int kk = 0; kk < DH / 16; ++kk) {
@@ -495,7 +551,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j == s.j0 && m == 0 && segc > 0 && !wait(o_empty, (segc - 1) & 1)) break;
           pv_it = it;
           pv_m = m;
-          pv_stage = st;
           pv_first = j == s.j0;
           pv_lastm = m == NM - 1;
           pv_t = kvt;
@@ -529,6 +584,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ptx::mbar_wait(bar, par, abort_flag, kWaitNs)) ok = false;
       return ok;
     };
+    // barrier and parity of the P V MMAs of item i
+    auto pe_idx = [&](int i) { return kPT ? (i & 1) : i % kNP; };
+    auto pe_par = [&](int i) -> uint32_t { return kPT ? ((i >> 1) & 1) : ((i / kNP) & 1); };
     // value of this row from the other warp of the pair (exchange number xc)
     auto exchange = [&](float mine) -> float {
       float* slot = xbuf + (xc & 1) * 256;
@@ -649,9 +707,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float f = need ? ex2(mold - mnew) : 1.f;
             if (kSplitO || half == 0) {
               // rescale this tile's O: every earlier P V must be complete.  The
-              // commit on p_empty after P V (it - 1) covers all earlier MMAs;
-              // P V (it - 3) was awaited one item ago, so the phase is exact.
-              if (!wait(&p_empty[(it - 1) % kNP], ((it - 1) / kNP) & 1)) break;
+              // commit on p_empty after P V (it - 1) covers all earlier MMAs.
+              // Shared-memory P: P V (it - 3) was awaited one item ago, so the
+              // phase is exact; tensor-memory P: S(it) was issued after P V
+              // (it - 2) completed, so that barrier is at most one phase behind.
+              if (!wait(&p_empty[pe_idx(it - 1)], pe_par(it - 1))) break;
               ptx::tc_fence_after();
               const uint32_t ocol =
                   lane_base + kOCol0 + (uint32_t)((kSplitO ? half : m) * DH);
@@ -690,6 +750,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             pk[c / 2] = *reinterpret_cast<const uint32_t*>(&b2);
           }
           lsum[m] += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
+          if constexpr (kPT) {
+            // over the first half of this warp's own S columns (already read)
+            tmem_st32u(lane_base + kSCol0 + (uint32_t)(sb * kBN + half * kWC), pk);
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&p_full[sb]);
+            continue;
+          }
           const int pbuf = it % kNP;
           if (!wait(&p_empty[pbuf], ((it / kNP) & 1) ^ 1u)) break;
           // this warp's keys [half kWC, half kWC + kWC) of the row: 16-byte
@@ -736,7 +804,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
       }
       // every P V of the segment is complete once P V (it - 1) is
-      if (!wait(&p_empty[(it - 1) % kNP], ((it - 1) / kNP) & 1)) break;
+      if (!wait(&p_empty[pe_idx(it - 1)], pe_par(it - 1))) break;
       ptx::tc_fence_after();
       constexpr int kHalfCols = DH / 2;
       for (int m = 0; m < NM && ok; ++m) {
@@ -912,7 +980,7 @@ int seg_cost() {
 }
 
 struct Plan {
-  int NM, n_mg, stages, G, BN, n_grp, Gg;
+  int NM, n_mg, sk, sv, G, BN, n_grp, Gg;
   size_t smem;
 };
 
@@ -934,12 +1002,20 @@ Plan plan(int N, int g, int dh, int num_sms) {
   p.G = p.Gg * p.n_grp;
   p.BN = p.NM == 1 ? 128 : 64;
   const size_t q = (size_t)p.NM * 128 * dh * 2;
-  const size_t pbuf = (p.BN == 128 ? 1 : 2) * (size_t)128 * p.BN * 2;
-  const size_t stage = 2 * (size_t)p.BN * dh * 2;
+  // one query tile per unit keeps P in tensor memory
+  const size_t pbuf = p.NM == 1 ? 0 : 2 * (size_t)128 * p.BN * 2;
+  const size_t slot = (size_t)p.BN * dh * 2;          // one K or V tile
   const size_t fixed = 1024 /*align*/ + 54 * 8 + 512 * 4 + 3 * (kMaxBAttn + 1) * 4;
-  int st = (int)((kSmemLimit - q - pbuf - fixed) / stage);
-  p.stages = st > 6 ? 6 : st;
-  p.smem = q + pbuf + (size_t)p.stages * stage + fixed;
+  const int n = (int)((kSmemLimit - q - pbuf - fixed) / slot);   // K and V slots
+  if (p.NM == 1) {
+    // K runs ahead of V (a K slot frees after the S MMAs, a V slot only
+    // after P V), so an odd slot goes to K: 3 K + 2 V at d_h = 128
+    p.sv = n / 2 > 6 ? 6 : n / 2;
+    p.sk = n - p.sv > 6 ? 6 : n - p.sv;
+  } else {
+    p.sk = p.sv = n / 2 > 6 ? 6 : n / 2;
+  }
+  p.smem = q + pbuf + (size_t)(p.sk + p.sv) * slot + fixed;
   // more than half of the SM's shared memory: no two CTAs holding all 512
   // TMEM columns (this kernel's or the projection GEMM's) share an SM
   if (p.smem < (size_t)kSmemLimit / 2 + 1024) p.smem = (size_t)kSmemLimit / 2 + 1024;
@@ -998,7 +1074,7 @@ int attention_tc_supported(int B, int N, int g, int dh) {
   if (dh != 64 && dh != 128) return 0;
   if (B > kMaxBAttn) return 0;
   const Plan p = plan(N, g, dh, kMaxCtaAttn);
-  return p.stages >= 2 ? 1 : 0;
+  return p.sk >= 2 && p.sv >= 2 ? 1 : 0;
 }
 
 int attention_tc(int B, int N, int Hq, int Hkv, int dh, int Pmax, const int32_t* P,
@@ -1024,7 +1100,8 @@ int attention_tc(int B, int N, int Hq, int Hkv, int dh, int Pmax, const int32_t*
   a.BN = p.BN;
   a.NM = p.NM;
   a.n_mg = p.n_mg;
-  a.stages = p.stages;
+  a.sk = p.sk;
+  a.sv = p.sv;
   a.G = p.G;
   a.n_grp = p.n_grp;
   a.Gg = p.Gg;
