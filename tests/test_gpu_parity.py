@@ -246,6 +246,22 @@ def test_tree_attention_edges(mds, w):
     check_attention(w, g, f64_inputs(w, x), P, tok.astype(np.int64), list(range(w.B)))
 
 
+def test_tree_attention_edges_ungrouped_form():
+    """The edge cases again with MDS_ATTN_GROUPED=0, i.e. with several query
+    tiles per work unit (64-key tiles, P in shared memory, a per-tile row
+    maximum exchange between the two warps of a lane quarter).  The switch is
+    read once per process, so the cases run in a child process."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, MDS_ATTN_GROUPED="0")
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu",
+                        "tests/test_gpu_parity.py::test_tree_attention_edges"],
+                       cwd=root, env=env, capture_output=True, text=True, timeout=1200)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
+
+
 # ---------------------------------------------------------------------------
 # lm_verify
 # ---------------------------------------------------------------------------
