@@ -27,7 +27,8 @@
 // covers the same keys at about the same time, so the K/V tile that one of
 // them reads from HBM the others find in L2.  With BN = 128 keys a tile
 // costs 16 tcgen05.mma per query tile, against 24 with three query tiles
-// over 64-key tiles (S at N = 64 costs a full MMA issue).
+// over 64-key tiles (an S MMA at N = 64 takes ~50 cycles against 64 at
+// N = 128, so 64-key tiles nearly double the S cost per key).
 //
 //   S = Q K^T      tcgen05, M = 128 query rows, N = BN keys, K = dh      -> TMEM
 //   softmax        one thread per query row reads its S row from TMEM,

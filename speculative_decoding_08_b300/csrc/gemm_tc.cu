@@ -8,14 +8,15 @@
 // Wqkv, Wo).  Each CTA owns a contiguous range of weight rows (features),
 // split evenly over the SMs in units of 16, and streams it through a TMA
 // ring as deep as shared memory allows; X tiles (the rows) are re-read from
-// L2.  Above 256 rows the CTAs are also split over the 256-row groups: each
-// takes one group and a correspondingly wider feature range, the CTAs of
-// one range reading its weights together (once from HBM, the rest from L2).
-// With at most 128 rows and few features (Wo, Wqkv, the heads) the k-blocks
-// are split over ks CTAs per feature range instead, and k_split_reduce adds
-// the fp32 partial sums and runs the epilogue: every tcgen05.mma costs the
-// issuing SM about 190 cycles for any N, so a CTA's Kd / 16 MMAs per chunk
-// would otherwise outlast its share of the weight stream.
+// L2.  Above 128 rows the CTAs are also split over row groups (one or two
+// 128-row tiles each, whichever gives the busiest CTA fewer MMAs): each takes
+// one group and a correspondingly wider feature range, the CTAs of one range
+// reading its weights together (once from HBM, the rest from L2).  With at
+// most 128 rows and few features (Wo) the k-blocks are split over ks CTAs
+// per feature range instead, and k_split_reduce adds the fp32 partial sums
+// and runs the epilogue: a CTA's Kd / 16 MMAs over its single chunk and the
+// K-long ring fill and drain would otherwise outlast its share of the
+// weight stream.
 // With at most 128 rows the MMA reads a 128-row X tile of which only
 // the first R rows matter (the other accumulator rows are never read), so the
 // X tiles of consecutive stages overlap: stage s starts ceil(R/8) KB after
@@ -25,12 +26,13 @@
 // issues tcgen05.mma with M = 128 rows (X) and N = up to 256 features (W);
 // the fp32 accumulators live in tensor memory (double-buffered for up to 128
 // rows, so that the epilogue of one feature chunk overlaps the MMAs of the
-// next; single-buffered 2 x 256 columns for more rows).  N is 256 features
-// per MMA where the CTA's range allows: a tcgen05.mma costs about the same
-// for any N up to 256.
+// next; single-buffered 2 x 256 columns for two row tiles).  A tcgen05.mma
+// takes N / 2 cycles for N >= 128 and ~50 below, so narrow chunks waste the
+// tensor core: N is 256 features per MMA where the CTA's range allows.
 //
-// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = TMEM allocator and
-// MMA issuer, warps 2..5 = epilogue (one TMEM lane = one row per thread).
+// Warp roles (320 threads, 192 for the sampling and fused kinds): warp 0 =
+// TMA producer, warp 1 = TMEM allocator and MMA issuer, the rest = epilogue,
+// two warps (one) per TMEM lane quarter, a lane = a row.
 //
 // Fused epilogues:
 //   STORE   Y -> bf16 out                                   (Wo projection)
@@ -41,9 +43,12 @@
 //   DRAFT   per row running top-8 (value desc, id asc) over the CTA's range
 //           ("From top-k heads to a sparse candidate tree")
 //   VERIFY  per row running max / argmax / sum e^(z-m) / sum z e^(z-m)
-//           (entropy for "Typical acceptance, not exact rejection sampling")
-// DRAFT and VERIFY leave one partial record per (feature range, row); a
-// merge kernel combines them.
+//           (entropy for "Typical acceptance, not exact rejection sampling"),
+//           and the row's children's logits as their tokens' columns go by
+//   VSAMPLE VERIFY plus a running Gumbel-max draw per row (exact sampling)
+//   VDRAFT  VERIFY rows and DRAFT rows in one pass (the fused loop)
+// DRAFT and VERIFY leave one partial record per (row, feature range,
+// epilogue warp of the lane quarter); a merge kernel combines them.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <stdlib.h>
@@ -97,9 +102,9 @@ struct TcArgs {
   // K split (at most 128 rows, STORE / HEADS / QKV): ks CTAs share a feature
   // range, each over 1 / ks of the k-blocks, writing fp32 partial sums to
   // kpart [ks][R][F]; k_split_reduce then adds them in split order and runs
-  // the epilogue.  Without the split a CTA issues Kd / 16 MMAs per chunk
-  // whatever its width (about 190 SM cycles each), which bounds the narrow
-  // projections (Wo, Wqkv, the heads) at batch 1 above their HBM time.
+  // the epilogue.  Without the split a CTA issues Kd / 16 MMAs over its
+  // single chunk and fills and drains a K-long ring, which keeps the narrow
+  // output projection (Wo) at batch 1 well above its HBM time.
   int ks;
   float* kpart;
   int kind;
@@ -1277,10 +1282,9 @@ int init_host() {
 }
 
 // K splits for a pass of at most 128 rows over F features and Kd inputs:
-// enough that a CTA's MMAs (Kd / 16 / ks per chunk, about 190 SM cycles each)
-// stay below its share of the weight stream (F Kd 2 / SMs bytes), while every
-// feature range keeps at most 256 features (one chunk) and every split at
-// least two k-blocks.
+// enough CTAs share a feature range that its k-blocks are spread over the
+// SMs, while every feature range keeps at most 256 features (one chunk) and
+// every split at least two k-blocks.
 // MDS_GEMM_ROWTILES=1 or 2 forces the row tiles per CTA of the passes above
 // 128 rows (the draft pass excepted); read once per process.
 int rowtiles_override() {
@@ -1293,9 +1297,9 @@ int rowtiles_override() {
 
 int k_splits(int F, int Kd, int sms) {
   // Measured at batch 1: the split pays for its reduce kernel on Wo
-  // (F = 4096: MMA floor ~4.6x the HBM time per CTA) but not on Wqkv or the
-  // heads (F >= 12288: ~1.2-1.5x), whose time is mostly fixed per-kernel
-  // costs (ramp-up, epilogue) rather than MMA issue.
+  // (F = 4096; tree-attention call 81.5 -> 78.2 us live) but not on Wqkv or
+  // the heads (F >= 12288), whose time is mostly fixed per-kernel costs
+  // (ramp-up, epilogue).
   if (F > 8192) return 1;
   const int nmin = (F + 255) / 256;
   int ks = sms / nmin;
@@ -1354,10 +1358,9 @@ int launch_tc(TcArgs& a, const void* X, const void* W, bool dependent, cudaStrea
     const int forced = rowtiles_override();
     a.G = forced ? forced : (8 * mmas(1) <= 7 * mmas(2) ? 1 : 2);
   }
-  // Features per MMA (N) and accumulator buffers.  Every tcgen05.mma costs
-  // about the same up to N = 256, so N is 256 where TMEM allows: with one
-  // 128-row group, double-buffered (the epilogue of one chunk overlaps the
-  // MMAs of the next).  With two groups, the verify pass (wide CTA ranges,
+  // Features per MMA (N) and accumulator buffers.  N is 256 where TMEM
+  // allows: with one 128-row tile, double-buffered (the epilogue of one chunk
+  // overlaps the MMAs of the next).  With two groups, the verify pass (wide CTA ranges,
   // light epilogue) takes one 2 x 256-column accumulator; the others keep
   // N = 128 double-buffered, since their ranges are narrow or their
   // epilogue is heavy.
