@@ -733,7 +733,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (mref[m] == -INFINITY) mref[m] = mnew;
           const float mr = mref[m];
-          // P = 2^(s - m) rounded to bf16; l sums the rounded values
+          // P = 2^(s - m) rounded to bf16 for the P V MMAs; l sums the fp32
+          // values (round to nearest is unbiased: l and the sum of the
+          // rounded P differ by a relative ~2^-9 / sqrt(keys))
           uint32_t pk[kWC / 2];
           float ls4[4] = {0.f, 0.f, 0.f, 0.f};
           const float sc = a.scale_log2;
@@ -746,8 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float p0 = ex2(fmaf(sv[c], sc, nmr));
             const float p1 = ex2(fmaf(sv[c + 1], sc, nmr));
             const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-            const float2 r2 = __bfloat1622float2(b2);
-            ls4[(c >> 1) & 3] += r2.x + r2.y;
+            ls4[(c >> 1) & 3] += p0 + p1;
             pk[c / 2] = *reinterpret_cast<const uint32_t*>(&b2);
           }
           lsum[m] += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
