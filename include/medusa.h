@@ -171,8 +171,9 @@ MDS_API int mds_medusa_heads(int dtype, int B, int d, int V, int K, const void* 
  * have no counterpart: this is a deployment variant, not a step of the
  * method).  A runtime that sizes all device memory once at start-up, or code
  * running inside an allocator callback, cannot hand over a fresh workspace;
- * this call takes none.  Its scratch (1 MiB of per-CTA candidate lists plus
- * a status word) is a fixed array inside the library, which every GPU that
+ * this call takes none.  Its scratch (2 MiB of candidate lists, one per
+ * feature range and epilogue warp, plus a status word) is a fixed array
+ * inside the library, which every GPU that
  * loads the library holds until the process exits.  Arithmetic and outputs
  * are those of mds_medusa_heads with dtype = MDS_BF16.
  *   Same arguments as mds_medusa_heads (bf16 only), without ws / ws_bytes.
