@@ -2,6 +2,7 @@
 and check that at least one pin in test_oracle_pins.py catches each one."""
 from __future__ import annotations
 
+import functools
 import math
 import types
 
@@ -98,6 +99,66 @@ def accept_own_row(mode, eps, delta, tok, parent, st):
                                                            "H": np.roll(st["H"], -1, axis=1)})
 
 
+def verify_child_own_row(y, lm, tok, parent):
+    # the child's logit read from its own row instead of its parent's
+    st = mo.verify_stats(y, lm, tok, parent)
+    st["childlogit"] = st["childlogit"].copy()
+    for b in range(y.shape[0]):
+        for c in range(1, tok.shape[1]):
+            st["childlogit"][b, c] = float(lm[tok[b, c]] @ y[b, c])
+    return st
+
+
+def verify_gap_to_lowest(y, lm, tok, parent):
+    # the margin taken against the row's lowest logit, not its second highest
+    st = mo.verify_stats(y, lm, tok, parent)
+    l = np.einsum("bnd,vd->bnv", y, lm)
+    return dict(st, argmax_gap=l.max(-1) - l.min(-1))
+
+
+def accept_own_draw(mode, eps, delta, tok, parent, st):
+    # a child checked against the token drawn at its own row
+    ok, margin = mo.accept_edges(mode, eps, delta, tok, parent, st)
+    if mode == "sample":
+        ok[:, 1:] = tok[:, 1:] == st["sample"][:, 1:]
+    return ok, margin
+
+
+def accept_greedy_own_argmax(mode, eps, delta, tok, parent, st):
+    ok, margin = mo.accept_edges(mode, eps, delta, tok, parent, st)
+    if mode == "greedy":
+        ok[:, 1:] = tok[:, 1:] == st["argmax"][:, 1:]
+    return ok, margin
+
+
+def accept_typical_no_exp(mode, eps, delta, tok, parent, st):
+    # threshold min(eps, delta * H) instead of min(eps, delta * exp(-H))
+    ok, margin = mo.accept_edges(mode, eps, delta, tok, parent, st)
+    if mode == "typical":
+        for b in range(tok.shape[0]):
+            for c in range(1, tok.shape[1]):
+                pa = parent[c]
+                p = math.exp(st["childlogit"][b, c] - st["lse"][b, pa])
+                ok[b, c] = p > min(eps, delta * st["H"][b, pa])
+    return ok, margin
+
+
+_gumbel_keys = mo.gumbel_keys
+
+
+def gumbel_lowest_key(logits, T, seed, words3):
+    # negated keys: the sampler then takes the lowest of the true keys
+    return -_gumbel_keys(logits, T, seed, words3)
+
+
+def gumbel_no_sequence(logits, T, seed, words3):
+    return _gumbel_keys(logits, T, seed, (words3[0], words3[1], 0))
+
+
+def gumbel_no_position(logits, T, seed, words3):
+    return _gumbel_keys(logits, T, seed, (words3[0], 0, words3[2]))
+
+
 def longest_path_high_index(ok, parent, depth, argmax, K):
     B, N = ok.shape
     r = mo.longest_path(ok[:, ::-1].copy(), parent, depth, argmax, K)   # wrong: reversed order
@@ -107,6 +168,14 @@ def longest_path_high_index(ok, parent, depth, argmax, K):
 def compact_skip_root(kc, vc, P, L, path):
     path2 = path.copy()
     path2[:, 0] = np.where(L > 0, path[:, 1], 0)
+    return mo.compact_kv(kc, vc, P, L, path2)
+
+
+def compact_reversed(kc, vc, P, L, path):
+    # the accepted rows written deepest first
+    path2 = path.copy()
+    for b in range(path.shape[0]):
+        path2[b, : L[b] + 1] = path[b, : L[b] + 1][::-1]
     return mo.compact_kv(kc, vc, P, L, path2)
 
 
@@ -215,12 +284,21 @@ CASES = [
     ("attention: prefix one short", dict(tree_attention=attention_with("prefix_short")), [pins.check_attention_per_path, pins.check_attention_uniform_weights]),
     ("verify: entropy in bits", dict(verify_stats=verify_entropy_log2), [pins.check_verify_stats, pins.check_verify_two_level]),
     ("accept: wrong row's entropy", dict(accept_edges=accept_own_row), [pins.check_typical_direct]),
+    ("verify: child logit from the child's own row", dict(verify_stats=verify_child_own_row), [pins.check_verify_stats]),
+    ("verify: margin against the lowest logit", dict(verify_stats=verify_gap_to_lowest), [pins.check_verify_stats, pins.check_verify_two_level]),
+    ("accept: greedy child against its own argmax", dict(accept_edges=accept_greedy_own_argmax), [functools.partial(pins.check_greedy_lossless, plant_depth=3, seed=0)]),
+    ("accept: typical threshold without exp", dict(accept_edges=accept_typical_no_exp), [pins.check_typical_direct]),
+    ("accept: sampled child against its own draw", dict(accept_edges=accept_own_draw), [pins.check_sample_acceptance]),
     ("path: ties to the highest index", dict(longest_path=longest_path_high_index), [pins.check_longest_path_golden, pins.check_longest_path_brute]),
     ("compaction: root row dropped", dict(compact_kv=compact_skip_root), [pins.check_compaction]),
+    ("compaction: accepted rows in reverse order", dict(compact_kv=compact_reversed), [pins.check_compaction]),
     ("bf16: truncation instead of rounding", dict(round_bf16=round_truncate), [pins.check_round_bf16]),
     ("philox: key not bumped between rounds", dict(philox4x64=philox_no_key_bump), [pins.check_philox_library]),
     ("sample: temperature ignored", dict(gumbel_keys=gumbel_no_temperature), [pins.check_sampler_distribution]),
     ("sample: Gumbel noise sign flipped", dict(gumbel_keys=gumbel_sign_flipped), [pins.check_sampler_distribution, pins.check_sampling_is_rejection_sampling]),
+    ("sample: the lowest key drawn", dict(sample_tokens=patched("gumbel_keys", gumbel_lowest_key, "sample_tokens")), [pins.check_sample_tokens_draws]),
+    ("sample: counter without the sequence number", dict(sample_tokens=patched("gumbel_keys", gumbel_no_sequence, "sample_tokens")), [pins.check_sample_tokens_draws]),
+    ("sample: counter without the position", dict(sample_tokens=patched("gumbel_keys", gumbel_no_position, "sample_tokens")), [pins.check_sample_tokens_draws]),
     ("rope: pairs (i, i + dh/2)", dict(rope=rope_half_pairs), [pins.check_rope]),
     ("backbone: position ids by node index", dict(backbone=patched("backbone_layer", layer_positions_by_index, "backbone")), [pins.check_backbone_per_path]),
     ("backbone: residual stream dropped", dict(backbone=patched("backbone_layer", layer_no_residual, "backbone")), [pins.check_backbone_per_path]),

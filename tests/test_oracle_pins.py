@@ -303,6 +303,8 @@ def check_verify_stats(orc):
             np.testing.assert_allclose(st["H"][b, n], scipy.stats.entropy(pr), rtol=1e-12)
             assert st["H"][b, n] <= math.log(w.V) + 1e-12
             assert st["argmax"][b, n] == int(np.argmax(l[n]))
+            top = np.sort(l[n])
+            np.testing.assert_allclose(st["argmax_gap"][b, n], top[-1] - top[-2], rtol=1e-12)
         for c in range(1, 6):
             np.testing.assert_allclose(st["childlogit"][b, c],
                                        float(f["lm"][tok[b, c]] @ y[b, parent[c]]), rtol=1e-12)
@@ -334,6 +336,8 @@ def check_verify_two_level(orc):
         np.testing.assert_allclose(st["H"][0], math.log(Z) - k * a * math.exp(a) / Z, rtol=1e-12)
         want = min(ids) if a > 0 else min(set(range(V)) - set(ids))
         assert np.all(st["argmax"][0] == want)
+        # the top two logits differ only when a > 0 is held by one id alone
+        np.testing.assert_allclose(st["argmax_gap"][0], a if (a > 0 and k == 1) else 0.0, atol=0)
         np.testing.assert_allclose(st["childlogit"][0, 1], a if 5 in ids else 0.0, atol=0)
 
 
@@ -641,6 +645,36 @@ def check_sampling_is_rejection_sampling(orc, rows=4000):
     assert np.all(np.abs(got - rows * want) < 5 * sd), (got, rows * want)
 
 
+def check_sample_tokens_draws(orc, rows=1000):
+    """The token drawn at a tree row follows softmax(l / T) of that row's
+    logits, and rows that differ in node, position or sequence number draw
+    independently: two such rows agree with probability sum_v p_v^2 (a
+    counter word left out would make them agree always)."""
+    logits = np.array([1.0, 0.2, -0.5, 2.0, 0.0])
+    T = 0.8
+    lm = np.zeros((5, 2))
+    lm[:, 0] = logits
+    lm[:, 1] = np.random.default_rng(2).standard_normal(5)    # multiplied by 0
+    y = np.zeros((4, rows, 2))
+    y[..., 0] = 1.0
+    # sequences 0/1 differ in sequence number only, 0/2 in position only
+    P = np.array([7, 7, 9, 9])
+    smp = orc.sample_tokens(y, lm, T, 5, P, seq=[0, 1, 0, 1])
+    s = smp["sample"]
+    assert np.all(smp["sample_gap"] >= 0.0)
+    p = scipy.special.softmax(logits / T)
+    n_all = s.size
+    counts = np.bincount(s.reshape(-1), minlength=5)
+    sd = np.sqrt(n_all * p * (1 - p))
+    assert np.all(np.abs(counts - n_all * p) < 5 * sd), (counts, n_all * p)
+    q = float(np.sum(p * p))
+    sd = math.sqrt(rows * q * (1 - q))
+    for a, b, sh in [(0, 1, 0), (0, 2, 0), (3, 3, 1)]:
+        agree = int(np.sum(s[a, sh:] == s[b, : rows - sh])) if sh else int(np.sum(s[a] == s[b]))
+        n = rows - sh
+        assert abs(agree - n * q) < 5 * sd, (a, b, sh, agree, n * q)
+
+
 def check_sample_acceptance(orc):
     """The accepted path follows the drawn tokens: plant the drawn token of
     each node as one of its children's tokens down one branch; the accepted
@@ -689,6 +723,10 @@ def test_sampler_distribution():
 
 def test_sampling_is_rejection_sampling():
     check_sampling_is_rejection_sampling(oracle)
+
+
+def test_sample_tokens_draws():
+    check_sample_tokens_draws(oracle)
 
 
 def test_sample_acceptance():
