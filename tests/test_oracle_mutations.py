@@ -235,6 +235,26 @@ def patched(name, repl, target):
     return f
 
 
+_accepted_rows = mo.accepted_rows
+
+
+def rows_all_last(y, L, path, K):
+    # every row the accepted node's: the heads lose the path's earlier states
+    out = _accepted_rows(y, L, path, K)
+    for b in range(y.shape[0]):
+        out[b, :] = y[b, int(path[b, int(L[b])])]
+    return out
+
+
+def rows_skip_root(y, L, path, K):
+    # the root's row left out: every state one position early
+    out = _accepted_rows(y, L, path, K)
+    for b in range(y.shape[0]):
+        for j in range(K + 1):
+            out[b, j] = y[b, int(path[b, min(j + 1, int(L[b]))])]
+    return out
+
+
 _backbone_layer = mo.backbone_layer
 
 
@@ -304,6 +324,8 @@ CASES = [
     ("backbone: residual stream dropped", dict(backbone=patched("backbone_layer", layer_no_residual, "backbone")), [pins.check_backbone_per_path]),
     ("mtp: output at the first row, not the last accepted", dict(mtp_heads=mtp_row_zero), [pins.check_mtp_heads]),
     ("mtp: residual around the MLP dropped", dict(mtp_heads=mtp_mlp_no_residual), [pins.check_mtp_heads, pins.check_mtp_zero_heads]),
+    ("mtp loop: every accepted row the last node's", dict(decode=patched("accepted_rows", rows_all_last, "decode")), [pins.check_decode_mtp]),
+    ("mtp loop: the root's row left out", dict(decode=patched("accepted_rows", rows_skip_root, "decode")), [pins.check_decode_mtp]),
     ("decode: next hidden state from the root row", dict(decode=decode_with_hidden(hidden_of_root)), [pins.check_decode_greedy_lossless]),
     ("decode: next hidden state from the accepted node's parent", dict(decode=decode_with_hidden(hidden_of_parent)), [pins.check_decode_greedy_lossless]),
 ]

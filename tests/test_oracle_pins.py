@@ -918,6 +918,55 @@ def check_mtp_heads(orc, base=10000.0):
             np.testing.assert_array_equal(kc[b][:, :Pb], hw["kc"][b][:, :Pb])
 
 
+def check_decode_mtp(orc, seed=12, n_steps=3, base=500.0):
+    """The decoding loop with MTP-style heads.  Greedy acceptance still emits
+    exactly sequential greedy decoding of the verifier, whatever the heads
+    draft.  The heads see the trunk's hidden states in position order: after
+    the loop, head i's cache rows at positions P_b - 1, P_b, ... (h, then the
+    verifier's output at each token emitted before the last step) and its
+    last draft equal a causal pass of head i's layer over that sequence of
+    hidden states, followed by x + W2 SiLU(W1 x) computed with torch."""
+    w, f, P = tiny(seed=seed, B=2, d=64, V=8, Hq=2, Hkv=1, dh=64, shortlist=(3, 2, 2),
+                   P=(5, 12))
+    heads = [{k: ms.as_f64(v, w.dtype) for k, v in hw.items()} for hw in ms.make_mtp_heads(w, 96)]
+    f["mtp"] = dict(heads=heads, rope_base=base)
+    rs = orc.decode(w, f, P, "greedy", n_steps)
+    last = rs[-1]["mtp"]
+    n_rows = 0
+    for b in range(w.B):
+        emitted = sum((r["emitted"][b] for r in rs), [])
+        Pb = int(P[b])
+        seq = brute.greedy_decode(f["kc"][b][:, :Pb], f["vc"][b][:, :Pb], emitted[0],
+                                  len(emitted), f["emb"], f["wq"], f["wk"], f["wv"], f["wo"],
+                                  f["lm"], w.Hq, w.Hkv, w.dh)
+        assert emitted + [int(rs[-1]["path"]["next_root"][b])] == seq
+        # the verifier's outputs at the emitted tokens (positions P_b, P_b + 1, ...)
+        y, _, _ = brute.causal_layer(f["kc"][b][:, :Pb], f["vc"][b][:, :Pb], emitted, f["emb"],
+                                     f["wq"], f["wk"], f["wv"], f["wo"], w.Hq, w.Hkv, w.dh)
+        n_prev = int(rs[-2]["P"][b]) - Pb          # tokens emitted before the last step
+        rows = np.concatenate([f["h"][b][None], y[:n_prev]])
+        n_rows += len(rows)
+        np.testing.assert_allclose(last["U"][b, 0], rows[-1], rtol=1e-9, atol=1e-9)
+        for i, hw in enumerate(heads):
+            lay = [dict(wq=hw["wq"], wk=hw["wk"], wv=hw["wv"], wo=hw["wo"])]
+            a, ks, vs = brute.causal_stack([hw["kc"][b][:, :Pb - 1]], [hw["vc"][b][:, :Pb - 1]],
+                                           Pb - 1, None, None, lay, w.Hq, w.Hkv, w.dh, base,
+                                           kv=True, x_rows=rows)
+            kc, vc = last["caches"][i]
+            for j in range(len(rows)):
+                np.testing.assert_allclose(kc[b][:, Pb - 1 + j].reshape(-1), ks[0][j], rtol=1e-9,
+                                           atol=1e-9)
+                np.testing.assert_allclose(vc[b][:, Pb - 1 + j].reshape(-1), vs[0][j], rtol=1e-9,
+                                           atol=1e-9)
+            np.testing.assert_array_equal(kc[b][:, :Pb - 1], hw["kc"][b][:, :Pb - 1])
+            at = torch.from_numpy(a[-1])
+            u = at + torch.nn.functional.silu(at @ torch.from_numpy(hw["w1"]).T) @ \
+                torch.from_numpy(hw["w2"]).T
+            np.testing.assert_allclose(last["U"][b, i + 1], u.numpy(), rtol=1e-9, atol=1e-9)
+    # more than one accepted row per sequence reached the heads
+    assert n_rows > 2 * w.B
+
+
 def check_mtp_zero_heads(orc):
     """With Wo = 0 and W2 = 0 a head passes its input through: every head's
     output is h (the input at the last accepted row)."""
@@ -926,6 +975,10 @@ def check_mtp_zero_heads(orc):
     for b in range(xrows.shape[0]):
         for i in range(len(heads) + 1):
             np.testing.assert_array_equal(r["U"][b, i], xrows[b, int(L[b])])
+
+
+def test_decode_mtp():
+    check_decode_mtp(oracle)
 
 
 def test_mtp_heads():
