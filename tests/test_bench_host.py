@@ -76,3 +76,38 @@ def test_committed_traffic_record():
     same = bench.source_hash(*r["sources"]) == r["sources_sha256"]
     want = r["dram_bytes_per_launch"] if same else None
     assert bench.profiled_traffic(bench.HEADLINE, "lm_verify") == want
+
+
+def _reference_run(env_extra):
+    import subprocess
+    import sys
+    env = dict(os.environ, **env_extra)
+    return subprocess.run([sys.executable, os.path.join(bench.ROOT, "bench.py"), "--impl",
+                           "reference", "--workload", "tiny-fp32", "--steps", "3", "--warmup", "3"],
+                          capture_output=True, text=True, timeout=300, env=env, cwd=bench.ROOT)
+
+
+def test_reference_arm_line():
+    """The oracle arm prints one JSON line with the contract's keys: the same
+    metric and unit as the GPU arm, its own timing counts, a cpu_baseline
+    describing the run and an e2e entry with no host-device copies."""
+    p = _reference_run({"RANK": "0"})
+    assert p.returncode == 0, p.stderr
+    lines = [ln for ln in p.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    j = json.loads(lines[0])
+    assert j["impl"] == "reference" and j["metric"] == bench.METRIC and j["unit"] == "steps/s"
+    assert j["value"] > 0 and j["higher_is_better"] is True and j["n_gpus"] == 1
+    assert 1 <= j["steps"] <= 3 and 0 <= j["warmup"] <= 3
+    assert j["config"]["workload"] == "tiny-fp32"
+    cb = j["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == j["value"] and cb["cores"] >= 1
+    assert "oracle step" in cb["sample"]
+    assert j["e2e"] == {"value": j["value"], "unit": "steps/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_other_ranks_print_nothing():
+    p = _reference_run({"RANK": "1"})
+    assert p.returncode == 0, p.stderr
+    assert p.stdout.strip() == ""
