@@ -55,7 +55,7 @@ def tdtype(w):
 
 TREES = [((2, 2, 2), -1), ((4, 3, 2, 2), -1), ((8, 4, 2, 2, 1), 3), ((3,), -1), ((1, 1, 1, 1), -1),
          ((5, 1, 3), 2), ((2, 2, 2, 2), 0), ((8, 8), -1), ((8, 4, 2, 2, 1, 1, 1, 1), 2),
-         ((6, 5, 4), 4)]
+         ((6, 5, 4), 4), ((5, 4, 2, 2), 6), ((8, 7, 3), 7)]
 
 
 @pytest.mark.parametrize("sl,mrs", TREES)

@@ -188,10 +188,23 @@ def compare_step(mds, w, sample, modes):
     return ties, compared, accepted
 
 
+# The largest tree the calls take (N = 128 nodes, two full mask words): with
+# grouped-query heads (g = 2, two query tiles per KV head) and with one query
+# tile per head at d_h = 128; unaligned prefixes make the tree keys straddle
+# two key tiles.
+MAX_TREE_GQA = ms.Workload("max-tree-gqa", "bf16", B=3, d=256, V=1000, Hq=4, Hkv=2, dh=64, K=4,
+                           shortlist=(5, 4, 2, 2), max_rank_sum=6, P=(60, 400), accept="both",
+                           seed=7)
+MAX_TREE_MHA = ms.Workload("max-tree-mha", "bf16", B=2, d=256, V=700, Hq=2, Hkv=2, dh=128, K=3,
+                           shortlist=(8, 7, 3), max_rank_sum=7, P=(100, 500), accept="both",
+                           seed=8)
+
 SMALL = [(ms.workload(0), ["greedy", ("sample", 1.0, 3)]),
          (MINI, ["greedy", ("sample", 0.8, 1), "typical"]),
          (MINI_GQA, [("sample", 1.0, 2), "typical"]),
-         (MINI_F32, ["greedy", ("sample", 1.5, 4), "typical"])]
+         (MINI_F32, ["greedy", ("sample", 1.5, 4), "typical"]),
+         (MAX_TREE_GQA, ["greedy", ("sample", 1.0, 9), "typical"]),
+         (MAX_TREE_MHA, [("sample", 0.9, 10), "typical", "greedy"])]
 
 
 @pytest.mark.parametrize("w,modes", SMALL, ids=lambda p: getattr(p, "name", None))
