@@ -199,12 +199,25 @@ MAX_TREE_MHA = ms.Workload("max-tree-mha", "bf16", B=2, d=256, V=700, Hq=2, Hkv=
                            shortlist=(8, 7, 3), max_rank_sum=7, P=(100, 500), accept="both",
                            seed=8)
 
+# Ragged shapes: d = 320 (not a multiple of 128), an odd vocabulary, five
+# query heads on one KV head, prefix lengths drawn from 1..200.
+RAGGED = ms.Workload("ragged-bf16", "bf16", B=2, d=320, V=1003, Hq=5, Hkv=1, dh=64, K=3,
+                     shortlist=(3, 3, 2), max_rank_sum=-1, P=(1, 200), accept="both", seed=9)
+# The deepest tree the calls take (K = 8) as a near-chain; delta = 0 makes
+# every edge pass, so the accepted path runs to depth 8 and nine rows are
+# compacted.
+DEEP = ms.Workload("deep-k8", "bf16", B=2, d=256, V=64, Hq=4, Hkv=4, dh=64, K=8,
+                   shortlist=(2, 2, 1, 1, 1, 1, 1, 1), max_rank_sum=-1, P=(10, 130),
+                   accept="both", seed=10)
+
 SMALL = [(ms.workload(0), ["greedy", ("sample", 1.0, 3)]),
          (MINI, ["greedy", ("sample", 0.8, 1), "typical"]),
          (MINI_GQA, [("sample", 1.0, 2), "typical"]),
          (MINI_F32, ["greedy", ("sample", 1.5, 4), "typical"]),
          (MAX_TREE_GQA, ["greedy", ("sample", 1.0, 9), "typical"]),
-         (MAX_TREE_MHA, [("sample", 0.9, 10), "typical", "greedy"])]
+         (MAX_TREE_MHA, [("sample", 0.9, 10), "typical", "greedy"]),
+         (RAGGED, ["greedy", ("sample", 1.0, 12), "typical"]),
+         (DEEP, [("typical", 0.09, 0.0), "greedy", ("sample", 1.0, 11)])]
 
 
 @pytest.mark.parametrize("w,modes", SMALL, ids=lambda p: getattr(p, "name", None))
