@@ -51,7 +51,9 @@
  *    per workspace).  Size it with mds_workspace_size; it must be 256-byte
  *    aligned and zero-filled once before first use.
  *  - Limits: N (tree rows incl. root) <= 128, K <= 8, s_i <= 8, d % 64 == 0,
- *    dh in {64, 128}, Hq % Hkv == 0.  Larger shapes return MDS_EUNSUPPORTED.
+ *    dh in {64, 128}, Hq % Hkv == 0; B <= 256 for the calls with bf16
+ *    attention (mds_tree_attention, mds_backbone_layer, mds_mtp_heads),
+ *    B <= 1024 for mds_compact_kv.  Larger shapes return MDS_EUNSUPPORTED.
  *  - Within one call, the second and later kernels are launched with
  *    programmatic stream serialisation: they may start while the previous
  *    kernel of the same call finishes, touching only the weights before that

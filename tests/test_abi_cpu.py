@@ -113,6 +113,9 @@ def test_host_validation_rejects_before_launch(lib):
                                   fake, fake, fake, null, fake, fake, 1 << 30, null) == -3
     assert lib.mds_tree_attention(1, 1, 7, 64, 100, 2, 2, 96, 256, 2, 2, *args, 1, fake, fake,
                                   fake, fake, fake, null, fake, fake, 1 << 30, null) == -3
+    # bf16 attention over more than 256 sequences
+    assert lib.mds_tree_attention(1, 257, 7, 64, 100, 2, 2, 64, 256, 2, 2, *args, 1, fake, fake,
+                                  fake, fake, fake, null, fake, fake, 1 << 30, null) == -3
     # compact: dh unsupported, B too large
     assert lib.mds_compact_kv(1, 1, 2, 96, 64, 2, fake, fake, fake, fake, fake, fake, 1 << 20,
                               null) == -3

@@ -225,6 +225,22 @@ def test_step_small(mds, w, modes):
     compare_step(mds, w, list(range(w.B)), modes)
 
 
+# The largest batch the bf16 attention takes: 256 sequences, one of them
+# with an empty prefix (P = 0); eight spread over the batch go through the
+# oracle.
+MAX_BATCH = ms.Workload("max-batch-256", "bf16", B=256, d=256, V=500, Hq=2, Hkv=1, dh=64, K=3,
+                        shortlist=(2, 2, 2), max_rank_sum=-1, P=(0, 300), accept="both",
+                        seed=11)
+
+
+def test_step_max_batch(mds):
+    w = MAX_BATCH
+    sample = [0, 37, 74, 111, 148, 185, 208, 255]
+    assert int(ms.make_inputs(w, only=())["P"][208]) == 0
+    _, compared, _ = compare_step(mds, w, sample, ["greedy", ("sample", 1.0, 13), "typical"])
+    assert compared > 0
+
+
 # Typical acceptance with eps = 1, delta = 1.05: an edge passes iff
 # ln p > ln 1.05 - H.  With the synthetic value laws the verify distributions
 # are nearly flat (H close to ln V) and ln p + H spreads over about
