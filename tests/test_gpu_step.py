@@ -199,6 +199,15 @@ MAX_TREE_MHA = ms.Workload("max-tree-mha", "bf16", B=2, d=256, V=700, Hq=2, Hkv=
                            shortlist=(8, 7, 3), max_rank_sum=7, P=(100, 500), accept="both",
                            seed=8)
 
+MAX_TREE_F32 = ms.Workload("max-tree-f32", "f32", B=2, d=192, V=600, Hq=6, Hkv=3, dh=64, K=3,
+                           shortlist=(8, 7, 3), max_rank_sum=7, P=(30, 300), accept="both",
+                           seed=14)
+# Eight heads with a top-8 shortlist at the first: the draft pass's full
+# running top-8 on every head's row.
+WIDE_DEEP = ms.Workload("wide-deep-k8", "bf16", B=2, d=256, V=300, Hq=4, Hkv=2, dh=64, K=8,
+                        shortlist=(8, 4, 2, 2, 1, 1, 1, 1), max_rank_sum=2, P=(20, 200),
+                        accept="both", seed=15)
+
 # Ragged shapes: d = 320 (not a multiple of 128), an odd vocabulary, five
 # query heads on one KV head, prefix lengths drawn from 1..200.
 RAGGED = ms.Workload("ragged-bf16", "bf16", B=2, d=320, V=1003, Hq=5, Hkv=1, dh=64, K=3,
@@ -217,7 +226,9 @@ SMALL = [(ms.workload(0), ["greedy", ("sample", 1.0, 3)]),
          (MAX_TREE_GQA, ["greedy", ("sample", 1.0, 9), "typical"]),
          (MAX_TREE_MHA, [("sample", 0.9, 10), "typical", "greedy"]),
          (RAGGED, ["greedy", ("sample", 1.0, 12), "typical"]),
-         (DEEP, [("typical", 0.09, 0.0), "greedy", ("sample", 1.0, 11)])]
+         (DEEP, [("typical", 0.09, 0.0), "greedy", ("sample", 1.0, 11)]),
+         (MAX_TREE_F32, ["greedy", ("sample", 1.2, 16), "typical"]),
+         (WIDE_DEEP, [("typical", 0.09, 0.0), ("sample", 1.0, 17), "typical"])]
 
 
 @pytest.mark.parametrize("w,modes", SMALL, ids=lambda p: getattr(p, "name", None))
