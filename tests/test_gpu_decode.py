@@ -22,7 +22,7 @@ import medusa_synth as ms
 import oracle
 from tests.gpu_util import NearTies, check_ranked_ids, close_float, dev, host, require_gpu, tol_logit
 from tests.test_gpu_parity import MINI, MINI_F32, MINI_GQA, f64_inputs
-from tests.test_gpu_step import MODE_CODE, make_step, sample_stats
+from tests.test_gpu_step import DEEP, MAX_TREE_GQA, MODE_CODE, make_step, sample_stats
 
 pytestmark = pytest.mark.gpu
 
@@ -148,7 +148,13 @@ SMALL = [(MINI, "greedy", None, None, False), (MINI, "typical", None, None, True
          (MINI_GQA, "greedy", None, None, False), (MINI_F32, "greedy", None, None, False),
          (ms.workload(0), "greedy", None, None, False),
          (MINI, ("sample", 0.9, 11), None, None, False),
-         (MINI_F32, ("sample", 1.0, 12), None, None, False)]
+         (MINI_F32, ("sample", 1.0, 12), None, None, False),
+         # the largest tree (128 nodes) and the deepest (K = 8, every edge
+         # passing: nine tokens a step), in both loop forms
+         (MAX_TREE_GQA, "greedy", None, None, True),
+         (MAX_TREE_GQA, ("sample", 1.0, 14), None, None, False),
+         (DEEP, ("typical", 0.09, 0.0), None, None, True),
+         (DEEP, ("typical", 0.09, 0.0), None, None, False)]
 
 
 def _mode(w, m):
