@@ -720,7 +720,9 @@ def mtp_heads(xrows: np.ndarray, L: np.ndarray, P0: np.ndarray,
     j <= L_b (later rows are padding, their outputs unused).  heads: per head
     wq, wk, wv, wo, w1 [dff, d], w2 [d, dff], kc, vc.  Returns U [B, K+1, d]
     (U[b, 0] = xrows[b, L_b]; U[b, i] = head i's output at row L_b) and the
-    heads' caches with rows P0_b .. P0_b + R - 1 written (R22)."""
+    heads' caches with rows P0_b .. P0_b + R - 1 written (R22).  Also A
+    [B, K+1, d]: each head's attention-layer output a at row L_b, as stored
+    (A[b, 0] = U[b, 0])."""
     B, R, d = xrows.shape
     K = len(heads)
     depth = np.arange(R)
@@ -728,16 +730,18 @@ def mtp_heads(xrows: np.ndarray, L: np.ndarray, P0: np.ndarray,
     U = np.empty((B, K + 1, d))
     U[:, 0] = xrows[np.arange(B), np.asarray(L, np.int64)]
     U_exact = U.copy()
+    A = U.copy()
     caches = []
     for i, hw in enumerate(heads):
         r = backbone_layer(xrows, P0, depth, chain, hw["wq"], hw["wk"], hw["wv"], hw["wo"],
                            hw["kc"], hw["vc"], Hq, Hkv, dh, dtype, rope_base)
         a = r["y"][np.arange(B), np.asarray(L, np.int64)]             # [B, d]
+        A[:, i + 1] = a
         t = maybe_round(silu(a @ hw["w1"].T), dtype)
         U_exact[:, i + 1] = a + t @ hw["w2"].T
         U[:, i + 1] = maybe_round(U_exact[:, i + 1], dtype)
         caches.append((r["kc"], r["vc"]))
-    return dict(U=U, U_exact=U_exact, caches=caches)
+    return dict(U=U, U_exact=U_exact, A=A, caches=caches)
 
 
 def accepted_rows(y: np.ndarray, L: np.ndarray, path: np.ndarray, K: int) -> np.ndarray:

@@ -102,17 +102,23 @@ def close_float(got: np.ndarray, want: np.ndarray, dtype: str, kind: str, what: 
     return float(np.max(np.abs(got - want) / np.maximum(np.abs(want), 1e-30)))
 
 
-def close_chain(got, want_exact, what: str = "", roundings: int = 2):
+def close_chain(got, want_exact, what: str = "", roundings: int = 2, through=None):
     """bf16 values produced through a chain of roundings (an attention output
     stored in bf16, then further residual steps stored again): within 1e-2 of
     the oracle's unrounded value plus one bf16 unit per rounding point of the
     chain.  A rounding flip at an earlier point passes unchanged through a
-    residual connection, so each rounding point adds up to one unit."""
+    residual connection, so each rounding point adds up to one unit of the
+    value rounded there.  ``through``: the oracle's stored values at the
+    earlier rounding point, when they can exceed the final ones in magnitude
+    (their unit is then the larger)."""
     got = np.asarray(got, np.float64)
     want_exact = np.asarray(want_exact, np.float64)
     assert got.shape == want_exact.shape, (what, got.shape, want_exact.shape)
     err = np.abs(got - want_exact)
-    lim = BF16_ATTN_ATOL + roundings * bf16_ulp(want_exact)
+    mag = np.abs(want_exact)
+    if through is not None:
+        mag = np.maximum(mag, np.abs(np.asarray(through, np.float64)))
+    lim = BF16_ATTN_ATOL + roundings * bf16_ulp(mag)
     assert not (err > lim).any(), (what, float(err.max()), float((err - lim).max()))
     return float(err.max())
 

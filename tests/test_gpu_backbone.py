@@ -19,6 +19,7 @@ import medusa_synth as ms
 import oracle
 from tests.gpu_util import NearTies, check_ranked_ids, close_float, dev, host, require_gpu, tol_logit
 from tests.test_gpu_parity import EDGE, MINI, MINI_GQA, f64_inputs
+from tests.test_gpu_step import MAX_TREE_GQA, MAX_TREE_MHA
 
 pytestmark = pytest.mark.gpu
 
@@ -32,7 +33,8 @@ def mds():
     return m
 
 
-@pytest.mark.parametrize("w", [MINI, MINI_GQA, EDGE[0], EDGE[3]], ids=lambda w: w.name)
+@pytest.mark.parametrize("w", [MINI, MINI_GQA, EDGE[0], EDGE[3], MAX_TREE_GQA, MAX_TREE_MHA],
+                         ids=lambda w: w.name)
 def test_backbone_layer(mds, w):
     tr = oracle.build_tree(w.shortlist, w.max_rank_sum)
     N = tr["N"]

@@ -17,6 +17,7 @@ import oracle
 from tests.gpu_util import (NearTies, check_ranked_ids, close_chain, close_float, dev, host,
                             require_gpu, tol_logit)
 from tests.test_gpu_parity import MINI, MINI_GQA, f64_inputs
+from tests.test_gpu_step import DEEP, WIDE_DEEP
 
 pytestmark = pytest.mark.gpu
 
@@ -46,13 +47,14 @@ def f64_heads(w, hs, sel=None):
     return out
 
 
-def check_draft(w, g_U, g_root, g_topk, U, lm, ties, what, U_exact):
+def check_draft(w, g_U, g_root, g_topk, U, lm, ties, what, U_exact, A):
     for b in range(U.shape[0]):
         # row 0 is h itself; the head rows come through the head layer's
-        # attention (stored in bf16), its residual and the MLP's residual
-        # (stored again): two rounding points of one chain
+        # attention, its residual a (stored in bf16) and the MLP's residual
+        # U = a + W2 t (stored again): two rounding points of one chain, the
+        # first in units of a, which can exceed U in magnitude
         np.testing.assert_array_equal(g_U[b, 0], U[b, 0])
-        close_chain(g_U[b, 1:], U_exact[b, 1:], f"{what} U[{b}]", roundings=2)
+        close_chain(g_U[b, 1:], U_exact[b, 1:], f"{what} U[{b}]", roundings=2, through=A[b, 1:])
         dr = oracle.draft(U[b:b + 1], lm, w.shortlist)
         z = U[b] @ lm.T
         tl = tol_logit(w.dtype, float(np.abs(z).max()))
@@ -62,7 +64,7 @@ def check_draft(w, g_U, g_root, g_topk, U, lm, ties, what, U_exact):
                              f"{what} topk[{b},{k}]")
 
 
-@pytest.mark.parametrize("w", [MINI, MINI_GQA], ids=lambda w: w.name)
+@pytest.mark.parametrize("w", [MINI, MINI_GQA, DEEP, WIDE_DEEP], ids=lambda w: w.name)
 def test_mtp_heads_call(mds, w):
     dff = 2 * w.d
     hs = ms.make_mtp_heads(w, dff)
@@ -88,7 +90,8 @@ def test_mtp_heads_call(mds, w):
     r = oracle.mtp_heads(ms.as_f64(xr, w.dtype), L, P0, f64_heads(w, hs), w.Hq, w.Hkv, w.dh,
                          w.dtype, ROPE_BASE)
     ties = NearTies()
-    check_draft(w, host(U), host(root), host(topk), r["U"], lm64, ties, "mtp", r["U_exact"])
+    check_draft(w, host(U), host(root), host(topk), r["U"], lm64, ties, "mtp", r["U_exact"],
+                r["A"])
     for i, hw in enumerate(heads):
         gk = host(hw["Kc"])
         kc = r["caches"][i][0]
@@ -143,7 +146,7 @@ def test_mtp_decode(mds):
         m = oracle.mtp_heads(ms.as_f64(ms.bf16_bits(g_rows.astype(np.float32)), w.dtype), g_L,
                              g_P0, o_heads, w.Hq, w.Hkv, w.dh, w.dtype, ROPE_BASE)
         check_draft(w, g["U"], g["root"], g["topk"], m["U"], f["lm"], ties, f"step {s}",
-                    m["U_exact"])
+                    m["U_exact"], m["A"])
         o_heads = [dict(hw, kc=kv[0], vc=kv[1]) for hw, kv in zip(o_heads, m["caches"])]
         tok = oracle.fill_tokens(g["root"].astype(np.int64), g["topk"].astype(np.int64), depth,
                                  rank)
