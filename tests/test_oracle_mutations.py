@@ -57,6 +57,17 @@ def tree_parent_shift(shortlist, mrs):
     return tr
 
 
+def fill_next_head(root, topk_id, depth, rank):
+    # a node at depth j takes head j + 1's token (clamped to the last head)
+    K = topk_id.shape[1]
+    return mo.fill_tokens(root, topk_id, np.minimum(np.asarray(depth) + 1, K), rank)
+
+
+def fill_rank_zero(root, topk_id, depth, rank):
+    # every node takes its head's top token
+    return mo.fill_tokens(root, topk_id, depth, np.zeros_like(rank))
+
+
 def sorted_ids_high_id_first(z):
     return np.lexsort((-np.arange(z.shape[0]), -z))
 
@@ -297,6 +308,8 @@ CASES = [
     ("heads: W transposed", dict(heads_residual=heads_untransposed), [pins.check_heads_torch]),
     ("tree: mask misses the node itself", dict(build_tree=tree_mask_no_self), [pins.check_tree_golden, pins.check_mask_is_ancestors]),
     ("tree: parent index shifted", dict(build_tree=tree_parent_shift), [pins.check_tree_golden, pins.check_mask_is_ancestors]),
+    ("fill: a node takes the next head's token", dict(fill_tokens=fill_next_head), [pins.check_fill_tokens_paths]),
+    ("fill: every node its head's top token", dict(fill_tokens=fill_rank_zero), [pins.check_fill_tokens_paths]),
     ("top-s: ties to the higher id", dict(sorted_ids=sorted_ids_high_id_first), [pins.check_topk]),
     ("attention: mask transposed", dict(tree_attention=attention_with("mask_T")), [pins.check_attention_per_path, pins.check_attention_uniform_weights]),
     ("attention: GQA head map j % Hkv", dict(tree_attention=attention_with("gqa_mod")), [pins.check_attention_per_path, pins.check_attention_uniform_weights]),

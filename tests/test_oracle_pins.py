@@ -189,6 +189,30 @@ def check_draft_vs_torch(orc):
             np.testing.assert_allclose(dr["topk_val"][b, i, :s], v.numpy(), rtol=1e-12)
 
 
+def check_fill_tokens_paths(orc):
+    """Each candidate is one element of the product of the heads' shortlists:
+    the node with rank tuple (t_1, ..., t_d) carries, along its root path,
+    the root and then head j's t_j-th token at depth j (full and sparse
+    trees)."""
+    rng = np.random.default_rng(9)
+    for s, mrs in [((3, 2, 2), -1), ((8, 4, 2, 2, 1), 3)]:
+        tr = orc.build_tree(s, mrs)
+        K = len(s)
+        B = 2
+        root = rng.integers(0, 1000, size=B)
+        topk = rng.integers(0, 1000, size=(B, K, max(s)))
+        tok = orc.fill_tokens(root, topk, tr["depth"], tr["rank"])
+        chains = brute.paths_from_parents(tr["parent"])
+        for b in range(B):
+            for n, tup in enumerate(tr["tuples"]):
+                want = [int(root[b])] + [int(topk[b, j, t]) for j, t in enumerate(tup)]
+                assert [int(tok[b, c]) for c in chains[n]] == want, (s, n, tup)
+
+
+def test_fill_tokens_paths():
+    check_fill_tokens_paths(oracle)
+
+
 def test_heads_torch():
     check_heads_torch(oracle)
 
