@@ -198,7 +198,7 @@ MAX_TREE_GQA = ms.Workload("max-tree-gqa", "bf16", B=3, d=256, V=1000, Hq=4, Hkv
 MAX_TREE_MHA = ms.Workload("max-tree-mha", "bf16", B=2, d=256, V=700, Hq=2, Hkv=2, dh=128, K=3,
                            shortlist=(8, 7, 3), max_rank_sum=7, P=(100, 500), accept="both",
                            seed=8)
-
+# The largest tree on the fp32 path.
 MAX_TREE_F32 = ms.Workload("max-tree-f32", "f32", B=2, d=192, V=600, Hq=6, Hkv=3, dh=64, K=3,
                            shortlist=(8, 7, 3), max_rank_sum=7, P=(30, 300), accept="both",
                            seed=14)
