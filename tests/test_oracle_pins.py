@@ -864,7 +864,8 @@ def test_backbone_per_path():
 def check_decode_backbone_lossless(orc, seed=12, n_layers=2, n_steps=3):
     """The decoding loop with a 2-layer backbone and greedy acceptance emits
     exactly sequential greedy decoding of that backbone (positions and both
-    layers' caches carried across steps)."""
+    layers' caches carried across steps), and leaves in every layer's cache
+    the rows sequential decoding of the emitted tokens writes."""
     w, f, P = tiny(seed=seed, B=2, d=64, V=8, Hq=2, Hkv=1, dh=64, shortlist=(3, 2, 2),
                    P=(5, 12))
     x = ms.make_inputs(w)
@@ -880,6 +881,20 @@ def check_decode_backbone_lossless(orc, seed=12, n_layers=2, n_steps=3):
                                         emitted[0], len(emitted), f["emb"], f["layers"], f["lm"],
                                         w.Hq, w.Hkv, w.dh, f["rope_base"])
         assert emitted + [int(rs[-1]["path"]["next_root"][b])] == seq
+        # every layer's cache: one rotated K and V row per emitted token, as a
+        # causal pass of the stack over them at positions P_b, P_b + 1, ...
+        _, ks, vs = brute.causal_stack([lw["kc"][b][:, :Pb] for lw in f["layers"]],
+                                       [lw["vc"][b][:, :Pb] for lw in f["layers"]], Pb, emitted,
+                                       f["emb"], f["layers"], w.Hq, w.Hkv, w.dh, f["rope_base"],
+                                       kv=True)
+        assert int(rs[-1]["P"][b]) == Pb + len(emitted)
+        for l, (kc, vc) in enumerate(rs[-1]["layers_kv"]):
+            for j in range(len(emitted)):
+                np.testing.assert_allclose(kc[b][:, Pb + j].reshape(-1), ks[l][j], rtol=1e-9,
+                                           atol=1e-9)
+                np.testing.assert_allclose(vc[b][:, Pb + j].reshape(-1), vs[l][j], rtol=1e-9,
+                                           atol=1e-9)
+            np.testing.assert_array_equal(kc[b][:, :Pb], f["layers"][l]["kc"][b][:, :Pb])
 
 
 def test_decode_backbone_lossless():
