@@ -396,6 +396,10 @@ def step(w, f64: Dict[str, np.ndarray], P: np.ndarray, mode: str,
     else:
         U = heads_residual(h, f64["W"], w.dtype)
     dr = draft(U, f64["lm"], w.shortlist)
+    if "root" in f64:
+        # a loop step after the first: its root is the last step's next_root
+        # (R10), the heads' shortlists still come from h
+        dr = dict(dr, root=np.asarray(f64["root"], np.int64)[sel])
     tr = build_tree(w.shortlist, w.max_rank_sum)
     tok = fill_tokens(dr["root"], dr["topk_id"], tr["depth"], tr["rank"])
     if "layers" in f64:
@@ -433,10 +437,13 @@ def step(w, f64: Dict[str, np.ndarray], P: np.ndarray, mode: str,
 # back, then draft again from the last accepted position).  R10 below.
 #   R10 The hidden state the next step's heads read is the verify layer's
 #       output y at the step's accepted node p_L: the base model's last hidden
-#       state at the last accepted token.  Its base-head argmax is therefore
-#       the step's next_root, which becomes the next step's root (R7), so the
-#       tokens emitted over consecutive steps are root, path tokens, then the
-#       next root, and so on.
+#       state at the last accepted token.  The step's next_root (the token the
+#       base model supplies after the accepted prefix) becomes the next step's
+#       root (R7), so the tokens emitted over consecutive steps are root, path
+#       tokens, then the next root, and so on.  Under greedy and typical
+#       acceptance next_root is the argmax at p_L, the next draft's own root;
+#       under exact sampling it is the token drawn at p_L (R11), which the
+#       next step must keep for the loop to sample from the base model.
 # ----------------------------------------------------------------------------
 
 def next_hidden(y: np.ndarray, L: np.ndarray, path: np.ndarray) -> np.ndarray:
@@ -450,7 +457,8 @@ def decode(w, f64: Dict[str, np.ndarray], P: np.ndarray, mode: str, n_steps: int
            sampling: Tuple = None) -> List[Dict]:
     """``n_steps`` consecutive steps from hidden state f64["h"]: each step as
     ``step`` on the carried caches and prefix lengths, the next step reading
-    next_hidden of this one (``sampling`` as in ``step``; the draws of each
+    next_hidden of this one and taking its next_root as root (R10)
+    (``sampling`` as in ``step``; the draws of each
     step are tied to its prefix lengths, R12).  Returns each step's
     intermediates plus its ``emitted`` tokens per sequence (root and accepted
     path tokens, L + 1)."""
@@ -482,6 +490,7 @@ def decode(w, f64: Dict[str, np.ndarray], P: np.ndarray, mode: str, n_steps: int
         out.append(r)
         cur = dict(cur)
         cur["h"] = next_hidden(r["attn"]["y"], r["path"]["L"], r["path"]["path"])
+        cur["root"] = r["path"]["next_root"].copy()
         cur["kc"], cur["vc"] = r["kc"], r["vc"]
         if "layers" in cur:
             cur["layers"] = [dict(lw, kc=kv[0], vc=kv[1])

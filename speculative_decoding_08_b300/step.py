@@ -51,6 +51,10 @@ class MedusaStep:
                         self.mask)
         self.U = torch.empty((B, K + 1, self.d), dtype=self.dtype, device=dev)
         self.root = torch.empty(B, dtype=i32, device=dev)
+        # the heads' own argmax root in loop steps after the first, whose root
+        # is the previous step's next_root
+        self.root_draft = torch.empty(B, dtype=i32, device=dev)
+        self._carried = False
         self.topk_id = torch.empty((B, K, self.smax), dtype=i32, device=dev)
         self.topk_val = torch.empty((B, K, self.smax), dtype=torch.float32, device=dev)
         self.tok = torch.empty((B, N), dtype=i32, device=dev)
@@ -134,10 +138,11 @@ class MedusaStep:
         if commit:
             self._commit()
 
-    def _draft(self, h):
-        """The step's draft from hidden state h: U, root and shortlists."""
-        medusa_heads(h, self.W, self.lm, self.shortlist, self.smax, self.U, self.root,
-                     self.topk_id, self.topk_val, self.ws)
+    def _draft(self, h, root=None):
+        """The step's draft from hidden state h: U, root (into ``root`` when
+        given, else self.root) and shortlists."""
+        medusa_heads(h, self.W, self.lm, self.shortlist, self.smax, self.U,
+                     self.root if root is None else root, self.topk_id, self.topk_val, self.ws)
 
     def _before_commit(self):
         pass
@@ -150,8 +155,8 @@ class MedusaStep:
                         tree_topk_val=self.tree_topk_val, h_next=h, root_out=self.root,
                         topk_id_out=self.topk_id, topk_val_out=self.topk_val)
         else:
-            next_inputs(self.L, self.path, self.ws, N=self.N, smax=self.smax, y=self.y,
-                        h_next=h)
+            next_inputs(self.L, self.path, self.ws, N=self.N, smax=self.smax,
+                        next_root=self.next_root, y=self.y, h_next=h, root_out=self.root)
 
     def _verify_layers(self):
         """Token fill and the verify layer(s): y for every tree row."""
@@ -185,7 +190,10 @@ class MedusaStep:
     # The decoding loop ("Medusa Heads", "How it works": draft, verify,
     # accept and roll back, then draft again from the last accepted
     # position).  Step s + 1 reads the verify layer's output at step s's
-    # accepted node as its hidden state; its root is step s's next_root.
+    # accepted node as its hidden state; its root is step s's next_root (the
+    # token the base model supplies after the accepted prefix: the argmax at
+    # the accepted node under greedy and typical acceptance, the token drawn
+    # there under exact sampling).
     #
     # Two forms of the steady-state step:
     #   separate (canonical order): medusa_heads(h) -> tree_attention ->
@@ -213,8 +221,9 @@ class MedusaStep:
 
     def begin_decode(self, h: torch.Tensor, fused: bool) -> None:
         """Before the first step of a loop: the fused form drafts the first
-        step from ``h`` (root and shortlists); the separate form needs
-        nothing."""
+        step from ``h`` (root and shortlists); the separate form drafts in
+        its first step, its root the base head's argmax."""
+        self._carried = False
         if fused:
             if not self.fused_ok:
                 raise ValueError("the fused verify pass needs bf16 weights")
@@ -225,14 +234,18 @@ class MedusaStep:
         """Enqueue one steady-state step (asynchronous).  Updates in place:
         the KV caches and P (the accepted path committed), ``h`` (the next
         step's hidden state) and, in the fused form, root / topk_id /
-        topk_val (the next step's draft)."""
+        topk_val (the next step's draft) or root alone (the separate form,
+        whose next step drafts its shortlists from ``h``)."""
         if not fused:
-            self._draft(h)
+            # after the first step the root is already in place (the last
+            # step's next_root); the heads' own argmax is not used
+            self._draft(h, self.root_draft if self._carried else None)
         self._verify_layers()
         self._verify_and_accept(mode, eps, delta, temperature, seed, fused)
         self._before_commit()
         self._commit()
         self._next(h, fused)
+        self._carried = True
 
     def decode(self, h: torch.Tensor, n_steps: int, fused="auto", mode: int = TYPICAL,
                eps: float = 0.09, delta: float = 0.3, record: bool = False,
@@ -354,17 +367,20 @@ class MTPStep(MedusaStep):
     def begin_decode(self, h, fused):
         if fused:
             raise ValueError("MTP heads run with the separate form of the loop")
+        self._carried = False
         self._start(h)
 
-    def _draft(self, h):
+    def _draft(self, h, root=None):
         mtp_heads(self.xrows, self.Lm, self.P0, self.chain_depth, self.chain_mask, self.heads,
-                  self.lm, self.shortlist, self.smax, self.U, self.root, self.topk_id,
-                  self.topk_val, self.ws, Hq=self.Hq, Hkv=self.Hkv, rope_base=self.rope_base)
+                  self.lm, self.shortlist, self.smax, self.U,
+                  self.root if root is None else root, self.topk_id, self.topk_val, self.ws,
+                  Hq=self.Hq, Hkv=self.Hkv, rope_base=self.rope_base)
 
     def _before_commit(self):
         self.P0.copy_(self.P)            # position of the accepted rows' first
 
     def _next(self, h, fused):
-        next_inputs(self.L, self.path, self.ws, N=self.N, smax=self.smax, y=self.y, h_next=h,
+        next_inputs(self.L, self.path, self.ws, N=self.N, smax=self.smax,
+                    next_root=self.next_root, y=self.y, h_next=h, root_out=self.root,
                     rows_out=self.xrows)
         self.Lm.copy_(self.L)

@@ -115,7 +115,7 @@ def compare_backbone_decode(mds, w, sample, n_layers, n_steps, mode="typical", e
         torch.cuda.synchronize()
         assert mds.status_check(step.ws) == 0, f"step {s}"
         gx = layer_outputs(step, n_layers)
-        g = dict(root=host(step.root), topk=host(step.topk_id), tok=host(step.tok),
+        g = dict(root=host(step.tok)[:, 0], topk=host(step.topk_id), tok=host(step.tok),
                  y=host(step.y), argmax=host(step.argmax), stats=host(step.stats),
                  child=host(step.childlogit), ok=host(step.ok).astype(bool), L=host(step.L),
                  path=host(step.path), nr=host(step.next_root), P=host(step.P), h=host(h))
@@ -125,7 +125,11 @@ def compare_backbone_decode(mds, w, sample, n_layers, n_steps, mode="typical", e
             dr = oracle.draft(U, f["lm"], w.shortlist)
             z = U[0] @ f["lm"].T
             tl = tol_logit(w.dtype, float(np.abs(z).max()))
-            check_ranked_ids([g["root"][b]], z[0], [dr["root"][0]], tl, ties, f"{what} root")
+            if s == 0:
+                check_ranked_ids([g["root"][b]], z[0], [dr["root"][0]], tl, ties, f"{what} root")
+            else:
+                # later steps: the last step's next_root
+                assert int(g["root"][b]) == int(prev_nr[b]), what
             for k, sk in enumerate(w.shortlist):
                 check_ranked_ids(g["topk"][b, k, :sk], z[k + 1], dr["topk_id"][0, k, :sk], tl,
                                  ties, f"{what} topk {k}")
@@ -182,6 +186,7 @@ def compare_backbone_decode(mds, w, sample, n_layers, n_steps, mode="typical", e
             o_h[i] = oracle.next_hidden(bb["y"], Lg, pg)[0]
             close_float(g["h"][b], o_h[i], w.dtype, "attn", f"{what} h_next",
                         exact=oracle.next_hidden(bb["y_exact"], Lg, pg)[0])
+        prev_nr = g["nr"]
     ties.report(f"{w.name} backbone x{n_layers}")
     if ties.count == 0:
         f2 = dict(f)

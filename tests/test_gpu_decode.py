@@ -56,7 +56,9 @@ def compare_decode(mds, w, sample, mode, eps, delta, n_steps, fused, T=1.0, seed
         torch.cuda.synchronize()
         assert mds.status_check(step.ws) == 0, f"step {s}"
         if not fused:
-            g_root, g_topk = host(step.root), host(step.topk_id)
+            # the step's root is its tree's row 0 (step.root already holds the
+            # next step's)
+            g_root, g_topk = host(step.tok)[:, 0], host(step.topk_id)
         g = dict(tok=host(step.tok), y=host(step.y), argmax=host(step.argmax),
                  stats=host(step.stats), child=host(step.childlogit), ok=host(step.ok).astype(bool),
                  L=host(step.L), path=host(step.path), nr=host(step.next_root), P=host(step.P),
@@ -68,7 +70,11 @@ def compare_decode(mds, w, sample, mode, eps, delta, n_steps, fused, T=1.0, seed
             dr = oracle.draft(U, f["lm"], w.shortlist)
             z = U[0] @ f["lm"].T
             tl = tol_logit(w.dtype, float(np.abs(z).max()))
-            check_ranked_ids([g_root[b]], z[0], [dr["root"][0]], tl, ties, f"{what} root")
+            if s == 0:
+                check_ranked_ids([g_root[b]], z[0], [dr["root"][0]], tl, ties, f"{what} root")
+            else:
+                # later steps: the last step's next_root
+                assert int(g_root[b]) == int(prev_nr[b]), what
             for k, sk in enumerate(w.shortlist):
                 check_ranked_ids(g_topk[b, k, :sk], z[k + 1], dr["topk_id"][0, k, :sk], tl, ties,
                                  f"{what} topk {k}")
@@ -130,6 +136,7 @@ def compare_decode(mds, w, sample, mode, eps, delta, n_steps, fused, T=1.0, seed
             o_h[i] = oracle.next_hidden(at["y"], g["L"][b:b + 1], g["path"][b:b + 1])[0]
             yx = oracle.next_hidden(at["y_exact"], g["L"][b:b + 1], g["path"][b:b + 1])[0]
             close_float(g["h"][b], o_h[i], w.dtype, "attn", f"{what} h_next", exact=yx)
+        prev_nr = g["nr"]
     ties.report(f"{w.name} decode fused={fused}")
     if ties.count == 0:
         ref = oracle.decode(w, f, x["P"][sample], mode, n_steps,

@@ -137,9 +137,14 @@ def test_mtp_decode(mds):
         step.decode_step(h, False, 1, eps, delta)
         torch.cuda.synchronize()
         assert mds.status_check(step.ws) == 0, s
-        g = dict(U=host(step.U), root=host(step.root), topk=host(step.topk_id),
+        g = dict(U=host(step.U), root=host(step.tok)[:, 0], topk=host(step.topk_id),
                  tok=host(step.tok), y=host(step.y), ok=host(step.ok).astype(bool),
-                 L=host(step.L), path=host(step.path), P=host(step.P))
+                 L=host(step.L), path=host(step.path), P=host(step.P),
+                 nr=host(step.next_root))
+        if s:
+            # later steps: the root is the last step's next_root
+            np.testing.assert_array_equal(g["root"], prev_nr)
+        prev_nr = g["nr"]
         np.testing.assert_array_equal(g_L, o_L)
         np.testing.assert_array_equal(g_P0, o_P0)
         close_chain(g_rows, o_rows, f"step {s} rows", roundings=1)

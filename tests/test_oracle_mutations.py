@@ -208,6 +208,14 @@ def decode_with_hidden(pick):
     return f
 
 
+_step = mo.step
+
+
+def step_root_from_heads(w, f64, *args, **kw):
+    # every step's root the base head's argmax: a drawn bonus token discarded
+    return _step(w, {k: v for k, v in f64.items() if k != "root"}, *args, **kw)
+
+
 def hidden_of_root(y, L, path):
     return y[:, 0].copy()
 
@@ -339,6 +347,7 @@ CASES = [
     ("mtp: residual around the MLP dropped", dict(mtp_heads=mtp_mlp_no_residual), [pins.check_mtp_heads, pins.check_mtp_zero_heads]),
     ("mtp loop: every accepted row the last node's", dict(decode=patched("accepted_rows", rows_all_last, "decode")), [pins.check_decode_mtp]),
     ("mtp loop: the root's row left out", dict(decode=patched("accepted_rows", rows_skip_root, "decode")), [pins.check_decode_mtp]),
+    ("decode: the next root the base head's argmax, the drawn token discarded", dict(decode=patched("step", step_root_from_heads, "decode")), [pins.check_decode_sample_lossless]),
     ("decode: next hidden state from the root row", dict(decode=decode_with_hidden(hidden_of_root)), [pins.check_decode_greedy_lossless]),
     ("decode: next hidden state from the accepted node's parent", dict(decode=decode_with_hidden(hidden_of_parent)), [pins.check_decode_greedy_lossless]),
 ]

@@ -577,6 +577,15 @@ def check_decode_greedy_lossless(orc, seed=12, n_steps=4):
             np.testing.assert_allclose(last["vc"][b][:, Pb + j].reshape(-1), v[j], rtol=1e-12,
                                        atol=1e-12)
         np.testing.assert_array_equal(last["kc"][b][:, :Pb], f["kc"][b][:, :Pb])
+        # each later step drafts from the verifier's output at the last token
+        # emitted before it (the base model's hidden state there)
+        y, _, _ = brute.causal_layer(f["kc"][b][:, :Pb], f["vc"][b][:, :Pb], emitted, f["emb"],
+                                     f["wq"], f["wk"], f["wv"], f["wo"], w.Hq, w.Hkv, w.dh)
+        n = 0
+        for s, r in enumerate(rs):
+            if s:
+                np.testing.assert_allclose(r["U"][b, 0], y[n - 1], rtol=1e-9, atol=1e-9)
+            n += len(r["emitted"][b])
     assert depths >= {0, 1, 2, 3}, depths
 
 
@@ -735,6 +744,39 @@ def _branch(tr, node):
         out.append(node)
         node = int(tr["parent"][node])
     return out
+
+
+def check_decode_sample_lossless(orc, rows=3000, T=0.8):
+    """Exact sampling keeps the verifier's output distribution, whatever the
+    heads draft: over many seeds, the first two tokens the decoding loop
+    emits after the root are distributed as two steps of sequential sampling
+    at temperature T from the one-layer verifier, p(t1 | root) p(t2 | root, t1)
+    (brute-force logits), each cell within 5 standard deviations."""
+    w, f, P = tiny(seed=3, B=1, d=16, V=4, Hq=1, Hkv=1, dh=16, shortlist=(2, 1), P=(6, 6))
+    Pb = int(P[0])
+    counts = np.zeros((w.V, w.V))
+    roots = set()
+    for sd in range(rows):
+        rs = orc.decode(w, f, P, "sample", 2, sampling=(T, sd))
+        seq = sum((r["emitted"][0] for r in rs), []) + [int(rs[-1]["path"]["next_root"][0])]
+        roots.add(seq[0])
+        counts[seq[1], seq[2]] += 1
+    assert len(roots) == 1          # the first root is the base head's argmax
+
+    def p_next(tokens):
+        y, _, _ = brute.causal_layer(f["kc"][0][:, :Pb], f["vc"][0][:, :Pb], tokens, f["emb"],
+                                     f["wq"], f["wk"], f["wv"], f["wo"], w.Hq, w.Hkv, w.dh)
+        return scipy.special.softmax((f["lm"] @ y[-1]) / T)
+
+    root = roots.pop()
+    p1 = p_next([root])
+    want = np.array([[p1[a] * p_next([root, a])[b] for b in range(w.V)] for a in range(w.V)])
+    sdev = np.sqrt(rows * want * (1 - want))
+    assert np.all(np.abs(counts - rows * want) < 5 * sdev + 2), (counts, rows * want)
+
+
+def test_decode_sample_lossless():
+    check_decode_sample_lossless(oracle)
 
 
 def test_philox_library():
