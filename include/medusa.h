@@ -341,7 +341,8 @@ MDS_API int mds_lm_verify_draft(int dtype, int B, int N, int d, int V, int K, co
  *   L        device [B] int32               out: accepted depth
  *   path     device [B, K+1] int32          out: node indices root..accepted,
  *                                           -1 after position L
- *   next_root device [B] int32              out: argmax at the accepted node */
+ *   next_root device [B] int32              out: argmax (mode 2: the draw) at
+ *                                            the accepted node */
 MDS_API int mds_verify_accept(int B, int N, int K, int mode, float eps, float delta,
                       const int32_t* parent, const int32_t* depth, const int32_t* tok,
                       const int32_t* argmax, const float* stats, const float* childlogit,
@@ -364,9 +365,12 @@ MDS_API int mds_compact_kv(int dtype, int B, int Hkv, int dh, int Pmax, int K, c
  *   h_next    device [B, d] or NULL   out: y[b, a, :], the hidden state the
  *                                     next step's heads read (the verify
  *                                     layer's output at the last accepted
- *                                     token; its base-head argmax is
- *                                     next_root)
- *   root_out  device [B] or NULL      out: next_root[b] (the next step's root)
+ *                                     token)
+ *   root_out  device [B] or NULL      out: next_root[b], the next step's root
+ *                                     (under greedy and typical acceptance
+ *                                     the base-head argmax of h_next; under
+ *                                     exact sampling the token drawn there,
+ *                                     which a re-draft would lose)
  *   topk_id_out, topk_val_out device [B, K, smax] or NULL
  *                                     out: tree_topk_id/val[b, a] from
  *                                     mds_lm_verify_draft (the next step's
