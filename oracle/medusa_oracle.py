@@ -454,14 +454,15 @@ def next_hidden(y: np.ndarray, L: np.ndarray, path: np.ndarray) -> np.ndarray:
 
 def decode(w, f64: Dict[str, np.ndarray], P: np.ndarray, mode: str, n_steps: int,
            batch: Sequence[int] = None, eps: float = None, delta: float = None,
-           sampling: Tuple = None) -> List[Dict]:
+           sampling: Tuple = None, root: np.ndarray = None) -> List[Dict]:
     """``n_steps`` consecutive steps from hidden state f64["h"]: each step as
     ``step`` on the carried caches and prefix lengths, the next step reading
     next_hidden of this one and taking its next_root as root (R10)
     (``sampling`` as in ``step``; the draws of each
     step are tied to its prefix lengths, R12).  Returns each step's
     intermediates plus its ``emitted`` tokens per sequence (root and accepted
-    path tokens, L + 1)."""
+    path tokens, L + 1).  ``root`` [B]: the first step's root (default: the
+    base head's argmax), e.g. the prefill's own draw under exact sampling."""
     sel = list(range(w.B)) if batch is None else list(batch)
     wk = w if eps is None and delta is None else w.with_(
         eps=w.eps if eps is None else eps, delta=w.delta if delta is None else delta)
@@ -481,6 +482,8 @@ def decode(w, f64: Dict[str, np.ndarray], P: np.ndarray, mode: str, n_steps: int
                           L=np.zeros(len(sel), np.int64),
                           P0=np.asarray(P)[sel].astype(np.int64) - 1)
     Pc = np.asarray(P)[sel].astype(np.int64)
+    if root is not None:
+        cur["root"] = np.asarray(root, np.int64)[sel]
     idx = list(range(len(sel)))
     out = []
     for _ in range(n_steps):

@@ -219,15 +219,20 @@ class MedusaStep:
         return (self.fused_ok and self.W is not None
                 and self.B * self.N * (self.K + 1) <= self.FUSED_MAX_ROWS)
 
-    def begin_decode(self, h: torch.Tensor, fused: bool) -> None:
+    def begin_decode(self, h: torch.Tensor, fused: bool, root: torch.Tensor = None) -> None:
         """Before the first step of a loop: the fused form drafts the first
         step from ``h`` (root and shortlists); the separate form drafts in
-        its first step, its root the base head's argmax."""
+        its first step.  The first root is the base head's argmax unless
+        ``root`` (device [B] int32) gives it, e.g. the prefill's own draw
+        under exact sampling."""
         self._carried = False
         if fused:
             if not self.fused_ok:
                 raise ValueError("the fused verify pass needs bf16 weights")
             self._draft(h)
+        if root is not None:
+            self.root.copy_(root)
+            self._carried = True
 
     def decode_step(self, h: torch.Tensor, fused: bool, mode: int = TYPICAL, eps: float = 0.09,
                     delta: float = 0.3, temperature: float = 1.0, seed: int = 0) -> None:
@@ -249,14 +254,15 @@ class MedusaStep:
 
     def decode(self, h: torch.Tensor, n_steps: int, fused="auto", mode: int = TYPICAL,
                eps: float = 0.09, delta: float = 0.3, record: bool = False,
-               temperature: float = 1.0, seed: int = 0):
+               temperature: float = 1.0, seed: int = 0, root: torch.Tensor = None):
         """``n_steps`` consecutive steps from hidden state ``h`` (updated in
-        place).  ``fused``: True, False or "auto" (``fused_auto``).  With
-        ``record`` the host waits after every step and the per-step L, path,
-        tree tokens and next_root are returned (host tensors)."""
+        place).  ``fused``: True, False or "auto" (``fused_auto``).  ``root``:
+        the first step's root (see ``begin_decode``).  With ``record`` the
+        host waits after every step and the per-step L, path, tree tokens and
+        next_root are returned (host tensors)."""
         if fused == "auto":
             fused = self.fused_auto() and mode != SAMPLE
-        self.begin_decode(h, fused)
+        self.begin_decode(h, fused, root)
         out = []
         for _ in range(n_steps):
             self.decode_step(h, fused, mode, eps, delta, temperature, seed)
@@ -364,11 +370,14 @@ class MTPStep(MedusaStep):
         self._start(h)
         super().run(h, *args, **kw)
 
-    def begin_decode(self, h, fused):
+    def begin_decode(self, h, fused, root=None):
         if fused:
             raise ValueError("MTP heads run with the separate form of the loop")
         self._carried = False
         self._start(h)
+        if root is not None:
+            self.root.copy_(root)
+            self._carried = True
 
     def _draft(self, h, root=None):
         mtp_heads(self.xrows, self.Lm, self.P0, self.chain_depth, self.chain_mask, self.heads,

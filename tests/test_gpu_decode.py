@@ -34,7 +34,7 @@ def mds():
     return m
 
 
-def compare_decode(mds, w, sample, mode, eps, delta, n_steps, fused, T=1.0, seed=0):
+def compare_decode(mds, w, sample, mode, eps, delta, n_steps, fused, T=1.0, seed=0, root=None):
     x = ms.make_inputs(w)
     step, h = make_step(mds, w, x)
     mcode = MODE_CODE[mode]
@@ -47,7 +47,7 @@ def compare_decode(mds, w, sample, mode, eps, delta, n_steps, fused, T=1.0, seed
     o_P = x["P"][sample].astype(np.int64)
     ties = NearTies()
     emitted = {b: [] for b in sample}
-    step.begin_decode(h, fused)
+    step.begin_decode(h, fused, None if root is None else dev(root, "i32"))
     for s in range(n_steps):
         if fused:
             torch.cuda.synchronize()
@@ -70,7 +70,9 @@ def compare_decode(mds, w, sample, mode, eps, delta, n_steps, fused, T=1.0, seed
             dr = oracle.draft(U, f["lm"], w.shortlist)
             z = U[0] @ f["lm"].T
             tl = tol_logit(w.dtype, float(np.abs(z).max()))
-            if s == 0:
+            if s == 0 and root is not None:
+                assert int(g_root[b]) == int(root[b]), what
+            elif s == 0:
                 check_ranked_ids([g_root[b]], z[0], [dr["root"][0]], tl, ties, f"{what} root")
             else:
                 # later steps: the last step's next_root
@@ -141,7 +143,8 @@ def compare_decode(mds, w, sample, mode, eps, delta, n_steps, fused, T=1.0, seed
     if ties.count == 0:
         ref = oracle.decode(w, f, x["P"][sample], mode, n_steps,
                             batch=list(range(len(sample))), eps=eps, delta=delta,
-                            sampling=(T, seed, list(sample)) if mode == "sample" else None)
+                            sampling=(T, seed, list(sample)) if mode == "sample" else None,
+                            root=None if root is None else np.asarray(root)[sample])
         for i, b in enumerate(sample):
             want = sum((r["emitted"][i] for r in ref), [])
             assert emitted[b] == want, (b, emitted[b], want)
@@ -179,6 +182,15 @@ def _mode(w, m):
 def test_decode_small(mds, w, m, _a, _b, fused):
     mode, eps, delta, T, seed = _mode(w, m)
     compare_decode(mds, w, list(range(w.B)), mode, eps, delta, 4, fused, T, seed)
+
+
+def test_decode_given_first_root(mds):
+    """The first root given by the caller (under exact sampling, the
+    prefill's own draw): the loop starts from it, in both forms where they
+    apply, and continues as the oracle's loop from the same root."""
+    roots = np.array([5, 17, 250], np.int32)
+    compare_decode(mds, MINI, [0, 1, 2], "sample", 0.0, 0.0, 3, False, 0.9, 21, root=roots)
+    compare_decode(mds, MINI, [0, 1, 2], "typical", MINI.eps, MINI.delta, 3, True, root=roots)
 
 
 FULL = [(1, [0], ("typical", 1.0, 1.05), True),
