@@ -237,6 +237,11 @@ def gumbel_no_temperature(logits, T, seed, words3):
     return mo.gumbel_keys(logits, 1.0, seed, words3)
 
 
+def gumbel_times_temperature(logits, T, seed, words3):
+    # l * T + G instead of l / T + G
+    return _gumbel_keys(logits * T * T, T, seed, words3)
+
+
 def gumbel_sign_flipped(logits, T, seed, words3):
     g = mo.gumbel_keys(logits, T, seed, words3) - logits / T
     return logits / T - g
@@ -336,6 +341,7 @@ CASES = [
     ("bf16: truncation instead of rounding", dict(round_bf16=round_truncate), [pins.check_round_bf16]),
     ("philox: key not bumped between rounds", dict(philox4x64=philox_no_key_bump), [pins.check_philox_library]),
     ("sample: temperature ignored", dict(gumbel_keys=gumbel_no_temperature), [pins.check_sampler_distribution]),
+    ("sample: logits times T", dict(decode=patched("gumbel_keys", gumbel_times_temperature, "decode")), [pins.check_decode_sample_cold_is_greedy]),
     ("sample: Gumbel noise sign flipped", dict(gumbel_keys=gumbel_sign_flipped), [pins.check_sampler_distribution, pins.check_sampling_is_rejection_sampling]),
     ("sample: the lowest key drawn", dict(sample_tokens=patched("gumbel_keys", gumbel_lowest_key, "sample_tokens")), [pins.check_sample_tokens_draws]),
     ("sample: counter without the sequence number", dict(sample_tokens=patched("gumbel_keys", gumbel_no_sequence, "sample_tokens")), [pins.check_sample_tokens_draws]),

@@ -775,6 +775,24 @@ def check_decode_sample_lossless(orc, rows=3000, T=0.8):
     assert np.all(np.abs(counts - rows * want) < 5 * sdev + 2), (counts, rows * want)
 
 
+def check_decode_sample_cold_is_greedy(orc, n_steps=4):
+    """At a temperature far below every logit gap the draw is the argmax, so
+    the sampled decoding loop emits exactly what the greedy loop emits, step
+    for step (the same accepted paths and bonus tokens)."""
+    w, f, P = tiny(seed=12, B=3, d=64, V=8, Hq=2, Hkv=1, dh=64, shortlist=(3, 2, 2), P=(5, 12))
+    g = orc.decode(w, f, P, "greedy", n_steps)
+    c = orc.decode(w, f, P, "sample", n_steps, sampling=(1e-7, 3))
+    for rg, rc in zip(g, c):
+        assert rc["emitted"] == rg["emitted"]
+        np.testing.assert_array_equal(rc["path"]["L"], rg["path"]["L"])
+        np.testing.assert_array_equal(rc["path"]["next_root"], rg["path"]["next_root"])
+    assert {int(L) for r in g for L in r["path"]["L"]} - {0}     # some drafts accepted
+
+
+def test_decode_sample_cold_is_greedy():
+    check_decode_sample_cold_is_greedy(oracle)
+
+
 def test_decode_sample_lossless():
     check_decode_sample_lossless(oracle)
 
