@@ -43,8 +43,9 @@ the function that uses it):
   R7  Longest accepted path: deepest node whose every edge passes; ties go to
       the lowest breadth-first index.  L = its depth; the step emits L + 1
       tokens (the root and the path); next_root = argmax of the verify row at
-      the path's last node ([GL] early stop, rollback, next token from the
-      base model).
+      the path's last node (under exact sampling, R11, the token drawn there)
+      and the next step's root (R10) ([GL] early stop, rollback, next token
+      from the base model).
   R8  KV compaction: cache rows P_b + path[j] move to P_b + j for j = 0..L,
       then P_b += L + 1 ([GL] "Speculative KV Cache", rollback).
   R9  bf16 workloads: the oracle rounds to bf16 exactly where the stored
