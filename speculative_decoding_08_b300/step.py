@@ -131,7 +131,9 @@ class MedusaStep:
             seed: int = 0) -> None:
         """Enqueue one step on the current stream (asynchronous).  mode GREEDY,
         TYPICAL or SAMPLE (exact sampling at ``temperature`` with key
-        ``seed``)."""
+        ``seed``).  A single step: its root is the base head's argmax, and a
+        decoding loop started after it begins afresh."""
+        self._carried = False
         self._draft(h)
         self._verify_layers()
         self._verify_and_accept(mode, eps, delta, temperature, seed)
