@@ -199,7 +199,7 @@ class MedusaStep:
     #
     # Two forms of the steady-state step:
     #   separate (canonical order): medusa_heads(h) -> tree_attention ->
-    #       lm_verify -> verify_accept -> compact_kv -> next_inputs(h)
+    #       lm_verify -> verify_accept -> compact_kv -> next_inputs(root, h)
     #       (two LM-projection streams per step: draft rows, verify rows);
     #   fused: tree_attention -> lm_verify_draft -> verify_accept ->
     #       compact_kv -> next_inputs(root, shortlists, h): the K heads run on
